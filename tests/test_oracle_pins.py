@@ -1,0 +1,274 @@
+"""Pins for the CPU oracle: each check compares it with something other than
+itself (hand-worked examples, library routines, brute force, closed forms and
+invariants), so that a dropped term, a wrong index, sign or tie-break, or a
+transposed operand in the oracle fails at least one of them."""
+import itertools
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import oracle
+from int4_grouped_gemm_gb300 import synthetic
+
+
+def _fx(fixture_loader, name):
+    return fixture_loader(name)
+
+
+# ------------------------------------------------------------------ bf16
+
+
+def test_bf16_rounding_matches_torch():
+    g = torch.Generator().manual_seed(11)
+    vals = torch.randn(20000, generator=g) * torch.exp(torch.randn(20000, generator=g) * 10)
+    edge = torch.tensor([0.0, -0.0, 1.0, -1.0, 3.0e38, -3.0e38, 1e-40, -1e-40, 1e-45],
+                        dtype=torch.float32)
+    ties = torch.tensor([0x3F808000, 0x3F818000, 0xBF808000, 0x3F80FFFF, 0x00008000],
+                        dtype=torch.int64).to(torch.int32).view(torch.float32)
+    x = torch.cat([vals.float(), edge, ties])
+    ours = oracle.bf16_round(x.numpy())
+    ref = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(ours, ref)
+
+
+# ------------------------------------------------------------- quantiser
+
+
+def test_quantize_hand_packed(fixture_loader):
+    fx = fixture_loader("quant_hand_packed.txt")
+    G = int(fx["G"][0])
+    w = np.array([fx["w_row0"], fx["w_row1"]], np.float32)
+    q, s, b = oracle.quantize(w, G)
+    np.testing.assert_array_equal(q, np.array([fx["q_row0"], fx["q_row1"]], np.uint32))
+    np.testing.assert_array_equal(s, np.array([fx["scale_row0"], fx["scale_row1"]], np.uint16))
+    np.testing.assert_array_equal(b, np.array([fx["bias_row0"], fx["bias_row1"]], np.uint16))
+    deq = oracle.dequant(q, s, b, 16, G)
+    np.testing.assert_array_equal(deq, np.array([fx["deq_row0"], fx["deq_row1"]], np.float64))
+
+
+def test_nibble_order_low_first():
+    # codes 0..7 and 15..8 in one row: word k/8 holds element k at bits 4*(k%8)
+    s_bits = 0x3F80  # scale 1, bias 0 -> w == code
+    w = np.array([[0, 15, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14]], np.float32)
+    q, s, b = oracle.quantize(w, 16)
+    assert s[0, 0] == s_bits and b[0, 0] == 0
+    assert q[0, 0] == 0x6543_21F0 and q[0, 1] == 0xEDCB_A987
+
+
+def _bf16_of(x):
+    return torch.tensor(np.float32(x)).to(torch.bfloat16).view(torch.int16).item() & 0xFFFF
+
+
+@pytest.mark.parametrize("G", [32, 64])
+def test_quantize_scale_bias_and_nearest_code(G):
+    rng = np.random.default_rng(5)
+    rows, K = 24, 256
+    w = (rng.standard_normal((rows, K)) * 0.02).astype(np.float32)
+    w[3, :G] = 0.125                       # constant group -> s = 0, codes 0
+    q, s, b = oracle.quantize(w, G)
+    deq = oracle.dequant(q, s, b, K, G)
+    for r in range(rows):
+        for g in range(K // G):
+            v = w[r, g * G:(g + 1) * G]
+            mn, mx = np.float32(v.min()), np.float32(v.max())
+            assert s[r, g] == _bf16_of(np.float32(mx - mn) / np.float32(15.0))
+            assert b[r, g] == _bf16_of(mn)
+            sv = float(torch.tensor(int(s[r, g]), dtype=torch.int32).to(torch.int16)
+                       .view(torch.bfloat16).float())
+            bv = float(torch.tensor(int(b[r, g]), dtype=torch.int32).to(torch.int16)
+                       .view(torch.bfloat16).float())
+            grid = bv + sv * np.arange(16, dtype=np.float64)
+            d = deq[r, g * G:(g + 1) * G]
+            # each dequantised value is one of the 16 grid points and (brute
+            # force over all codes) a nearest one to the input
+            for vi, di in zip(v.astype(np.float64), d):
+                assert np.any(grid == di)
+                assert abs(vi - di) <= np.min(np.abs(grid - vi)) + 1e-7 * abs(vi) + 1e-12
+            # closed-form bound on the round-trip error
+            bound = sv / 2 + 2.0 ** -8 * (float(mx - mn) + abs(float(mn))) + 1e-7
+            assert np.max(np.abs(d - v)) <= bound
+
+
+def test_quantize_constant_group_is_code_zero():
+    w = np.full((1, 64), -0.7, np.float32)
+    q, s, b = oracle.quantize(w, 64)
+    assert s[0, 0] == 0 and b[0, 0] == _bf16_of(-0.7)
+    assert np.all(q == 0)
+
+
+# ---------------------------------------------------------------- router
+
+
+def test_router_logits_within_fp32_bound():
+    rng = np.random.default_rng(7)
+    T, H, E = 32, 512, 24
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    xb = synthetic.bf16_bits(x).numpy().view(np.uint16)
+    Wr = (rng.standard_normal((E, H)) * 0.02).astype(np.float32)
+    bias = rng.standard_normal(E).astype(np.float32)
+    l = oracle.router_logits(xb, Wr, bias)
+    xf = x.float().numpy().astype(np.float64)
+    exact = xf @ Wr.astype(np.float64).T + bias.astype(np.float64)
+    gamma = (H + 1) * 2.0 ** -24 / (1 - (H + 1) * 2.0 ** -24)
+    bound = gamma * (np.abs(xf) @ np.abs(Wr.astype(np.float64)).T + np.abs(bias))
+    assert np.all(np.abs(l - exact) <= bound)
+    # an operand mix-up (Wr read transposed, bias dropped) is far outside the bound
+    assert np.max(np.abs(l - exact)) < 1e-4
+
+
+# ----------------------------------------------------------------- top-k
+
+
+def test_topk_hand_ties(fixture_loader):
+    fx = fixture_loader("topk_ties.txt")
+    l = np.array([fx["logits"]], np.float32)
+    for k in (3, 4):
+        idx, w = oracle.topk(l, k)
+        np.testing.assert_array_equal(idx[0], np.array(fx[f"k{k}_idx"], np.int32))
+        np.testing.assert_allclose(w[0], np.array(fx[f"k{k}_w"]), rtol=1e-15, atol=1e-16)
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties"])
+@pytest.mark.parametrize("E,k", [(16, 2), (16, 4), (8, 8), (256, 8)])
+def test_topk_brute_force(kind, E, k):
+    l = synthetic.make_logits(64, E, seed=E * 10 + k, kind=kind).numpy()
+    idx, w = oracle.topk(l, k)
+    for t in range(l.shape[0]):
+        row = l[t]
+        # rank = competitors strictly greater, plus equal ones with a lower index
+        rank = np.array([np.sum(row > row[e]) + np.sum((row == row[e]) & (np.arange(E) < e))
+                         for e in range(E)])
+        expect = np.argsort(rank, kind="stable")[:k]
+        np.testing.assert_array_equal(idx[t], expect)
+        assert set(idx[t]) == set(np.nonzero(rank < k)[0])
+        # library cross-check: lexsort by (-logit, index)
+        np.testing.assert_array_equal(idx[t], np.lexsort((np.arange(E), -row.astype(np.float64)))[:k])
+        # weights: softmax over the picked logits (library), summing to one
+        ref = scipy.special.softmax(row[idx[t]].astype(np.float64))
+        np.testing.assert_allclose(w[t], ref, rtol=1e-12, atol=1e-15)
+        assert abs(w[t].sum() - 1.0) < 1e-12
+
+
+def test_topk_all_equal_picks_lowest_indices():
+    l = np.zeros((5, 256), np.float32)
+    idx, w = oracle.topk(l, 8)
+    assert np.all(idx == np.arange(8, dtype=np.int32))
+    np.testing.assert_allclose(w, 1.0 / 8, rtol=1e-15)
+
+
+def test_topk_weights_equal_full_softmax_renormalised():
+    l = synthetic.make_logits(16, 32, seed=3).numpy()
+    idx, w = oracle.topk(l, 4)
+    p = scipy.special.softmax(l.astype(np.float64), axis=1)
+    sel = np.take_along_axis(p, idx, axis=1)
+    np.testing.assert_allclose(w, sel / sel.sum(axis=1, keepdims=True), rtol=1e-12)
+
+
+# ----------------------------------------------------- routing tables
+
+
+def _random_idx(T, E, k, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.choice(E, size=k, replace=False) for _ in range(T)]).astype(np.int32)
+
+
+@pytest.mark.parametrize("T,E,k,BN,shared", [(37, 16, 2, 8, True), (64, 256, 8, 16, True),
+                                              (5, 8, 8, 4, False), (1, 256, 8, 256, True)])
+def test_route_invariants_and_brute_force(T, E, k, BN, shared):
+    idx = _random_idx(T, E, k, seed=T + E)
+    R = oracle.route(idx, E, shared, BN)
+    counts, offsets, perm, inv = R["counts"], R["offsets"], R["perm"], R["inv_perm"]
+    G = E + (1 if shared else 0)
+    assert counts[:E].sum() == T * k
+    assert offsets[E] == T * k and offsets[G] == T * k + (T if shared else 0)
+    if shared:
+        assert counts[E] == T
+    np.testing.assert_array_equal(np.bincount(idx.ravel(), minlength=E), counts[:E])
+    assert sorted(perm.tolist()) == list(range(T * k))           # bijection
+    np.testing.assert_array_equal(inv[perm], np.arange(T * k))   # inverse
+    # brute force: sort every (expert, token, slot) triple
+    triples = sorted((int(idx[t, j]), t, j) for t in range(T) for j in range(k))
+    np.testing.assert_array_equal(perm, np.array([t * k + j for _, t, j in triples]))
+    # tiles cover every group's rows exactly once, in blocks of at most BN
+    covered = np.zeros(offsets[G], np.int32)
+    for g_, r0, n in zip(R["tile_group"], R["tile_row"], R["tile_rows"]):
+        assert 1 <= n <= BN and offsets[g_] <= r0 and r0 + n <= offsets[g_ + 1]
+        covered[r0:r0 + n] += 1
+    assert np.all(covered == 1)
+    assert len(R["tile_group"]) == sum(-(-int(c) // BN) for c in counts)
+
+
+# ------------------------------------------------------------- experts
+
+
+def _dense_swiglu(xf, Wg, Wu, Wd):
+    g = xf @ Wg.T
+    u = xf @ Wu.T
+    return (g / (1.0 + np.exp(-g)) * u) @ Wd.T
+
+
+@pytest.mark.parametrize("shared", [False, True])
+def test_single_expert_reduces_to_dense_swiglu(shared):
+    """E = 1, k = 1: the layer is a dense SwiGLU MLP (plus the shared one)."""
+    cfg = synthetic.MoEConfig("dense", T=6, H=128, E=1, k=1, I=64, group=32, seed=21,
+                              has_shared=shared)
+    L = synthetic.make_layer(cfg)
+    gate = oracle.quantize_stack(L.w_gate.numpy(), 32)
+    up = oracle.quantize_stack(L.w_up.numpy(), 32)
+    down = oracle.quantize_stack(L.w_down.numpy(), 32)
+    xb = synthetic.bf16_bits(L.x).numpy().view(np.uint16)
+    out = oracle.moe_layer(xb, L.router_w.numpy(), None, gate, up, down, E=1, k=1,
+                           has_shared=shared)
+    assert np.all(out["idx"] == 0) and np.allclose(out["w"], 1.0)
+    xf = L.x.float().numpy().astype(np.float64)
+    nexp = 2 if shared else 1
+    ref = np.zeros((cfg.T, cfg.H))
+    for e in range(nexp):
+        Wg = oracle.dequant(gate.q[e], gate.s[e], gate.b[e], cfg.H, 32)
+        Wu = oracle.dequant(up.q[e], up.s[e], up.b[e], cfg.H, 32)
+        Wd = oracle.dequant(down.q[e], down.s[e], down.b[e], cfg.I, 32)
+        ref += _dense_swiglu(xf, Wg, Wu, Wd)
+    np.testing.assert_allclose(out["y"], ref, rtol=1e-10, atol=1e-12)
+
+
+def test_identity_experts_pass_input_through():
+    T, E, k, H = 40, 16, 4, 64
+    l = synthetic.make_logits(T, E, seed=9).numpy()
+    idx, w = oracle.topk(l, k)
+    x = synthetic.make_tokens(H, T, seed=4)
+    xb = synthetic.bf16_bits(x).numpy().view(np.uint16)
+    y = oracle.dispatch_combine_identity(xb, E, True, idx, w)
+    np.testing.assert_allclose(y, x.float().numpy().astype(np.float64), rtol=1e-14, atol=0)
+
+
+def test_tiny_layer_against_numpy_evaluation():
+    """Whole tiny layer vs an independent numpy evaluation (library sort and
+    matmul) of the same definition, on the oracle's own quantised weights."""
+    cfg = synthetic.CONFIGS["tiny"]
+    L = synthetic.make_layer(cfg)
+    G = cfg.group
+    gate = oracle.quantize_stack(L.w_gate.numpy(), G)
+    up = oracle.quantize_stack(L.w_up.numpy(), G)
+    down = oracle.quantize_stack(L.w_down.numpy(), G)
+    xb = synthetic.bf16_bits(L.x).numpy().view(np.uint16)
+    out = oracle.moe_layer(xb, L.router_w.numpy(), None, gate, up, down, cfg.E, cfg.k, True)
+    xf = L.x.float().numpy().astype(np.float64)
+    logits = xf @ L.router_w.numpy().astype(np.float64).T
+    y = np.zeros((cfg.T, cfg.H))
+    deq = {}
+    for e in range(cfg.E + 1):
+        deq[e] = (oracle.dequant(gate.q[e], gate.s[e], gate.b[e], cfg.H, G),
+                  oracle.dequant(up.q[e], up.s[e], up.b[e], cfg.H, G),
+                  oracle.dequant(down.q[e], down.s[e], down.b[e], cfg.I, G))
+    for t in range(cfg.T):
+        order = np.lexsort((np.arange(cfg.E), -logits[t]))[:cfg.k]
+        np.testing.assert_array_equal(out["idx"][t], order)
+        p = scipy.special.softmax(logits[t][order])
+        for j, e in enumerate(order):
+            y[t] += p[j] * _dense_swiglu(xf[t:t + 1], *deq[e])[0]
+        y[t] += _dense_swiglu(xf[t:t + 1], *deq[cfg.E])[0]
+    # the oracle's router is fp32 (weights move by ~1e-7 relative), the numpy
+    # evaluation's is fp64
+    np.testing.assert_allclose(out["y"], y, rtol=1e-5, atol=1e-6 * np.abs(y).max())
