@@ -1,0 +1,187 @@
+/*
+ * int4 grouped-GEMM sparse Mixture-of-Experts layer for one GB300 (sm_103a).
+ *
+ * C ABI of libmoe_gb300.so.  The operation follows the pages on Lily, the
+ * engine Perplexity built for Qwen3.6-35B-A3B:
+ *   - "Lily: Perplexity's Custom Inference Engine for Apple Silicon",
+ *     section "The architecture that forces the issue: MoE plus Gated
+ *     DeltaNet": a router scores 256 experts and picks 8, a shared expert
+ *     runs on every token, expert loads are uneven;
+ *   - same page, section "Why Apple Silicon isn't just a smaller datacenter
+ *     GPU": prefill is GEMM work (weights reused across rows), batch-1 decode
+ *     is bandwidth-bound GEMV work on the vector ALUs;
+ *   - same page, section "The measured wins": 4-bit checkpoint, unpacked in
+ *     on-chip memory inside the matmul instead of being expanded in memory;
+ *   - "Inside Lily: How Perplexity's Rust and Metal Engine Accelerates Qwen
+ *     Inference on Apple Silicon", list under "Performance Gains and Workload
+ *     Patterns": fused prefill (4-bit weights rebuilt tile by tile inside the
+ *     grouped GEMM), routing histograms and block maps kept on the GPU with no
+ *     CPU synchronisation per MoE layer, decode kernel chains fused.
+ *
+ * Layer definition (the pages give no formulas; this is the plainest reading):
+ *   logits[t][e] = sum_h x[t][h] * router_w[e][h] (+ router_bias[e])    fp32
+ *   slots j = 0..k-1 of token t: the k largest logits, equal logits ordered
+ *     by lower expert index, slot j holding the j-th largest
+ *   w[t][j] = softmax over all E logits, renormalised over the k picked
+ *   expert e: o = (silu(x Wg_e^T) * (x Wu_e^T)) Wd_e^T      (SwiGLU MLP)
+ *   y[t] = sum_j w[t][j] * o_{e_j}(x[t]) + o_shared(x[t])   (shared weight 1)
+ *
+ * Weight format (int4 asymmetric, groups of `group` consecutive K elements):
+ *   value = scale * q + bias, q unsigned in 0..15, scale and bias bf16.
+ *   q:      uint32 [rows][K/8]; element k of a row is in word k/8 at bits
+ *           4*(k%8) .. 4*(k%8)+3 (low nibble first).
+ *   scale, bias: bf16 bit patterns, uint16 [rows][K/group].
+ * Matrices are stacked over experts, expert index E being the shared expert:
+ *   gate, up: [E+1][I][H] (K = H);  down: [E+1][H][I] (K = I).
+ *
+ * Memory and ownership: every pointer passed to a compute call is device
+ * memory owned by the caller (the e2e helper is the one exception: it takes
+ * host pointers).  The library never allocates, frees or synchronises inside
+ * moe_prefill / moe_decode / pack_int4 / moe_route_logits: all work is
+ * enqueued on `stream` and runs asynchronously.  Device pointers must be
+ * 16-byte aligned.
+ *
+ * Errors: each call returns MOE_OK (0) or a negative MOE_ERR_* code.
+ * Argument errors are found on the host before anything is launched.  Errors
+ * found on the device (a bounded wait that ran out) are written to a status
+ * word in the workspace and read with moe_read_device_status().
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    MOE_OK = 0,
+    MOE_ERR_NULL = -1,          /* a required pointer is NULL */
+    MOE_ERR_ALIGN = -2,         /* a pointer is not 16-byte aligned */
+    MOE_ERR_SHAPE = -3,         /* (E, k, H, I, group) outside the supported set */
+    MOE_ERR_TOKENS = -4,        /* T < 1 or too large */
+    MOE_ERR_WORKSPACE = -5,     /* workspace smaller than moe_workspace_bytes() */
+    MOE_ERR_CUDA = -6,          /* a CUDA runtime call or launch failed */
+    MOE_ERR_TENSOR_MAP = -7,    /* TMA descriptor could not be encoded */
+    MOE_ERR_DEVICE = -8,        /* current device is not an sm_103 GPU */
+    MOE_ERR_TIMEOUT = -100      /* device: a bounded wait ran out (-100 - site) */
+};
+
+/* One stacked int4 matrix set (see "Weight format" above). */
+typedef struct {
+    const uint32_t *q;
+    const uint16_t *scale;
+    const uint16_t *bias;
+} moe_qweight;
+
+/*
+ * One MoE layer.  Supported: 1 <= E <= 256, 1 <= k <= min(8, E),
+ * H % 256 == 0, I % 64 == 0, group in {32, 64}, H/group and I/group even,
+ * H/group <= 32 and I/group <= 32.  has_shared is 0 or 1.
+ */
+typedef struct {
+    int32_t E, k, H, I, group, has_shared;
+    const float *router_w;    /* [E][H] fp32 */
+    const float *router_bias; /* [E] fp32, or NULL for none */
+    moe_qweight gate, up, down;
+} moe_layer_desc;
+
+/* Byte offsets, inside the workspace, of the routing tables that the last
+ * moe_prefill / moe_route_logits call with this T wrote (for inspection). */
+typedef struct {
+    int64_t logits;      /* fp32 [T][E] (moe_prefill only) */
+    int64_t topk_idx;    /* int32 [T][k], slot order: descending logit */
+    int64_t topk_w;      /* fp32 [T][k], renormalised softmax weights */
+    int64_t counts;      /* int32 [E+1]: rows per group (group E = shared) */
+    int64_t offsets;     /* int32 [E+2]: exclusive prefix sum of counts */
+    int64_t perm;        /* int32 [T*k]: routed row -> t*k + j, by (expert, token) */
+    int64_t inv_perm;    /* int32 [T*k]: t*k + j -> routed row */
+    int64_t tile_group;  /* int32 [max_tiles]: canonical tile map, groups in order */
+    int64_t tile_row;    /* int32 [max_tiles]: first row of the tile */
+    int64_t tile_rows;   /* int32 [max_tiles]: rows in the tile (<= tile size) */
+    int64_t tile_sched;  /* int32 [max_tiles]: launch order (largest tiles first) */
+    int64_t num_tiles;   /* int32 [1] */
+    int32_t max_tiles;
+    int32_t tile_size;   /* rows per tile (tokens per grouped-GEMM block) */
+} moe_routing_views;
+
+/* Workspace bytes for moe_prefill with up to T_max tokens and for
+ * moe_decode; 0 if the shape is unsupported.  The workspace must be
+ * zero-filled once before first use (moe_workspace_init does it). */
+size_t moe_workspace_bytes(const moe_layer_desc *desc, int32_t T_max);
+
+/* Clear the control block (status word, counters) of a workspace. */
+int moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Fill `views` with the offsets of the routing tables for T tokens. */
+int moe_routing_views_for(const moe_layer_desc *desc, int32_t T, moe_routing_views *views);
+
+/*
+ * Prefill: y[T][H] (bf16) = MoE layer of x[T][H] (bf16), on the GPU end to
+ * end: router GEMM, top-k and weights, histogram, scan, permutation and tile
+ * map, grouped int4 gate/up GEMM with SwiGLU, grouped int4 down GEMM with the
+ * weighted combine.  No host synchronisation inside.  x and y must not alias.
+ */
+int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
+                cudaStream_t stream);
+
+/*
+ * Batch-1 decode: y[1][H] (bf16) = MoE layer of x[1][H] (bf16) as
+ * bandwidth-bound dequant-GEMVs that read only the router and the k+1
+ * touched experts; the weighted combine is fused into the down GEMV.
+ * x and y must not alias.
+ */
+int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, size_t ws_bytes,
+               cudaStream_t stream);
+
+/*
+ * Routing only, from given fp32 logits [T][E]: top-k and weights, histogram,
+ * scan, permutation and tile map into the workspace (see moe_routing_views).
+ * desc supplies E, k and has_shared; its pointers are not read.
+ */
+int moe_route_logits(const moe_layer_desc *desc, const float *logits, int32_t T, void *ws, size_t ws_bytes,
+                     cudaStream_t stream);
+
+/*
+ * Quantise w[rows][K] (fp32, device) to the int4 format above: per group,
+ * scale = bf16((max - min) / 15), bias = bf16(min), q = clamp(rint((w - bias)
+ * / scale), 0, 15) in fp32 with the bf16-rounded scale and bias (q = 0 when
+ * scale == 0).  Requires K % 8 == 0, K % group == 0, group % 8 == 0.
+ */
+int pack_int4(const float *w, int64_t rows, int32_t K, int32_t group, uint32_t *q, uint16_t *scale,
+              uint16_t *bias, cudaStream_t stream);
+
+/* Synchronise `stream`, return the device status word of `ws` (0 = fine,
+ * MOE_ERR_TIMEOUT - site after a bounded wait ran out) and clear it. */
+int moe_read_device_status(void *ws, cudaStream_t stream);
+
+/* Upper bound, in SM clock cycles, of every device-side wait (default about
+ * two seconds).  Returns the previous value. */
+long long moe_set_wait_limit(long long cycles);
+
+/* Launch one block that waits on an mbarrier nobody arrives at, with the
+ * library's bounded wait and the given limit; it must record MOE_ERR_TIMEOUT
+ * in the workspace status word.  Exercises the failure path without a fault. */
+int moe_selftest_wait_timeout(void *ws, size_t ws_bytes, long long limit_cycles, cudaStream_t stream);
+
+/*
+ * End to end from host memory: copy x (host, T x H bf16) to the device, run
+ * moe_prefill (T > 1) or moe_decode (T == 1) on `stream`, copy y back to host
+ * memory and synchronise.  x_dev / y_dev are caller-owned device staging
+ * buffers of T x H bf16 each.  Pinned host memory makes the copies async.
+ */
+int moe_forward_host(const moe_layer_desc *desc, const void *x_host, int32_t T, void *y_host, void *x_dev,
+                     void *y_dev, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Human-readable text for a status code. */
+const char *moe_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,161 @@
+"""ctypes binding of libmoe_gb300.so: same names as the C ABI in include/moe.h.
+
+Argument marshalling only: torch tensors are passed as raw device pointers and
+every step of the layer runs in the library's CUDA kernels.  There is no CPU
+fallback; loading fails loudly when the library has not been built.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe_gb300.so")
+
+c_i32, c_i64, c_p, c_sz, c_ll = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_longlong
+
+MOE_OK = 0
+MOE_ERR_NULL = -1
+MOE_ERR_ALIGN = -2
+MOE_ERR_SHAPE = -3
+MOE_ERR_TOKENS = -4
+MOE_ERR_WORKSPACE = -5
+MOE_ERR_CUDA = -6
+MOE_ERR_TENSOR_MAP = -7
+MOE_ERR_DEVICE = -8
+MOE_ERR_TIMEOUT = -100
+
+
+class moe_qweight(ctypes.Structure):
+    _fields_ = [("q", c_p), ("scale", c_p), ("bias", c_p)]
+
+
+class moe_layer_desc(ctypes.Structure):
+    _fields_ = [("E", c_i32), ("k", c_i32), ("H", c_i32), ("I", c_i32), ("group", c_i32),
+                ("has_shared", c_i32), ("router_w", c_p), ("router_bias", c_p),
+                ("gate", moe_qweight), ("up", moe_qweight), ("down", moe_qweight)]
+
+
+class moe_routing_views(ctypes.Structure):
+    _fields_ = [(n, c_i64) for n in ("logits", "topk_idx", "topk_w", "counts", "offsets", "perm",
+                                      "inv_perm", "tile_group", "tile_row", "tile_rows", "tile_sched",
+                                      "num_tiles")] + [("max_tiles", c_i32), ("tile_size", c_i32)]
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+
+
+_lib = None
+
+# name -> (restype, argtypes); mirrors include/moe.h
+SIGNATURES = {
+    "moe_workspace_bytes": (c_sz, [c_p, c_i32]),
+    "moe_workspace_init": (ctypes.c_int, [c_p, c_sz, c_p]),
+    "moe_routing_views_for": (ctypes.c_int, [c_p, c_i32, c_p]),
+    "moe_prefill": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_sz, c_p]),
+    "moe_decode": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_sz, c_p]),
+    "moe_route_logits": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_sz, c_p]),
+    "pack_int4": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_p]),
+    "moe_read_device_status": (ctypes.c_int, [c_p, c_p]),
+    "moe_set_wait_limit": (c_ll, [c_ll]),
+    "moe_selftest_wait_timeout": (ctypes.c_int, [c_p, c_sz, c_ll, c_p]),
+    "moe_forward_host": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_sz, c_p]),
+    "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def load(path: str = LIB_PATH):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(path):
+            raise ImportError(f"{path} not found: build it first (python -m int4_grouped_gemm_gb300.build)")
+        L = ctypes.CDLL(path)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().moe_status_string(int(code)).decode()
+
+
+def _check(rc: int, what: str):
+    if rc != MOE_OK:
+        raise MoEError(rc, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return int(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream)
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+# --------------------------------------------------------------- calls
+
+
+def moe_workspace_bytes(desc: moe_layer_desc, T_max: int) -> int:
+    return int(load().moe_workspace_bytes(ctypes.byref(desc), T_max))
+
+
+def moe_workspace_init(ws, stream=None):
+    _check(load().moe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_workspace_init")
+
+
+def moe_routing_views_for(desc: moe_layer_desc, T: int) -> moe_routing_views:
+    v = moe_routing_views()
+    _check(load().moe_routing_views_for(ctypes.byref(desc), T, ctypes.byref(v)), "moe_routing_views_for")
+    return v
+
+
+def moe_prefill(desc: moe_layer_desc, x, T: int, y, ws, stream=None):
+    _check(load().moe_prefill(ctypes.byref(desc), _ptr(x), T, _ptr(y), _ptr(ws), ws.numel() * ws.element_size(),
+                              _stream(stream)), "moe_prefill")
+
+
+def moe_decode(desc: moe_layer_desc, x, y, ws, stream=None):
+    _check(load().moe_decode(ctypes.byref(desc), _ptr(x), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(),
+                             _stream(stream)), "moe_decode")
+
+
+def moe_route_logits(desc: moe_layer_desc, logits, T: int, ws, stream=None):
+    _check(load().moe_route_logits(ctypes.byref(desc), _ptr(logits), T, _ptr(ws), ws.numel() * ws.element_size(),
+                                   _stream(stream)), "moe_route_logits")
+
+
+def pack_int4(w, rows: int, K: int, group: int, q, scale, bias, stream=None):
+    _check(load().pack_int4(_ptr(w), rows, K, group, _ptr(q), _ptr(scale), _ptr(bias), _stream(stream)),
+           "pack_int4")
+
+
+def moe_read_device_status(ws, stream=None) -> int:
+    return int(load().moe_read_device_status(_ptr(ws), _stream(stream)))
+
+
+def moe_set_wait_limit(cycles: int) -> int:
+    return int(load().moe_set_wait_limit(int(cycles)))
+
+
+def moe_selftest_wait_timeout(ws, limit_cycles: int, stream=None):
+    _check(load().moe_selftest_wait_timeout(_ptr(ws), ws.numel() * ws.element_size(), int(limit_cycles),
+                                            _stream(stream)), "moe_selftest_wait_timeout")
+
+
+def moe_forward_host(desc: moe_layer_desc, x_host, T: int, y_host, x_dev, y_dev, ws, stream=None):
+    _check(load().moe_forward_host(ctypes.byref(desc), _ptr(x_host), T, _ptr(y_host), _ptr(x_dev), _ptr(y_dev),
+                                   _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_forward_host")

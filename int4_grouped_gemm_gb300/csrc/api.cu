@@ -1,0 +1,364 @@
+// C ABI of the int4 MoE library: argument checks, workspace layout, TMA
+// descriptors and the launch sequence of each call.  See include/moe.h for
+// the contract of every entry point.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "kernels.cuh"
+
+
+namespace moe {
+
+static long long g_wait_limit = 4000000000LL;  // ~2 s at 2 GHz
+
+struct DeviceInfo {
+    bool ready = false;
+    bool ok = false;
+    int num_sms = 0;
+};
+
+static std::mutex g_mu;
+static DeviceInfo g_dev[64];
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+static int current_device(DeviceInfo *&info) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        cudaDeviceProp p{};
+        if (cudaGetDeviceProperties(&p, dev) != cudaSuccess) return MOE_ERR_DEVICE;
+        d.ok = (p.major == 10 && p.minor == 3);
+        d.num_sms = p.multiProcessorCount;
+        d.ready = true;
+    }
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            return MOE_ERR_DEVICE;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    info = &d;
+    return d.ok ? MOE_OK : MOE_ERR_DEVICE;
+}
+
+static int encode_2d(CUtensorMap *map, CUtensorMapDataType type, int elem_bytes, const void *ptr, uint64_t inner,
+                     uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * static_cast<uint64_t>(elem_bytes)};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, type, 2, const_cast<void *>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_TENSOR_MAP;
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int check_ptr(const void *p) {
+    if (!p) return MOE_ERR_NULL;
+    return aligned16(p) ? MOE_OK : MOE_ERR_ALIGN;
+}
+
+static int check_shape(const moe_layer_desc *d) {
+    if (!d) return MOE_ERR_NULL;
+    if (d->E < 1 || d->E > 256) return MOE_ERR_SHAPE;
+    if (d->k < 1 || d->k > 8 || d->k > d->E) return MOE_ERR_SHAPE;
+    if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_SHAPE;
+    if (d->group != 32 && d->group != 64) return MOE_ERR_SHAPE;
+    if (d->H < 256 || d->H % 256 != 0 || d->H > 16384) return MOE_ERR_SHAPE;
+    if (d->I < 64 || d->I % 64 != 0 || d->I > 4096) return MOE_ERR_SHAPE;
+    const int gh = d->H / d->group, gi = d->I / d->group;
+    if (gh % 2 || gi % 2 || gh > 32 || gi > 32) return MOE_ERR_SHAPE;
+    return MOE_OK;
+}
+
+static int check_weights(const moe_layer_desc *d) {
+    int rc;
+    if ((rc = check_ptr(d->router_w))) return rc;
+    if (d->router_bias && !aligned16(d->router_bias)) return MOE_ERR_ALIGN;
+    const moe_qweight *ws[3] = {&d->gate, &d->up, &d->down};
+    for (const moe_qweight *w : ws) {
+        if ((rc = check_ptr(w->q))) return rc;
+        if ((rc = check_ptr(w->scale))) return rc;
+        if ((rc = check_ptr(w->bias))) return rc;
+    }
+    return MOE_OK;
+}
+
+static int check_tokens(const moe_layer_desc *d, int32_t T) {
+    if (T < 1) return MOE_ERR_TOKENS;
+    if (static_cast<int64_t>(T) * (d->k + 1) >= (int64_t(1) << 30)) return MOE_ERR_TOKENS;
+    return MOE_OK;
+}
+
+static int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// One thread waits, with the library's bounded wait, on an mbarrier that no
+// thread ever arrives at; the wait must run out and record the status.
+__global__ void selftest_wait_kernel(Ctrl *ctrl, long long limit) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        if (!mbar_wait(&bar, 0, limit)) record_status(&ctrl->status, MOE_ERR_TIMEOUT);
+    }
+}
+
+static cudaError_t launch_selftest_wait(Ctrl *ctrl, long long limit, cudaStream_t s) {
+    selftest_wait_kernel<<<1, 32, 0, s>>>(ctrl, limit);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_layer_desc *desc, int32_t T_max) {
+    if (check_shape(desc) != MOE_OK || check_tokens(desc, T_max) != MOE_OK) return 0;
+    const PrefillLayout P = prefill_layout(T_max, desc->E, desc->k, desc->H, desc->I);
+    const DecodeLayout D = decode_layout(desc->E, desc->k, desc->I);
+    return P.total > D.total ? P.total : D.total;
+}
+
+int moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
+    int rc = check_ptr(ws);
+    if (rc) return rc;
+    if (ws_bytes < static_cast<size_t>(kCtrlBytes)) return MOE_ERR_WORKSPACE;
+    return cuda_rc(cudaMemsetAsync(ws, 0, kCtrlBytes, stream));
+}
+
+int moe_routing_views_for(const moe_layer_desc *desc, int32_t T, moe_routing_views *v) {
+    int rc = check_shape(desc);
+    if (rc) return rc;
+    if (!v) return MOE_ERR_NULL;
+    if ((rc = check_tokens(desc, T))) return rc;
+    const PrefillLayout L = prefill_layout(T, desc->E, desc->k, desc->H, desc->I);
+    v->logits = L.logits;
+    v->topk_idx = L.topk_idx;
+    v->topk_w = L.topk_w;
+    v->counts = L.counts;
+    v->offsets = L.offsets;
+    v->perm = L.perm;
+    v->inv_perm = L.inv_perm;
+    v->tile_group = L.tile_group;
+    v->tile_row = L.tile_row;
+    v->tile_rows = L.tile_rows;
+    v->tile_sched = L.tile_sched;
+    v->num_tiles = L.num_tiles;
+    v->max_tiles = L.max_tiles;
+    v->tile_size = kTileRows;
+    return MOE_OK;
+}
+
+int moe_route_logits(const moe_layer_desc *desc, const float *logits, int32_t T, void *ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+    int rc = check_shape(desc);
+    if (rc) return rc;
+    if ((rc = check_ptr(logits)) || (rc = check_ptr(ws))) return rc;
+    if ((rc = check_tokens(desc, T))) return rc;
+    const PrefillLayout L = prefill_layout(T, desc->E, desc->k, desc->H, desc->I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    const RoutingBufs rb = routing_bufs(static_cast<char *>(ws), L);
+    return cuda_rc(launch_routing_tables(logits, T, desc->E, desc->k, desc->has_shared, rb, stream));
+}
+
+int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
+                cudaStream_t stream) {
+    int rc = check_shape(desc);
+    if (rc) return rc;
+    if ((rc = check_weights(desc))) return rc;
+    if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
+    if ((rc = check_tokens(desc, T))) return rc;
+    const int E = desc->E, k = desc->k, H = desc->H, I = desc->I, G = desc->group;
+    const PrefillLayout L = prefill_layout(T, E, k, H, I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+
+    char *w = static_cast<char *>(ws);
+    const RoutingBufs rb = routing_bufs(w, L);
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(w + L.ctrl);
+    __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(w + L.h);
+    float *y_acc = reinterpret_cast<float *>(w + L.y_acc);
+    const int nexp = E + 1;
+
+    CUtensorMap tm_qg, tm_qu, tm_qd, tm_x, tm_h;
+    if ((rc = encode_2d(&tm_qg, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, desc->gate.q, H / 8,
+                        static_cast<uint64_t>(nexp) * I, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return rc;
+    if ((rc = encode_2d(&tm_qu, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, desc->up.q, H / 8,
+                        static_cast<uint64_t>(nexp) * I, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return rc;
+    if ((rc = encode_2d(&tm_qd, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, desc->down.q, I / 8,
+                        static_cast<uint64_t>(nexp) * H, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE)))
+        return rc;
+    if ((rc = encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, T, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return rc;
+    if ((rc = encode_2d(&tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, I, L.R, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return rc;
+
+    cudaError_t e = launch_router(static_cast<const __nv_bfloat16 *>(x), desc->router_w, desc->router_bias, T, H, E,
+                                  rb.logits, y_acc, static_cast<int64_t>(T) * H, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if ((e = launch_routing_tables(rb.logits, T, E, k, desc->has_shared, rb, stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+
+    GemmArgs ga{};
+    ga.G = G;
+    ga.H = H;
+    ga.I = I;
+    ga.rb = rb;
+    ga.h = h;
+    ga.y_acc = y_acc;
+    ga.status = &ctrl->status;
+    ga.wait_limit = g_wait_limit;
+
+    // gate/up + SwiGLU
+    ga.K = H;
+    ga.ngroups = H / G;
+    ga.n_mtiles = 2 * I / 128;
+    ga.s0 = desc->gate.scale;
+    ga.b0 = desc->gate.bias;
+    ga.s1 = desc->up.scale;
+    ga.b1 = desc->up.bias;
+    const int max_units1 = L.max_tiles * ga.n_mtiles;
+    int grid = dev->num_sms < max_units1 ? dev->num_sms : max_units1;
+    if ((e = launch_gemm(0, tm_qg, tm_qu, tm_x, ga, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+
+    // down + weighted combine
+    ga.K = I;
+    ga.ngroups = I / G;
+    ga.n_mtiles = H / 128;
+    ga.s0 = desc->down.scale;
+    ga.b0 = desc->down.bias;
+    ga.s1 = desc->down.scale;
+    ga.b1 = desc->down.bias;
+    const int max_units2 = L.max_tiles * ga.n_mtiles;
+    grid = dev->num_sms < max_units2 ? dev->num_sms : max_units2;
+    if ((e = launch_gemm(1, tm_qd, tm_qd, tm_h, ga, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+
+    if ((e = launch_convert(y_acc, static_cast<__nv_bfloat16 *>(y), static_cast<int64_t>(T) * H, dev->num_sms,
+                            stream)) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
+
+int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    int rc = check_shape(desc);
+    if (rc) return rc;
+    if ((rc = check_weights(desc))) return rc;
+    if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
+    const DecodeLayout L = decode_layout(desc->E, desc->k, desc->I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    char *w = static_cast<char *>(ws);
+    DecodeArgs a{};
+    a.x = static_cast<const __nv_bfloat16 *>(x);
+    a.y = static_cast<__nv_bfloat16 *>(y);
+    a.Wr = desc->router_w;
+    a.bias = desc->router_bias;
+    a.qg = desc->gate.q;
+    a.qu = desc->up.q;
+    a.qd = desc->down.q;
+    a.sg = desc->gate.scale;
+    a.bg = desc->gate.bias;
+    a.su = desc->up.scale;
+    a.bu = desc->up.bias;
+    a.sd = desc->down.scale;
+    a.bd = desc->down.bias;
+    a.E = desc->E;
+    a.k = desc->k;
+    a.H = desc->H;
+    a.I = desc->I;
+    a.G = desc->group;
+    a.has_shared = desc->has_shared;
+    a.ctrl = reinterpret_cast<Ctrl *>(w + L.ctrl);
+    a.logits = reinterpret_cast<float *>(w + L.logits);
+    a.topk_idx = reinterpret_cast<int *>(w + L.topk_idx);
+    a.topk_w = reinterpret_cast<float *>(w + L.topk_w);
+    a.h = reinterpret_cast<float *>(w + L.h);
+    return cuda_rc(launch_decode(a, stream));
+}
+
+int pack_int4(const float *w, int64_t rows, int32_t K, int32_t group, uint32_t *q, uint16_t *scale,
+              uint16_t *bias, cudaStream_t stream) {
+    int rc;
+    if ((rc = check_ptr(w)) || (rc = check_ptr(q)) || (rc = check_ptr(scale)) || (rc = check_ptr(bias))) return rc;
+    if (rows < 0 || K <= 0 || group <= 0 || K % 8 || group % 8 || K % group) return MOE_ERR_SHAPE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    return cuda_rc(launch_pack_int4(w, rows, K, group, q, scale, bias, stream));
+}
+
+int moe_read_device_status(void *ws, cudaStream_t stream) {
+    int rc = check_ptr(ws);
+    if (rc) return rc;
+    int status = 0;
+    if (cudaMemcpyAsync(&status, ws, sizeof(int), cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (status != 0) {
+        if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return MOE_ERR_CUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return status;
+}
+
+long long moe_set_wait_limit(long long cycles) {
+    const long long prev = g_wait_limit;
+    if (cycles > 0) g_wait_limit = cycles;
+    return prev;
+}
+
+int moe_selftest_wait_timeout(void *ws, size_t ws_bytes, long long limit_cycles, cudaStream_t stream) {
+    int rc = check_ptr(ws);
+    if (rc) return rc;
+    if (ws_bytes < static_cast<size_t>(kCtrlBytes)) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    return cuda_rc(launch_selftest_wait(reinterpret_cast<Ctrl *>(ws), limit_cycles, stream));
+}
+
+int moe_forward_host(const moe_layer_desc *desc, const void *x_host, int32_t T, void *y_host, void *x_dev,
+                     void *y_dev, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    int rc = check_shape(desc);
+    if (rc) return rc;
+    if (!x_host || !y_host) return MOE_ERR_NULL;
+    if ((rc = check_tokens(desc, T))) return rc;
+    const size_t bytes = static_cast<size_t>(T) * desc->H * 2;
+    if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    rc = T == 1 ? moe_decode(desc, x_dev, y_dev, ws, ws_bytes, stream)
+                : moe_prefill(desc, x_dev, T, y_dev, ws, ws_bytes, stream);
+    if (rc) return rc;
+    if (cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_rc(cudaStreamSynchronize(stream));
+}
+
+const char *moe_status_string(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_NULL: return "a required pointer is NULL";
+        case MOE_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case MOE_ERR_SHAPE: return "unsupported shape (E, k, H, I, group)";
+        case MOE_ERR_TOKENS: return "token count out of range";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA runtime error or failed launch";
+        case MOE_ERR_TENSOR_MAP: return "TMA descriptor could not be encoded";
+        case MOE_ERR_DEVICE: return "current device is not an sm_103 GPU";
+        default: break;
+    }
+    if (code <= MOE_ERR_TIMEOUT && code > MOE_ERR_TIMEOUT - 100) return "device: a bounded wait ran out";
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,128 @@
+// Workspace layout and the device-pointer bundles handed to the kernels.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kTileRows = 256;      // tokens per grouped-GEMM block (MMA N <= 256)
+constexpr int kRouteChunk = 64;     // tokens per routing block (histogram granularity)
+constexpr int kCtrlBytes = 256;     // status word, decode ticket, ...
+
+// Control block at the start of every workspace.
+struct Ctrl {
+    int status;         // first device-side error (0 = none)
+    unsigned ticket;    // decode: blocks of the router kernel that finished
+    int pad[62];
+};
+
+struct RoutingBufs {
+    float *logits;      // [T][E]
+    int *topk_idx;      // [T][k]
+    float *topk_w;      // [T][k]
+    int *counts_blk;    // [nblk][E]
+    int *base_blk;      // [nblk][E]
+    int *counts;        // [E+1]
+    int *offsets;       // [E+2]
+    int *perm;          // [T*k]
+    int *inv_perm;      // [T*k]
+    int *row_token;     // [R]
+    float *row_weight;  // [R]
+    int *tile_group;    // [max_tiles]
+    int *tile_row;
+    int *tile_rows;
+    int *tile_sched;
+    int *num_tiles;     // [1]
+    int max_tiles;
+    int nblk;
+};
+
+struct PrefillLayout {
+    size_t ctrl, logits, topk_idx, topk_w, counts_blk, base_blk, counts, offsets, perm, inv_perm, row_token,
+        row_weight, tile_group, tile_row, tile_rows, tile_sched, num_tiles, h, y_acc, total;
+    int max_tiles, nblk, R;
+};
+
+struct DecodeLayout {
+    size_t ctrl, logits, topk_idx, topk_w, h, total;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+inline PrefillLayout prefill_layout(int T, int E, int k, int H, int I) {
+    PrefillLayout L{};
+    const int G = E + 1;
+    L.R = T * k + T;
+    L.nblk = (T + kRouteChunk - 1) / kRouteChunk;
+    L.max_tiles = (L.R + kTileRows - 1) / kTileRows + G + 1;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.ctrl = take(kCtrlBytes);
+    L.logits = take(sizeof(float) * (size_t)T * E);
+    L.topk_idx = take(sizeof(int) * (size_t)T * k);
+    L.topk_w = take(sizeof(float) * (size_t)T * k);
+    L.counts_blk = take(sizeof(int) * (size_t)L.nblk * E);
+    L.base_blk = take(sizeof(int) * (size_t)L.nblk * E);
+    L.counts = take(sizeof(int) * (size_t)(G));
+    L.offsets = take(sizeof(int) * (size_t)(G + 1));
+    L.perm = take(sizeof(int) * (size_t)T * k);
+    L.inv_perm = take(sizeof(int) * (size_t)T * k);
+    L.row_token = take(sizeof(int) * (size_t)L.R);
+    L.row_weight = take(sizeof(float) * (size_t)L.R);
+    L.tile_group = take(sizeof(int) * (size_t)L.max_tiles);
+    L.tile_row = take(sizeof(int) * (size_t)L.max_tiles);
+    L.tile_rows = take(sizeof(int) * (size_t)L.max_tiles);
+    L.tile_sched = take(sizeof(int) * (size_t)L.max_tiles);
+    L.num_tiles = take(sizeof(int));
+    L.h = take(sizeof(uint16_t) * (size_t)L.R * I);
+    L.y_acc = take(sizeof(float) * (size_t)T * H);
+    L.total = o;
+    return L;
+}
+
+inline DecodeLayout decode_layout(int E, int k, int I) {
+    DecodeLayout L{};
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = o;
+        o = align_up(o + bytes, 256);
+        return at;
+    };
+    L.ctrl = take(kCtrlBytes);
+    L.logits = take(sizeof(float) * (size_t)E);
+    L.topk_idx = take(sizeof(int) * 8);
+    L.topk_w = take(sizeof(float) * 8);
+    L.h = take(sizeof(float) * (size_t)(k + 1) * I);
+    L.total = o;
+    return L;
+}
+
+inline RoutingBufs routing_bufs(char *ws, const PrefillLayout &L) {
+    RoutingBufs b{};
+    b.logits = reinterpret_cast<float *>(ws + L.logits);
+    b.topk_idx = reinterpret_cast<int *>(ws + L.topk_idx);
+    b.topk_w = reinterpret_cast<float *>(ws + L.topk_w);
+    b.counts_blk = reinterpret_cast<int *>(ws + L.counts_blk);
+    b.base_blk = reinterpret_cast<int *>(ws + L.base_blk);
+    b.counts = reinterpret_cast<int *>(ws + L.counts);
+    b.offsets = reinterpret_cast<int *>(ws + L.offsets);
+    b.perm = reinterpret_cast<int *>(ws + L.perm);
+    b.inv_perm = reinterpret_cast<int *>(ws + L.inv_perm);
+    b.row_token = reinterpret_cast<int *>(ws + L.row_token);
+    b.row_weight = reinterpret_cast<float *>(ws + L.row_weight);
+    b.tile_group = reinterpret_cast<int *>(ws + L.tile_group);
+    b.tile_row = reinterpret_cast<int *>(ws + L.tile_row);
+    b.tile_rows = reinterpret_cast<int *>(ws + L.tile_rows);
+    b.tile_sched = reinterpret_cast<int *>(ws + L.tile_sched);
+    b.num_tiles = reinterpret_cast<int *>(ws + L.num_tiles);
+    b.max_tiles = L.max_tiles;
+    b.nblk = L.nblk;
+    return b;
+}
+
+}  // namespace moe

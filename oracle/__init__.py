@@ -14,6 +14,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 from typing import Optional
 
@@ -28,10 +29,16 @@ CFLAGS = ["-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math", 
 
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (plain C, OpenMP, no contraction)."""
+    stamp = _LIB + ".host"
+    host = platform.machine()
+    if not os.path.exists(stamp) or open(stamp).read().strip() != host:
+        force = True
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)
+        with open(stamp, "w") as f:
+            f.write(host + "\n")
     return _LIB
 
 

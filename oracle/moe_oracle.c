@@ -167,7 +167,7 @@ void oracle_dequant(const uint32_t *q, const uint16_t *scale, const uint16_t *bi
 
 /*
  * l[t][e] = sum_h x[t][h] * Wr[e][h] (+ bias[e]), accumulated in fp32 in
- * increasing h ([MoE]: "a router scores 256 expert subnetworks").  x is bf16
+ * increasing h ([MoE]: the router gives every expert a score).  x is bf16
  * (widened exactly), Wr and bias are fp32.
  */
 void oracle_router_logits(const uint16_t *x, int32_t T, int32_t H, const float *Wr,
@@ -258,6 +258,8 @@ int32_t oracle_route(const int32_t *idx, int32_t T, int32_t k, int32_t E, int32_
                      int32_t *tile_rows, int32_t max_tiles)
 {
     const int32_t ngroups = E + (has_shared ? 1 : 0);
+    if (E < 1 || k < 1 || T < 0 || BN < 1)
+        return -1;
     for (int32_t g = 0; g < ngroups; ++g)
         counts[g] = 0;
     for (int64_t i = 0; i < (int64_t)T * k; ++i)

@@ -1,0 +1,95 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function declared in include/moe.h, and rejects bad arguments on the
+host before anything touches a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from int4_grouped_gemm_gb300 import _lib, build
+    build.build()
+    return _lib.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "sizeof")))
+
+
+def test_header_declares_the_boundary():
+    names = header_functions()
+    for required in ("moe_prefill", "moe_decode", "pack_int4", "moe_workspace_bytes",
+                     "moe_route_logits", "moe_read_device_status", "moe_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from int4_grouped_gemm_gb300 import _lib
+    names = header_functions()
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/moe.h but not exported"
+    # the binding marshals every declared call, under the same name
+    assert sorted(_lib.SIGNATURES) == names
+
+
+def test_status_strings(lib):
+    from int4_grouped_gemm_gb300 import _lib
+    assert _lib.status_string(0) == "ok"
+    assert "NULL" in _lib.status_string(_lib.MOE_ERR_NULL)
+    assert "bounded wait" in _lib.status_string(_lib.MOE_ERR_TIMEOUT - 3)
+
+
+def _desc(E=256, k=8, H=2048, I=512, G=64, shared=1):
+    from int4_grouped_gemm_gb300._lib import moe_layer_desc
+    return moe_layer_desc(E, k, H, I, G, shared, None, None)
+
+
+def test_workspace_sizes_and_shape_checks(lib):
+    from int4_grouped_gemm_gb300 import _lib
+    d = _desc()
+    n512 = _lib.moe_workspace_bytes(d, 512)
+    n4096 = _lib.moe_workspace_bytes(d, 4096)
+    assert 0 < n512 < n4096
+    # h [T*(k+1)][I] bf16 and the fp32 combine accumulator dominate
+    assert n4096 >= 4096 * 9 * 512 * 2 + 4096 * 2048 * 4
+    for bad in (_desc(E=0), _desc(E=257), _desc(k=9), _desc(k=0), _desc(E=4, k=5), _desc(H=200),
+                _desc(I=100), _desc(G=16), _desc(H=4096, G=64), _desc(shared=2)):
+        assert _lib.moe_workspace_bytes(bad, 16) == 0
+    assert _lib.moe_workspace_bytes(d, 0) == 0
+
+
+def test_argument_errors_are_caught_on_the_host(lib):
+    from int4_grouped_gemm_gb300 import _lib
+    d = _desc()
+    rc = lib.moe_prefill(None, None, 16, None, None, 0, None)
+    assert rc == _lib.MOE_ERR_NULL
+    rc = lib.moe_prefill(ctypes.byref(d), None, 16, None, None, 0, None)   # weights NULL
+    assert rc == _lib.MOE_ERR_NULL
+    bad = _desc(k=9)
+    assert lib.moe_decode(ctypes.byref(bad), None, None, None, 0, None) == _lib.MOE_ERR_SHAPE
+    # misaligned pointer
+    assert lib.pack_int4(ctypes.c_void_p(8), 4, 64, 32, ctypes.c_void_p(16), ctypes.c_void_p(32),
+                         ctypes.c_void_p(48), None) == _lib.MOE_ERR_ALIGN
+    # group must divide K and be a multiple of 8
+    assert lib.pack_int4(ctypes.c_void_p(16), 4, 64, 24, ctypes.c_void_p(16), ctypes.c_void_p(32),
+                         ctypes.c_void_p(48), None) == _lib.MOE_ERR_SHAPE
+    assert lib.moe_read_device_status(None, None) == _lib.MOE_ERR_NULL
+
+
+def test_routing_views_layout(lib):
+    from int4_grouped_gemm_gb300 import _lib
+    d = _desc()
+    v = _lib.moe_routing_views_for(d, 4096)
+    offs = [v.logits, v.topk_idx, v.topk_w, v.counts, v.offsets, v.perm, v.inv_perm, v.tile_group,
+            v.tile_row, v.tile_rows, v.tile_sched, v.num_tiles]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert v.tile_size == 256
+    assert v.max_tiles >= (4096 * 9) // 256 + 257

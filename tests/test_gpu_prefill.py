@@ -1,0 +1,108 @@
+"""Prefill parity: the whole MoE layer on the GPU (router, routing tables,
+grouped int4 GEMMs with SwiGLU, weighted combine) against the CPU oracle."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from int4_grouped_gemm_gb300 import _lib, synthetic
+from int4_grouped_gemm_gb300.moe import PackedLayer
+
+from moe_helpers import ambiguous, assert_close, oracle_layer, oracle_stacks, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(L, x):
+    cfg = L.cfg
+    layer = PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down)
+    ws = layer.workspace(x.shape[0])
+    y = layer.prefill(x.cuda(), ws)
+    torch.cuda.synchronize()
+    assert _lib.moe_read_device_status(ws.buf) == 0
+    return layer, ws, y.float().cpu().numpy()
+
+
+def check_layer(L, x, tokens=None):
+    cfg = L.cfg
+    T = x.shape[0]
+    layer, ws, y = run_gpu(L, x)
+    ref = oracle_layer(L, x, tokens=tokens)
+    toks = ref["tokens"]
+    ok = ~ambiguous(ref["logits"], cfg.k, cfg.E)
+    assert ok.mean() > 0.95
+    rt = ws.routing(layer.desc, T)
+    g_logits = rt["logits"].cpu().numpy()[toks]
+    # logits agree with the oracle's fp32 router up to summation order
+    assert np.abs(g_logits - ref["logits"]).max() <= 1e-5 * np.abs(ref["logits"]).max()
+    # the GPU picked the same experts for every unambiguous token
+    g_idx = rt["topk_idx"].cpu().numpy()[toks]
+    assert np.array_equal(np.sort(g_idx[ok], axis=1), np.sort(ref["idx"][ok], axis=1))
+    return assert_close(y[toks][ok], ref["y"][ok], cfg.name)
+
+
+def test_tiny_all_tokens():
+    cfg = synthetic.CONFIGS["tiny"]
+    L = synthetic.make_layer(cfg)
+    check_layer(L, L.x)
+
+
+@pytest.mark.parametrize("T", [1, 3, 17, 100, 300])
+def test_tiny_shapes_ragged_T(T):
+    cfg = dataclasses.replace(synthetic.CONFIGS["tiny"], T=T, seed=100 + T)
+    L = synthetic.make_layer(cfg)
+    check_layer(L, L.x)
+
+
+def test_mid_shapes_multi_tile_groups():
+    """E=8 experts with ~300 rows each and a 600-row shared group: several
+    token tiles per group with ragged tails."""
+    cfg = synthetic.MoEConfig("mid", T=600, H=512, E=8, k=4, I=128, group=64, seed=7)
+    L = synthetic.make_layer(cfg)
+    check_layer(L, L.x)
+
+
+def test_no_shared_expert():
+    cfg = synthetic.MoEConfig("noshared", T=70, H=256, E=16, k=2, I=64, group=32, seed=8, has_shared=False)
+    L = synthetic.make_layer(cfg)
+    check_layer(L, L.x)
+
+
+def test_one_expert_takes_all_tokens_and_empty_experts():
+    cfg = synthetic.MoEConfig("skewtiny", T=300, H=256, E=16, k=2, I=128, group=32, seed=9)
+    L = synthetic.make_layer(cfg)
+    bias = torch.full((cfg.E,), -30.0)
+    bias[3] = 30.0          # every token picks expert 3
+    bias[5] = 0.0
+    bias[11] = 0.0          # the second slot goes to 5 or 11; the rest stay empty
+    L.router_bias = bias
+    check_layer(L, L.x)
+
+
+@pytest.mark.parametrize("name,n", [("prefill512", 40), ("prefill4096", 40)])
+def test_full_size_sampled(name, n):
+    cfg = synthetic.CONFIGS[name]
+    L = synthetic.make_layer(cfg, device="cuda")
+    toks = sample_tokens(cfg.T, n, seed=cfg.seed)
+    check_layer(L, L.x, tokens=toks)
+
+
+@pytest.mark.slow
+def test_full_size_skew16384_sampled():
+    cfg = synthetic.CONFIGS["skew16384"]
+    L = synthetic.make_layer(cfg, device="cuda")
+    toks = sample_tokens(cfg.T, 32, seed=cfg.seed)
+    check_layer(L, L.x, tokens=toks)
+
+
+def test_host_buffers_end_to_end_equals_device_path():
+    cfg = synthetic.CONFIGS["tiny"]
+    L = synthetic.make_layer(cfg)
+    layer, ws, y_dev = run_gpu(L, L.x)
+    x_host = L.x.clone().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    xd = torch.empty_like(L.x, device="cuda")
+    yd = torch.empty_like(xd)
+    _lib.moe_forward_host(layer.desc, x_host, cfg.T, y_host, xd, yd, ws.buf)
+    np.testing.assert_array_equal(y_host.float().numpy(), y_dev)
