@@ -130,6 +130,17 @@ int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, v
                 cudaStream_t stream);
 
 /*
+ * moe_prefill that also records CUDA events on `stream` at the stage
+ * boundaries, for timing the kernels one by one: events[0] before the router
+ * GEMM, [1] after it, [2] after the routing tables (top-k, scan,
+ * permutation), [3] after the gate/up grouped GEMM, [4] after the down
+ * grouped GEMM with the combine, [5] after the bf16 conversion of y.
+ * events must hold 6 entries (created by the caller); NULL entries are skipped.
+ */
+int moe_prefill_profiled(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws,
+                         size_t ws_bytes, cudaEvent_t *events, cudaStream_t stream);
+
+/*
  * Batch-1 decode: y[1][H] (bf16) = MoE layer of x[1][H] (bf16) as
  * bandwidth-bound dequant-GEMVs that read only the router and the k+1
  * touched experts; the weighted combine is fused into the down GEMV.

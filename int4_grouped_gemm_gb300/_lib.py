@@ -56,6 +56,7 @@ SIGNATURES = {
     "moe_workspace_init": (ctypes.c_int, [c_p, c_sz, c_p]),
     "moe_routing_views_for": (ctypes.c_int, [c_p, c_i32, c_p]),
     "moe_prefill": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_sz, c_p]),
+    "moe_prefill_profiled": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_sz, c_p, c_p]),
     "moe_decode": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_sz, c_p]),
     "moe_route_logits": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_sz, c_p]),
     "pack_int4": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_p]),
@@ -125,6 +126,14 @@ def moe_routing_views_for(desc: moe_layer_desc, T: int) -> moe_routing_views:
 def moe_prefill(desc: moe_layer_desc, x, T: int, y, ws, stream=None):
     _check(load().moe_prefill(ctypes.byref(desc), _ptr(x), T, _ptr(y), _ptr(ws), ws.numel() * ws.element_size(),
                               _stream(stream)), "moe_prefill")
+
+
+def moe_prefill_profiled(desc: moe_layer_desc, x, T: int, y, ws, events, stream=None):
+    """events: 6 torch.cuda.Event(enable_timing=True) recorded at the stage boundaries."""
+    arr = (c_p * 6)(*[int(e.cuda_event) if e is not None else None for e in events])
+    _check(load().moe_prefill_profiled(ctypes.byref(desc), _ptr(x), T, _ptr(y), _ptr(ws),
+                                       ws.numel() * ws.element_size(), arr, _stream(stream)),
+           "moe_prefill_profiled")
 
 
 def moe_decode(desc: moe_layer_desc, x, y, ws, stream=None):

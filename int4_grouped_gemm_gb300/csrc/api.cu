@@ -99,6 +99,11 @@ static int check_tokens(const moe_layer_desc *d, int32_t T) {
 
 static int cuda_rc(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+static cudaError_t mark(cudaEvent_t *events, int i, cudaStream_t s) {
+    if (!events || !events[i]) return cudaSuccess;
+    return cudaEventRecord(events[i], s);
+}
+
 // One thread waits, with the library's bounded wait, on an mbarrier that no
 // thread ever arrives at; the wait must run out and record the status.
 __global__ void selftest_wait_kernel(Ctrl *ctrl, long long limit) {
@@ -172,8 +177,8 @@ int moe_route_logits(const moe_layer_desc *desc, const float *logits, int32_t T,
     return cuda_rc(launch_routing_tables(logits, T, desc->E, desc->k, desc->has_shared, rb, stream));
 }
 
-int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
-                cudaStream_t stream) {
+static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
+                        cudaEvent_t *events, cudaStream_t stream) {
     int rc = check_shape(desc);
     if (rc) return rc;
     if ((rc = check_weights(desc))) return rc;
@@ -207,11 +212,14 @@ int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, v
     if ((rc = encode_2d(&tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, I, L.R, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B)))
         return rc;
 
-    cudaError_t e = launch_router(static_cast<const __nv_bfloat16 *>(x), desc->router_w, desc->router_bias, T, H, E,
-                                  rb.logits, y_acc, static_cast<int64_t>(T) * H, stream);
+    cudaError_t e = mark(events, 0, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = launch_router(static_cast<const __nv_bfloat16 *>(x), desc->router_w, desc->router_bias, T, H, E, rb.logits,
+                      y_acc, static_cast<int64_t>(T) * H, stream);
+    if (e != cudaSuccess || mark(events, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
     if ((e = launch_routing_tables(rb.logits, T, E, k, desc->has_shared, rb, stream)) != cudaSuccess)
         return MOE_ERR_CUDA;
+    if (mark(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
     GemmArgs ga{};
     ga.G = G;
@@ -234,6 +242,7 @@ int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, v
     const int max_units1 = L.max_tiles * ga.n_mtiles;
     int grid = dev->num_sms < max_units1 ? dev->num_sms : max_units1;
     if ((e = launch_gemm(0, tm_qg, tm_qu, tm_x, ga, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(events, 3, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
     // down + weighted combine
     ga.K = I;
@@ -246,11 +255,23 @@ int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, v
     const int max_units2 = L.max_tiles * ga.n_mtiles;
     grid = dev->num_sms < max_units2 ? dev->num_sms : max_units2;
     if ((e = launch_gemm(1, tm_qd, tm_qd, tm_h, ga, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(events, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
 
     if ((e = launch_convert(y_acc, static_cast<__nv_bfloat16 *>(y), static_cast<int64_t>(T) * H, dev->num_sms,
                             stream)) != cudaSuccess)
         return MOE_ERR_CUDA;
+    if (mark(events, 5, stream) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
+}
+
+int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
+                cudaStream_t stream) {
+    return prefill_impl(desc, x, T, y, ws, ws_bytes, nullptr, stream);
+}
+
+int moe_prefill_profiled(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
+                         cudaEvent_t *events, cudaStream_t stream) {
+    return prefill_impl(desc, x, T, y, ws, ws_bytes, events, stream);
 }
 
 int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, size_t ws_bytes, cudaStream_t stream) {
