@@ -30,7 +30,9 @@
  *   value = scale * q + bias, q unsigned in 0..15, scale and bias bf16.
  *   q:      uint32 [rows][K/8]; element k of a row is in word k/8 at bits
  *           4*(k%8) .. 4*(k%8)+3 (low nibble first).
- *   scale, bias: bf16 bit patterns, uint16 [rows][K/group].
+ *   scale, bias: bf16 bit patterns, uint16 [rows][ldg] with the row pitch
+ *           ldg = K/group rounded up to a multiple of 8 (16 bytes, so that
+ *           8-group blocks can be moved by TMA); entries past K/group are 0.
  * Matrices are stacked over experts, expert index E being the shared expert:
  *   gate, up: [E+1][I][H] (K = H);  down: [E+1][H][I] (K = I).
  *
@@ -80,8 +82,8 @@ typedef struct {
 
 /*
  * One MoE layer.  Supported: 1 <= E <= 256, 1 <= k <= min(8, E),
- * H % 256 == 0, I % 64 == 0, group in {32, 64}, H/group and I/group even,
- * H/group <= 32 and I/group <= 32.  has_shared is 0 or 1.
+ * 256 <= H <= 16384 with H % 256 == 0, 128 <= I <= 4096 with I % 128 == 0,
+ * group in {32, 64}.  has_shared is 0 or 1.
  */
 typedef struct {
     int32_t E, k, H, I, group, has_shared;
@@ -132,7 +134,8 @@ int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, v
 /*
  * moe_prefill that also records CUDA events on `stream` at the stage
  * boundaries, for timing the kernels one by one: events[0] before the router
- * GEMM, [1] after it, [2] after the routing tables (top-k, scan,
+ * (bf16 split of the router weights, then the router GEMM on the tensor
+ * cores), [1] after it, [2] after the routing tables (top-k, scan,
  * permutation), [3] after the gate/up grouped GEMM, [4] after the down
  * grouped GEMM with the combine, [5] after the bf16 conversion of y.
  * events must hold 6 entries (created by the caller); NULL entries are skipped.
@@ -158,7 +161,8 @@ int moe_route_logits(const moe_layer_desc *desc, const float *logits, int32_t T,
                      cudaStream_t stream);
 
 /*
- * Quantise w[rows][K] (fp32, device) to the int4 format above: per group,
+ * Quantise w[rows][K] (fp32, device) to the int4 format above (scale and
+ * bias rows with the padded pitch ldg): per group,
  * scale = bf16((max - min) / 15), bias = bf16(min), q = clamp(rint((w - bias)
  * / scale), 0, 15) in fp32 with the bf16-rounded scale and bias (q = 0 when
  * scale == 0).  Requires K % 8 == 0, K % group == 0, group % 8 == 0.

@@ -72,9 +72,7 @@ static int check_shape(const moe_layer_desc *d) {
     if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_SHAPE;
     if (d->group != 32 && d->group != 64) return MOE_ERR_SHAPE;
     if (d->H < 256 || d->H % 256 != 0 || d->H > 16384) return MOE_ERR_SHAPE;
-    if (d->I < 64 || d->I % 64 != 0 || d->I > 4096) return MOE_ERR_SHAPE;
-    const int gh = d->H / d->group, gi = d->I / d->group;
-    if (gh % 2 || gi % 2 || gh > 32 || gi > 32) return MOE_ERR_SHAPE;
+    if (d->I < 128 || d->I % 128 != 0 || d->I > 4096) return MOE_ERR_SHAPE;
     return MOE_OK;
 }
 
@@ -174,7 +172,8 @@ int moe_route_logits(const moe_layer_desc *desc, const float *logits, int32_t T,
     DeviceInfo *dev = nullptr;
     if ((rc = current_device(dev))) return rc;
     const RoutingBufs rb = routing_bufs(static_cast<char *>(ws), L);
-    return cuda_rc(launch_routing_tables(logits, T, desc->E, desc->k, desc->has_shared, rb, stream));
+    return cuda_rc(
+        launch_routing_tables(nullptr, 0, logits, nullptr, T, desc->E, desc->k, desc->has_shared, rb, stream));
 }
 
 static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
@@ -197,68 +196,92 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     float *y_acc = reinterpret_cast<float *>(w + L.y_acc);
     const int nexp = E + 1;
 
-    CUtensorMap tm_qg, tm_qu, tm_qd, tm_x, tm_h;
-    if ((rc = encode_2d(&tm_qg, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, desc->gate.q, H / 8,
-                        static_cast<uint64_t>(nexp) * I, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE)))
-        return rc;
-    if ((rc = encode_2d(&tm_qu, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, desc->up.q, H / 8,
-                        static_cast<uint64_t>(nexp) * I, 8, 64, CU_TENSOR_MAP_SWIZZLE_NONE)))
-        return rc;
-    if ((rc = encode_2d(&tm_qd, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, desc->down.q, I / 8,
-                        static_cast<uint64_t>(nexp) * H, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE)))
-        return rc;
-    if ((rc = encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, H, T, 64, 1, CU_TENSOR_MAP_SWIZZLE_128B)))
-        return rc;
-    if ((rc = encode_2d(&tm_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, h, I, L.R, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B)))
-        return rc;
+    __nv_bfloat16 *wr3 = reinterpret_cast<__nv_bfloat16 *>(w + L.wr3);
+    __nv_bfloat16 *xperm = reinterpret_cast<__nv_bfloat16 *>(w + L.xperm);
+    float *logits_part = reinterpret_cast<float *>(w + L.logits_part);
+    const int routed = T * k;
+    const int ldg_h = ld_groups(H, G), ldg_i = ld_groups(I, G);
+    const auto U16 = CU_TENSOR_MAP_DATA_TYPE_UINT16, U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32,
+               BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const auto SW0 = CU_TENSOR_MAP_SWIZZLE_NONE, SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
+    const uint64_t gu_rows = static_cast<uint64_t>(nexp) * I, dn_rows = static_cast<uint64_t>(nexp) * H;
 
-    cudaError_t e = mark(events, 0, stream);
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    e = launch_router(static_cast<const __nv_bfloat16 *>(x), desc->router_w, desc->router_bias, T, H, E, rb.logits,
-                      y_acc, static_cast<int64_t>(T) * H, stream);
-    if (e != cudaSuccess || mark(events, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    if ((e = launch_routing_tables(rb.logits, T, E, k, desc->has_shared, rb, stream)) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    if (mark(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    // router: A = x tiles, B = bf16 parts of the router weights
+    GemmMaps mr{}, m1{}, m2{};
+    if ((rc = encode_2d(&mr.a0, BF16, 2, x, H, T, 64, 128, SW128)) ||
+        (rc = encode_2d(&mr.w0, BF16, 2, wr3, H, 3 * static_cast<uint64_t>(L.E_pad16), 64, L.E_pad16, SW128)))
+        return rc;
+    mr.a1 = mr.a0;
+    mr.w1 = mr.s0 = mr.b0 = mr.s1 = mr.b1 = mr.w0;
+    // gate/up: A = permuted x (routed rows) or x (shared rows); B = gate rows
+    // f0..f0+127 and up rows f0..f0+127 of one expert
+    if ((rc = encode_2d(&m1.a0, BF16, 2, routed > 0 ? static_cast<const void *>(xperm) : x, H,
+                        routed > 0 ? routed : T, 64, 128, SW128)) ||
+        (rc = encode_2d(&m1.a1, BF16, 2, x, H, T, 64, 128, SW128)) ||
+        (rc = encode_2d(&m1.w0, U32, 4, desc->gate.q, H / 8, gu_rows, 8, 128, SW0)) ||
+        (rc = encode_2d(&m1.w1, U32, 4, desc->up.q, H / 8, gu_rows, 8, 128, SW0)) ||
+        (rc = encode_2d(&m1.s0, U16, 2, desc->gate.scale, ldg_h, gu_rows, 8, 128, SW0)) ||
+        (rc = encode_2d(&m1.b0, U16, 2, desc->gate.bias, ldg_h, gu_rows, 8, 128, SW0)) ||
+        (rc = encode_2d(&m1.s1, U16, 2, desc->up.scale, ldg_h, gu_rows, 8, 128, SW0)) ||
+        (rc = encode_2d(&m1.b1, U16, 2, desc->up.bias, ldg_h, gu_rows, 8, 128, SW0)))
+        return rc;
+    // down: A = h rows, B = 256 down rows of one expert
+    if ((rc = encode_2d(&m2.a0, BF16, 2, h, I, L.R, 64, 128, SW128)) ||
+        (rc = encode_2d(&m2.w0, U32, 4, desc->down.q, I / 8, dn_rows, 8, 256, SW0)) ||
+        (rc = encode_2d(&m2.s0, U16, 2, desc->down.scale, ldg_i, dn_rows, 8, 256, SW0)) ||
+        (rc = encode_2d(&m2.b0, U16, 2, desc->down.bias, ldg_i, dn_rows, 8, 256, SW0)))
+        return rc;
+    m2.a1 = m2.a0;
+    m2.w1 = m2.w0;
+    m2.s1 = m2.s0;
+    m2.b1 = m2.b0;
 
     GemmArgs ga{};
     ga.G = G;
     ga.H = H;
     ga.I = I;
+    ga.T = T;
+    ga.E = E;
+    ga.routed_rows = routed;
+    ga.E_pad16 = L.E_pad16;
     ga.rb = rb;
     ga.h = h;
     ga.y_acc = y_acc;
+    ga.logits_part = logits_part;
     ga.status = &ctrl->status;
     ga.wait_limit = g_wait_limit;
+    auto grid_for = [&](int units) { return dev->num_sms < units ? dev->num_sms : (units > 0 ? units : 1); };
 
+    cudaError_t e = mark(events, 0, stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    // router: bf16 split of the weights (and clearing of the combine
+    // accumulator), then the six partial router GEMMs on the tensor cores
+    if (launch_prep(desc->router_w, E, L.E_pad16, H, wr3, y_acc, static_cast<int64_t>(T) * H, dev->num_sms,
+                    stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    ga.K = H;
+    if (launch_gemm(2, mr, ga, grid_for(router_units(T)), stream) != cudaSuccess) return MOE_ERR_CUDA;
+    if (mark(events, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    // routing tables and the permuted copy of x
+    if (launch_routing_tables(logits_part, L.E_pad16, nullptr, desc->router_bias, T, E, k, desc->has_shared, rb,
+                              stream) !=
+            cudaSuccess ||
+        launch_xperm(static_cast<const __nv_bfloat16 *>(x), xperm, rb.row_token, routed, H, dev->num_sms, stream) !=
+            cudaSuccess)
+        return MOE_ERR_CUDA;
+    if (mark(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
     // gate/up + SwiGLU
     ga.K = H;
-    ga.ngroups = H / G;
-    ga.n_mtiles = 2 * I / 128;
-    ga.s0 = desc->gate.scale;
-    ga.b0 = desc->gate.bias;
-    ga.s1 = desc->up.scale;
-    ga.b1 = desc->up.bias;
-    const int max_units1 = L.max_tiles * ga.n_mtiles;
-    int grid = dev->num_sms < max_units1 ? dev->num_sms : max_units1;
-    if ((e = launch_gemm(0, tm_qg, tm_qu, tm_x, ga, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+    ga.n_ntiles = I / 128;
+    if (launch_gemm(0, m1, ga, grid_for(L.max_tiles * ga.n_ntiles), stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(events, 3, stream) != cudaSuccess) return MOE_ERR_CUDA;
-
     // down + weighted combine
     ga.K = I;
-    ga.ngroups = I / G;
-    ga.n_mtiles = H / 128;
-    ga.s0 = desc->down.scale;
-    ga.b0 = desc->down.bias;
-    ga.s1 = desc->down.scale;
-    ga.b1 = desc->down.bias;
-    const int max_units2 = L.max_tiles * ga.n_mtiles;
-    grid = dev->num_sms < max_units2 ? dev->num_sms : max_units2;
-    if ((e = launch_gemm(1, tm_qd, tm_qd, tm_h, ga, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+    ga.n_ntiles = H / 256;
+    if (launch_gemm(1, m2, ga, grid_for(L.max_tiles * ga.n_ntiles), stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(events, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
-
-    if ((e = launch_convert(y_acc, static_cast<__nv_bfloat16 *>(y), static_cast<int64_t>(T) * H, dev->num_sms,
-                            stream)) != cudaSuccess)
+    if (launch_convert(y_acc, static_cast<__nv_bfloat16 *>(y), static_cast<int64_t>(T) * H, dev->num_sms, stream) !=
+        cudaSuccess)
         return MOE_ERR_CUDA;
     if (mark(events, 5, stream) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
@@ -304,6 +327,8 @@ int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, siz
     a.I = desc->I;
     a.G = desc->group;
     a.has_shared = desc->has_shared;
+    a.ldg_h = ld_groups(desc->H, desc->group);
+    a.ldg_i = ld_groups(desc->I, desc->group);
     a.ctrl = reinterpret_cast<Ctrl *>(w + L.ctrl);
     a.logits = reinterpret_cast<float *>(w + L.logits);
     a.topk_idx = reinterpret_cast<int *>(w + L.topk_idx);

@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(256) decode_gate_up_kernel(DecodeArgs a) {
     const int e = j < a.k ? a.topk_idx[j] : a.E;
     const int64_t row = static_cast<int64_t>(e) * a.I + f;
     const int nwords = a.H / 8;
-    const int ngroups = a.H / a.G;
+    const int ngroups = a.ldg_h;  // scale/bias row pitch
     const uint32_t *qg = a.qg + row * nwords;
     const uint32_t *qu = a.qu + row * nwords;
     const uint16_t *sg = a.sg + row * ngroups, *bg = a.bg + row * ngroups;
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(256) decode_down_kernel(DecodeArgs a) {
     }
     __syncthreads();
     const int f = blockIdx.x * 8 + warp;
-    const int ngroups = a.I / a.G;
+    const int ngroups = a.ldg_i;  // scale/bias row pitch
     float y = 0.f;
     if ((nw & 63) == 0) {
         // 64-bit loads: lane handles 2 consecutive words per step

@@ -1,4 +1,5 @@
-// Grouped int4 expert GEMMs for prefill on the fifth-generation tensor cores.
+// Grouped int4 expert GEMMs (and the router GEMM) for prefill on the
+// fifth-generation tensor cores.
 //
 // "Inside Lily: How Perplexity's Rust and Metal Engine Accelerates Qwen
 // Inference on Apple Silicon" ("Fused Prefill"): the 4-bit weights are rebuilt
@@ -7,21 +8,29 @@
 // measured wins"): unpacking in on-chip memory avoids a full extra
 // read/write pass, and the MoE work is about 90% of prefill.
 //
-// One persistent kernel per projection, one CTA per SM.  A work unit is
-// (token tile of one expert group, 128-row weight tile).  Weights are the MMA
-// "A" operand (M = 128 rows), the group's tokens are "B" (N = tile rows
-// rounded up to 16, at most 256), so small expert groups waste little work.
+// Tile shape.  One tcgen05.mma (kind::f16, K = 16) costs the same time for
+// any M <= 128 and N <= 256, so the kernel keeps every instruction at
+// M = 128 x N = 256: the token rows of one expert group are the "A" operand
+// (M = 128 rows, the last tile of a group padded), and 256 dequantised weight
+// rows are "B" (N = 256, never padded).  A work unit is (128-row token tile
+// of one group, 256-row weight tile); units run on a persistent grid of one
+// CTA per SM in a largest-tile-first order.
 //
-//   warp 4      TMA producer: packed nibbles (tile loads) and the token rows
-//               (gather4 of x rows for gate/up, tile loads of h for down)
-//   warps 6-13  dequantisers: nibbles -> bf16 s*q+b in the 128-byte swizzled
-//               K-major layout the tensor core reads; scale/bias strips are
-//               staged per unit with cp.async
-//   warp 5      one thread issues tcgen05.mma (bf16 x bf16 -> fp32 in tensor
-//               memory), double-buffered accumulators (2 x 256 columns)
-//   warps 0-3   epilogue, one warp per 32-lane quarter of tensor memory:
+//   warp 6      A producer: TMA loads of the token tile (16 KB boxes) from the
+//               permuted copy of x (gate/up), from x itself (shared expert,
+//               router) or from h (down)
+//   warp 4      W producer: TMA loads of packed nibbles (8 KB per stage) and
+//               of scale/bias blocks (8 groups x 256 rows); router mode: the
+//               bf16 router weight tile straight into the B ring
+//   warps 8-15  dequantisers, one weight row per thread: nibbles -> bf16
+//               s*q+b in the 128-byte swizzled K-major layout of the B ring
+//   warp 5      one thread issues the MMAs (bf16 x bf16 -> fp32 in tensor
+//               memory), two 256-column accumulators
+//   warps 0-3   epilogue, thread = token row of the tile:
 //               MODE 0 (gate/up): h = silu(gate) * up -> bf16 h rows
-//               MODE 1 (down):    y_acc[token] += w * o  (fp32 reductions)
+//               MODE 1 (down):    y_acc[token] += w * o  (fp32 v4 reductions
+//                                 after a transpose through shared memory)
+//               MODE 2 (router):  partial logits of one bf16 part and K half
 //
 // Every mbarrier wait is bounded; a wait that runs out records a status code,
 // raises a block-wide abort flag and the block unwinds.
@@ -29,23 +38,26 @@
 
 namespace moe {
 
-constexpr int GM = 128;                          // weight rows per tile (MMA M)
+constexpr int BM = 128;                          // token rows per tile (MMA M)
+constexpr int BN = 256;                          // weight rows per tile (MMA N)
 constexpr int GK = 64;                           // K elements per stage
-constexpr int NS_B = 3, NS_A = 3, NS_Q = 6;      // ring depths
-constexpr int kEpiWarp0 = 0, kProdWarp = 4, kMmaWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
-constexpr int kGemmThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 448
-constexpr int kDeqThreads = kDeqWarps * 32;                  // 256
-constexpr int B_STAGE = kTileRows * 128;         // 32 KB: 256 token rows x 64 bf16
-constexpr int A_STAGE = GM * 128;                // 16 KB: 128 weight rows x 64 bf16
-constexpr int Q_STAGE = GM * GK / 2;             // 4 KB: 128 rows x 64 nibbles
+constexpr int SG = 8;                            // quantisation groups per scale block
+constexpr int NS_A = 4, NS_B = 3, NS_Q = 4, NS_S = 2;  // ring depths
+constexpr int kEpiWarp0 = 0, kWProdWarp = 4, kMmaWarp = 5, kAProdWarp = 6, kDeqWarp0 = 8, kDeqWarps = 8;
+constexpr int kGemmThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 512
+constexpr int A_STAGE = BM * 128;                // 16 KB: 128 token rows x 64 bf16
+constexpr int B_STAGE = BN * 128;                // 32 KB: 256 weight rows x 64 bf16
+constexpr int Q_STAGE = BN * GK / 2;             // 8 KB: 256 rows x 64 nibbles
+constexpr int S_STAGE = 2 * BN * SG * 2;         // 8 KB: [scale|bias][256 rows][8 groups] bf16
+constexpr int T_PITCH = 20;                      // fp32 pitch of the epilogue transpose rows
 constexpr uint32_t kTmemCols = 512;              // two 256-column fp32 accumulators
 
 struct Smem {
-    uint64_t q_full[NS_Q], q_empty[NS_Q];
     uint64_t a_full[NS_A], a_empty[NS_A];
     uint64_t b_full[NS_B], b_empty[NS_B];
+    uint64_t q_full[NS_Q], q_empty[NS_Q];
+    uint64_t s_full[NS_S], s_empty[NS_S];
     uint64_t acc_full[2], acc_empty[2];
-    uint64_t sb_full[2], sb_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -53,35 +65,54 @@ struct Smem {
 
 // dynamic shared memory map (offsets from a 1024-aligned base)
 struct SmemMap {
-    int b, a, q, sb, tab, ctl, total;
+    int a, b, q, s, t, ctl, total;
 };
 
-__host__ __device__ inline SmemMap smem_map(int ngroups) {
+__host__ __device__ inline SmemMap smem_map(int mode) {
     SmemMap m{};
-    m.b = 0;
-    m.a = m.b + NS_B * B_STAGE;
-    m.q = m.a + NS_A * A_STAGE;
-    m.sb = m.q + NS_Q * Q_STAGE;
-    const int sb_bytes = 2 * 2 * GM * ngroups * 2;  // [buf][scale|bias][row][group] bf16
-    m.tab = m.sb + ((sb_bytes + 127) / 128) * 128;
-    m.ctl = m.tab + 4 * kTileRows * 8;             // per epilogue warp: token + weight per row
+    m.a = 0;
+    m.b = m.a + NS_A * A_STAGE;
+    m.q = m.b + NS_B * B_STAGE;
+    const bool deq = mode != 2;
+    m.s = m.q + (deq ? NS_Q * Q_STAGE : 0);
+    m.t = m.s + (deq ? NS_S * S_STAGE : 0);
+    m.ctl = m.t + (mode == 1 ? 4 * 32 * T_PITCH * 4 : 0);
     m.total = m.ctl + static_cast<int>(sizeof(Smem)) + 1024;  // + alignment slack
     return m;
 }
 
 struct Unit {
-    int m, g, row0, n, n_pad;
+    int nt;      // weight tile (MODE 0/1)
+    int g;       // group (MODE 0/1)
+    int row0;    // first token row: permuted row (MODE 0/1) or token (MODE 2)
+    int n;       // valid rows
+    int part;    // MODE 2: bf16 part (0 hi, 1 mid, 2 lo) and K half
+    int khalf;
 };
 
+template <int MODE>
 __device__ __forceinline__ Unit load_unit(const GemmArgs &a, int u) {
-    Unit t;
-    const int tile = a.rb.tile_sched[u / a.n_mtiles];
-    t.m = u % a.n_mtiles;
-    t.g = a.rb.tile_group[tile];
-    t.row0 = a.rb.tile_row[tile];
-    t.n = a.rb.tile_rows[tile];
-    t.n_pad = (t.n + 15) & ~15;
+    Unit t{};
+    if (MODE == 2) {
+        const int tt = u / 6, rem = u % 6;
+        t.part = rem / 2;
+        t.khalf = rem % 2;
+        t.row0 = tt * BM;
+        t.n = min(BM, a.T - t.row0);
+    } else {
+        const int tile = a.rb.tile_sched[u / a.n_ntiles];
+        t.nt = u % a.n_ntiles;
+        t.g = a.rb.tile_group[tile];
+        t.row0 = a.rb.tile_row[tile];
+        t.n = a.rb.tile_rows[tile];
+    }
     return t;
+}
+
+template <int MODE>
+__device__ __forceinline__ int num_units(const GemmArgs &a) {
+    if (MODE == 2) return 6 * ((a.T + BM - 1) / BM);
+    return a.rb.num_tiles[0] * a.n_ntiles;
 }
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -100,104 +131,75 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, uint32_t parity, co
     return true;
 }
 
-// Global weight row of A-tile row r.  MODE 0: each 32-row quarter holds 16
-// gate rows then the 16 up rows of the same intermediate features, so that
-// one warp of the epilogue sees both halves of SwiGLU.
-template <int MODE>
-__device__ __forceinline__ void a_row_source(const GemmArgs &a, const Unit &u, int r, int &nib_row, int &matrix,
-                                             int64_t &wrow) {
-    if (MODE == 0) {
-        const int q = r >> 5, l = r & 31;
-        const int feat = q * 16 + (l & 15);
-        matrix = l < 16 ? 0 : 1;
-        nib_row = matrix * 64 + feat;
-        wrow = static_cast<int64_t>(u.g) * a.I + u.m * 64 + feat;
-    } else {
-        matrix = 0;
-        nib_row = r;
-        wrow = static_cast<int64_t>(u.g) * a.H + u.m * GM + r;
-    }
+__device__ __forceinline__ void red_add_v4(float *addr, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w)
+                 : "memory");
 }
 
-// Issue the cp.async copies of one unit's scale/bias strip (all 128 rows).
-template <int MODE, int CH>
-__device__ __forceinline__ void issue_strip(const GemmArgs &a, const Unit &u, uint16_t *strip, int dt) {
-    const int row_bytes = a.ngroups * 2;
-    const int cpr = row_bytes / CH;              // chunks per row per array
-    const int total = GM * 2 * cpr;
-    for (int c = dt; c < total; c += kDeqThreads) {
-        const int r = c / (2 * cpr);
-        const int rem = c % (2 * cpr);
-        const int arr = rem / cpr;               // 0 = scale, 1 = bias
-        const int ci = rem % cpr;
-        int nib_row, matrix;
-        int64_t wrow;
-        a_row_source<MODE>(a, u, r, nib_row, matrix, wrow);
-        const uint16_t *src = arr == 0 ? (matrix == 0 ? a.s0 : a.s1) : (matrix == 0 ? a.b0 : a.b1);
-        const char *g = reinterpret_cast<const char *>(src + wrow * a.ngroups) + ci * CH;
-        char *d = reinterpret_cast<char *>(strip + (arr * GM + r) * a.ngroups) + ci * CH;
-        cp_async<CH>(d, g);
-    }
-}
-
-template <int MODE>
-__device__ __forceinline__ void issue_strip_any(const GemmArgs &a, const Unit &u, uint16_t *strip, int dt) {
-    const int row_bytes = a.ngroups * 2;
-    if ((row_bytes & 15) == 0) issue_strip<MODE, 16>(a, u, strip, dt);
-    else if ((row_bytes & 7) == 0) issue_strip<MODE, 8>(a, u, strip, dt);
-    else issue_strip<MODE, 4>(a, u, strip, dt);
-}
-
-__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t *bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void red_add_f32(float *addr, float v) {
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+__device__ __forceinline__ void drain_ring(uint64_t *full, int depth, uint32_t issued, long long limit) {
+    for (uint32_t i = (issued > static_cast<uint32_t>(depth) ? issued - depth : 0); i < issued; ++i)
+        mbar_wait(&full[i % depth], (i / depth) & 1, limit);
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_q0, const __grid_constant__ CUtensorMap tm_q1,
-                        const __grid_constant__ CUtensorMap tm_b, const GemmArgs a) {
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                        const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
+                        const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_b0,
+                        const __grid_constant__ CUtensorMap tm_s1, const __grid_constant__ CUtensorMap tm_b1,
+                        const GemmArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const SmemMap map = smem_map(a.ngroups);
-    uint8_t *sB = base + map.b;
+    const SmemMap map = smem_map(MODE);
     uint8_t *sA = base + map.a;
+    uint8_t *sB = base + map.b;
     uint8_t *sQ = base + map.q;
-    uint16_t *sSB = reinterpret_cast<uint16_t *>(base + map.sb);
+    uint8_t *sS = base + map.s;
     Smem *s = reinterpret_cast<Smem *>(base + map.ctl);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
+        for (int i = 0; i < NS_A; ++i) {
+            mbar_init(&s->a_full[i], 1);
+            mbar_init(&s->a_empty[i], 1);
+        }
+        for (int i = 0; i < NS_B; ++i) {
+            mbar_init(&s->b_full[i], MODE == 2 ? 1 : kDeqWarps);
+            mbar_init(&s->b_empty[i], 1);
+        }
         for (int i = 0; i < NS_Q; ++i) {
             mbar_init(&s->q_full[i], 1);
             mbar_init(&s->q_empty[i], kDeqWarps);
         }
-        for (int i = 0; i < NS_A; ++i) {
-            mbar_init(&s->a_full[i], kDeqWarps);
-            mbar_init(&s->a_empty[i], 1);
-        }
-        for (int i = 0; i < NS_B; ++i) {
-            mbar_init(&s->b_full[i], 1);
-            mbar_init(&s->b_empty[i], 1);
+        for (int i = 0; i < NS_S; ++i) {
+            mbar_init(&s->s_full[i], 1);
+            mbar_init(&s->s_empty[i], kDeqWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s->acc_full[i], 1);
             mbar_init(&s->acc_empty[i], 4);
-            mbar_init(&s->sb_full[i], kDeqThreads);
-            mbar_init(&s->sb_empty[i], kDeqWarps);
         }
         mbar_init(&s->drain, 1);
         s->abort = 0;
         fence_mbar_init();
     }
-    if (warp == kProdWarp && lane == 0) {
-        prefetch_tmap(&tm_q0);
-        if (MODE == 0) prefetch_tmap(&tm_q1);
-        prefetch_tmap(&tm_b);
+    if (warp == kAProdWarp && lane == 0) {
+        prefetch_tmap(&tm_a0);
+        if (MODE == 0) prefetch_tmap(&tm_a1);
+    }
+    if (warp == kWProdWarp && lane == 0) {
+        prefetch_tmap(&tm_w0);
+        if (MODE != 2) {
+            prefetch_tmap(&tm_s0);
+            prefetch_tmap(&tm_b0);
+        }
+        if (MODE == 0) {
+            prefetch_tmap(&tm_w1);
+            prefetch_tmap(&tm_s1);
+            prefetch_tmap(&tm_b1);
+        }
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&s->tmem_base, kTmemCols);
@@ -208,103 +210,113 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = s->tmem_base;
 
-    const int num_units = a.rb.num_tiles[0] * a.n_mtiles;
-    const int ksteps = a.K / GK;
+    const int nunits = num_units<MODE>(a);
+    const int ksteps = MODE == 2 ? (a.K / 2) / GK : a.K / GK;
+    const int ks_per_sblock = SG * a.G / GK;            // stages per scale block
+    const int nb = MODE == 2 ? a.E_pad16 : BN;          // MMA N
 
-    if (warp == kProdWarp) {
-        // ------------------------------------------------------------ producer
-        uint32_t qit = 0, bit = 0;
-        bool ok = true;
-        for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x) {
-            const Unit t = load_unit(a, u);
-            int tok[8];
-            if (MODE == 0) {
-#pragma unroll
-                for (int sgrp = 0; sgrp < 2; ++sgrp) {
-                    const int gi = lane + 32 * sgrp;
-#pragma unroll
-                    for (int r = 0; r < 4; ++r) {
-                        const int row = min(4 * gi + r, t.n - 1);
-                        tok[4 * sgrp + r] = (4 * gi < t.n_pad) ? a.rb.row_token[t.row0 + row] : 0;
-                    }
+    if (warp == kAProdWarp) {
+        // ------------------------------------------------------- token tiles
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+                const Unit t = load_unit<MODE>(a, u);
+                const bool shared = MODE == 0 && t.g == a.E;
+                const CUtensorMap *map_a = shared ? &tm_a1 : &tm_a0;
+                const int arow = shared ? t.row0 - a.routed_rows : t.row0;
+                const int kcol0 = MODE == 2 ? t.khalf * (a.K / 2) : 0;
+                for (int ks = 0; ks < ksteps; ++ks, ++it) {
+                    const int st = it % NS_A;
+                    ok = wait_or_abort(&s->a_empty[st], ((it / NS_A) & 1) ^ 1, a, s, 1);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&s->a_full[st], A_STAGE);
+                    tma_load_2d(sA + st * A_STAGE, map_a, &s->a_full[st], kcol0 + ks * GK, arow);
                 }
             }
-            int wrow0, wrow1;
-            if (MODE == 0) {
-                wrow0 = t.g * a.I + t.m * 64;
-                wrow1 = wrow0;
-            } else {
-                wrow0 = t.g * a.H + t.m * GM;
-                wrow1 = 0;
-            }
-            for (int ks = 0; ks < ksteps; ++ks) {
-                const int qs = qit % NS_Q;
-                const uint32_t qph = (qit / NS_Q) & 1;
-                if (lane == 0) {
-                    ok = wait_or_abort(&s->q_empty[qs], qph ^ 1, a, s, 1);
-                    if (ok) {
-                        mbar_arrive_expect_tx(&s->q_full[qs], Q_STAGE);
-                        uint8_t *dst = sQ + qs * Q_STAGE;
+            if (!ok) drain_ring(s->a_full, NS_A, it, a.wait_limit);
+        }
+        __syncwarp();
+    } else if (warp == kWProdWarp) {
+        // ------------------------------------------------------ weight tiles
+        if (lane == 0) {
+            uint32_t bit = 0, qit = 0, sit = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+                const Unit t = load_unit<MODE>(a, u);
+                if (MODE == 2) {
+                    const int kcol0 = t.khalf * (a.K / 2);
+                    for (int ks = 0; ks < ksteps; ++ks, ++bit) {
+                        const int st = bit % NS_B;
+                        ok = wait_or_abort(&s->b_empty[st], ((bit / NS_B) & 1) ^ 1, a, s, 2);
+                        if (!ok) break;
+                        mbar_arrive_expect_tx(&s->b_full[st], nb * 128);
+                        tma_load_2d(sB + st * B_STAGE, &tm_w0, &s->b_full[st], kcol0 + ks * GK, t.part * a.E_pad16);
+                    }
+                    continue;
+                }
+                // weight rows of this tile: gate rows f0.. and up rows f0.. (MODE 0),
+                // down rows f0.. (MODE 1)
+                const int w_row = MODE == 0 ? t.g * a.I + t.nt * (BN / 2) : t.g * a.H + t.nt * BN;
+                for (int ks = 0; ks < ksteps; ++ks) {
+                    if (ks % ks_per_sblock == 0) {
+                        const int st = sit % NS_S;
+                        ok = wait_or_abort(&s->s_empty[st], ((sit / NS_S) & 1) ^ 1, a, s, 3);
+                        if (!ok) break;
+                        const int g0 = (ks * GK) / a.G;
+                        uint8_t *dst = sS + st * S_STAGE;
+                        mbar_arrive_expect_tx(&s->s_full[st], S_STAGE);
                         if (MODE == 0) {
-                            tma_load_2d(dst, &tm_q0, &s->q_full[qs], ks * (GK / 8), wrow0);
-                            tma_load_2d(dst + Q_STAGE / 2, &tm_q1, &s->q_full[qs], ks * (GK / 8), wrow1);
+                            tma_load_2d(dst, &tm_s0, &s->s_full[st], g0, w_row);
+                            tma_load_2d(dst + BN * SG, &tm_s1, &s->s_full[st], g0, w_row);
+                            tma_load_2d(dst + BN * SG * 2, &tm_b0, &s->s_full[st], g0, w_row);
+                            tma_load_2d(dst + BN * SG * 3, &tm_b1, &s->s_full[st], g0, w_row);
                         } else {
-                            tma_load_2d(dst, &tm_q0, &s->q_full[qs], ks * (GK / 8), wrow0);
+                            tma_load_2d(dst, &tm_s0, &s->s_full[st], g0, w_row);
+                            tma_load_2d(dst + BN * SG * 2, &tm_b0, &s->s_full[st], g0, w_row);
                         }
+                        ++sit;
                     }
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                ++qit;
-
-                const int bs = bit % NS_B;
-                const uint32_t bph = (bit / NS_B) & 1;
-                if (lane == 0) {
-                    ok = wait_or_abort(&s->b_empty[bs], bph ^ 1, a, s, 2);
-                    if (ok) mbar_arrive_expect_tx(&s->b_full[bs], t.n_pad * 128);
-                }
-                ok = __shfl_sync(0xffffffffu, ok, 0);
-                if (!ok) break;
-                uint8_t *bdst = sB + bs * B_STAGE;
-                if (MODE == 0) {
-#pragma unroll
-                    for (int sgrp = 0; sgrp < 2; ++sgrp) {
-                        const int gi = lane + 32 * sgrp;
-                        if (4 * gi < t.n_pad)
-                            tma_gather4(bdst + gi * 512, &tm_b, &s->b_full[bs], ks * GK, tok[4 * sgrp],
-                                        tok[4 * sgrp + 1], tok[4 * sgrp + 2], tok[4 * sgrp + 3]);
+                    const int st = qit % NS_Q;
+                    ok = wait_or_abort(&s->q_empty[st], ((qit / NS_Q) & 1) ^ 1, a, s, 4);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(&s->q_full[st], Q_STAGE);
+                    uint8_t *dst = sQ + st * Q_STAGE;
+                    if (MODE == 0) {
+                        tma_load_2d(dst, &tm_w0, &s->q_full[st], ks * (GK / 8), w_row);
+                        tma_load_2d(dst + Q_STAGE / 2, &tm_w1, &s->q_full[st], ks * (GK / 8), w_row);
+                    } else {
+                        tma_load_2d(dst, &tm_w0, &s->q_full[st], ks * (GK / 8), w_row);
                     }
+                    ++qit;
+                }
+            }
+            if (!ok) {
+                if (MODE == 2) {
+                    drain_ring(s->b_full, NS_B, bit, a.wait_limit);
                 } else {
-                    for (int ci = lane; ci * 16 < t.n_pad; ci += 32)
-                        tma_load_2d(bdst + ci * 2048, &tm_b, &s->b_full[bs], ks * GK, t.row0 + ci * 16);
+                    drain_ring(s->q_full, NS_Q, qit, a.wait_limit);
+                    drain_ring(s->s_full, NS_S, sit, a.wait_limit);
                 }
-                ++bit;
             }
         }
-        // On abort, let copies already in flight land before the block exits.
-        if (!ok && lane == 0) {
-            for (uint32_t i = (qit > NS_Q ? qit - NS_Q : 0); i < qit; ++i)
-                mbar_wait(&s->q_full[i % NS_Q], (i / NS_Q) & 1, a.wait_limit);
-            for (uint32_t i = (bit > NS_B ? bit - NS_B : 0); i < bit; ++i)
-                mbar_wait(&s->b_full[i % NS_B], (i / NS_B) & 1, a.wait_limit);
-        }
+        __syncwarp();
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------------- MMA
         if (lane == 0) {
             uint32_t ait = 0, bit = 0, local = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++local) {
-                const Unit t = load_unit(a, u);
+            const uint32_t idesc = idesc_bf16(BM, nb);
+            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++local) {
                 const uint32_t acc = local & 1;
-                ok = wait_or_abort(&s->acc_empty[acc], ((local >> 1) & 1) ^ 1, a, s, 3);
+                ok = wait_or_abort(&s->acc_empty[acc], ((local >> 1) & 1) ^ 1, a, s, 5);
                 if (!ok) break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * 256;
-                const uint32_t idesc = idesc_bf16(GM, t.n_pad);
                 for (int ks = 0; ks < ksteps; ++ks) {
                     const int as = ait % NS_A, bs = bit % NS_B;
-                    ok = wait_or_abort(&s->a_full[as], (ait / NS_A) & 1, a, s, 4) &&
-                         wait_or_abort(&s->b_full[bs], (bit / NS_B) & 1, a, s, 5);
+                    ok = wait_or_abort(&s->a_full[as], (ait / NS_A) & 1, a, s, 6) &&
+                         wait_or_abort(&s->b_full[bs], (bit / NS_B) & 1, a, s, 7);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sA + as * A_STAGE);
@@ -326,117 +338,126 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_wait(&s->drain, 0, a.wait_limit);
         }
         __syncwarp();
-    } else if (warp >= kDeqWarp0) {
+    } else if (warp >= kDeqWarp0 && MODE != 2) {
         // ---------------------------------------------------------- dequantise
-        const int dt = tid - kDeqWarp0 * 32;
-        const int r = dt >> 1, hh = dt & 1;
-        const int strip_elems = 2 * GM * a.ngroups;
-        uint32_t qit = 0, ait = 0, local = 0;
+        const int r = tid - kDeqWarp0 * 32;  // weight row of the tile, 0..255
+        uint32_t bit = 0, qit = 0, sit = 0;
         bool ok = true;
-        int u = blockIdx.x;
-        if (u < num_units) {
-            issue_strip_any<MODE>(a, load_unit(a, u), sSB, dt);
-            cp_async_arrive_noinc(&s->sb_full[0]);
-        }
-        for (; u < num_units && ok; u += gridDim.x, ++local) {
-            const Unit t = load_unit(a, u);
-            // stage the next unit's strip into the other buffer once it is free
-            const int un = u + gridDim.x;
-            if (un < num_units) {
-                const uint32_t nb = (local + 1) & 1;
-                ok = wait_or_abort(&s->sb_empty[nb], (((local + 1) >> 1) & 1) ^ 1, a, s, 9);
-                if (!ok) break;
-                issue_strip_any<MODE>(a, load_unit(a, un), sSB + nb * strip_elems, dt);
-                cp_async_arrive_noinc(&s->sb_full[nb]);
-            }
-            const uint32_t cb = local & 1;
-            ok = wait_or_abort(&s->sb_full[cb], (local >> 1) & 1, a, s, 10);
-            if (!ok) break;
-            const uint16_t *strip_s = sSB + cb * strip_elems;
-            const uint16_t *strip_b = strip_s + GM * a.ngroups;
-            int nib_row, matrix;
-            int64_t wrow;
-            a_row_source<MODE>(a, t, r, nib_row, matrix, wrow);
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
             for (int ks = 0; ks < ksteps; ++ks) {
-                const int qs = qit % NS_Q, as = ait % NS_A;
-                ok = wait_or_abort(&s->q_full[qs], (qit / NS_Q) & 1, a, s, 6) &&
-                     wait_or_abort(&s->a_empty[as], ((ait / NS_A) & 1) ^ 1, a, s, 7);
+                const int ss = sit % NS_S;
+                if (ks % ks_per_sblock == 0) {
+                    ok = wait_or_abort(&s->s_full[ss], (sit / NS_S) & 1, a, s, 8);
+                    if (!ok) break;
+                }
+                const int qs = qit % NS_Q, bs = bit % NS_B;
+                ok = wait_or_abort(&s->q_full[qs], (qit / NS_Q) & 1, a, s, 9) &&
+                     wait_or_abort(&s->b_empty[bs], ((bit / NS_B) & 1) ^ 1, a, s, 10);
                 if (!ok) break;
-                const uint4 nib = *reinterpret_cast<const uint4 *>(sQ + qs * Q_STAGE + nib_row * 32 + hh * 16);
-                const int grp = (ks * GK + hh * 32) / a.G;
-                const uint16_t sv = strip_s[r * a.ngroups + grp];
-                const uint16_t bv = strip_b[r * a.ngroups + grp];
-                const __nv_bfloat162 s2 = u32_as_bf162(static_cast<uint32_t>(sv) * 0x10001u);
-                const __nv_bfloat162 b2 = u32_as_bf162(static_cast<uint32_t>(bv) * 0x10001u);
-                uint8_t *arow = sA + as * A_STAGE + r * 128;
-                const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
+                const uint4 n0 = *reinterpret_cast<const uint4 *>(sQ + qs * Q_STAGE + r * 32);
+                const uint4 n1 = *reinterpret_cast<const uint4 *>(sQ + qs * Q_STAGE + r * 32 + 16);
+                const uint16_t *sblk = reinterpret_cast<const uint16_t *>(sS + ss * S_STAGE) + r * SG;
+                const uint16_t *bblk = sblk + 2 * BN * SG;
+                // element groups of the two 32-element halves of this stage
+                const int gl0 = ((ks * GK) / a.G) % SG;
+                const int gl1 = ((ks * GK + 32) / a.G) % SG;
+                const __nv_bfloat162 s0 = u32_as_bf162(static_cast<uint32_t>(sblk[gl0]) * 0x10001u);
+                const __nv_bfloat162 b0 = u32_as_bf162(static_cast<uint32_t>(bblk[gl0]) * 0x10001u);
+                const __nv_bfloat162 s1 = u32_as_bf162(static_cast<uint32_t>(sblk[gl1]) * 0x10001u);
+                const __nv_bfloat162 b1 = u32_as_bf162(static_cast<uint32_t>(bblk[gl1]) * 0x10001u);
+                uint8_t *brow = sB + bs * B_STAGE + r * 128;
+                const uint32_t words[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint4 out = dequant8_bf16(words[w], s2, b2);
-                    const int chunk = hh * 4 + w;
-                    *reinterpret_cast<uint4 *>(arow + ((chunk ^ (r & 7)) << 4)) = out;
+                for (int w = 0; w < 8; ++w) {
+                    const uint4 out = dequant8_bf16(words[w], w < 4 ? s0 : s1, w < 4 ? b0 : b1);
+                    *reinterpret_cast<uint4 *>(brow + ((w ^ (r & 7)) << 4)) = out;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&s->a_full[as]);
+                    mbar_arrive(&s->b_full[bs]);
                     mbar_arrive(&s->q_empty[qs]);
                 }
                 ++qit;
-                ++ait;
+                ++bit;
+                if (ks % ks_per_sblock == ks_per_sblock - 1 || ks == ksteps - 1) {
+                    if (lane == 0) mbar_arrive(&s->s_empty[ss]);
+                    ++sit;
+                }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s->sb_empty[cb]);
         }
-        cp_async_wait<0>();
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------------------ epilogue
         const int quarter = warp - kEpiWarp0;
-        int *tab_tok = reinterpret_cast<int *>(base + map.tab) + quarter * 2 * kTileRows;
-        float *tab_w = reinterpret_cast<float *>(tab_tok + kTileRows);
+        const int rr = quarter * 32 + lane;  // token row of the tile
+        float *tbuf = reinterpret_cast<float *>(base + map.t) + quarter * 32 * T_PITCH;
         uint32_t local = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x, ++local) {
-            const Unit t = load_unit(a, u);
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++local) {
+            const Unit t = load_unit<MODE>(a, u);
             const uint32_t acc = local & 1;
-            if (MODE == 1) {
-                for (int c = lane; c < t.n; c += 32) {
-                    tab_tok[c] = a.rb.row_token[t.row0 + c];
-                    tab_w[c] = a.rb.row_weight[t.row0 + c];
-                }
+            const bool valid = rr < t.n;
+            int tok = 0;
+            float wgt = 0.f;
+            if (MODE == 1 && valid) {
+                tok = a.rb.row_token[t.row0 + rr];
+                wgt = a.rb.row_weight[t.row0 + rr];
             }
-            ok = wait_or_abort(&s->acc_full[acc], (local >> 1) & 1, a, s, 8);
-            ok = __shfl_sync(0xffffffffu, ok, 0) && __all_sync(0xffffffffu, ok);
+            ok = wait_or_abort(&s->acc_full[acc], (local >> 1) & 1, a, s, 11);
+            ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            __syncwarp();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * 256;
             if (MODE == 0) {
-                const bool is_gate = lane < 16;
-                const int f = t.m * 64 + quarter * 16 + (lane & 15);
-                for (int c0 = 0; c0 < t.n_pad; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(tbase + c0, v);
+                __nv_bfloat16 *hrow = a.h + static_cast<int64_t>(t.row0 + rr) * a.I + t.nt * (BN / 2);
+                for (int c0 = 0; c0 < BN / 2; c0 += 16) {
+                    float g[16], up[16];
+                    tmem_ld16(tbase + c0, g);
+                    tmem_ld16(tbase + BN / 2 + c0, up);
+                    uint32_t o[8];
 #pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const float send = is_gate ? v[8 + jj] : v[jj];
-                        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-                        const float g = is_gate ? v[jj] : recv;
-                        const float up = is_gate ? recv : v[8 + jj];
-                        const int c = c0 + jj + (is_gate ? 0 : 8);
-                        const float hv = g / (1.0f + __expf(-g)) * up;
-                        if (c < t.n) a.h[static_cast<int64_t>(t.row0 + c) * a.I + f] = __float2bfloat16_rn(hv);
+                    for (int j = 0; j < 8; ++j) {
+                        const float h0 = g[2 * j] / (1.0f + __expf(-g[2 * j])) * up[2 * j];
+                        const float h1 = g[2 * j + 1] / (1.0f + __expf(-g[2 * j + 1])) * up[2 * j + 1];
+                        o[j] = bf162_as_u32(__floats2bfloat162_rn(h0, h1));
+                    }
+                    if (valid) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(hrow + c0);
+                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
                     }
                 }
-            } else {
-                const int f = t.m * GM + quarter * 32 + lane;
-                for (int c0 = 0; c0 < t.n_pad; c0 += 16) {
+            } else if (MODE == 1) {
+                const int f0 = t.nt * BN;
+                for (int c0 = 0; c0 < BN; c0 += 16) {
                     float v[16];
                     tmem_ld16(tbase + c0, v);
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const int c = c0 + j;
-                        if (c < t.n) red_add_f32(a.y_acc + static_cast<int64_t>(tab_tok[c]) * a.H + f, tab_w[c] * v[j]);
+                    for (int j = 0; j < 16; j += 4)
+                        *reinterpret_cast<float4 *>(tbuf + lane * T_PITCH + j) =
+                            make_float4(wgt * v[j], wgt * v[j + 1], wgt * v[j + 2], wgt * v[j + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int src = 8 * i + lane / 4;  // row of the warp whose values this lane adds
+                        const int tk = __shfl_sync(0xffffffffu, tok, src);
+                        const bool vv = __shfl_sync(0xffffffffu, valid, src);
+                        const float4 val = *reinterpret_cast<const float4 *>(tbuf + src * T_PITCH + 4 * (lane % 4));
+                        if (vv) red_add_v4(a.y_acc + static_cast<int64_t>(tk) * a.H + f0 + c0 + 4 * (lane % 4), val);
+                    }
+                    __syncwarp();
+                }
+            } else {
+                float *lrow = a.logits_part + (static_cast<int64_t>(t.part * 2 + t.khalf) * a.T + t.row0 + rr) *
+                                                  a.E_pad16;
+                for (int c0 = 0; c0 < nb; c0 += 16) {
+                    float v[16];
+                    tmem_ld16(tbase + c0, v);
+                    if (valid) {
+                        float4 *dst = reinterpret_cast<float4 *>(lrow + c0);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
                     }
                 }
             }
@@ -454,6 +475,32 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
 }
 
+// ------------------------------------------------------- small kernels
+
+// Router weights fp32 [E][H] -> three bf16 parts [3][E_pad16][H] with
+// w = hi + mid + lo exactly (each part is the bf16 rounding of what the
+// previous parts leave; rows E..E_pad16-1 are zero); also clears the fp32
+// combine accumulator.
+__global__ void __launch_bounds__(256) prep_kernel(const float *__restrict__ Wr, int E, int E_pad, int H,
+                                                   __nv_bfloat16 *__restrict__ wr3, float4 *__restrict__ y_acc,
+                                                   int64_t y_acc_n4) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    const int64_t n = static_cast<int64_t>(E_pad) * H;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const int64_t e = i / H;
+        const float w = e < E ? Wr[i] : 0.0f;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+        const float r1 = __fsub_rn(w, __bfloat162float(hi));
+        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+        const float r2 = __fsub_rn(r1, __bfloat162float(mid));
+        wr3[i] = hi;
+        wr3[n + i] = mid;
+        wr3[2 * n + i] = __float2bfloat16_rn(r2);
+    }
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < y_acc_n4; i += stride)
+        y_acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+}
+
 // y (bf16) = y_acc (fp32), four elements per thread
 __global__ void __launch_bounds__(256) convert_out_kernel(const float4 *__restrict__ y_acc,
                                                           uint2 *__restrict__ y, int64_t n4) {
@@ -469,21 +516,29 @@ __global__ void __launch_bounds__(256) convert_out_kernel(const float4 *__restri
 
 // ------------------------------------------------------------------- host
 
-int gemm_smem_bytes(int ngroups) { return smem_map(ngroups).total; }
+int gemm_smem_bytes(int mode) { return smem_map(mode).total; }
 
 template <int MODE>
-cudaError_t launch_gemm_t(const CUtensorMap &q0, const CUtensorMap &q1, const CUtensorMap &b, const GemmArgs &a,
-                          int grid, cudaStream_t s) {
-    const int smem = gemm_smem_bytes(a.ngroups);
+cudaError_t launch_gemm_t(const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t s) {
+    const int smem = gemm_smem_bytes(MODE);
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<MODE><<<grid, kGemmThreads, smem, s>>>(q0, q1, b, a);
+    grouped_gemm_kernel<MODE><<<grid, kGemmThreads, smem, s>>>(m.a0, m.a1, m.w0, m.w1, m.s0, m.b0, m.s1, m.b1, a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(int mode, const CUtensorMap &q0, const CUtensorMap &q1, const CUtensorMap &b,
-                        const GemmArgs &a, int grid, cudaStream_t s) {
-    return mode == 0 ? launch_gemm_t<0>(q0, q1, b, a, grid, s) : launch_gemm_t<1>(q0, q1, b, a, grid, s);
+cudaError_t launch_gemm(int mode, const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t s) {
+    if (mode == 0) return launch_gemm_t<0>(m, a, grid, s);
+    if (mode == 1) return launch_gemm_t<1>(m, a, grid, s);
+    return launch_gemm_t<2>(m, a, grid, s);
+}
+
+int router_units(int T) { return 6 * ((T + BM - 1) / BM); }
+
+cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 *wr3, float *y_acc, int64_t y_elems,
+                        int num_sms, cudaStream_t s) {
+    prep_kernel<<<4 * num_sms, 256, 0, s>>>(Wr, E, E_pad, H, wr3, reinterpret_cast<float4 *>(y_acc), y_elems / 4);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_convert(const float *y_acc, __nv_bfloat16 *y, int64_t n, int num_sms, cudaStream_t s) {

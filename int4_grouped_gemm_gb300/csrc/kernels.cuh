@@ -8,18 +8,25 @@
 namespace moe {
 
 struct GemmArgs {
-    int K;            // reduction length: H (gate/up) or I (down)
+    int K;            // reduction length: H (gate/up, router) or I (down)
     int G;            // quantisation group
-    int ngroups;      // K / G
-    int n_mtiles;     // 128-row weight tiles per expert
-    int H, I;
-    const uint16_t *s0, *b0;   // gate (gate/up pass) or down (down pass) scale / bias
-    const uint16_t *s1, *b1;   // up (gate/up pass)
+    int n_ntiles;     // 256-row weight tiles per group: I/128 (gate/up) or H/256 (down)
+    int H, I, T, E;
+    int routed_rows;  // T * k: first permuted row of the shared expert
+    int E_pad16;      // router: experts rounded up to 16 (MMA N)
     RoutingBufs rb;
     __nv_bfloat16 *h;          // [R][I]
     float *y_acc;              // [T][H]
+    float *logits_part;        // router: [6][T][E_pad16]
     int *status;
     long long wait_limit;
+};
+
+// TMA descriptors of one grouped GEMM launch (unused ones may be copies)
+struct GemmMaps {
+    CUtensorMap a0, a1;        // token rows
+    CUtensorMap w0, w1;        // packed nibbles (router: bf16 weights)
+    CUtensorMap s0, b0, s1, b1;  // scale / bias blocks
 };
 
 struct DecodeArgs {
@@ -30,6 +37,7 @@ struct DecodeArgs {
     const uint32_t *qg, *qu, *qd;
     const uint16_t *sg, *bg, *su, *bu, *sd, *bd;
     int E, k, H, I, G, has_shared;
+    int ldg_h, ldg_i;  // row pitch (in groups) of the gate/up and down scale arrays
     Ctrl *ctrl;
     float *logits;
     int *topk_idx;
@@ -39,13 +47,15 @@ struct DecodeArgs {
 
 cudaError_t launch_pack_int4(const float *w, int64_t rows, int K, int G, uint32_t *q, uint16_t *scale,
                              uint16_t *bias, cudaStream_t stream);
-cudaError_t launch_router(const __nv_bfloat16 *x, const float *Wr, const float *bias, int T, int H, int E,
-                          float *logits, float *y_acc, int64_t y_acc_elems, cudaStream_t s);
-cudaError_t launch_routing_tables(const float *logits, int T, int E, int k, int has_shared, const RoutingBufs &rb,
-                                  cudaStream_t s);
-int gemm_smem_bytes(int ngroups);
-cudaError_t launch_gemm(int mode, const CUtensorMap &q0, const CUtensorMap &q1, const CUtensorMap &b,
-                        const GemmArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
+                                  int E, int k, int has_shared, const RoutingBufs &rb, cudaStream_t s);
+int gemm_smem_bytes(int mode);
+int router_units(int T);
+cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 *wr3, float *y_acc, int64_t y_elems,
+                        int num_sms, cudaStream_t s);
+cudaError_t launch_gemm(int mode, const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_xperm(const __nv_bfloat16 *x, __nv_bfloat16 *xp, const int *row_token, int rows, int H,
+                         int num_sms, cudaStream_t s);
 cudaError_t launch_convert(const float *y_acc, __nv_bfloat16 *y, int64_t n, int num_sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 

@@ -6,9 +6,12 @@
 
 namespace moe {
 
-constexpr int kTileRows = 256;      // tokens per grouped-GEMM block (MMA N <= 256)
+constexpr int kTileRows = 128;      // token rows per grouped-GEMM tile (MMA M)
 constexpr int kRouteChunk = 64;     // tokens per routing block (histogram granularity)
 constexpr int kCtrlBytes = 256;     // status word, decode ticket, ...
+
+// Scale/bias row pitch in groups: K/G rounded up to a multiple of 8 (16 bytes).
+inline int ld_groups(int K, int G) { return (K / G + 7) / 8 * 8; }
 
 // Control block at the start of every workspace.
 struct Ctrl {
@@ -40,8 +43,9 @@ struct RoutingBufs {
 
 struct PrefillLayout {
     size_t ctrl, logits, topk_idx, topk_w, counts_blk, base_blk, counts, offsets, perm, inv_perm, row_token,
-        row_weight, tile_group, tile_row, tile_rows, tile_sched, num_tiles, h, y_acc, total;
-    int max_tiles, nblk, R;
+        row_weight, tile_group, tile_row, tile_rows, tile_sched, num_tiles, h, y_acc, wr3, logits_part, xperm,
+        total;
+    int max_tiles, nblk, R, E_pad16;
 };
 
 struct DecodeLayout {
@@ -81,6 +85,10 @@ inline PrefillLayout prefill_layout(int T, int E, int k, int H, int I) {
     L.num_tiles = take(sizeof(int));
     L.h = take(sizeof(uint16_t) * (size_t)L.R * I);
     L.y_acc = take(sizeof(float) * (size_t)T * H);
+    L.E_pad16 = (E + 15) / 16 * 16;
+    L.wr3 = take(sizeof(uint16_t) * 3 * (size_t)L.E_pad16 * H);
+    L.logits_part = take(sizeof(float) * 6 * (size_t)T * L.E_pad16);
+    L.xperm = take(sizeof(uint16_t) * (size_t)T * k * H);
     L.total = o;
     return L;
 }

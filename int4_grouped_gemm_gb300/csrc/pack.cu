@@ -6,6 +6,8 @@
 // the group left to right for min and max (strict comparisons, first of equal
 // values wins), rounds scale and bias to bf16 (nearest even) and codes every
 // element in fp32 with IEEE subtraction and division, round half to even.
+// Scale and bias rows have a pitch of K/G rounded up to 8 groups (16 bytes);
+// the padding is written as zero.
 #include "kernels.cuh"
 
 namespace moe {
@@ -14,10 +16,16 @@ __global__ void __launch_bounds__(256) pack_int4_kernel(const float *__restrict_
                                                         uint32_t *__restrict__ q, uint16_t *__restrict__ scale,
                                                         uint16_t *__restrict__ bias) {
     const int ngroups = K / G;
+    const int ldg = (ngroups + 7) / 8 * 8;  // scale/bias row pitch in groups
     const int64_t gid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (gid >= rows * ngroups) return;
-    const int64_t r = gid / ngroups;
-    const int g = static_cast<int>(gid % ngroups);
+    if (gid >= rows * ldg) return;
+    const int64_t r = gid / ldg;
+    const int g = static_cast<int>(gid % ldg);
+    if (g >= ngroups) {  // padding of the row pitch
+        scale[r * ldg + g] = 0;
+        bias[r * ldg + g] = 0;
+        return;
+    }
     const float *v = w + r * K + static_cast<int64_t>(g) * G;
 
     float mn = v[0], mx = v[0];
@@ -31,8 +39,8 @@ __global__ void __launch_bounds__(256) pack_int4_kernel(const float *__restrict_
     const __nv_bfloat16 b_b = __float2bfloat16_rn(mn);
     const float s = __bfloat162float(s_b);
     const float b = __bfloat162float(b_b);
-    scale[r * ngroups + g] = __bfloat16_as_ushort(s_b);
-    bias[r * ngroups + g] = __bfloat16_as_ushort(b_b);
+    scale[r * ldg + g] = __bfloat16_as_ushort(s_b);
+    bias[r * ldg + g] = __bfloat16_as_ushort(b_b);
 
     uint32_t *qrow = q + r * (K / 8) + g * (G / 8);
     for (int w8 = 0; w8 < G / 8; ++w8) {
@@ -53,7 +61,7 @@ __global__ void __launch_bounds__(256) pack_int4_kernel(const float *__restrict_
 
 cudaError_t launch_pack_int4(const float *w, int64_t rows, int K, int G, uint32_t *q, uint16_t *scale,
                              uint16_t *bias, cudaStream_t stream) {
-    const int64_t n = rows * (K / G);
+    const int64_t n = rows * ((K / G + 7) / 8 * 8);
     if (n == 0) return cudaSuccess;
     const int64_t blocks = (n + 255) / 256;
     pack_int4_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(w, rows, K, G, q, scale, bias);

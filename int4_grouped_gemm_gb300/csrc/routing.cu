@@ -3,120 +3,34 @@
 // "Inside Lily: How Perplexity's Rust and Metal Engine Accelerates Qwen
 // Inference on Apple Silicon" (list under "Performance Gains and Workload
 // Patterns", "Unified Command Buffers"): routing histograms and block maps
-// stay on the GPU, so a MoE layer needs no CPU synchronisation.  Here:
-//   router_logits_kernel  fp32 logits = x . Wr^T (+ bias); also clears the
-//                         fp32 combine accumulator
-//   topk_hist_kernel      per token: top-k (ties -> lower expert index),
-//                         softmax weights renormalised over the picked k,
-//                         per-block expert histogram
+// stay on the GPU, so a MoE layer needs no CPU synchronisation.  The router
+// GEMM itself runs on the tensor cores (grouped_gemm.cu, router mode, six
+// partial sums per logit); here, from those partial sums:
+//   topk_hist_kernel      per token: fp32 logits (partials summed in a fixed
+//                         order, + bias), top-k (ties -> lower expert
+//                         index), softmax weights renormalised over the
+//                         picked k, per-block expert histogram
 //   scan_tiles_kernel     per-expert block bases, counts, exclusive scan
 //                         (offsets), canonical tile map, launch schedule
 //   permute_kernel        stable (expert, token) permutation, its inverse and
 //                         the per-row token / combine weight tables
+//   xperm_kernel          the permuted copy of x that the gate/up GEMM reads
+//                         in whole tiles
 // Every table is deterministic: counts and ranks come from per-block counts
 // scanned in token order, never from the order in which atomics land.
 #include "kernels.cuh"
 
 namespace moe {
 
-// ------------------------------------------------------------------ router
-
-constexpr int RT_TOK = 64, RT_EXP = 64, RT_K = 32;
-
-__global__ void __launch_bounds__(256) router_logits_kernel(const __nv_bfloat16 *__restrict__ x,
-                                                            const float *__restrict__ Wr,
-                                                            const float *__restrict__ bias, int T, int H, int E,
-                                                            float *__restrict__ logits, float *__restrict__ y_acc,
-                                                            int64_t y_acc_elems) {
-    __shared__ __align__(16) float xs[RT_K][RT_TOK + 4];
-    __shared__ __align__(16) float wsm[RT_K][RT_EXP + 4];
-    const int tid = threadIdx.x;
-    const int t0 = blockIdx.y * RT_TOK, e0 = blockIdx.x * RT_EXP;
-
-    // Clear this block's share of the fp32 combine accumulator.
-    if (y_acc) {
-        const int64_t nblocks = static_cast<int64_t>(gridDim.x) * gridDim.y;
-        const int64_t b = static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x;
-        const int64_t n4 = y_acc_elems / 4;
-        const int64_t per = (n4 + nblocks - 1) / nblocks;
-        float4 *y4 = reinterpret_cast<float4 *>(y_acc);
-        const int64_t end = min(n4, (b + 1) * per);
-        for (int64_t i = b * per + tid; i < end; i += blockDim.x) y4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-
-    const int tx = tid % 16, ty = tid / 16;
-    float acc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-
-    const int lrow = tid / 4, lk = (tid % 4) * 8;
-    for (int k0 = 0; k0 < H; k0 += RT_K) {
-        {
-            const int t = t0 + lrow;
-            float v[8];
-            if (t < T) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(x + static_cast<int64_t>(t) * H + k0 + lk);
-                const __nv_bfloat16 *p = reinterpret_cast<const __nv_bfloat16 *>(&raw);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = __bfloat162float(p[i]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) xs[lk + i][lrow] = v[i];
-        }
-        {
-            const int e = e0 + lrow;
-            float v[8];
-            if (e < E) {
-                const float4 a = *reinterpret_cast<const float4 *>(Wr + static_cast<int64_t>(e) * H + k0 + lk);
-                const float4 c = *reinterpret_cast<const float4 *>(Wr + static_cast<int64_t>(e) * H + k0 + lk + 4);
-                v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-                v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) wsm[lk + i][lrow] = v[i];
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int kk = 0; kk < RT_K; ++kk) {
-            const float4 a = *reinterpret_cast<const float4 *>(&xs[kk][4 * ty]);
-            const float4 b = *reinterpret_cast<const float4 *>(&wsm[kk][4 * tx]);
-            const float av[4] = {a.x, a.y, a.z, a.w};
-            const float bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int t = t0 + 4 * ty + i;
-        if (t >= T) continue;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int e = e0 + 4 * tx + j;
-            if (e < E) logits[static_cast<int64_t>(t) * E + e] = acc[i][j] + (bias ? bias[e] : 0.f);
-        }
-    }
-}
-
-// ------------------------------------------------------------------- top-k
-
 // Better candidate: larger logit, or equal logit and lower expert index.
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
 }
 
-__global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict__ logits, int T, int E, int k,
+// logits_part == nullptr: the fp32 logits are given in `given` instead.
+__global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict__ logits_part, int ld,
+                                                        const float *__restrict__ given,
+                                                        const float *__restrict__ bias, int T, int E, int k,
                                                         int has_shared, RoutingBufs rb) {
     __shared__ int hist[256];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
@@ -131,7 +45,24 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int e = lane + 32 * i;
-            v[i] = e < E ? logits[static_cast<int64_t>(t) * E + e] : -INFINITY;
+            float l = -INFINITY;
+            if (e < E) {
+                if (logits_part) {
+                    // six partial sums: hi, mid, lo bf16 parts of the router
+                    // weights, two K halves each; small parts first
+                    const int64_t pstride = static_cast<int64_t>(T) * ld;
+                    const float *p = logits_part + static_cast<int64_t>(t) * ld + e;
+                    const float lo = p[4 * pstride] + p[5 * pstride];
+                    const float mid = p[2 * pstride] + p[3 * pstride];
+                    const float hi = p[0] + p[pstride];
+                    l = (lo + mid) + hi;
+                    if (bias) l += bias[e];
+                    rb.logits[static_cast<int64_t>(t) * E + e] = l;
+                } else {
+                    l = given[static_cast<int64_t>(t) * E + e];
+                }
+            }
+            v[i] = l;
         }
         unsigned taken = 0;
         float sel_v[8];
@@ -228,11 +159,20 @@ __global__ void __launch_bounds__(512) scan_tiles_kernel(int T, int E, int k, in
 
     int cnt = 0;
     if (g < E) {
+        // running sum over the token chunks; loads batched so that many are
+        // in flight at once
         int run = 0;
-        for (int b = 0; b < rb.nblk; ++b) {
-            const int64_t at = static_cast<int64_t>(b) * E + g;
-            rb.base_blk[at] = run;
-            run += rb.counts_blk[at];
+        constexpr int BATCH = 16;
+        for (int b0 = 0; b0 < rb.nblk; b0 += BATCH) {
+            int c[BATCH];
+#pragma unroll
+            for (int i = 0; i < BATCH; ++i)
+                c[i] = (b0 + i < rb.nblk) ? rb.counts_blk[static_cast<int64_t>(b0 + i) * E + g] : 0;
+#pragma unroll
+            for (int i = 0; i < BATCH; ++i) {
+                if (b0 + i < rb.nblk) rb.base_blk[static_cast<int64_t>(b0 + i) * E + g] = run;
+                run += c[i];
+            }
         }
         cnt = run;
     } else if (g == E && has_shared) {
@@ -278,28 +218,35 @@ __global__ void __launch_bounds__(512) scan_tiles_kernel(int T, int E, int k, in
 
 // ------------------------------------------------------------- permutation
 
+// One warp per chunk of kRouteChunk tokens: the chunk's expert picks and the
+// experts' first rows are loaded first, then ranks follow token order
+// (match_any within a pass of 32/k tokens, a counter per expert across passes).
 __global__ void __launch_bounds__(32) permute_kernel(int T, int E, int k, RoutingBufs rb) {
-    __shared__ int cnt[256];
+    __shared__ int base[256];
+    __shared__ int pick[kRouteChunk * 8];
     const int lane = threadIdx.x;
-    for (int e = lane; e < E; e += 32) cnt[e] = 0;
-    __syncwarp();
     const int blk = blockIdx.x;
     const int t_begin = blk * kRouteChunk;
     const int t_end = min(T, t_begin + kRouteChunk);
+    const int nslots = (t_end - t_begin) * k;
+    for (int e = lane; e < E; e += 32)
+        base[e] = rb.offsets[e] + rb.base_blk[static_cast<int64_t>(blk) * E + e];
+    for (int i = lane; i < nslots; i += 32) pick[i] = rb.topk_idx[static_cast<int64_t>(t_begin) * k + i];
+    __syncwarp();
     const int per_pass = 32 / k;
     const unsigned lt_mask = (1u << lane) - 1u;
     for (int t0 = t_begin; t0 < t_end; t0 += per_pass) {
         const int tt = lane / k, j = lane % k;
         const int t = t0 + tt;
         const bool active = tt < per_pass && t < t_end;
-        const int e = active ? rb.topk_idx[static_cast<int64_t>(t) * k + j] : -1 - lane;
+        const int e = active ? pick[(t - t_begin) * k + j] : -1 - lane;
         const unsigned same = __match_any_sync(0xffffffffu, e);
         const int rank = __popc(same & lt_mask);
-        const int before = active ? cnt[e] : 0;
+        const int before = active ? base[e] : 0;
         __syncwarp();
         if (active) {
-            if (rank == 0) cnt[e] = before + __popc(same);
-            const int pos = rb.offsets[e] + rb.base_blk[static_cast<int64_t>(blk) * E + e] + before + rank;
+            if (rank == 0) base[e] = before + __popc(same);
+            const int pos = before + rank;
             const int slot = t * k + j;
             rb.perm[pos] = slot;
             rb.inv_perm[slot] = pos;
@@ -310,20 +257,50 @@ __global__ void __launch_bounds__(32) permute_kernel(int T, int E, int k, Routin
     }
 }
 
+// x_perm[r] = x[row_token[r]] for the routed rows: one warp per row, every
+// lane issues all its 16-byte loads before its stores.
+__global__ void __launch_bounds__(256) xperm_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xp,
+                                                    const int *__restrict__ row_token, int rows, int n16) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    const int nwarps = (gridDim.x * blockDim.x) >> 5;
+    for (int r = warp; r < rows; r += nwarps) {
+        const uint4 *src = x + static_cast<int64_t>(row_token[r]) * n16;
+        uint4 *dst = xp + static_cast<int64_t>(r) * n16;
+        constexpr int U = 8;
+        for (int i0 = 0; i0 < n16; i0 += 32 * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = i0 + u * 32 + lane;
+                if (i < n16) v[u] = src[i];
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = i0 + u * 32 + lane;
+                if (i < n16) dst[i] = v[u];
+            }
+        }
+    }
+}
+
 // --------------------------------------------------------------- launches
 
-cudaError_t launch_router(const __nv_bfloat16 *x, const float *Wr, const float *bias, int T, int H, int E,
-                          float *logits, float *y_acc, int64_t y_acc_elems, cudaStream_t s) {
-    dim3 grid((E + RT_EXP - 1) / RT_EXP, (T + RT_TOK - 1) / RT_TOK);
-    router_logits_kernel<<<grid, 256, 0, s>>>(x, Wr, bias, T, H, E, logits, y_acc, y_acc_elems);
+cudaError_t launch_routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
+                                  int E, int k, int has_shared, const RoutingBufs &rb, cudaStream_t s) {
+    topk_hist_kernel<<<rb.nblk, 256, 0, s>>>(logits_part, ld, given, bias, T, E, k, has_shared, rb);
+    scan_tiles_kernel<<<1, 512, 0, s>>>(T, E, k, has_shared, rb);
+    permute_kernel<<<rb.nblk, 32, 0, s>>>(T, E, k, rb);
     return cudaGetLastError();
 }
 
-cudaError_t launch_routing_tables(const float *logits, int T, int E, int k, int has_shared, const RoutingBufs &rb,
-                                  cudaStream_t s) {
-    topk_hist_kernel<<<rb.nblk, 256, 0, s>>>(logits, T, E, k, has_shared, rb);
-    scan_tiles_kernel<<<1, 512, 0, s>>>(T, E, k, has_shared, rb);
-    permute_kernel<<<rb.nblk, 32, 0, s>>>(T, E, k, rb);
+cudaError_t launch_xperm(const __nv_bfloat16 *x, __nv_bfloat16 *xp, const int *row_token, int rows, int H,
+                         int num_sms, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    const int n16 = H * 2 / 16;
+    int blocks = (rows + 7) / 8;
+    if (blocks > 8 * num_sms) blocks = 8 * num_sms;
+    xperm_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(xp), row_token,
+                                        rows, n16);
     return cudaGetLastError();
 }
 

@@ -16,11 +16,16 @@ from . import _lib
 from ._lib import moe_layer_desc, moe_qweight
 
 
+def ld_groups(K: int, group: int) -> int:
+    """Row pitch (in groups) of the scale/bias arrays: K/group rounded up to 8."""
+    return (K // group + 7) // 8 * 8
+
+
 @dataclass
 class QMatrix:
     """One stacked int4 matrix set [n_exp][rows][K] in the library format."""
     q: torch.Tensor      # int32 view of uint32 words [n_exp, rows, K/8]
-    scale: torch.Tensor  # int16 view of bf16 bits [n_exp, rows, K/G]
+    scale: torch.Tensor  # int16 view of bf16 bits [n_exp, rows, ld_groups(K, G)] (zero padded)
     bias: torch.Tensor
     rows: int
     K: int
@@ -37,7 +42,7 @@ def pack_matrix(w: torch.Tensor, group: int, stream=None) -> QMatrix:
     *lead, rows, K = w.shape
     total_rows = w.numel() // K
     q = torch.empty(*lead, rows, K // 8, dtype=torch.int32, device=w.device)
-    s = torch.empty(*lead, rows, K // group, dtype=torch.int16, device=w.device)
+    s = torch.empty(*lead, rows, ld_groups(K, group), dtype=torch.int16, device=w.device)
     b = torch.empty_like(s)
     _lib.pack_int4(w, total_rows, K, group, q, s, b, stream)
     return QMatrix(q, s, b, rows, K, group)

@@ -11,10 +11,16 @@ pytestmark = pytest.mark.gpu
 
 
 def _gpu_pack(w: torch.Tensor, group: int):
+    """GPU pack; returns words and the scale/bias without the row-pitch padding
+    (after checking that the padding is zero)."""
     qm = pack_matrix(w.cuda(), group)
     torch.cuda.synchronize()
-    return (qm.q.cpu().numpy().view(np.uint32), qm.scale.cpu().numpy().view(np.uint16),
-            qm.bias.cpu().numpy().view(np.uint16))
+    ng = w.shape[-1] // group
+    s = qm.scale.cpu().numpy().view(np.uint16)
+    b = qm.bias.cpu().numpy().view(np.uint16)
+    assert s.shape[-1] % 8 == 0 and s.shape[-1] >= ng
+    assert np.all(s[..., ng:] == 0) and np.all(b[..., ng:] == 0)
+    return qm.q.cpu().numpy().view(np.uint32), s[..., :ng], b[..., :ng]
 
 
 def test_hand_packed_fixture(fixture_loader):

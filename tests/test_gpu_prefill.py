@@ -64,7 +64,7 @@ def test_mid_shapes_multi_tile_groups():
 
 
 def test_no_shared_expert():
-    cfg = synthetic.MoEConfig("noshared", T=70, H=256, E=16, k=2, I=64, group=32, seed=8, has_shared=False)
+    cfg = synthetic.MoEConfig("noshared", T=70, H=256, E=16, k=2, I=128, group=32, seed=8, has_shared=False)
     L = synthetic.make_layer(cfg)
     check_layer(L, L.x)
 
@@ -105,4 +105,9 @@ def test_host_buffers_end_to_end_equals_device_path():
     xd = torch.empty_like(L.x, device="cuda")
     yd = torch.empty_like(xd)
     _lib.moe_forward_host(layer.desc, x_host, cfg.T, y_host, xd, yd, ws.buf)
-    np.testing.assert_array_equal(y_host.float().numpy(), y_dev)
+    got = y_host.float().numpy()
+    # the weighted combine adds fp32 partial sums with reductions whose order
+    # is not fixed, so two runs may differ by one bf16 rounding step
+    assert np.all(np.abs(got - y_dev) <= 2.0 ** -8 * np.abs(y_dev) + 1e-30)
+    ref = oracle_layer(L, L.x)
+    assert_close(got, ref["y"], "host buffers")

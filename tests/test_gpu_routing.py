@@ -20,7 +20,7 @@ def expected_schedule(tg, tr, tn, BN):
 
 
 def run_case(T, E, k, shared, kind, seed):
-    desc = moe_layer_desc(E, k, 256, 64, 32, int(shared), None, None)
+    desc = moe_layer_desc(E, k, 256, 128, 32, int(shared), None, None)
     ws = Workspace(desc, T)
     logits = synthetic.make_logits(T, E, seed, kind)
     _lib.moe_route_logits(desc, logits.cuda(), T, ws.buf)
