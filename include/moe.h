@@ -107,6 +107,9 @@ typedef struct {
     int64_t tile_rows;   /* int32 [max_tiles]: rows in the tile (<= tile size) */
     int64_t tile_sched;  /* int32 [max_tiles]: launch order (largest tiles first) */
     int64_t num_tiles;   /* int32 [1] */
+    int64_t xperm;       /* bf16 [T*k][H]: x rows in routed-row order */
+    int64_t h;           /* bf16 [T*k + T][I]: SwiGLU output per routed/shared row */
+    int64_t y_acc;       /* fp32 [T][H]: combine accumulator */
     int32_t max_tiles;
     int32_t tile_size;   /* rows per tile (tokens per grouped-GEMM block) */
 } moe_routing_views;

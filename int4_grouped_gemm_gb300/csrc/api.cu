@@ -156,6 +156,9 @@ int moe_routing_views_for(const moe_layer_desc *desc, int32_t T, moe_routing_vie
     v->tile_rows = L.tile_rows;
     v->tile_sched = L.tile_sched;
     v->num_tiles = L.num_tiles;
+    v->xperm = L.xperm;
+    v->h = L.h;
+    v->y_acc = L.y_acc;
     v->max_tiles = L.max_tiles;
     v->tile_size = kTileRows;
     return MOE_OK;

@@ -357,7 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint4 n0 = *reinterpret_cast<const uint4 *>(sQ + qs * Q_STAGE + r * 32);
                 const uint4 n1 = *reinterpret_cast<const uint4 *>(sQ + qs * Q_STAGE + r * 32 + 16);
                 const uint16_t *sblk = reinterpret_cast<const uint16_t *>(sS + ss * S_STAGE) + r * SG;
-                const uint16_t *bblk = sblk + 2 * BN * SG;
+                const uint16_t *bblk = sblk + BN * SG;  // bias block: 4096 bytes after the scales
                 // element groups of the two 32-element halves of this stage
                 const int gl0 = ((ks * GK) / a.G) % SG;
                 const int gl1 = ((ks * GK + 32) / a.G) % SG;

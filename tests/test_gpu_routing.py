@@ -26,7 +26,11 @@ def run_case(T, E, k, shared, kind, seed):
     _lib.moe_route_logits(desc, logits.cuda(), T, ws.buf)
     torch.cuda.synchronize()
     assert _lib.moe_read_device_status(ws.buf) == 0
-    g = {key: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for key, v in ws.routing(desc, T).items()}
+    keys = ("topk_idx", "topk_w", "counts", "offsets", "perm", "inv_perm", "tile_group", "tile_row", "tile_rows",
+            "tile_sched")
+    views = ws.routing(desc, T)
+    g = {key: views[key].cpu().numpy() for key in keys}
+    g["tile_size"] = views["tile_size"]
     idx, w = oracle.topk(logits.numpy(), k)
     R = oracle.route(idx, E, shared, g["tile_size"])
     np.testing.assert_array_equal(g["topk_idx"], idx)
