@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer prefill tok/s @T=4096; batch-1 decode tok/s; % of roofline"
 PREFILL_CFG = "prefill4096"
 DECODE_CFG = "decode40"
-KERNELS_PER_PREFILL = 7      # router, top-k, scan, permute, gate/up GEMM, down GEMM, convert
+KERNELS_PER_PREFILL = 9      # prep, router GEMM, top-k, scan, permute, x copy, gate/up GEMM, down GEMM, convert
 KERNELS_PER_DECODE_LAYER = 3  # router+top-k, gate/up GEMV, down GEMV + combine
 
 

@@ -175,6 +175,8 @@ int moe_route_logits(const moe_layer_desc *desc, const float *logits, int32_t T,
     DeviceInfo *dev = nullptr;
     if ((rc = current_device(dev))) return rc;
     const RoutingBufs rb = routing_bufs(static_cast<char *>(ws), L);
+    if (launch_zero_i32(rb.counts_blk, static_cast<int64_t>(rb.nblk) * desc->E, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
     return cuda_rc(
         launch_routing_tables(nullptr, 0, logits, nullptr, T, desc->E, desc->k, desc->has_shared, rb, stream));
 }
@@ -212,7 +214,7 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     // router: A = x tiles, B = bf16 parts of the router weights
     GemmMaps mr{}, m1{}, m2{};
     if ((rc = encode_2d(&mr.a0, BF16, 2, x, H, T, 64, 128, SW128)) ||
-        (rc = encode_2d(&mr.w0, BF16, 2, wr3, H, 3 * static_cast<uint64_t>(L.E_pad16), 64, L.E_pad16, SW128)))
+        (rc = encode_2d(&mr.w0, BF16, 2, wr3, H, 2 * static_cast<uint64_t>(L.E_pad16), 64, L.E_pad16, SW128)))
         return rc;
     mr.a1 = mr.a0;
     mr.w1 = mr.s0 = mr.b0 = mr.s1 = mr.b1 = mr.w0;
@@ -258,9 +260,10 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     cudaError_t e = mark(events, 0, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     // router: bf16 split of the weights (and clearing of the combine
-    // accumulator), then the six partial router GEMMs on the tensor cores
-    if (launch_prep(desc->router_w, E, L.E_pad16, H, wr3, y_acc, static_cast<int64_t>(T) * H, dev->num_sms,
-                    stream) != cudaSuccess)
+    // accumulator and histogram), then the four partial router GEMMs on the
+    // tensor cores
+    if (launch_prep(desc->router_w, E, L.E_pad16, H, wr3, y_acc, static_cast<int64_t>(T) * H, rb.counts_blk,
+                    static_cast<int64_t>(rb.nblk) * E, dev->num_sms, stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     ga.K = H;
     if (launch_gemm(2, mr, ga, grid_for(router_units(T)), stream) != cudaSuccess) return MOE_ERR_CUDA;

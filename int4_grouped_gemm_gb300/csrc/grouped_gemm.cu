@@ -51,6 +51,8 @@ constexpr int Q_STAGE = BN * GK / 2;             // 8 KB: 256 rows x 64 nibbles
 constexpr int S_STAGE = 2 * BN * SG * 2;         // 8 KB: [scale|bias][256 rows][8 groups] bf16
 constexpr int T_PITCH = 20;                      // fp32 pitch of the epilogue transpose rows
 constexpr uint32_t kTmemCols = 512;              // two 256-column fp32 accumulators
+constexpr int kRouterParts = 2;                  // bf16 parts of the fp32 router weights
+constexpr int kRouterUnits = 2 * kRouterParts;   // router units per token tile (parts x K halves)
 
 struct Smem {
     uint64_t a_full[NS_A], a_empty[NS_A];
@@ -86,7 +88,7 @@ struct Unit {
     int g;       // group (MODE 0/1)
     int row0;    // first token row: permuted row (MODE 0/1) or token (MODE 2)
     int n;       // valid rows
-    int part;    // MODE 2: bf16 part (0 hi, 1 mid, 2 lo) and K half
+    int part;    // MODE 2: bf16 part (0 hi, 1 lo) and K half
     int khalf;
 };
 
@@ -94,7 +96,7 @@ template <int MODE>
 __device__ __forceinline__ Unit load_unit(const GemmArgs &a, int u) {
     Unit t{};
     if (MODE == 2) {
-        const int tt = u / 6, rem = u % 6;
+        const int tt = u / kRouterUnits, rem = u % kRouterUnits;
         t.part = rem / 2;
         t.khalf = rem % 2;
         t.row0 = tt * BM;
@@ -111,7 +113,7 @@ __device__ __forceinline__ Unit load_unit(const GemmArgs &a, int u) {
 
 template <int MODE>
 __device__ __forceinline__ int num_units(const GemmArgs &a) {
-    if (MODE == 2) return 6 * ((a.T + BM - 1) / BM);
+    if (MODE == 2) return kRouterUnits * ((a.T + BM - 1) / BM);
     return a.rb.num_tiles[0] * a.n_ntiles;
 }
 
@@ -477,28 +479,26 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // ------------------------------------------------------- small kernels
 
-// Router weights fp32 [E][H] -> three bf16 parts [3][E_pad16][H] with
-// w = hi + mid + lo exactly (each part is the bf16 rounding of what the
-// previous parts leave; rows E..E_pad16-1 are zero); also clears the fp32
-// combine accumulator.
+// Router weights fp32 [E][H] -> two bf16 parts [2][E_pad16][H]: hi = bf16(w)
+// and lo = bf16(w - hi), so that |w - hi - lo| <= 2^-17 |w| and every product
+// with a bf16 input is exact; rows E..E_pad16-1 are zero.  Also clears the
+// fp32 combine accumulator and the per-chunk expert histogram.
 __global__ void __launch_bounds__(256) prep_kernel(const float *__restrict__ Wr, int E, int E_pad, int H,
-                                                   __nv_bfloat16 *__restrict__ wr3, float4 *__restrict__ y_acc,
-                                                   int64_t y_acc_n4) {
+                                                   __nv_bfloat16 *__restrict__ wr2, float4 *__restrict__ y_acc,
+                                                   int64_t y_acc_n4, int *__restrict__ counts_blk, int64_t n_counts) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t n = static_cast<int64_t>(E_pad) * H;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
         const int64_t e = i / H;
         const float w = e < E ? Wr[i] : 0.0f;
         const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-        const float r1 = __fsub_rn(w, __bfloat162float(hi));
-        const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-        const float r2 = __fsub_rn(r1, __bfloat162float(mid));
-        wr3[i] = hi;
-        wr3[n + i] = mid;
-        wr3[2 * n + i] = __float2bfloat16_rn(r2);
+        wr2[i] = hi;
+        wr2[n + i] = __float2bfloat16_rn(__fsub_rn(w, __bfloat162float(hi)));
     }
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < y_acc_n4; i += stride)
         y_acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_counts; i += stride)
+        counts_blk[i] = 0;
 }
 
 // y (bf16) = y_acc (fp32), four elements per thread
@@ -533,11 +533,12 @@ cudaError_t launch_gemm(int mode, const GemmMaps &m, const GemmArgs &a, int grid
     return launch_gemm_t<2>(m, a, grid, s);
 }
 
-int router_units(int T) { return 6 * ((T + BM - 1) / BM); }
+int router_units(int T) { return kRouterUnits * ((T + BM - 1) / BM); }
 
-cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 *wr3, float *y_acc, int64_t y_elems,
-                        int num_sms, cudaStream_t s) {
-    prep_kernel<<<4 * num_sms, 256, 0, s>>>(Wr, E, E_pad, H, wr3, reinterpret_cast<float4 *>(y_acc), y_elems / 4);
+cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 *wr2, float *y_acc, int64_t y_elems,
+                        int *counts_blk, int64_t n_counts, int num_sms, cudaStream_t s) {
+    prep_kernel<<<4 * num_sms, 256, 0, s>>>(Wr, E, E_pad, H, wr2, reinterpret_cast<float4 *>(y_acc), y_elems / 4,
+                                            counts_blk, n_counts);
     return cudaGetLastError();
 }
 

@@ -17,7 +17,7 @@ struct GemmArgs {
     RoutingBufs rb;
     __nv_bfloat16 *h;          // [R][I]
     float *y_acc;              // [T][H]
-    float *logits_part;        // router: [6][T][E_pad16]
+    float *logits_part;        // router: [4][T][E_pad16] (parts x K halves)
     int *status;
     long long wait_limit;
 };
@@ -51,9 +51,10 @@ cudaError_t launch_routing_tables(const float *logits_part, int ld, const float 
                                   int E, int k, int has_shared, const RoutingBufs &rb, cudaStream_t s);
 int gemm_smem_bytes(int mode);
 int router_units(int T);
-cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 *wr3, float *y_acc, int64_t y_elems,
-                        int num_sms, cudaStream_t s);
+cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 *wr2, float *y_acc, int64_t y_elems,
+                        int *counts_blk, int64_t n_counts, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm(int mode, const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t s);
+cudaError_t launch_zero_i32(int *p, int64_t n, cudaStream_t s);
 cudaError_t launch_xperm(const __nv_bfloat16 *x, __nv_bfloat16 *xp, const int *row_token, int rows, int H,
                          int num_sms, cudaStream_t s);
 cudaError_t launch_convert(const float *y_acc, __nv_bfloat16 *y, int64_t n, int num_sms, cudaStream_t s);

@@ -86,8 +86,8 @@ inline PrefillLayout prefill_layout(int T, int E, int k, int H, int I) {
     L.h = take(sizeof(uint16_t) * (size_t)L.R * I);
     L.y_acc = take(sizeof(float) * (size_t)T * H);
     L.E_pad16 = (E + 15) / 16 * 16;
-    L.wr3 = take(sizeof(uint16_t) * 3 * (size_t)L.E_pad16 * H);
-    L.logits_part = take(sizeof(float) * 6 * (size_t)T * L.E_pad16);
+    L.wr3 = take(sizeof(uint16_t) * 2 * (size_t)L.E_pad16 * H);
+    L.logits_part = take(sizeof(float) * 4 * (size_t)T * L.E_pad16);
     L.xperm = take(sizeof(uint16_t) * (size_t)T * k * H);
     L.total = o;
     return L;

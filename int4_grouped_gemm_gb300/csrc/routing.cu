@@ -4,7 +4,7 @@
 // Inference on Apple Silicon" (list under "Performance Gains and Workload
 // Patterns", "Unified Command Buffers"): routing histograms and block maps
 // stay on the GPU, so a MoE layer needs no CPU synchronisation.  The router
-// GEMM itself runs on the tensor cores (grouped_gemm.cu, router mode, six
+// GEMM itself runs on the tensor cores (grouped_gemm.cu, router mode, four
 // partial sums per logit); here, from those partial sums:
 //   topk_hist_kernel      per token: fp32 logits (partials summed in a fixed
 //                         order, + bias), top-k (ties -> lower expert
@@ -27,7 +27,10 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
     return v > bv || (v == bv && i < bi);
 }
 
-// logits_part == nullptr: the fp32 logits are given in `given` instead.
+// One warp per token.  logits_part == nullptr: the fp32 logits are given in
+// `given` instead of being summed from the router's partial products.  The
+// chunk histogram counts_blk (cleared beforehand) receives the block's counts
+// with atomic adds: a sum, so its value does not depend on their order.
 __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict__ logits_part, int ld,
                                                         const float *__restrict__ given,
                                                         const float *__restrict__ bias, int T, int E, int k,
@@ -37,10 +40,8 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
     for (int e = tid; e < 256; e += blockDim.x) hist[e] = 0;
     __syncthreads();
 
-    const int blk = blockIdx.x;
-    for (int tt = 0; tt < kRouteChunk / 8; ++tt) {
-        const int t = blk * kRouteChunk + warp * (kRouteChunk / 8) + tt;
-        if (t >= T) break;
+    const int t = blockIdx.x * 8 + warp;  // 8 tokens per block, all in one chunk
+    if (t < T) {
         float v[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -48,14 +49,13 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
             float l = -INFINITY;
             if (e < E) {
                 if (logits_part) {
-                    // six partial sums: hi, mid, lo bf16 parts of the router
-                    // weights, two K halves each; small parts first
+                    // partial sums: hi and lo bf16 parts of the router weights,
+                    // two K halves each; the small part first
                     const int64_t pstride = static_cast<int64_t>(T) * ld;
                     const float *p = logits_part + static_cast<int64_t>(t) * ld + e;
-                    const float lo = p[4 * pstride] + p[5 * pstride];
-                    const float mid = p[2 * pstride] + p[3 * pstride];
+                    const float lo = p[2 * pstride] + p[3 * pstride];
                     const float hi = p[0] + p[pstride];
-                    l = (lo + mid) + hi;
+                    l = lo + hi;
                     if (bias) l += bias[e];
                     rb.logits[static_cast<int64_t>(t) * E + e] = l;
                 } else {
@@ -117,7 +117,9 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
         }
     }
     __syncthreads();
-    for (int e = tid; e < E; e += blockDim.x) rb.counts_blk[static_cast<int64_t>(blk) * E + e] = hist[e];
+    const int chunk = (blockIdx.x * 8) / kRouteChunk;
+    for (int e = tid; e < E; e += blockDim.x)
+        if (hist[e]) atomicAdd(&rb.counts_blk[static_cast<int64_t>(chunk) * E + e], hist[e]);
 }
 
 // ------------------------------------------------------- scan and tile map
@@ -224,6 +226,7 @@ __global__ void __launch_bounds__(512) scan_tiles_kernel(int T, int E, int k, in
 __global__ void __launch_bounds__(32) permute_kernel(int T, int E, int k, RoutingBufs rb) {
     __shared__ int base[256];
     __shared__ int pick[kRouteChunk * 8];
+    __shared__ float pw[kRouteChunk * 8];
     const int lane = threadIdx.x;
     const int blk = blockIdx.x;
     const int t_begin = blk * kRouteChunk;
@@ -231,7 +234,10 @@ __global__ void __launch_bounds__(32) permute_kernel(int T, int E, int k, Routin
     const int nslots = (t_end - t_begin) * k;
     for (int e = lane; e < E; e += 32)
         base[e] = rb.offsets[e] + rb.base_blk[static_cast<int64_t>(blk) * E + e];
-    for (int i = lane; i < nslots; i += 32) pick[i] = rb.topk_idx[static_cast<int64_t>(t_begin) * k + i];
+    for (int i = lane; i < nslots; i += 32) {
+        pick[i] = rb.topk_idx[static_cast<int64_t>(t_begin) * k + i];
+        pw[i] = rb.topk_w[static_cast<int64_t>(t_begin) * k + i];
+    }
     __syncwarp();
     const int per_pass = 32 / k;
     const unsigned lt_mask = (1u << lane) - 1u;
@@ -251,7 +257,7 @@ __global__ void __launch_bounds__(32) permute_kernel(int T, int E, int k, Routin
             rb.perm[pos] = slot;
             rb.inv_perm[slot] = pos;
             rb.row_token[pos] = t;
-            rb.row_weight[pos] = rb.topk_w[slot];
+            rb.row_weight[pos] = pw[slot - t_begin * k];
         }
         __syncwarp();
     }
@@ -283,11 +289,25 @@ __global__ void __launch_bounds__(256) xperm_kernel(const uint4 *__restrict__ x,
     }
 }
 
+__global__ void zero_i32_kernel(int *__restrict__ p, int64_t n) {
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        p[i] = 0;
+}
+
 // --------------------------------------------------------------- launches
+
+cudaError_t launch_zero_i32(int *p, int64_t n, cudaStream_t s) {
+    if (n <= 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 1024) blocks = 1024;
+    zero_i32_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(p, n);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
                                   int E, int k, int has_shared, const RoutingBufs &rb, cudaStream_t s) {
-    topk_hist_kernel<<<rb.nblk, 256, 0, s>>>(logits_part, ld, given, bias, T, E, k, has_shared, rb);
+    topk_hist_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits_part, ld, given, bias, T, E, k, has_shared, rb);
     scan_tiles_kernel<<<1, 512, 0, s>>>(T, E, k, has_shared, rb);
     permute_kernel<<<rb.nblk, 32, 0, s>>>(T, E, k, rb);
     return cudaGetLastError();

@@ -108,6 +108,7 @@ def test_host_buffers_end_to_end_equals_device_path():
     got = y_host.float().numpy()
     # the weighted combine adds fp32 partial sums with reductions whose order
     # is not fixed, so two runs may differ by one bf16 rounding step
-    assert np.all(np.abs(got - y_dev) <= 2.0 ** -8 * np.abs(y_dev) + 1e-30)
+    # (one bf16 step is at most 2^-7 of the value)
+    assert np.all(np.abs(got - y_dev) <= 2.0 ** -7 * np.maximum(np.abs(got), np.abs(y_dev)) + 1e-30)
     ref = oracle_layer(L, L.x)
     assert_close(got, ref["y"], "host buffers")
