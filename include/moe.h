@@ -150,10 +150,21 @@ int moe_prefill_profiled(const moe_layer_desc *desc, const void *x, int32_t T, v
  * Batch-1 decode: y[1][H] (bf16) = MoE layer of x[1][H] (bf16) as
  * bandwidth-bound dequant-GEMVs that read only the router and the k+1
  * touched experts; the weighted combine is fused into the down GEMV.
- * x and y must not alias.
+ * Requires H <= 4096.  x and y may be the same buffer.
  */
 int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, size_t ws_bytes,
                cudaStream_t stream);
+
+/*
+ * Batch-1 decode through a stack of n_layers layers of the same shape:
+ * layer 0 reads x, layer l+1 reads layer l's output (kept in the workspace),
+ * the last layer writes y.  x and y may be the same buffer, so that a
+ * token's output becomes the next step's input in place on the device.
+ * Each layer runs the moe_decode kernels; the next layer's router weights
+ * are prefetched into L2 while the current layer finishes.
+ */
+int moe_decode_layers(const moe_layer_desc *descs, int32_t n_layers, const void *x, void *y, void *ws,
+                      size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Routing only, from given fp32 logits [T][E]: top-k and weights, histogram,

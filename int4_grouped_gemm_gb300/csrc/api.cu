@@ -127,7 +127,7 @@ extern "C" {
 size_t moe_workspace_bytes(const moe_layer_desc *desc, int32_t T_max) {
     if (check_shape(desc) != MOE_OK || check_tokens(desc, T_max) != MOE_OK) return 0;
     const PrefillLayout P = prefill_layout(T_max, desc->E, desc->k, desc->H, desc->I);
-    const DecodeLayout D = decode_layout(desc->E, desc->k, desc->I);
+    const DecodeLayout D = decode_stack_layout(desc->E, desc->k, desc->H, desc->I);
     return P.total > D.total ? P.total : D.total;
 }
 
@@ -303,16 +303,15 @@ int moe_prefill_profiled(const moe_layer_desc *desc, const void *x, int32_t T, v
     return prefill_impl(desc, x, T, y, ws, ws_bytes, events, stream);
 }
 
-int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, size_t ws_bytes, cudaStream_t stream) {
+static int decode_check(const moe_layer_desc *desc) {
     int rc = check_shape(desc);
     if (rc) return rc;
     if ((rc = check_weights(desc))) return rc;
-    if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
-    const DecodeLayout L = decode_layout(desc->E, desc->k, desc->I);
-    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-    DeviceInfo *dev = nullptr;
-    if ((rc = current_device(dev))) return rc;
-    char *w = static_cast<char *>(ws);
+    if (desc->H > kDecodeMaxH) return MOE_ERR_SHAPE;
+    return MOE_OK;
+}
+
+static DecodeArgs decode_args(const moe_layer_desc *desc, const void *x, void *y, char *w, const DecodeLayout &L) {
     DecodeArgs a{};
     a.x = static_cast<const __nv_bfloat16 *>(x);
     a.y = static_cast<__nv_bfloat16 *>(y);
@@ -340,7 +339,49 @@ int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, siz
     a.topk_idx = reinterpret_cast<int *>(w + L.topk_idx);
     a.topk_w = reinterpret_cast<float *>(w + L.topk_w);
     a.h = reinterpret_cast<float *>(w + L.h);
-    return cuda_rc(launch_decode(a, stream));
+    a.next_Wr = nullptr;
+    return a;
+}
+
+int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    int rc = decode_check(desc);
+    if (rc) return rc;
+    if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
+    const DecodeLayout L = decode_layout(desc->E, desc->k, desc->I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    return cuda_rc(launch_decode(decode_args(desc, x, y, static_cast<char *>(ws), L), stream));
+}
+
+int moe_decode_layers(const moe_layer_desc *descs, int32_t n_layers, const void *x, void *y, void *ws,
+                      size_t ws_bytes, cudaStream_t stream) {
+    if (!descs) return MOE_ERR_NULL;
+    if (n_layers < 1) return MOE_ERR_SHAPE;
+    int rc;
+    for (int l = 0; l < n_layers; ++l) {
+        if ((rc = decode_check(&descs[l]))) return rc;
+        const moe_layer_desc &a = descs[0], &b = descs[l];
+        if (a.E != b.E || a.k != b.k || a.H != b.H || a.I != b.I || a.group != b.group ||
+            a.has_shared != b.has_shared)
+            return MOE_ERR_SHAPE;
+    }
+    if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
+    const moe_layer_desc &d0 = descs[0];
+    const DecodeLayout L = decode_stack_layout(d0.E, d0.k, d0.H, d0.I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    char *w = static_cast<char *>(ws);
+    __nv_bfloat16 *act = reinterpret_cast<__nv_bfloat16 *>(w + L.act);
+    for (int l = 0; l < n_layers; ++l) {
+        const void *in = l == 0 ? x : static_cast<const void *>(act + ((l - 1) % 2) * d0.H);
+        void *out = l == n_layers - 1 ? y : static_cast<void *>(act + (l % 2) * d0.H);
+        DecodeArgs a = decode_args(&descs[l], in, out, w, L);
+        if (l + 1 < n_layers) a.next_Wr = descs[l + 1].router_w;
+        if (launch_decode(a, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
 }
 
 int pack_int4(const float *w, int64_t rows, int32_t K, int32_t group, uint32_t *q, uint16_t *scale,

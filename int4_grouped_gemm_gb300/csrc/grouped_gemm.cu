@@ -419,8 +419,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     uint32_t o[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const float h0 = g[2 * j] / (1.0f + __expf(-g[2 * j])) * up[2 * j];
-                        const float h1 = g[2 * j + 1] / (1.0f + __expf(-g[2 * j + 1])) * up[2 * j + 1];
+                        const float h0 = __fdividef(g[2 * j], 1.0f + __expf(-g[2 * j])) * up[2 * j];
+                        const float h1 = __fdividef(g[2 * j + 1], 1.0f + __expf(-g[2 * j + 1])) * up[2 * j + 1];
                         o[j] = bf162_as_u32(__floats2bfloat162_rn(h0, h1));
                     }
                     if (valid) {

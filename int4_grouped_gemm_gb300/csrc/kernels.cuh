@@ -29,6 +29,8 @@ struct GemmMaps {
     CUtensorMap s0, b0, s1, b1;  // scale / bias blocks
 };
 
+constexpr int kDecodeMaxH = 4096;  // largest hidden size of the decode kernels
+
 struct DecodeArgs {
     const __nv_bfloat16 *x;
     __nv_bfloat16 *y;
@@ -43,6 +45,7 @@ struct DecodeArgs {
     int *topk_idx;
     float *topk_w;
     float *h;  // [(k+1)][I]
+    const float *next_Wr;  // router of the next layer of a stack (prefetched into L2), or NULL
 };
 
 cudaError_t launch_pack_int4(const float *w, int64_t rows, int K, int G, uint32_t *q, uint16_t *scale,

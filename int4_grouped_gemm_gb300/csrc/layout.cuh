@@ -49,7 +49,7 @@ struct PrefillLayout {
 };
 
 struct DecodeLayout {
-    size_t ctrl, logits, topk_idx, topk_w, h, total;
+    size_t ctrl, logits, topk_idx, topk_w, h, act, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -106,7 +106,16 @@ inline DecodeLayout decode_layout(int E, int k, int I) {
     L.topk_idx = take(sizeof(int) * 8);
     L.topk_w = take(sizeof(float) * 8);
     L.h = take(sizeof(float) * (size_t)(k + 1) * I);
+    L.act = 0;
     L.total = o;
+    return L;
+}
+
+// decode workspace plus two bf16 activation rows for a stack of layers
+inline DecodeLayout decode_stack_layout(int E, int k, int H, int I) {
+    DecodeLayout L = decode_layout(E, k, I);
+    L.act = L.total;
+    L.total = align_up(L.act + 2 * sizeof(uint16_t) * (size_t)H, 256);
     return L;
 }
 

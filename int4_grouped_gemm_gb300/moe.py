@@ -132,34 +132,47 @@ class Workspace:
 class DecodeChain:
     """Batch-1 decode through a stack of independent layers.
 
-    Layer l reads ``outs[l-1]`` and writes ``outs[l]``; layer 0 reads the last
-    layer's output, so one pass (a step) leaves the next step's input in place
-    on the device, with no host round trip between tokens.  ``capture()``
-    records one step as a CUDA graph.
+    One step runs every layer once (``moe_decode_layers``): the token in
+    ``tok`` goes through all layers and the last layer's output is written
+    back into ``tok``, so the next step's input is already in place on the
+    device, with no host round trip between tokens.  ``capture()`` records
+    one step as a CUDA graph.
     """
 
     def __init__(self, layers, device="cuda"):
         self.layers = list(layers)
         H = self.layers[0].H
+        self.descs = (moe_layer_desc * len(self.layers))(*[l.desc for l in self.layers])
         self.ws = Workspace(self.layers[0].desc, 1, device=device)
-        self.outs = [torch.zeros(1, H, dtype=torch.bfloat16, device=device) for _ in self.layers]
+        self.tok = torch.zeros(1, H, dtype=torch.bfloat16, device=device)
         self.graph = None
 
     def set_input(self, x: torch.Tensor):
-        self.outs[-1].copy_(x.reshape(self.outs[-1].shape))
+        self.tok.copy_(x.reshape(self.tok.shape))
 
     def step_eager(self, stream=None):
-        n = len(self.layers)
-        for l, layer in enumerate(self.layers):
-            _lib.moe_decode(layer.desc, self.outs[l - 1 if l > 0 else n - 1], self.outs[l], self.ws.buf, stream)
+        _lib.moe_decode_layers(self.descs, self.tok, self.tok, self.ws.buf, stream)
+
+    def layer_outputs_eager(self, x: torch.Tensor):
+        """Run the layers one moe_decode call at a time and keep every output."""
+        outs = []
+        cur = x.reshape(self.tok.shape).contiguous()
+        for layer in self.layers:
+            nxt = torch.empty_like(cur)
+            _lib.moe_decode(layer.desc, cur, nxt, self.ws.buf)
+            outs.append(nxt)
+            cur = nxt
+        return outs
 
     def capture(self):
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
+        saved = self.tok.clone()
         with torch.cuda.stream(s):
             self.step_eager(s)  # warm-up outside the graph (lazy init, module load)
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
+        self.tok.copy_(saved)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self.step_eager(torch.cuda.current_stream())
@@ -172,4 +185,4 @@ class DecodeChain:
         self.graph.replay()
 
     def output(self) -> torch.Tensor:
-        return self.outs[-1]
+        return self.tok
