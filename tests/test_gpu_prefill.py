@@ -107,8 +107,10 @@ def test_host_buffers_end_to_end_equals_device_path():
     _lib.moe_forward_host(layer.desc, x_host, cfg.T, y_host, xd, yd, ws.buf)
     got = y_host.float().numpy()
     # the weighted combine adds fp32 partial sums with reductions whose order
-    # is not fixed, so two runs may differ by one bf16 rounding step
-    # (one bf16 step is at most 2^-7 of the value)
-    assert np.all(np.abs(got - y_dev) <= 2.0 ** -7 * np.maximum(np.abs(got), np.abs(y_dev)) + 1e-30)
+    # is not fixed: two runs may differ by one bf16 rounding step (at most
+    # 2^-7 of the value) plus the fp32 reassociation error of a sum of k+1
+    # terms, which matters only where the terms cancel (1e-5 of the scale)
+    bound = 2.0 ** -7 * np.maximum(np.abs(got), np.abs(y_dev)) + 1e-5 * np.abs(y_dev).max()
+    assert np.all(np.abs(got - y_dev) <= bound)
     ref = oracle_layer(L, L.x)
     assert_close(got, ref["y"], "host buffers")
