@@ -63,15 +63,41 @@ __device__ __forceinline__ float dot8_codes(uint32_t word, const float *xv) {
     return acc;
 }
 
-// Input vector to shared memory as fp32, plus the sum of every 8-element word.
+// Shared-memory positions of the staged vectors.  Lane l of a warp reads the
+// elements 32l.. of x (gate/up rows) or 16l.. of h (down rows); one padding
+// float after every 32 (x) or 16 (h) elements puts those lanes on different
+// banks.  Blocks of 8 (x) or 16 (h) consecutive elements stay contiguous.
+__device__ __forceinline__ int xpos(int k) { return k + (k >> 5); }
+__device__ __forceinline__ int hpos(int k) { return k + (k >> 4); }
+
+// Input vector to shared memory as fp32 (padded positions), plus the sum of
+// every 8-element word: one 16-byte load per word, all issued before any is
+// used.
 __device__ __forceinline__ void stage_x(const __nv_bfloat16 *x, int H, float *xs, float *xsum8) {
-    for (int i = threadIdx.x; i < H; i += blockDim.x) xs[i] = __bfloat162float(x[i]);
-    __syncthreads();
-    for (int w = threadIdx.x; w < H / 8; w += blockDim.x) {
-        float s = 0.f;
+    constexpr int U = kDecodeMaxH / 8 / 256;  // words per thread with 256 threads
+    const int nw = H / 8;
+    uint4 raw[U];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s += xs[w * 8 + i];
-        xsum8[w] = s;
+    for (int u = 0; u < U; ++u) {
+        const int w = threadIdx.x + u * blockDim.x;
+        if (w < nw) raw[u] = *reinterpret_cast<const uint4 *>(x + w * 8);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int w = threadIdx.x + u * blockDim.x;
+        if (w < nw) {
+            const uint32_t p[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 v = u32_as_bf162(p[i]);
+                const float lo = __low2float(v), hi = __high2float(v);
+                xs[xpos(w * 8) + 2 * i] = lo;
+                xs[xpos(w * 8) + 2 * i + 1] = hi;
+                sum += lo + hi;
+            }
+            xsum8[w] = sum;
+        }
     }
     __syncthreads();
 }
@@ -117,8 +143,8 @@ __device__ __forceinline__ void gate_up_dot(const DecodeArgs &a, int64_t row, in
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int w = w0 + i;
-                dg += dot8_codes(gw[i], xs + w * 8);
-                du += dot8_codes(uw[i], xs + w * 8);
+                dg += dot8_codes(gw[i], xs + xpos(w * 8));
+                du += dot8_codes(uw[i], xs + xpos(w * 8));
                 xs4 += xsum8[w];
             }
             gacc += sgv * dg + bgv * xs4;
@@ -139,7 +165,7 @@ __device__ __forceinline__ void prefetch_down_rows(const DecodeArgs &a, int e, i
 // blocks [0, nr): router, 2 experts per block; blocks [nr, nr + I/8): the
 // shared expert's gate/up rows, 8 per block (one per warp).
 __global__ void __launch_bounds__(256) decode_k1_kernel(DecodeArgs a) {
-    __shared__ float xs[kDecodeMaxH];
+    __shared__ float xs[kDecodeMaxH + kDecodeMaxH / 32];
     __shared__ float xsum8[kDecodeMaxH / 8];
     __shared__ float part[8];
     __shared__ int is_last;
@@ -274,7 +300,7 @@ __global__ void __launch_bounds__(256) decode_k1_kernel(DecodeArgs a) {
 
 // Block = 8 warps = 8 intermediate features of routed slot j.
 __global__ void __launch_bounds__(256) decode_k2_kernel(DecodeArgs a) {
-    __shared__ float xs[kDecodeMaxH];
+    __shared__ float xs[kDecodeMaxH + kDecodeMaxH / 32];
     __shared__ float xsum8[kDecodeMaxH / 8];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int fblocks = a.I / 8;
@@ -307,10 +333,9 @@ constexpr int kMaxSlots = 9;  // k <= 8 routed + 1 shared
 __global__ void __launch_bounds__(256) decode_k3_kernel(DecodeArgs a) {
     extern __shared__ float sm[];
     const int nslots = a.k + (a.has_shared ? 1 : 0);
-    float *hs = sm;                          // [nslots][I]
-    float *hsum8 = sm + nslots * a.I;        // [nslots][I/8]
-    __shared__ int s_e[kMaxSlots];
-    __shared__ float s_w[kMaxSlots];
+    const int ip = a.I + a.I / 16;           // padded row of h
+    float *hs = sm;                          // [nslots][ip]
+    float *hsum8 = sm + nslots * ip;         // [nslots][I/8]
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     pdl_launch_dependents();
     pdl_wait();
@@ -324,56 +349,91 @@ __global__ void __launch_bounds__(256) decode_k3_kernel(DecodeArgs a) {
             prefetch_range(reinterpret_cast<const char *>(a.next_Wr) + off,
                            off + slice <= wr_bytes ? slice : wr_bytes - off);
     }
-    for (int i = tid; i < nslots * a.I; i += blockDim.x) hs[i] = __ldcg(a.h + i);
-    if (tid < nslots) {
-        s_e[tid] = tid < a.k ? __ldcg(a.topk_idx + tid) : a.E;
-        s_w[tid] = tid < a.k ? __ldcg(a.topk_w + tid) : 1.0f;
+    // this warp's down rows of every touched expert: issued first, so that
+    // their latency overlaps the staging of h
+    const int f = blockIdx.x * 8 + warp;
+    const int nw = a.I / 8;
+    const bool vec = (nw & 63) == 0;  // lane handles 2 consecutive words per step
+    int e_j[kMaxSlots];
+    float w_j[kMaxSlots];
+    uint2 qw[kMaxSlots];
+    float sv[kMaxSlots], bv[kMaxSlots];
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j) {
+        e_j[j] = j < a.k ? __ldcg(a.topk_idx + j) : a.E;
+        w_j[j] = j < a.k ? __ldcg(a.topk_w + j) : 1.0f;
+    }
+    if (vec && nw == 64) {
+        const int w0 = lane * 2;
+        const int grp = (w0 * 8) / a.G;  // both words share a group (G >= 16)
+#pragma unroll
+        for (int j = 0; j < kMaxSlots; ++j) {
+            if (j < nslots) {
+                const int64_t row = static_cast<int64_t>(e_j[j]) * a.H + f;
+                qw[j] = *reinterpret_cast<const uint2 *>(a.qd + row * nw + w0);
+                sv[j] = bf16_bits_to_float(a.sd[row * a.ldg_i + grp]);
+                bv[j] = bf16_bits_to_float(a.bd[row * a.ldg_i + grp]);
+            }
+        }
+    }
+    // h of every slot into shared memory (16-byte loads, all issued first)
+    {
+        const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
+        const int n4 = nslots * a.I / 4;
+        const int r4 = a.I / 4;  // float4 per slot
+        auto put = [&](int i, float4 v) {
+            float *d = hs + (i / r4) * ip + hpos((i % r4) * 4);  // 4 elements never straddle a pad
+            d[0] = v.x;
+            d[1] = v.y;
+            d[2] = v.z;
+            d[3] = v.w;
+        };
+        constexpr int U = 6;
+        float4 tmp[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = tid + u * blockDim.x;
+            if (i < n4) tmp[u] = __ldcg(h4 + i);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = tid + u * blockDim.x;
+            if (i < n4) put(i, tmp[u]);
+        }
+        for (int i = tid + U * blockDim.x; i < n4; i += blockDim.x) put(i, __ldcg(h4 + i));
     }
     __syncthreads();
-    const int nw = a.I / 8;
     for (int w = tid; w < nslots * nw; w += blockDim.x) {
+        const float *src = hs + (w / nw) * ip + hpos((w % nw) * 8);
         float s = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s += hs[w * 8 + i];
+        for (int i = 0; i < 8; ++i) s += src[i];
         hsum8[w] = s;
     }
     __syncthreads();
-    const int f = blockIdx.x * 8 + warp;
     float y = 0.f;
-    if ((nw & 63) == 0) {
-        // 64-bit loads: lane handles 2 consecutive words per step
-        for (int w0 = lane * 2; w0 < nw; w0 += 64) {
-            uint2 qw[kMaxSlots];
+    if (vec && nw == 64) {
+        const int w0 = lane * 2;
 #pragma unroll
-            for (int j = 0; j < kMaxSlots; ++j) {
-                if (j < nslots) {
-                    const int64_t row = static_cast<int64_t>(s_e[j]) * a.H + f;
-                    qw[j] = *reinterpret_cast<const uint2 *>(a.qd + row * nw + w0);
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < kMaxSlots; ++j) {
-                if (j < nslots) {
-                    const int64_t row = static_cast<int64_t>(s_e[j]) * a.H + f;
-                    const int grp = (w0 * 8) / a.G;  // both words share a group (G >= 16)
-                    const float s = bf16_bits_to_float(a.sd[row * a.ldg_i + grp]);
-                    const float b = bf16_bits_to_float(a.bd[row * a.ldg_i + grp]);
-                    const float *hv = hs + j * a.I + w0 * 8;
-                    const float d = dot8_codes(qw[j].x, hv) + dot8_codes(qw[j].y, hv + 8);
-                    const float hsum = hsum8[j * nw + w0] + hsum8[j * nw + w0 + 1];
-                    y += s_w[j] * (s * d + b * hsum);
-                }
+        for (int j = 0; j < kMaxSlots; ++j) {
+            if (j < nslots) {
+                const float *hv = hs + j * ip + hpos(w0 * 8);  // 16 contiguous elements
+                const float d = dot8_codes(qw[j].x, hv) + dot8_codes(qw[j].y, hv + 8);
+                const float hsum = hsum8[j * nw + w0] + hsum8[j * nw + w0 + 1];
+                y += w_j[j] * (sv[j] * d + bv[j] * hsum);
             }
         }
     } else {
         for (int w = lane; w < nw; w += 32) {
             for (int j = 0; j < nslots; ++j) {
-                const int64_t row = static_cast<int64_t>(s_e[j]) * a.H + f;
+                const int e = j < a.k ? __ldcg(a.topk_idx + j) : a.E;
+                const float wgt = j < a.k ? __ldcg(a.topk_w + j) : 1.0f;
+                const int64_t row = static_cast<int64_t>(e) * a.H + f;
                 const int grp = (w * 8) / a.G;
                 const float s = bf16_bits_to_float(a.sd[row * a.ldg_i + grp]);
                 const float b = bf16_bits_to_float(a.bd[row * a.ldg_i + grp]);
-                const float d = dot8_codes(a.qd[row * nw + w], hs + j * a.I + w * 8);
-                y += s_w[j] * (s * d + b * hsum8[j * nw + w]);
+                const float d = dot8_codes(a.qd[row * nw + w], hs + j * ip + hpos(w * 8));
+                y += wgt * (s * d + b * hsum8[j * nw + w]);
             }
         }
     }
@@ -404,7 +464,7 @@ cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if ((e = launch_pdl(decode_k2_kernel, a.k * (a.I / 8), 256, 0, s, a)) != cudaSuccess) return e;
     const int nslots = a.k + (a.has_shared ? 1 : 0);
-    const size_t sm_dn = sizeof(float) * (nslots * a.I + nslots * a.I / 8);
+    const size_t sm_dn = sizeof(float) * (nslots * (a.I + a.I / 16) + nslots * a.I / 8);
     if (sm_dn > 48 * 1024 &&
         (e = cudaFuncSetAttribute(decode_k3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   static_cast<int>(sm_dn))) != cudaSuccess)
