@@ -184,6 +184,27 @@ int moe_route_logits(const moe_layer_desc *desc, const float *logits, int32_t T,
 int pack_int4(const float *w, int64_t rows, int32_t K, int32_t group, uint32_t *q, uint16_t *scale,
               uint16_t *bias, cudaStream_t stream);
 
+/*
+ * moe_decode without a caller workspace: the decode scratch lives in a fixed
+ * 64 KiB device array inside the library, so the call allocates nothing and
+ * takes no workspace pointer.  It is an addition of this library; the method
+ * itself has no counterpart.  It serves callers that may not allocate device
+ * memory at all: a host that owns every device allocation through its own
+ * pool, or a latency-critical token loop in which an allocator call (which
+ * may synchronise the device) is not allowed.
+ *
+ * Limit: the layer's decode scratch must fit the 64 KiB (E = 256, k = 8
+ * fits up to I = 1664); larger layers return MOE_ERR_WORKSPACE before
+ * anything is launched.  Other requirements are those of moe_decode.
+ * Set-up: the first call on each device, with that device current, looks up
+ * the array's address; make that first call before any stream capture
+ * starts.  Every call clears the array's control block on `stream` before
+ * the kernels run.  All calls on one device share the one array, so two
+ * calls in flight at once (other streams or threads) race: issue them in
+ * order on one stream.
+ */
+int moe_decode_static_scratch(const moe_layer_desc *desc, const void *x, void *y, cudaStream_t stream);
+
 /* Synchronise `stream`, return the device status word of `ws` (0 = fine,
  * MOE_ERR_TIMEOUT - site after a bounded wait ran out) and clear it. */
 int moe_read_device_status(void *ws, cudaStream_t stream);

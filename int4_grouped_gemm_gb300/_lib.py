@@ -60,6 +60,7 @@ SIGNATURES = {
     "moe_prefill_profiled": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_sz, c_p, c_p]),
     "moe_decode": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_sz, c_p]),
     "moe_decode_layers": (ctypes.c_int, [c_p, c_i32, c_p, c_p, c_p, c_sz, c_p]),
+    "moe_decode_static_scratch": (ctypes.c_int, [c_p, c_p, c_p, c_p]),
     "moe_route_logits": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_sz, c_p]),
     "pack_int4": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_p]),
     "moe_read_device_status": (ctypes.c_int, [c_p, c_p]),
@@ -147,6 +148,12 @@ def moe_decode_layers(descs, x, y, ws, stream=None):
     """descs: a ctypes array of moe_layer_desc (one per layer)."""
     _check(load().moe_decode_layers(ctypes.cast(descs, c_p), len(descs), _ptr(x), _ptr(y), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)), "moe_decode_layers")
+
+
+def moe_decode_static_scratch(desc: moe_layer_desc, x, y, stream=None):
+    """moe_decode on the library's fixed scratch array (no workspace)."""
+    _check(load().moe_decode_static_scratch(ctypes.byref(desc), _ptr(x), _ptr(y), _stream(stream)),
+           "moe_decode_static_scratch")
 
 
 def moe_route_logits(desc: moe_layer_desc, logits, T: int, ws, stream=None):

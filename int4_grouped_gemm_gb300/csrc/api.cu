@@ -122,6 +122,30 @@ static cudaError_t launch_selftest_wait(Ctrl *ctrl, long long limit, cudaStream_
 
 using namespace moe;
 
+// Fixed decode scratch for moe_decode_static_scratch: one array per device,
+// zero when the module loads, and from then on holding whatever the last call
+// left in it.  64 KiB holds the decode scratch (control block, E logits,
+// top-k, k + 1 fp32 rows of I) of E = 256, k = 8 layers up to I = 1664.
+static constexpr size_t kStaticScratchBytes = 64 * 1024;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+static void *g_static_scratch_ptr[64];
+
+// Look the array's device address up once per device, with that device
+// current, and keep it for later calls on the same device.
+static int static_scratch(char *&out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_DEVICE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_static_scratch_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_static_scratch_ptr[dev] = p;
+    }
+    out = static_cast<char *>(g_static_scratch_ptr[dev]);
+    return MOE_OK;
+}
+
 extern "C" {
 
 size_t moe_workspace_bytes(const moe_layer_desc *desc, int32_t T_max) {
@@ -452,6 +476,22 @@ const char *moe_status_string(int code) {
     }
     if (code <= MOE_ERR_TIMEOUT && code > MOE_ERR_TIMEOUT - 100) return "device: a bounded wait ran out";
     return "unknown status";
+}
+
+int moe_decode_static_scratch(const moe_layer_desc *desc, const void *x, void *y, cudaStream_t stream) {
+    int rc = decode_check(desc);
+    if (rc) return rc;
+    if ((rc = check_ptr(x)) || (rc = check_ptr(y))) return rc;
+    const DecodeLayout L = decode_layout(desc->E, desc->k, desc->I);
+    if (L.total > kStaticScratchBytes) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    char *w = nullptr;
+    if ((rc = static_scratch(w))) return rc;
+    // The top-k ticket must start at zero; a call that gave up part way may
+    // have left it set.  Logits, top-k and h are written before they are read.
+    if (cudaMemsetAsync(w + L.ctrl, 0, kCtrlBytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_rc(launch_decode(decode_args(desc, x, y, w, L), stream));
 }
 
 }  // extern "C"

@@ -1,0 +1,83 @@
+"""moe_decode_static_scratch: batch-1 decode on the library's fixed scratch
+array, with no caller workspace.  Compared with moe_decode (caller workspace)
+on the same layer and tokens, over consecutive calls, so that whatever one
+call leaves in the shared array cannot leak into the next.  The file name
+keeps it last in collection order, after every other test has used the
+library; it also passes on its own in a fresh process."""
+import ctypes
+
+import pytest
+import torch
+
+from int4_grouped_gemm_gb300 import _lib, synthetic
+from int4_grouped_gemm_gb300.moe import PackedLayer
+
+from moe_helpers import assert_close
+
+
+def _fake_desc(E, k, H, I, G):
+    # 16-byte aligned stand-in pointers: the call must reject the shape on
+    # the host, before it reads any of them or touches a device.
+    q = _lib.moe_qweight(256, 512, 768)
+    return _lib.moe_layer_desc(E, k, H, I, G, 1, 1024, None, q, q, q)
+
+
+def test_oversized_layer_rejected_on_host():
+    from int4_grouped_gemm_gb300 import build
+    build.build()
+    lib = _lib.load()
+    # at E=256, k=8 the 64 KiB array holds I <= 1664; each of these needs more
+    for E, k, H, I, G in [(256, 8, 2048, 1792, 64), (256, 8, 4096, 4096, 32), (128, 8, 2048, 2048, 64)]:
+        d = _fake_desc(E, k, H, I, G)
+        rc = lib.moe_decode_static_scratch(ctypes.byref(d), ctypes.c_void_p(2048), ctypes.c_void_p(4096), None)
+        assert rc == _lib.MOE_ERR_WORKSPACE, (E, k, H, I, G, rc)
+    assert "workspace" in _lib.status_string(_lib.MOE_ERR_WORKSPACE)
+    # shape errors are still shape errors
+    d = _fake_desc(256, 9, 2048, 512, 64)
+    assert lib.moe_decode_static_scratch(ctypes.byref(d), ctypes.c_void_p(2048), ctypes.c_void_p(4096),
+                                         None) == _lib.MOE_ERR_SHAPE
+    assert lib.moe_decode_static_scratch(None, None, None, None) == _lib.MOE_ERR_NULL
+
+
+def _layer(name, layer=0):
+    cfg = synthetic.CONFIGS[name]
+    L = synthetic.make_layer(cfg, layer=layer, device="cuda", with_x=False)
+    packed = PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down)
+    del L
+    return cfg, packed
+
+
+def _static(layer: PackedLayer, x: torch.Tensor) -> torch.Tensor:
+    y = torch.empty_like(x)
+    rc = _lib.load().moe_decode_static_scratch(ctypes.byref(layer.desc), ctypes.c_void_p(x.data_ptr()),
+                                               ctypes.c_void_p(y.data_ptr()),
+                                               ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == _lib.MOE_OK, _lib.status_string(rc)
+    return y
+
+
+@pytest.mark.gpu
+def test_static_scratch_matches_workspace_decode():
+    cfg, big = _layer("decode40", layer=5)
+    tcfg, tiny = _layer("tiny")
+    ws_big = big.workspace(1)
+    ws_tiny = tiny.workspace(1)
+    xs = synthetic.make_tokens(cfg.H, 3, seed=71).cuda()
+    xt = synthetic.make_tokens(tcfg.H, 2, seed=72).cuda()
+    # consecutive calls: two tokens of the large layer, then the small layer
+    # (a different scratch layout), then the large layer again
+    calls = [(big, ws_big, xs[0:1]), (big, ws_big, xs[1:2]), (tiny, ws_tiny, xt[0:1]),
+             (tiny, ws_tiny, xt[1:2]), (big, ws_big, xs[2:3])]
+    for i, (layer, ws, x) in enumerate(calls):
+        x = x.contiguous()
+        got = _static(layer, x)
+        want = layer.decode(x, ws)
+        torch.cuda.synchronize()
+        assert torch.isfinite(got.float()).all()
+        assert_close(got.float().cpu().numpy(), want.float().cpu().numpy(), f"call {i}")
+    # the same token twice in a row gives the same output
+    a = _static(big, xs[0:1].contiguous())
+    b = _static(big, xs[0:1].contiguous())
+    torch.cuda.synchronize()
+    assert_close(b.float().cpu().numpy(), a.float().cpu().numpy(), "repeat")
+    assert _lib.moe_read_device_status(ws_big.buf) == 0
