@@ -270,6 +270,7 @@ def run_prefill(args, rank, world, pk):
     counts = rt["counts"].cpu()
     rows = int(counts.sum().item())
     n_tiles = int(rt["tile_group"].numel())
+    n_units = int(rt["tile_sched"].numel())
 
     # --- e2e through the C ABI with host buffers
     x_host = x.cpu().pin_memory()
@@ -300,7 +301,7 @@ def run_prefill(args, rank, world, pk):
     del flush
     return dict(
         cfg=cfg, ms_step=ms_step, tokens=cfg.T, clocks=clocks, launches=launches,
-        stage_ms=stage_ms, rows=rows, n_tiles=n_tiles, counts_max=int(counts[:cfg.E].max()),
+        stage_ms=stage_ms, rows=rows, n_tiles=n_tiles, n_units=n_units, counts_max=int(counts[:cfg.E].max()),
         counts_zero=int((counts[:cfg.E] == 0).sum()), total_flops=total_flops,
         e2e_s=e2e_s, bytes_io=2 * cfg.T * cfg.H * 2,
         roofline={"bound": "tensor", "kernel": "grouped_gemm_gate_up" if dominant == 0 else "grouped_gemm_down",
@@ -491,7 +492,7 @@ def main():
                                    f"seed {cfg.seed}",
                        "parallelism": f"replicas x{world}", "l2": "256 MB L2 flush before every timed step; "
                        "int4 weights (455 MB) exceed the 129 MB L2",
-                       "routed_rows": P["rows"], "tiles": P["n_tiles"], "max_rows_per_expert": P["counts_max"],
+                       "routed_rows": P["rows"], "tiles": P["n_tiles"], "gemm_units": P["n_units"], "max_rows_per_expert": P["counts_max"],
                        "empty_experts": P["counts_zero"]},
             "roofline": P["roofline"],
             "layer": {"expert_tflops_per_step": round(P["layer_tflops"], 1),

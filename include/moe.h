@@ -105,8 +105,12 @@ typedef struct {
     int64_t tile_group;  /* int32 [max_tiles]: canonical tile map, groups in order */
     int64_t tile_row;    /* int32 [max_tiles]: first row of the tile */
     int64_t tile_rows;   /* int32 [max_tiles]: rows in the tile (<= tile size) */
-    int64_t tile_sched;  /* int32 [max_tiles]: launch order (largest tiles first) */
-    int64_t num_tiles;   /* int32 [1] */
+    int64_t tile_sched;  /* int32 [max_tiles]: grouped-GEMM work units in launch
+                          * order, each given by its first tile; a unit is a
+                          * group's tiles 2i and 2i+1 (the last one alone when
+                          * the group has an odd count); units of 2 full tiles
+                          * first, then by rows descending, ties lower group */
+    int64_t num_tiles;   /* int32 [2]: tiles, work units */
     int64_t xperm;       /* bf16 [T*k][H]: x rows in routed-row order */
     int64_t h;           /* bf16 [T*k + T][I]: SwiGLU output per routed/shared row */
     int64_t y_acc;       /* fp32 [T][H]: combine accumulator */

@@ -247,8 +247,8 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     if ((rc = encode_2d(&m1.a0, BF16, 2, routed > 0 ? static_cast<const void *>(xperm) : x, H,
                         routed > 0 ? routed : T, 64, 128, SW128)) ||
         (rc = encode_2d(&m1.a1, BF16, 2, x, H, T, 64, 128, SW128)) ||
-        (rc = encode_2d(&m1.w0, U32, 4, desc->gate.q, H / 8, gu_rows, 8, 128, SW0)) ||
-        (rc = encode_2d(&m1.w1, U32, 4, desc->up.q, H / 8, gu_rows, 8, 128, SW0)) ||
+        (rc = encode_2d(&m1.w0, U32, 4, desc->gate.q, H / 8, gu_rows, 4, 128, SW0)) ||
+        (rc = encode_2d(&m1.w1, U32, 4, desc->up.q, H / 8, gu_rows, 4, 128, SW0)) ||
         (rc = encode_2d(&m1.s0, U16, 2, desc->gate.scale, ldg_h, gu_rows, 8, 128, SW0)) ||
         (rc = encode_2d(&m1.b0, U16, 2, desc->gate.bias, ldg_h, gu_rows, 8, 128, SW0)) ||
         (rc = encode_2d(&m1.s1, U16, 2, desc->up.scale, ldg_h, gu_rows, 8, 128, SW0)) ||
@@ -256,7 +256,7 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
         return rc;
     // down: A = h rows, B = 256 down rows of one expert
     if ((rc = encode_2d(&m2.a0, BF16, 2, h, I, L.R, 64, 128, SW128)) ||
-        (rc = encode_2d(&m2.w0, U32, 4, desc->down.q, I / 8, dn_rows, 8, 256, SW0)) ||
+        (rc = encode_2d(&m2.w0, U32, 4, desc->down.q, I / 8, dn_rows, 4, 256, SW0)) ||
         (rc = encode_2d(&m2.s0, U16, 2, desc->down.scale, ldg_i, dn_rows, 8, 256, SW0)) ||
         (rc = encode_2d(&m2.b0, U16, 2, desc->down.bias, ldg_i, dn_rows, 8, 256, SW0)))
         return rc;

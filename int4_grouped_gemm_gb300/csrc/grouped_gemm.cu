@@ -8,29 +8,39 @@
 // measured wins"): unpacking in on-chip memory avoids a full extra
 // read/write pass, and the MoE work is about 90% of prefill.
 //
-// Tile shape.  One tcgen05.mma (kind::f16, K = 16) costs the same time for
-// any M <= 128 and N <= 256, so the kernel keeps every instruction at
-// M = 128 x N = 256: the token rows of one expert group are the "A" operand
-// (M = 128 rows, the last tile of a group padded), and 256 dequantised weight
-// rows are "B" (N = 256, never padded).  A work unit is (128-row token tile
-// of one group, 256-row weight tile); units run on a persistent grid of one
-// CTA per SM in a largest-tile-first order.
+// Tile shape.  A tcgen05.mma of kind::f16 with M = 128 and N = 256 takes
+// 128 cycles per K = 16 step (N = 128: 64 cycles, the same rate), so the
+// contraction itself runs at full speed for any N >= 128.  What costs is
+// rebuilding the bf16 weights from int4 and bringing operand bytes from L2:
+// both scale with the weight rows per unit of tensor-core work.  A work unit
+// therefore pairs two 128-row token tiles of one expert group with one
+// 256-row weight tile: every dequantised weight stage feeds two MMAs
+// (M = 128 each, N = 256) into two 256-column TMEM accumulators, which halves
+// the dequant work and cuts the operand bytes per FLOP compared with one
+// token tile per unit.  Units run on a persistent grid of one CTA per SM in a
+// largest-first order.
 //
-//   warp 6      A producer: TMA loads of the token tile (16 KB boxes) from the
-//               permuted copy of x (gate/up), from x itself (shared expert,
-//               router) or from h (down)
-//   warp 4      W producer: TMA loads of packed nibbles (8 KB per stage) and
-//               of scale/bias blocks (8 groups x 256 rows); router mode: the
-//               bf16 router weight tile straight into the B ring
-//   warps 8-15  dequantisers, one weight row per thread: nibbles -> bf16
-//               s*q+b in the 128-byte swizzled K-major layout of the B ring
-//   warp 5      one thread issues the MMAs (bf16 x bf16 -> fp32 in tensor
-//               memory), two 256-column accumulators
-//   warps 0-3   epilogue, thread = token row of the tile:
+//   warp 10     A producer: TMA loads of both token tiles (2 x 16 KB boxes per
+//               stage) from the permuted copy of x (gate/up), from x itself
+//               (shared expert, router) or from h (down)
+//   warp 8      W producer: TMA loads of packed nibbles (8 KB per stage, two
+//               16-byte halves per row so that each dequant thread reads 16
+//               contiguous bytes) and of scale/bias blocks (8 groups x 256
+//               rows); router mode: the bf16 router weight tile straight into
+//               the B ring
+//   warps 11-26 dequantisers, two threads per weight row (one per 32-element
+//               half of the stage): nibbles -> bf16 s*q+b in the 128-byte
+//               swizzled K-major layout of the B ring
+//   warp 9      one thread issues the MMAs (bf16 x bf16 -> fp32 in tensor
+//               memory): token tile 0 into columns 0-255, tile 1 into 256-511
+//   warps 0-7   epilogue, warp w reads TMEM lanes 32*(w%4).. (token rows) and
+//               every other 16-column chunk (w/4 picks which):
 //               MODE 0 (gate/up): h = silu(gate) * up -> bf16 h rows
 //               MODE 1 (down):    y_acc[token] += w * o  (fp32 v4 reductions
 //                                 after a transpose through shared memory)
 //               MODE 2 (router):  partial logits of one bf16 part and K half
+//               Tile 0's accumulator is handed back first, so that the next
+//               unit's tile-0 MMAs overlap the draining of tile 1.
 //
 // Every mbarrier wait is bounded; a wait that runs out records a status code,
 // raises a block-wide abort flag and the block unwinds.
@@ -39,27 +49,32 @@
 namespace moe {
 
 constexpr int BM = 128;                          // token rows per tile (MMA M)
+constexpr int TPU = 2;                           // token tiles per work unit
 constexpr int BN = 256;                          // weight rows per tile (MMA N)
 constexpr int GK = 64;                           // K elements per stage
 constexpr int SG = 8;                            // quantisation groups per scale block
-constexpr int NS_A = 4, NS_B = 3, NS_Q = 4, NS_S = 2;  // ring depths
-constexpr int kEpiWarp0 = 0, kWProdWarp = 4, kMmaWarp = 5, kAProdWarp = 6, kDeqWarp0 = 8, kDeqWarps = 8;
-constexpr int kGemmThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 512
-constexpr int A_STAGE = BM * 128;                // 16 KB: 128 token rows x 64 bf16
+constexpr int NS_A = 3, NS_B = 2, NS_S = 2;      // ring depths
+constexpr int kMaxNsQ = 4;
+__host__ __device__ constexpr int ns_q(int mode) { return mode == 1 ? 3 : 4; }
+constexpr int kEpiWarps = 8, kWProdWarp = 8, kMmaWarp = 9, kAProdWarp = 10, kDeqWarp0 = 11, kDeqWarps = 16;
+constexpr int kGemmThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 864
+constexpr int TILE_A = BM * 128;                 // 16 KB: 128 token rows x 64 bf16
+constexpr int A_STAGE = TPU * TILE_A;            // 32 KB: both token tiles
 constexpr int B_STAGE = BN * 128;                // 32 KB: 256 weight rows x 64 bf16
-constexpr int Q_STAGE = BN * GK / 2;             // 8 KB: 256 rows x 64 nibbles
+constexpr int Q_HALF = BN * 16;                  // 4 KB: 256 rows x 32 nibbles
+constexpr int Q_STAGE = 2 * Q_HALF;              // 8 KB
 constexpr int S_STAGE = 2 * BN * SG * 2;         // 8 KB: [scale|bias][256 rows][8 groups] bf16
 constexpr int T_PITCH = 20;                      // fp32 pitch of the epilogue transpose rows
 constexpr uint32_t kTmemCols = 512;              // two 256-column fp32 accumulators
 constexpr int kRouterParts = 2;                  // bf16 parts of the fp32 router weights
-constexpr int kRouterUnits = 2 * kRouterParts;   // router units per token tile (parts x K halves)
+constexpr int kRouterUnits = 2 * kRouterParts;   // router units per token-tile pair (parts x K halves)
 
 struct Smem {
     uint64_t a_full[NS_A], a_empty[NS_A];
     uint64_t b_full[NS_B], b_empty[NS_B];
-    uint64_t q_full[NS_Q], q_empty[NS_Q];
+    uint64_t q_full[kMaxNsQ], q_empty[kMaxNsQ];
     uint64_t s_full[NS_S], s_empty[NS_S];
-    uint64_t acc_full[2], acc_empty[2];
+    uint64_t acc_full[TPU], acc_empty[TPU];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
@@ -76,9 +91,9 @@ __host__ __device__ inline SmemMap smem_map(int mode) {
     m.b = m.a + NS_A * A_STAGE;
     m.q = m.b + NS_B * B_STAGE;
     const bool deq = mode != 2;
-    m.s = m.q + (deq ? NS_Q * Q_STAGE : 0);
+    m.s = m.q + (deq ? ns_q(mode) * Q_STAGE : 0);
     m.t = m.s + (deq ? NS_S * S_STAGE : 0);
-    m.ctl = m.t + (mode == 1 ? 4 * 32 * T_PITCH * 4 : 0);
+    m.ctl = m.t + (mode == 1 ? kEpiWarps * 32 * T_PITCH * 4 : 0);
     m.total = m.ctl + static_cast<int>(sizeof(Smem)) + 1024;  // + alignment slack
     return m;
 }
@@ -87,34 +102,41 @@ struct Unit {
     int nt;      // weight tile (MODE 0/1)
     int g;       // group (MODE 0/1)
     int row0;    // first token row: permuted row (MODE 0/1) or token (MODE 2)
-    int n;       // valid rows
+    int n;       // valid rows of the unit (<= TPU * BM)
+    int ntiles;  // token tiles holding them (1 or 2)
     int part;    // MODE 2: bf16 part (0 hi, 1 lo) and K half
     int khalf;
 };
 
+// A unit of MODE 0/1 is tiles t0 and t0 + 1 of one group when the scheduled
+// tile t0 is full and the next tile belongs to the same group (units pair a
+// group's tiles 0-1, 2-3, ..., so a full scheduled tile followed by a tile of
+// its group is always the first of a pair).
 template <int MODE>
 __device__ __forceinline__ Unit load_unit(const GemmArgs &a, int u) {
     Unit t{};
     if (MODE == 2) {
-        const int tt = u / kRouterUnits, rem = u % kRouterUnits;
+        const int pair = u / kRouterUnits, rem = u % kRouterUnits;
         t.part = rem / 2;
         t.khalf = rem % 2;
-        t.row0 = tt * BM;
-        t.n = min(BM, a.T - t.row0);
+        t.row0 = pair * TPU * BM;
+        t.n = min(TPU * BM, a.T - t.row0);
     } else {
-        const int tile = a.rb.tile_sched[u / a.n_ntiles];
+        const int t0 = a.rb.tile_sched[u / a.n_ntiles];
         t.nt = u % a.n_ntiles;
-        t.g = a.rb.tile_group[tile];
-        t.row0 = a.rb.tile_row[tile];
-        t.n = a.rb.tile_rows[tile];
+        t.g = a.rb.tile_group[t0];
+        t.row0 = a.rb.tile_row[t0];
+        t.n = a.rb.tile_rows[t0];
+        if (t.n == BM && t0 + 1 < a.rb.num_tiles[0] && a.rb.tile_group[t0 + 1] == t.g) t.n += a.rb.tile_rows[t0 + 1];
     }
+    t.ntiles = t.n > BM ? 2 : 1;
     return t;
 }
 
 template <int MODE>
 __device__ __forceinline__ int num_units(const GemmArgs &a) {
-    if (MODE == 2) return kRouterUnits * ((a.T + BM - 1) / BM);
-    return a.rb.num_tiles[0] * a.n_ntiles;
+    if (MODE == 2) return kRouterUnits * ((a.T + TPU * BM - 1) / (TPU * BM));
+    return a.rb.num_tiles[1] * a.n_ntiles;
 }
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -151,6 +173,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_s1, const __grid_constant__ CUtensorMap tm_b1,
                         const GemmArgs a) {
+    constexpr int NS_Q = ns_q(MODE);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const SmemMap map = smem_map(MODE);
@@ -179,9 +202,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_init(&s->s_full[i], 1);
             mbar_init(&s->s_empty[i], kDeqWarps);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < TPU; ++i) {
             mbar_init(&s->acc_full[i], 1);
-            mbar_init(&s->acc_empty[i], 4);
+            mbar_init(&s->acc_empty[i], kEpiWarps);
         }
         mbar_init(&s->drain, 1);
         s->abort = 0;
@@ -232,8 +255,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const int st = it % NS_A;
                     ok = wait_or_abort(&s->a_empty[st], ((it / NS_A) & 1) ^ 1, a, s, 1);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(&s->a_full[st], A_STAGE);
-                    tma_load_2d(sA + st * A_STAGE, map_a, &s->a_full[st], kcol0 + ks * GK, arow);
+                    mbar_arrive_expect_tx(&s->a_full[st], t.ntiles * TILE_A);
+                    for (int i = 0; i < t.ntiles; ++i)
+                        tma_load_2d(sA + st * A_STAGE + i * TILE_A, map_a, &s->a_full[st], kcol0 + ks * GK,
+                                    arow + i * BM);
                 }
             }
             if (!ok) drain_ring(s->a_full, NS_A, it, a.wait_limit);
@@ -284,11 +309,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     if (!ok) break;
                     mbar_arrive_expect_tx(&s->q_full[st], Q_STAGE);
                     uint8_t *dst = sQ + st * Q_STAGE;
-                    if (MODE == 0) {
-                        tma_load_2d(dst, &tm_w0, &s->q_full[st], ks * (GK / 8), w_row);
-                        tma_load_2d(dst + Q_STAGE / 2, &tm_w1, &s->q_full[st], ks * (GK / 8), w_row);
-                    } else {
-                        tma_load_2d(dst, &tm_w0, &s->q_full[st], ks * (GK / 8), w_row);
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int col = ks * (GK / 8) + hf * 4;  // first nibble word of this half
+                        if (MODE == 0) {
+                            tma_load_2d(dst + hf * Q_HALF, &tm_w0, &s->q_full[st], col, w_row);
+                            tma_load_2d(dst + hf * Q_HALF + (BN / 2) * 16, &tm_w1, &s->q_full[st], col, w_row);
+                        } else {
+                            tma_load_2d(dst + hf * Q_HALF, &tm_w0, &s->q_full[st], col, w_row);
+                        }
                     }
                     ++qit;
                 }
@@ -306,15 +335,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------------- MMA
         if (lane == 0) {
-            uint32_t ait = 0, bit = 0, local = 0;
+            uint32_t ait = 0, bit = 0;
+            uint32_t uses[TPU] = {0, 0};
             bool ok = true;
             const uint32_t idesc = idesc_bf16(BM, nb);
-            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++local) {
-                const uint32_t acc = local & 1;
-                ok = wait_or_abort(&s->acc_empty[acc], ((local >> 1) & 1) ^ 1, a, s, 5);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * 256;
+            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+                const Unit t = load_unit<MODE>(a, u);
                 for (int ks = 0; ks < ksteps; ++ks) {
                     const int as = ait % NS_A, bs = bit % NS_B;
                     ok = wait_or_abort(&s->a_full[as], (ait / NS_A) & 1, a, s, 6) &&
@@ -323,17 +349,29 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sA + as * A_STAGE);
                     const uint32_t b_addr = smem_u32(sB + bs * B_STAGE);
+                    for (int i = 0; i < t.ntiles; ++i) {
+                        if (ks == 0) {
+                            // this accumulator's previous contents have been drained
+                            ok = wait_or_abort(&s->acc_empty[i], (uses[i] & 1) ^ 1, a, s, 5);
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        const uint32_t d_tmem = tmem_base + i * 256;
+                        const uint32_t ai = a_addr + i * TILE_A;
 #pragma unroll
-                    for (int kk = 0; kk < GK / 16; ++kk)
-                        umma_bf16(d_tmem, sdesc_k128(a_addr + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
-                                  (ks | kk) != 0);
+                        for (int kk = 0; kk < GK / 16; ++kk)
+                            umma_bf16(d_tmem, sdesc_k128(ai + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
+                                      (ks | kk) != 0);
+                        if (ks == ksteps - 1) umma_commit(&s->acc_full[i]);
+                    }
+                    if (!ok) break;
                     umma_commit(&s->a_empty[as]);
                     umma_commit(&s->b_empty[bs]);
                     ++ait;
                     ++bit;
                 }
                 if (!ok) break;
-                umma_commit(&s->acc_full[acc]);
+                for (int i = 0; i < t.ntiles; ++i) ++uses[i];
             }
             // every MMA issued by this thread has finished before tensor memory is freed
             umma_commit(&s->drain);
@@ -342,7 +380,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
     } else if (warp >= kDeqWarp0 && MODE != 2) {
         // ---------------------------------------------------------- dequantise
-        const int r = tid - kDeqWarp0 * 32;  // weight row of the tile, 0..255
+        const int dt = tid - kDeqWarp0 * 32;
+        const int hf = dt / BN;  // 32-element half of the stage
+        const int r = dt % BN;   // weight row of the tile
         uint32_t bit = 0, qit = 0, sit = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
@@ -356,23 +396,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 ok = wait_or_abort(&s->q_full[qs], (qit / NS_Q) & 1, a, s, 9) &&
                      wait_or_abort(&s->b_empty[bs], ((bit / NS_B) & 1) ^ 1, a, s, 10);
                 if (!ok) break;
-                const uint4 n0 = *reinterpret_cast<const uint4 *>(sQ + qs * Q_STAGE + r * 32);
-                const uint4 n1 = *reinterpret_cast<const uint4 *>(sQ + qs * Q_STAGE + r * 32 + 16);
+                const uint4 nib = *reinterpret_cast<const uint4 *>(sQ + qs * Q_STAGE + hf * Q_HALF + r * 16);
                 const uint16_t *sblk = reinterpret_cast<const uint16_t *>(sS + ss * S_STAGE) + r * SG;
                 const uint16_t *bblk = sblk + BN * SG;  // bias block: 4096 bytes after the scales
-                // element groups of the two 32-element halves of this stage
-                const int gl0 = ((ks * GK) / a.G) % SG;
-                const int gl1 = ((ks * GK + 32) / a.G) % SG;
-                const __nv_bfloat162 s0 = u32_as_bf162(static_cast<uint32_t>(sblk[gl0]) * 0x10001u);
-                const __nv_bfloat162 b0 = u32_as_bf162(static_cast<uint32_t>(bblk[gl0]) * 0x10001u);
-                const __nv_bfloat162 s1 = u32_as_bf162(static_cast<uint32_t>(sblk[gl1]) * 0x10001u);
-                const __nv_bfloat162 b1 = u32_as_bf162(static_cast<uint32_t>(bblk[gl1]) * 0x10001u);
+                const int gl = ((ks * GK + hf * 32) / a.G) % SG;
+                const __nv_bfloat162 s2 = u32_as_bf162(static_cast<uint32_t>(sblk[gl]) * 0x10001u);
+                const __nv_bfloat162 b2 = u32_as_bf162(static_cast<uint32_t>(bblk[gl]) * 0x10001u);
                 uint8_t *brow = sB + bs * B_STAGE + r * 128;
-                const uint32_t words[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+                const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
 #pragma unroll
-                for (int w = 0; w < 8; ++w) {
-                    const uint4 out = dequant8_bf16(words[w], w < 4 ? s0 : s1, w < 4 ? b0 : b1);
-                    *reinterpret_cast<uint4 *>(brow + ((w ^ (r & 7)) << 4)) = out;
+                for (int w = 0; w < 4; ++w) {
+                    const uint4 out = dequant8_bf16(words[w], s2, b2);
+                    *reinterpret_cast<uint4 *>(brow + (((hf * 4 + w) ^ (r & 7)) << 4)) = out;
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -388,84 +423,90 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 }
             }
         }
-    } else if (warp < 4) {
+    } else if (warp < kEpiWarps) {
         // ------------------------------------------------------------ epilogue
-        const int quarter = warp - kEpiWarp0;
-        const int rr = quarter * 32 + lane;  // token row of the tile
-        float *tbuf = reinterpret_cast<float *>(base + map.t) + quarter * 32 * T_PITCH;
-        uint32_t local = 0;
+        const int quarter = warp & 3;      // TMEM lane quarter = token rows 32*quarter..
+        const int chalf = warp >> 2;       // this warp's 16-column chunks: chalf, chalf + 2, ...
+        float *tbuf = reinterpret_cast<float *>(base + map.t) + warp * 32 * T_PITCH;
+        uint32_t uses[TPU] = {0, 0};
         bool ok = true;
-        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x, ++local) {
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
             const Unit t = load_unit<MODE>(a, u);
-            const uint32_t acc = local & 1;
-            const bool valid = rr < t.n;
-            int tok = 0;
-            float wgt = 0.f;
-            if (MODE == 1 && valid) {
-                tok = a.rb.row_token[t.row0 + rr];
-                wgt = a.rb.row_weight[t.row0 + rr];
+            for (int i = 0; i < t.ntiles; ++i) {
+                const int rr = i * BM + quarter * 32 + lane;  // row of the unit
+                const bool valid = rr < t.n;
+                int tok = 0;
+                float wgt = 0.f;
+                if (MODE == 1 && valid) {
+                    tok = a.rb.row_token[t.row0 + rr];
+                    wgt = a.rb.row_weight[t.row0 + rr];
+                }
+                ok = wait_or_abort(&s->acc_full[i], uses[i] & 1, a, s, 11);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + i * 256;
+                if (MODE == 0) {
+                    __nv_bfloat16 *hrow = a.h + static_cast<int64_t>(t.row0 + rr) * a.I + t.nt * (BN / 2);
+                    for (int c0 = chalf * 16; c0 < BN / 2; c0 += 32) {
+                        float g[16], up[16];
+                        tmem_ld16(tbase + c0, g);
+                        tmem_ld16(tbase + BN / 2 + c0, up);
+                        uint32_t o[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float h0 = __fdividef(g[2 * j], 1.0f + __expf(-g[2 * j])) * up[2 * j];
+                            const float h1 =
+                                __fdividef(g[2 * j + 1], 1.0f + __expf(-g[2 * j + 1])) * up[2 * j + 1];
+                            o[j] = bf162_as_u32(__floats2bfloat162_rn(h0, h1));
+                        }
+                        if (valid) {
+                            uint4 *dst = reinterpret_cast<uint4 *>(hrow + c0);
+                            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+                        }
+                    }
+                } else if (MODE == 1) {
+                    const int f0 = t.nt * BN;
+                    for (int c0 = chalf * 16; c0 < BN; c0 += 32) {
+                        float v[16];
+                        tmem_ld16(tbase + c0, v);
+#pragma unroll
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<float4 *>(tbuf + lane * T_PITCH + j) =
+                                make_float4(wgt * v[j], wgt * v[j + 1], wgt * v[j + 2], wgt * v[j + 3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int src = 8 * q + lane / 4;  // row of the warp whose values this lane adds
+                            const int tk = __shfl_sync(0xffffffffu, tok, src);
+                            const bool vv = __shfl_sync(0xffffffffu, valid, src);
+                            const float4 val =
+                                *reinterpret_cast<const float4 *>(tbuf + src * T_PITCH + 4 * (lane % 4));
+                            if (vv)
+                                red_add_v4(a.y_acc + static_cast<int64_t>(tk) * a.H + f0 + c0 + 4 * (lane % 4), val);
+                        }
+                        __syncwarp();
+                    }
+                } else {
+                    float *lrow = a.logits_part +
+                                  (static_cast<int64_t>(t.part * 2 + t.khalf) * a.T + t.row0 + rr) * a.E_pad16;
+                    for (int c0 = chalf * 16; c0 < nb; c0 += 32) {
+                        float v[16];
+                        tmem_ld16(tbase + c0, v);
+                        if (valid) {
+                            float4 *dst = reinterpret_cast<float4 *>(lrow + c0);
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s->acc_empty[i]);
+                ++uses[i];
             }
-            ok = wait_or_abort(&s->acc_full[acc], (local >> 1) & 1, a, s, 11);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * 256;
-            if (MODE == 0) {
-                __nv_bfloat16 *hrow = a.h + static_cast<int64_t>(t.row0 + rr) * a.I + t.nt * (BN / 2);
-                for (int c0 = 0; c0 < BN / 2; c0 += 16) {
-                    float g[16], up[16];
-                    tmem_ld16(tbase + c0, g);
-                    tmem_ld16(tbase + BN / 2 + c0, up);
-                    uint32_t o[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const float h0 = __fdividef(g[2 * j], 1.0f + __expf(-g[2 * j])) * up[2 * j];
-                        const float h1 = __fdividef(g[2 * j + 1], 1.0f + __expf(-g[2 * j + 1])) * up[2 * j + 1];
-                        o[j] = bf162_as_u32(__floats2bfloat162_rn(h0, h1));
-                    }
-                    if (valid) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(hrow + c0);
-                        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-                    }
-                }
-            } else if (MODE == 1) {
-                const int f0 = t.nt * BN;
-                for (int c0 = 0; c0 < BN; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(tbase + c0, v);
-#pragma unroll
-                    for (int j = 0; j < 16; j += 4)
-                        *reinterpret_cast<float4 *>(tbuf + lane * T_PITCH + j) =
-                            make_float4(wgt * v[j], wgt * v[j + 1], wgt * v[j + 2], wgt * v[j + 3]);
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int src = 8 * i + lane / 4;  // row of the warp whose values this lane adds
-                        const int tk = __shfl_sync(0xffffffffu, tok, src);
-                        const bool vv = __shfl_sync(0xffffffffu, valid, src);
-                        const float4 val = *reinterpret_cast<const float4 *>(tbuf + src * T_PITCH + 4 * (lane % 4));
-                        if (vv) red_add_v4(a.y_acc + static_cast<int64_t>(tk) * a.H + f0 + c0 + 4 * (lane % 4), val);
-                    }
-                    __syncwarp();
-                }
-            } else {
-                float *lrow = a.logits_part + (static_cast<int64_t>(t.part * 2 + t.khalf) * a.T + t.row0 + rr) *
-                                                  a.E_pad16;
-                for (int c0 = 0; c0 < nb; c0 += 16) {
-                    float v[16];
-                    tmem_ld16(tbase + c0, v);
-                    if (valid) {
-                        float4 *dst = reinterpret_cast<float4 *>(lrow + c0);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s->acc_empty[acc]);
         }
     }
 
@@ -533,7 +574,7 @@ cudaError_t launch_gemm(int mode, const GemmMaps &m, const GemmArgs &a, int grid
     return launch_gemm_t<2>(m, a, grid, s);
 }
 
-int router_units(int T) { return kRouterUnits * ((T + BM - 1) / BM); }
+int router_units(int T) { return kRouterUnits * ((T + TPU * BM - 1) / (TPU * BM)); }
 
 cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 *wr2, float *y_acc, int64_t y_elems,
                         int *counts_blk, int64_t n_counts, int num_sms, cudaStream_t s) {

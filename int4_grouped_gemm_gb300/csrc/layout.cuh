@@ -36,7 +36,7 @@ struct RoutingBufs {
     int *tile_row;
     int *tile_rows;
     int *tile_sched;
-    int *num_tiles;     // [1]
+    int *num_tiles;     // [2]: tiles, work units (pairs of tiles)
     int max_tiles;
     int nblk;
 };
@@ -82,7 +82,7 @@ inline PrefillLayout prefill_layout(int T, int E, int k, int H, int I) {
     L.tile_row = take(sizeof(int) * (size_t)L.max_tiles);
     L.tile_rows = take(sizeof(int) * (size_t)L.max_tiles);
     L.tile_sched = take(sizeof(int) * (size_t)L.max_tiles);
-    L.num_tiles = take(sizeof(int));
+    L.num_tiles = take(2 * sizeof(int));
     L.h = take(sizeof(uint16_t) * (size_t)L.R * I);
     L.y_acc = take(sizeof(float) * (size_t)T * H);
     L.E_pad16 = (E + 15) / 16 * 16;

@@ -199,23 +199,32 @@ __global__ void __launch_bounds__(512) scan_tiles_kernel(int T, int E, int k, in
     }
     if (g == 0) rb.num_tiles[0] = total_tiles;
 
-    // Launch order: full tiles in canonical order, then each group's partial
-    // tile by row count descending (ties: lower group first).
-    const int full = cnt / kTileRows;
-    const int part_rows = cnt % kTileRows;
+    // Work units of the grouped GEMMs: a group's tiles in pairs (0-1, 2-3,
+    // ...; the last one alone when the count is odd); tile_sched holds each
+    // unit's first tile.  Launch order: units of 2 full tiles in canonical
+    // order, then each group's last, smaller unit by row count descending
+    // (ties: lower group first).
+    constexpr int kUnitRows = 2 * kTileRows;
+    const int full = cnt / kUnitRows;
+    const int part_rows = cnt % kUnitRows;
     int fbase = 0;
     const int total_full = block_exclusive_scan_512(full, &fbase, warp_tot);
-    for (int i = 0; i < full; ++i) rb.tile_sched[fbase + i] = tbase + i;
-    s_key[g] = part_rows;  // 0 = no partial tile
+    for (int i = 0; i < full; ++i) rb.tile_sched[fbase + i] = tbase + 2 * i;
+    s_key[g] = part_rows;  // 0 = no smaller unit
     __syncthreads();
+    int nparts = 0;
     if (part_rows > 0) {
         int rank = 0;
         for (int o = 0; o < G; ++o) {
             const int ko = s_key[o];
             rank += (ko > part_rows) || (ko == part_rows && o < g);
         }
-        rb.tile_sched[total_full + rank] = tbase + full;
+        rb.tile_sched[total_full + rank] = tbase + 2 * full;
+        nparts = 1;
     }
+    int pbase = 0;
+    const int total_parts = block_exclusive_scan_512(nparts, &pbase, warp_tot);
+    if (g == 0) rb.num_tiles[1] = total_full + total_parts;
 }
 
 // ------------------------------------------------------------- permutation

@@ -109,7 +109,7 @@ class Workspace:
         v = _lib.moe_routing_views_for(desc, T)
         E, k = desc.E, desc.k
         ng = E + desc.has_shared
-        n_tiles = int(self.view(v.num_tiles, torch.int32, 1).item())
+        n_tiles, n_units = (int(c) for c in self.view(v.num_tiles, torch.int32, 2).tolist())
         return dict(
             logits=self.view(v.logits, torch.float32, T * E).view(T, E),
             topk_idx=self.view(v.topk_idx, torch.int32, T * k).view(T, k),
@@ -121,7 +121,7 @@ class Workspace:
             tile_group=self.view(v.tile_group, torch.int32, n_tiles),
             tile_row=self.view(v.tile_row, torch.int32, n_tiles),
             tile_rows=self.view(v.tile_rows, torch.int32, n_tiles),
-            tile_sched=self.view(v.tile_sched, torch.int32, n_tiles),
+            tile_sched=self.view(v.tile_sched, torch.int32, n_units),
             tile_size=v.tile_size,
             xperm=self.view(v.xperm, torch.bfloat16, T * k * desc.H).view(T * k, desc.H),
             h=self.view(v.h, torch.bfloat16, (T * k + T) * desc.I).view(T * k + T, desc.I),

@@ -13,10 +13,20 @@ pytestmark = pytest.mark.gpu
 
 
 def expected_schedule(tg, tr, tn, BN):
-    full = [i for i in range(len(tg)) if tn[i] == BN]
-    part = [i for i in range(len(tg)) if tn[i] < BN]
-    part.sort(key=lambda i: (-tn[i], tg[i]))
-    return np.array(full + part, np.int32)
+    """Grouped-GEMM work units: each group's tiles in pairs (the last alone
+    if odd), given by their first tile; units of two full tiles first in
+    canonical order, then the rest by rows descending (ties: lower group)."""
+    units = []
+    first = {}
+    for i, g in enumerate(tg):
+        first.setdefault(g, i)
+    for i, g in enumerate(tg):
+        if (i - first[g]) % 2 == 0:
+            rows = tn[i] + (tn[i + 1] if i + 1 < len(tg) and tg[i + 1] == g else 0)
+            units.append((i, g, rows))
+    full = [u for u in units if u[2] == 2 * BN]
+    part = sorted([u for u in units if u[2] < 2 * BN], key=lambda u: (-u[2], u[1]))
+    return np.array([u[0] for u in full + part], np.int32)
 
 
 def run_case(T, E, k, shared, kind, seed):
