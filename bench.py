@@ -34,7 +34,7 @@ METRIC = "MoE-layer prefill tok/s @T=4096; batch-1 decode tok/s; % of roofline"
 PREFILL_CFG = "prefill4096"
 DECODE_CFG = "decode40"
 KERNELS_PER_PREFILL = 9      # prep, router GEMM, top-k, scan, permute, x copy, gate/up GEMM, down GEMM, convert
-KERNELS_PER_DECODE_LAYER = 3  # router+top-k, gate/up GEMV, down GEMV + combine
+DECODE_LAYERS_PER_KERNEL = 64  # one persistent decode kernel runs up to 64 layers of a step
 
 
 def parse():
@@ -350,7 +350,7 @@ def run_decode(args, pk):
     return dict(tok_s=1000.0 / ms, ms_per_step=ms, steps=steps, layers=cfg.layers,
                 roofline={"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                           "frac": round(gbs / pk["hbm"], 4), "bytes_per_step": bytes_step},
-                clocks=clk.summary(), launches=KERNELS_PER_DECODE_LAYER * cfg.layers * steps)
+                clocks=clk.summary(), launches=-(-cfg.layers // DECODE_LAYERS_PER_KERNEL) * steps)
 
 
 # ------------------------------------------------------------ CPU oracle

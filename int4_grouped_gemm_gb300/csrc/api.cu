@@ -335,36 +335,58 @@ static int decode_check(const moe_layer_desc *desc) {
     return MOE_OK;
 }
 
-static DecodeArgs decode_args(const moe_layer_desc *desc, const void *x, void *y, char *w, const DecodeLayout &L) {
-    DecodeArgs a{};
+static DecodeLayerPtrs decode_ptrs(const moe_layer_desc &d) {
+    DecodeLayerPtrs P{};
+    P.Wr = d.router_w;
+    P.bias = d.router_bias;
+    P.qg = d.gate.q;
+    P.qu = d.up.q;
+    P.qd = d.down.q;
+    P.sg = d.gate.scale;
+    P.bg = d.gate.bias;
+    P.su = d.up.scale;
+    P.bu = d.up.bias;
+    P.sd = d.down.scale;
+    P.bd = d.down.bias;
+    return P;
+}
+
+// Launches of the decode kernel for layers [0, n) of a stack whose layers
+// share d0's shape; the workspace holds the layout L.  Each launch clears the
+// grid-barrier counter and abort flag first.
+static int decode_run(const moe_layer_desc *descs, int n, const void *x, void *y, char *w, const DecodeLayout &L,
+                      int num_sms, cudaStream_t stream) {
+    const moe_layer_desc &d0 = descs[0];
+    DecodeStack a{};
+    a.E = d0.E;
+    a.k = d0.k;
+    a.H = d0.H;
+    a.I = d0.I;
+    a.G = d0.group;
+    a.has_shared = d0.has_shared;
+    a.ldg_h = ld_groups(d0.H, d0.group);
+    a.ldg_i = ld_groups(d0.I, d0.group);
+    a.n_total = n;
     a.x = static_cast<const __nv_bfloat16 *>(x);
     a.y = static_cast<__nv_bfloat16 *>(y);
-    a.Wr = desc->router_w;
-    a.bias = desc->router_bias;
-    a.qg = desc->gate.q;
-    a.qu = desc->up.q;
-    a.qd = desc->down.q;
-    a.sg = desc->gate.scale;
-    a.bg = desc->gate.bias;
-    a.su = desc->up.scale;
-    a.bu = desc->up.bias;
-    a.sd = desc->down.scale;
-    a.bd = desc->down.bias;
-    a.E = desc->E;
-    a.k = desc->k;
-    a.H = desc->H;
-    a.I = desc->I;
-    a.G = desc->group;
-    a.has_shared = desc->has_shared;
-    a.ldg_h = ld_groups(desc->H, desc->group);
-    a.ldg_i = ld_groups(desc->I, desc->group);
-    a.ctrl = reinterpret_cast<Ctrl *>(w + L.ctrl);
-    a.logits = reinterpret_cast<float *>(w + L.logits);
+    a.act = n > 1 ? reinterpret_cast<__nv_bfloat16 *>(w + L.act) : nullptr;
+    Ctrl *ctrl = reinterpret_cast<Ctrl *>(w + L.ctrl);
+    a.ctrl = ctrl;
+    a.logits_part = reinterpret_cast<float *>(w + L.logits);
     a.topk_idx = reinterpret_cast<int *>(w + L.topk_idx);
     a.topk_w = reinterpret_cast<float *>(w + L.topk_w);
     a.h = reinterpret_cast<float *>(w + L.h);
-    a.next_Wr = nullptr;
-    return a;
+    a.wait_limit = g_wait_limit;
+    for (int l0 = 0; l0 < n; l0 += kMaxStackLayers) {
+        const int nl = n - l0 < kMaxStackLayers ? n - l0 : kMaxStackLayers;
+        a.l0 = l0;
+        a.n_layers = nl;
+        for (int i = 0; i < nl; ++i) a.L[i] = decode_ptrs(descs[l0 + i]);
+        a.next_Wr = l0 + nl < n ? descs[l0 + nl].router_w : nullptr;
+        if (cudaMemsetAsync(&ctrl->bar, 0, 2 * sizeof(unsigned), stream) != cudaSuccess) return MOE_ERR_CUDA;
+        if (launch_decode(a, num_sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
 }
 
 int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, size_t ws_bytes, cudaStream_t stream) {
@@ -375,7 +397,7 @@ int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, siz
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     DeviceInfo *dev = nullptr;
     if ((rc = current_device(dev))) return rc;
-    return cuda_rc(launch_decode(decode_args(desc, x, y, static_cast<char *>(ws), L), stream));
+    return decode_run(desc, 1, x, y, static_cast<char *>(ws), L, dev->num_sms, stream);
 }
 
 int moe_decode_layers(const moe_layer_desc *descs, int32_t n_layers, const void *x, void *y, void *ws,
@@ -396,16 +418,7 @@ int moe_decode_layers(const moe_layer_desc *descs, int32_t n_layers, const void 
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     DeviceInfo *dev = nullptr;
     if ((rc = current_device(dev))) return rc;
-    char *w = static_cast<char *>(ws);
-    __nv_bfloat16 *act = reinterpret_cast<__nv_bfloat16 *>(w + L.act);
-    for (int l = 0; l < n_layers; ++l) {
-        const void *in = l == 0 ? x : static_cast<const void *>(act + ((l - 1) % 2) * d0.H);
-        void *out = l == n_layers - 1 ? y : static_cast<void *>(act + (l % 2) * d0.H);
-        DecodeArgs a = decode_args(&descs[l], in, out, w, L);
-        if (l + 1 < n_layers) a.next_Wr = descs[l + 1].router_w;
-        if (launch_decode(a, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    }
-    return MOE_OK;
+    return decode_run(descs, n_layers, x, y, static_cast<char *>(ws), L, dev->num_sms, stream);
 }
 
 int pack_int4(const float *w, int64_t rows, int32_t K, int32_t group, uint32_t *q, uint16_t *scale,
@@ -488,10 +501,11 @@ int moe_decode_static_scratch(const moe_layer_desc *desc, const void *x, void *y
     if ((rc = current_device(dev))) return rc;
     char *w = nullptr;
     if ((rc = static_scratch(w))) return rc;
-    // The top-k ticket must start at zero; a call that gave up part way may
-    // have left it set.  Logits, top-k and h are written before they are read.
+    // The control block's counters must start at zero; a call that gave up
+    // part way may have left them set.  Logits, top-k and h are written
+    // before they are read.
     if (cudaMemsetAsync(w + L.ctrl, 0, kCtrlBytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    return cuda_rc(launch_decode(decode_args(desc, x, y, w, L), stream));
+    return decode_run(desc, 1, x, y, w, L, dev->num_sms, stream);
 }
 
 }  // extern "C"

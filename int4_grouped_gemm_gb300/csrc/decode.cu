@@ -7,24 +7,32 @@
 // ("Optimized Decode"): kernel chains are fused, the next step's input stays
 // on the GPU, intermediates stay close.
 //
-// Three kernels per layer, chained with programmatic dependent launch so that
-// each one starts while its predecessor drains and loads every weight that
-// does not depend on the predecessor's result before it waits:
-//   decode_k1_kernel   router logits (2 experts per block, 4 warps each) with
-//                      the last block doing top-k and the weights; the shared
-//                      expert's gate/up rows (it needs no routing) in the
-//                      same grid
-//   decode_k2_kernel   gate/up rows of the k routed experts, h = silu(g) * u;
-//                      also prefetches those experts' down rows into L2
-//   decode_k3_kernel   one warp per output feature over all k+1 experts'
-//                      down rows, weighted combine fused, bf16 out; prefetches
-//                      the next layer's router into L2
-// Only the router and the k+1 touched experts are read.  The int4 dot
+// One persistent kernel runs a whole stack of layers (one block per SM,
+// launched cooperatively so that every block is resident).  Each layer is
+// three phases separated by grid barriers (a counter in the workspace,
+// bounded waits):
+//   A  router partial sums over K quarters (one warp per expert and quarter)
+//      and the shared expert's gate/up rows (one warp per feature; it needs
+//      no routing); every block stages the layer input in shared memory
+//   B  every block computes the same top-k from the partial sums, prefetches
+//      its share of the picked experts' down rows into L2, then the gate/up
+//      rows of the k routed experts: a block owns a contiguous range of
+//      (slot, feature) pairs, its warps take K quarters, h = silu(g) * u
+//   C  one warp per output feature over the down rows of all k + 1 experts,
+//      weighted combine fused, bf16 out; the next layer's router and shared
+//      expert are prefetched into L2 meanwhile
+// Loads that do not depend on the previous phase (router rows, shared rows,
+// down rows) are issued before the barrier wait, so their latency overlaps
+// it.  Only the router and the k + 1 touched experts are read.  The int4 dot
 // products use sum_i x_i (s q_i + b) = s sum_i x_i q_i + b sum_i x_i per
 // 8-element word, with the per-word input sums computed once per block.
 #include "kernels.cuh"
 
 namespace moe {
+
+constexpr int kDecThreads = 512;
+constexpr int kDecWarps = kDecThreads / 32;
+constexpr int kMaxSlots = 9;        // k <= 8 routed + 1 shared
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -32,444 +40,556 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
-
 __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
     // bulk prefetch needs 16-byte alignment and a multiple of 16 bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// Prefetch [p, p + bytes) into L2 in pieces of at most 64 KB (the range is
-// 16-byte aligned and a multiple of 16 bytes).
-__device__ __forceinline__ void prefetch_range(const void *p, size_t bytes) {
-    const char *c = static_cast<const char *>(p);
-    while (bytes > 0) {
-        const uint32_t n = bytes > 65536 ? 65536u : static_cast<uint32_t>(bytes);
-        prefetch_l2(c, n);
-        c += n;
-        bytes -= n;
+// Slice `part` of `parts` of [p, p + bytes) into L2 (16-byte granules, at
+// most 64 KB per instruction); p is 16-byte aligned.
+__device__ __forceinline__ void prefetch_slice(const void *p, size_t bytes, int part, int parts) {
+    const size_t granules = bytes / 16;
+    const size_t per = (granules + parts - 1) / parts;
+    size_t g0 = per * part, g1 = g0 + per;
+    if (g1 > granules) g1 = granules;
+    const char *c = static_cast<const char *>(p) + g0 * 16;
+    while (g0 < g1) {
+        const size_t n = (g1 - g0) > 4096 ? 4096 : (g1 - g0);
+        prefetch_l2(c, static_cast<uint32_t>(n * 16));
+        c += n * 16;
+        g0 += n;
     }
 }
 
-// 8 int4 codes -> sum_i x_i * q_i (x from shared memory, fp32).
-__device__ __forceinline__ float dot8_codes(uint32_t word, const float *xv) {
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid barrier, split into arrive and wait so that independent loads can be
+// issued in between.  The counter only grows within a launch (reset to 0
+// before it); barrier number n completes at (n + 1) * gridDim.x arrivals.
+__device__ __forceinline__ void grid_arrive(Ctrl *c) {
+    __syncthreads();  // every thread of the block has written its results
+    if (threadIdx.x == 0) {
+        // release: the block's writes, ordered before this by the barrier,
+        // are visible to whoever observes the new count
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(&c->bar) : "memory");
+    }
+}
+
+__device__ __forceinline__ bool grid_wait(Ctrl *c, unsigned target, long long limit, int site, int *s_ok) {
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        if (ld_acquire(&c->bar) < target) {
+            const long long t0 = clock64();
+            while (ld_acquire(&c->bar) < target) {
+                if (*reinterpret_cast<volatile int *>(&c->abort)) {
+                    ok = 0;
+                    break;
+                }
+                if (clock64() - t0 > limit) {
+                    record_status(&c->status, MOE_ERR_TIMEOUT - site);
+                    *reinterpret_cast<volatile int *>(&c->abort) = 1;
+                    ok = 0;
+                    break;
+                }
+            }
+        }
+        *s_ok = ok;
+    }
+    __syncthreads();
+    return *s_ok != 0;
+}
+
+// 8 int4 codes -> sum_i x_i * (128 + q_i) (x: 8 consecutive fp32 in shared
+// memory, 16-byte aligned).  Codes j and j + 4 are lifted together into the
+// two bf16 halves of one register as 128 + q (exact), and each half widens to
+// fp32 with one shift or mask; callers subtract 128 * sum_i x_i (folded into
+// the bias term).  Two accumulators halve the dependent FMA chain.
+__device__ __forceinline__ float dot8_codes128(uint32_t word, const float *xv) {
+    const float4 x0 = *reinterpret_cast<const float4 *>(xv);
+    const float4 x1 = *reinterpret_cast<const float4 *>(xv + 4);
+    const float xl[4] = {x0.x, x0.y, x0.z, x0.w}, xh[4] = {x1.x, x1.y, x1.z, x1.w};
+    float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const uint32_t p = ((word >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
+        acc0 = fmaf(xl[j], __uint_as_float(p << 16), acc0);
+        acc1 = fmaf(xh[j], __uint_as_float(p & 0xFFFF0000u), acc1);
+    }
+    return acc0 + acc1;
+}
+
+// Shared-memory position of element k of a staged vector: four padding
+// floats after every 32 elements.  Blocks of 32 consecutive elements stay
+// contiguous and 16-byte aligned, and lanes reading blocks one apart start
+// four banks apart, so eight lanes' 16-byte reads never collide.
+__device__ __forceinline__ int vpos(int k) { return k + ((k >> 5) << 2); }
+__host__ __device__ constexpr int vlen(int n) { return n + n / 8; }  // padded length (n % 32 == 0)
+
+// Layer input to shared memory as fp32 (padded positions) plus the sum of
+// every 8-element word; it was written by other blocks, so it is read from L2.
+__device__ __forceinline__ void stage_x(const __nv_bfloat16 *x, int H, float *xs, float *xsum8) {
+    const int nw = H / 8;
+    for (int w = threadIdx.x; w < nw; w += blockDim.x) {
+        const uint4 raw = __ldcg(reinterpret_cast<const uint4 *>(x) + w);
+        const uint32_t p[4] = {raw.x, raw.y, raw.z, raw.w};
+        float sum = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const __nv_bfloat162 v = u32_as_bf162(p[i]);
+            const float lo = __low2float(v), hi = __high2float(v);
+            xs[vpos(w * 8) + 2 * i] = lo;  // the 8 elements of a word never straddle a pad
+            xs[vpos(w * 8) + 2 * i + 1] = hi;
+            sum += lo + hi;
+        }
+        xsum8[w] = sum;
+    }
+}
+
+// ------------------------------------------------------------ phase A parts
+
+// Register arrays are sized for the largest hidden size a kernel instance
+// serves (HMAX = 2048 or 4096): router quarter float4 per lane HMAX / 512,
+// packed-row uint4 per lane HMAX / 1024, K-quarter words per lane HMAX / 1024.
+// One register buffer holds either a router quarter (float4 per lane) or a
+// shared-expert gate/up row pair (uint4 per lane): both take HMAX / 512.
+template <int HMAX>
+struct UnitRegs {
+    static constexpr int V = HMAX / 512;
+    uint4 r[V];
+    uint16_t sb[V * 2];  // shared rows: scale and bias of each 32-element span (gate, up)
+};
+
+template <int HMAX>
+__device__ __forceinline__ void router_load(const DecodeStack &a, const float *Wr, int unit, int lane,
+                                            UnitRegs<HMAX> &r) {
+    constexpr int kMaxRouterVec = UnitRegs<HMAX>::V;
+    const int e = unit >> 2, q = unit & 3;
+    const int span = a.H / 4;
+    const float *wrow = Wr + static_cast<int64_t>(e) * a.H + q * span;
+#pragma unroll
+    for (int v = 0; v < kMaxRouterVec; ++v) {
+        const int c = lane * 4 + v * 128;
+        r.r[v] = c < span ? __ldg(reinterpret_cast<const uint4 *>(wrow + c)) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+template <int HMAX>
+__device__ __forceinline__ float router_dot(const DecodeStack &a, int unit, int lane, const UnitRegs<HMAX> &r,
+                                            const float *xs) {
+    constexpr int kMaxRouterVec = UnitRegs<HMAX>::V;
+    const int q = unit & 3;
+    const int span = a.H / 4;
     float acc = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float q = __uint_as_float(((word >> (4 * i)) & 0xFu) | 0x4B000000u) - 8388608.0f;
-        acc = fmaf(xv[i], q, acc);
+    for (int v = 0; v < kMaxRouterVec; ++v) {
+        const int c = lane * 4 + v * 128;
+        if (c < span) {
+            const float *xv = xs + vpos(q * span + c);  // 4 elements never straddle a pad
+            acc = fmaf(__uint_as_float(r.r[v].x), xv[0], acc);
+            acc = fmaf(__uint_as_float(r.r[v].y), xv[1], acc);
+            acc = fmaf(__uint_as_float(r.r[v].z), xv[2], acc);
+            acc = fmaf(__uint_as_float(r.r[v].w), xv[3], acc);
+        }
     }
     return acc;
 }
 
-// Shared-memory positions of the staged vectors.  Lane l of a warp reads the
-// elements 32l.. of x (gate/up rows) or 16l.. of h (down rows); one padding
-// float after every 32 (x) or 16 (h) elements puts those lanes on different
-// banks.  Blocks of 8 (x) or 16 (h) consecutive elements stay contiguous.
-__device__ __forceinline__ int xpos(int k) { return k + (k >> 5); }
-__device__ __forceinline__ int hpos(int k) { return k + (k >> 4); }
+// One gate/up row pair of the shared expert in registers: lane holds words
+// lane*4 .. lane*4+3 of every 128-word span of each row (16-byte loads).
 
-// Input vector to shared memory as fp32 (padded positions), plus the sum of
-// every 8-element word: one 16-byte load per word, all issued before any is
-// used.
-__device__ __forceinline__ void stage_x(const __nv_bfloat16 *x, int H, float *xs, float *xsum8) {
-    constexpr int U = kDecodeMaxH / 8 / 256;  // words per thread with 256 threads
-    const int nw = H / 8;
-    uint4 raw[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int w = threadIdx.x + u * blockDim.x;
-        if (w < nw) raw[u] = *reinterpret_cast<const uint4 *>(x + w * 8);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int w = threadIdx.x + u * blockDim.x;
-        if (w < nw) {
-            const uint32_t p[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
-            float sum = 0.f;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const __nv_bfloat162 v = u32_as_bf162(p[i]);
-                const float lo = __low2float(v), hi = __high2float(v);
-                xs[xpos(w * 8) + 2 * i] = lo;
-                xs[xpos(w * 8) + 2 * i + 1] = hi;
-                sum += lo + hi;
-            }
-            xsum8[w] = sum;
-        }
-    }
-    __syncthreads();
-}
-
-// One gate/up row pair in registers: lane holds words lane*4 .. lane*4+3 of
-// every 128-word span of each row (16-byte loads).
-constexpr int kMaxRowVec = kDecodeMaxH / 1024;
-
-struct RowPair {
-    uint4 g[kMaxRowVec], u[kMaxRowVec];
-};
-
-__device__ __forceinline__ void load_row_pair(const DecodeArgs &a, int64_t row, int lane, RowPair &rp) {
+template <int HMAX>
+__device__ __forceinline__ void row_pair_load(const DecodeStack &a, const DecodeLayerPtrs &P, int64_t row, int lane,
+                                              UnitRegs<HMAX> &rp) {
+    constexpr int kMaxRowVec = UnitRegs<HMAX>::V / 2;  // gate words in r[0..V/2), up words in r[V/2..V)
     const int nwords = a.H / 8;
-    const uint32_t *qg = a.qg + row * nwords;
-    const uint32_t *qu = a.qu + row * nwords;
+    const uint32_t *qg = P.qg + row * nwords;
+    const uint32_t *qu = P.qu + row * nwords;
 #pragma unroll
     for (int v = 0; v < kMaxRowVec; ++v) {
         const int w0 = lane * 4 + v * 128;
         if (w0 < nwords) {
-            rp.g[v] = *reinterpret_cast<const uint4 *>(qg + w0);
-            rp.u[v] = *reinterpret_cast<const uint4 *>(qu + w0);
-        }
-    }
-}
-
-// gate and up dot products of one row pair whose words are already loaded
-__device__ __forceinline__ void gate_up_dot(const DecodeArgs &a, int64_t row, int lane, const RowPair &rp,
-                                           const float *xs, const float *xsum8, float &gacc, float &uacc) {
-    const int nwords = a.H / 8;
-    const uint16_t *sg = a.sg + row * a.ldg_h, *bg = a.bg + row * a.ldg_h;
-    const uint16_t *su = a.su + row * a.ldg_h, *bu = a.bu + row * a.ldg_h;
-#pragma unroll
-    for (int v = 0; v < kMaxRowVec; ++v) {
-        const int w0 = lane * 4 + v * 128;
-        if (w0 < nwords) {
-            const uint32_t gw[4] = {rp.g[v].x, rp.g[v].y, rp.g[v].z, rp.g[v].w};
-            const uint32_t uw[4] = {rp.u[v].x, rp.u[v].y, rp.u[v].z, rp.u[v].w};
+            rp.r[v] = __ldg(reinterpret_cast<const uint4 *>(qg + w0));
+            rp.r[kMaxRowVec + v] = __ldg(reinterpret_cast<const uint4 *>(qu + w0));
             const int grp = (w0 * 8) / a.G;  // the 4 words (32 elements) share a group (G >= 32)
-            const float sgv = bf16_bits_to_float(sg[grp]), bgv = bf16_bits_to_float(bg[grp]);
-            const float suv = bf16_bits_to_float(su[grp]), buv = bf16_bits_to_float(bu[grp]);
+            rp.sb[4 * v + 0] = __ldg(P.sg + row * a.ldg_h + grp);
+            rp.sb[4 * v + 1] = __ldg(P.bg + row * a.ldg_h + grp);
+            rp.sb[4 * v + 2] = __ldg(P.su + row * a.ldg_h + grp);
+            rp.sb[4 * v + 3] = __ldg(P.bu + row * a.ldg_h + grp);
+        }
+    }
+}
+
+template <int HMAX>
+__device__ __forceinline__ void row_pair_dot(const DecodeStack &a, const DecodeLayerPtrs &P, int64_t row, int lane,
+                                             const UnitRegs<HMAX> &rp, const float *xs, const float *xsum8,
+                                             float &gacc, float &uacc) {
+    constexpr int kMaxRowVec = UnitRegs<HMAX>::V / 2;
+    const int nwords = a.H / 8;
+#pragma unroll
+    for (int v = 0; v < kMaxRowVec; ++v) {
+        const int w0 = lane * 4 + v * 128;
+        if (w0 < nwords) {
+            const uint4 gv = rp.r[v], uv = rp.r[kMaxRowVec + v];
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+            const float sgv = bf16_bits_to_float(rp.sb[4 * v + 0]), bgv = bf16_bits_to_float(rp.sb[4 * v + 1]);
+            const float suv = bf16_bits_to_float(rp.sb[4 * v + 2]), buv = bf16_bits_to_float(rp.sb[4 * v + 3]);
             float dg = 0.f, du = 0.f, xs4 = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int w = w0 + i;
-                dg += dot8_codes(gw[i], xs + xpos(w * 8));
-                du += dot8_codes(uw[i], xs + xpos(w * 8));
+                dg += dot8_codes128(gw[i], xs + vpos(w * 8));
+                du += dot8_codes128(uw[i], xs + vpos(w * 8));
                 xs4 += xsum8[w];
             }
-            gacc += sgv * dg + bgv * xs4;
-            uacc += suv * du + buv * xs4;
+            gacc += sgv * dg + (bgv - 128.0f * sgv) * xs4;
+            uacc += suv * du + (buv - 128.0f * suv) * xs4;
         }
     }
 }
 
-__device__ __forceinline__ void prefetch_down_rows(const DecodeArgs &a, int e, int r0, int rows) {
-    const int64_t drow = static_cast<int64_t>(e) * a.H + r0;
-    prefetch_range(a.qd + drow * (a.I / 8), static_cast<size_t>(rows) * (a.I / 8) * 4);
-    prefetch_range(a.sd + drow * a.ldg_i, static_cast<size_t>(rows) * a.ldg_i * 2);
-    prefetch_range(a.bd + drow * a.ldg_i, static_cast<size_t>(rows) * a.ldg_i * 2);
-}
+// ------------------------------------------------------------ phase C parts
 
-// ------------------------------------------------------------------ K1
+// Down rows of one output feature f: lane holds words 2*lane, 2*lane + 1 of
+// every slot's row (I = 512: the whole row; wider rows are read in place) and
+// the group's scale and bias (G >= 16, so both words share a group).
+struct DownLoad {
+    uint2 q[kMaxSlots];
+    uint16_t s[kMaxSlots], b[kMaxSlots];
+};
 
-// blocks [0, nr): router, 2 experts per block; blocks [nr, nr + I/8): the
-// shared expert's gate/up rows, 8 per block (one per warp).
-__global__ void __launch_bounds__(256) decode_k1_kernel(DecodeArgs a) {
-    __shared__ float xs[kDecodeMaxH + kDecodeMaxH / 32];
-    __shared__ float xsum8[kDecodeMaxH / 8];
-    __shared__ float part[8];
-    __shared__ int is_last;
-    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int nr = (a.E + 1) / 2;
-    pdl_launch_dependents();
-    if (static_cast<int>(blockIdx.x) < nr) {
-        // ---------------------------------------------------------- router
-        const int e = blockIdx.x * 2 + warp / 4;
-        const int quarter = warp % 4;
-        const int span = a.H / 4;
-        const float *wrow = a.Wr + static_cast<int64_t>(e) * a.H + quarter * span;
-        float4 wv[kDecodeMaxH / 512];
-        if (e < a.E) {
-#pragma unroll
-            for (int v = 0; v < kDecodeMaxH / 512; ++v) {
-                const int c = lane * 4 + v * 128;
-                wv[v] = c < span ? *reinterpret_cast<const float4 *>(wrow + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        pdl_wait();  // x is the previous layer's output
-        float acc = 0.f;
-        if (e < a.E) {
-            const __nv_bfloat16 *xq = a.x + quarter * span;
-#pragma unroll
-            for (int v = 0; v < kDecodeMaxH / 512; ++v) {
-                const int c = lane * 4 + v * 128;
-                if (c < span) {
-                    const uint2 xr = *reinterpret_cast<const uint2 *>(xq + c);
-                    const __nv_bfloat162 x01 = u32_as_bf162(xr.x), x23 = u32_as_bf162(xr.y);
-                    acc = fmaf(wv[v].x, __low2float(x01), acc);
-                    acc = fmaf(wv[v].y, __high2float(x01), acc);
-                    acc = fmaf(wv[v].z, __low2float(x23), acc);
-                    acc = fmaf(wv[v].w, __high2float(x23), acc);
-                }
-            }
-        }
-        acc = warp_sum(acc);
-        if (lane == 0) part[warp] = acc;
-        __syncthreads();
-        if ((tid == 0 || tid == 128) && e < a.E) {
-            const int w0 = warp;  // 0 or 4
-            float l = part[w0] + part[w0 + 1] + part[w0 + 2] + part[w0 + 3];
-            if (a.bias) l += a.bias[e];
-            a.logits[e] = l;
-        }
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) {
-            const unsigned ticket = atomicAdd(&a.ctrl->ticket, 1u);
-            is_last = ticket == static_cast<unsigned>(nr) - 1;
-        }
-        __syncthreads();
-        if (!is_last || warp != 0) return;
-        __threadfence();
-
-        // top-k over E logits (ties -> lower expert index), softmax over the picked
-        float v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int ee = lane + 32 * i;
-            v[i] = ee < a.E ? __ldcg(a.logits + ee) : -INFINITY;
-        }
-        unsigned taken = 0;
-        float sel_v[8];
-        int sel_i[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            sel_v[j] = 0.f;
-            sel_i[j] = 0;
-            if (j < a.k) {
-                float bv = -INFINITY;
-                int bi = 0x7fffffff;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int ee = lane + 32 * i;
-                    if (ee < a.E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && ee < bi))) {
-                        bv = v[i];
-                        bi = ee;
-                    }
-                }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                    if (ov > bv || (ov == bv && oi < bi)) {
-                        bv = ov;
-                        bi = oi;
-                    }
-                }
-                if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-                sel_v[j] = bv;
-                sel_i[j] = bi;
-            }
-        }
-        const float m = sel_v[0];
-        float sum = 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j < a.k) sum += expf(sel_v[j] - m);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            if (j < a.k && lane == j) {
-                a.topk_idx[j] = sel_i[j];
-                a.topk_w[j] = expf(sel_v[j] - m) / sum;
-            }
-        }
-        if (lane == 0) a.ctrl->ticket = 0u;  // ready for the next call on this workspace
-        return;
-    }
-    // ------------------------------------------------ shared expert gate/up
-    if (!a.has_shared) return;
-    const int fb = blockIdx.x - nr;
-    const int f = fb * 8 + warp;
-    const int64_t row = static_cast<int64_t>(a.E) * a.I + f;
-    RowPair rp;
-    load_row_pair(a, row, lane, rp);
-    if (tid == 0) {  // its down rows are needed by K3
-        const int rows = a.H / (a.I / 8);
-        prefetch_down_rows(a, a.E, fb * rows, rows);
-    }
-    pdl_wait();
-    stage_x(a.x, a.H, xs, xsum8);
-    float gacc = 0.f, uacc = 0.f;
-    gate_up_dot(a, row, lane, rp, xs, xsum8, gacc, uacc);
-    gacc = warp_sum(gacc);
-    uacc = warp_sum(uacc);
-    if (lane == 0) a.h[static_cast<int64_t>(a.k) * a.I + f] = gacc / (1.0f + expf(-gacc)) * uacc;
-}
-
-// ------------------------------------------------------------------ K2
-
-// Block = 8 warps = 8 intermediate features of routed slot j.
-__global__ void __launch_bounds__(256) decode_k2_kernel(DecodeArgs a) {
-    __shared__ float xs[kDecodeMaxH + kDecodeMaxH / 32];
-    __shared__ float xsum8[kDecodeMaxH / 8];
-    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int fblocks = a.I / 8;
-    const int j = blockIdx.x / fblocks, fb = blockIdx.x % fblocks;
-    const int f = fb * 8 + warp;
-    pdl_launch_dependents();
-    pdl_wait();  // top-k of this layer
-    const int e = a.topk_idx[j];
-    const int64_t row = static_cast<int64_t>(e) * a.I + f;
-    RowPair rp;
-    load_row_pair(a, row, lane, rp);
-    if (tid == 0) {  // this block's share of the expert's down rows, needed by K3
-        const int rows = a.H / fblocks;
-        prefetch_down_rows(a, e, fb * rows, rows);
-    }
-    stage_x(a.x, a.H, xs, xsum8);
-    float gacc = 0.f, uacc = 0.f;
-    gate_up_dot(a, row, lane, rp, xs, xsum8, gacc, uacc);
-    gacc = warp_sum(gacc);
-    uacc = warp_sum(uacc);
-    if (lane == 0) a.h[static_cast<int64_t>(j) * a.I + f] = gacc / (1.0f + expf(-gacc)) * uacc;
-}
-
-// ------------------------------------------------------------------ K3
-
-constexpr int kMaxSlots = 9;  // k <= 8 routed + 1 shared
-
-// Block = 8 warps = 8 output features; each warp reads the down row of its
-// feature for every touched expert and combines with the routing weights.
-__global__ void __launch_bounds__(256) decode_k3_kernel(DecodeArgs a) {
-    extern __shared__ float sm[];
-    const int nslots = a.k + (a.has_shared ? 1 : 0);
-    const int ip = a.I + a.I / 16;           // padded row of h
-    float *hs = sm;                          // [nslots][ip]
-    float *hsum8 = sm + nslots * ip;         // [nslots][I/8]
-    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    pdl_launch_dependents();
-    pdl_wait();
-    if (tid == 0 && a.next_Wr) {
-        // the next layer's router does not depend on this layer's result:
-        // start moving it into L2, one slice per block
-        const size_t wr_bytes = static_cast<size_t>(a.E) * a.H * 4;
-        const size_t slice = (wr_bytes / gridDim.x + 15) / 16 * 16;
-        const size_t off = slice * blockIdx.x;
-        if (off < wr_bytes)
-            prefetch_range(reinterpret_cast<const char *>(a.next_Wr) + off,
-                           off + slice <= wr_bytes ? slice : wr_bytes - off);
-    }
-    // this warp's down rows of every touched expert: issued first, so that
-    // their latency overlaps the staging of h
-    const int f = blockIdx.x * 8 + warp;
+__device__ __forceinline__ void down_load(const DecodeStack &a, const DecodeLayerPtrs &P, const int *e_j, int nslots,
+                                          int f, int lane, int gshift, DownLoad &d) {
+    // e_j: expert of each slot (shared memory)
     const int nw = a.I / 8;
-    const bool vec = (nw & 63) == 0;  // lane handles 2 consecutive words per step
-    int e_j[kMaxSlots];
-    float w_j[kMaxSlots];
-    uint2 qw[kMaxSlots];
-    float sv[kMaxSlots], bv[kMaxSlots];
+    const int w = 2 * lane;
 #pragma unroll
     for (int j = 0; j < kMaxSlots; ++j) {
-        e_j[j] = j < a.k ? __ldcg(a.topk_idx + j) : a.E;
-        w_j[j] = j < a.k ? __ldcg(a.topk_w + j) : 1.0f;
-    }
-    if (vec && nw == 64) {
-        const int w0 = lane * 2;
-        const int grp = (w0 * 8) / a.G;  // both words share a group (G >= 16)
-#pragma unroll
-        for (int j = 0; j < kMaxSlots; ++j) {
-            if (j < nslots) {
-                const int64_t row = static_cast<int64_t>(e_j[j]) * a.H + f;
-                qw[j] = *reinterpret_cast<const uint2 *>(a.qd + row * nw + w0);
-                sv[j] = bf16_bits_to_float(a.sd[row * a.ldg_i + grp]);
-                bv[j] = bf16_bits_to_float(a.bd[row * a.ldg_i + grp]);
-            }
+        if (j < nslots && w < nw) {
+            const int64_t row = static_cast<int64_t>(e_j[j]) * a.H + f;
+            d.q[j] = __ldg(reinterpret_cast<const uint2 *>(P.qd + row * nw + w));
+            d.s[j] = __ldg(P.sd + row * a.ldg_i + ((w * 8) >> gshift));
+            d.b[j] = __ldg(P.bd + row * a.ldg_i + ((w * 8) >> gshift));
         }
     }
-    // h of every slot into shared memory (16-byte loads, all issued first)
-    {
-        const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
-        const int n4 = nslots * a.I / 4;
-        const int r4 = a.I / 4;  // float4 per slot
-        auto put = [&](int i, float4 v) {
-            float *d = hs + (i / r4) * ip + hpos((i % r4) * 4);  // 4 elements never straddle a pad
-            d[0] = v.x;
-            d[1] = v.y;
-            d[2] = v.z;
-            d[3] = v.w;
-        };
-        constexpr int U = 6;
-        float4 tmp[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = tid + u * blockDim.x;
-            if (i < n4) tmp[u] = __ldcg(h4 + i);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int i = tid + u * blockDim.x;
-            if (i < n4) put(i, tmp[u]);
-        }
-        for (int i = tid + U * blockDim.x; i < n4; i += blockDim.x) put(i, __ldcg(h4 + i));
-    }
-    __syncthreads();
-    for (int w = tid; w < nslots * nw; w += blockDim.x) {
-        const float *src = hs + (w / nw) * ip + hpos((w % nw) * 8);
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) s += src[i];
-        hsum8[w] = s;
-    }
-    __syncthreads();
-    float y = 0.f;
-    if (vec && nw == 64) {
-        const int w0 = lane * 2;
-#pragma unroll
-        for (int j = 0; j < kMaxSlots; ++j) {
-            if (j < nslots) {
-                const float *hv = hs + j * ip + hpos(w0 * 8);  // 16 contiguous elements
-                const float d = dot8_codes(qw[j].x, hv) + dot8_codes(qw[j].y, hv + 8);
-                const float hsum = hsum8[j * nw + w0] + hsum8[j * nw + w0 + 1];
-                y += w_j[j] * (sv[j] * d + bv[j] * hsum);
-            }
-        }
-    } else {
-        for (int w = lane; w < nw; w += 32) {
-            for (int j = 0; j < nslots; ++j) {
-                const int e = j < a.k ? __ldcg(a.topk_idx + j) : a.E;
-                const float wgt = j < a.k ? __ldcg(a.topk_w + j) : 1.0f;
-                const int64_t row = static_cast<int64_t>(e) * a.H + f;
-                const int grp = (w * 8) / a.G;
-                const float s = bf16_bits_to_float(a.sd[row * a.ldg_i + grp]);
-                const float b = bf16_bits_to_float(a.bd[row * a.ldg_i + grp]);
-                const float d = dot8_codes(a.qd[row * nw + w], hs + j * ip + hpos(w * 8));
-                y += wgt * (s * d + b * hsum8[j * nw + w]);
-            }
-        }
-    }
-    y = warp_sum(y);
-    if (lane == 0) a.y[f] = __float2bfloat16_rn(y);
 }
 
-template <typename... Args>
-static cudaError_t launch_pdl(void (*kernel)(Args...), int grid, int block, size_t smem, cudaStream_t s,
-                              Args... args) {
+// This lane's share of y[f]: sum over slots of w_j (s * h.(128+q) + (b - 128 s) * sum h).
+__device__ __forceinline__ float down_dot(const DecodeStack &a, const DecodeLayerPtrs &P, const int *e_j,
+                                          const float *w_j, int nslots, int f, int lane, int gshift,
+                                          const DownLoad &d, bool preloaded, const float *hs, const float *hsum8,
+                                          int ip) {
+    const int nw = a.I / 8;
+    float y = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j) {
+        if (j < nslots) {
+            const int64_t row = static_cast<int64_t>(e_j[j]) * a.H + f;
+            const float *hv = hs + j * ip;
+            float acc = 0.f;
+            for (int w = 2 * lane; w < nw; w += 64) {
+                uint2 qv;
+                uint16_t sb, bb;
+                if (preloaded) {
+                    qv = d.q[j];
+                    sb = d.s[j];
+                    bb = d.b[j];
+                } else {
+                    qv = __ldg(reinterpret_cast<const uint2 *>(P.qd + row * nw + w));
+                    sb = __ldg(P.sd + row * a.ldg_i + ((w * 8) >> gshift));
+                    bb = __ldg(P.bd + row * a.ldg_i + ((w * 8) >> gshift));
+                }
+                const float s = bf16_bits_to_float(sb), b = bf16_bits_to_float(bb);
+                const float dsum = dot8_codes128(qv.x, hv + vpos(w * 8)) + dot8_codes128(qv.y, hv + vpos(w * 8 + 8));
+                const float hsum = hsum8[j * nw + w] + hsum8[j * nw + w + 1];
+                acc += s * dsum + (b - 128.0f * s) * hsum;
+            }
+            y += w_j[j] * acc;
+        }
+    }
+    return y;
+}
+
+// ------------------------------------------------------------------- top-k
+
+// Order-preserving 64-bit key of (logit, expert): larger logit first, then
+// lower expert index first; distinct for distinct experts.
+__device__ __forceinline__ unsigned long long topk_key(float l, int e) {
+    uint32_t u = __float_as_uint(l);
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<unsigned long long>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - e);
+}
+
+// Sort one key per lane across a warp, descending (bitonic network).
+__device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long key, int lane) {
+#pragma unroll
+    for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, stride);
+            // lanes whose bit `size` is clear sort their pair descending, the others ascending
+            const bool desc = ((lane & size) == 0) || size == 32;
+            const bool lower = (lane & stride) == 0;
+            const bool take_max = (lower == desc);
+            key = take_max ? (other > key ? other : key) : (other < key ? other : key);
+        }
+    }
+    return key;
+}
+
+// Top-k of E <= 256 logits (ties -> lower expert index) and the softmax over
+// the picked ones.  Warps 0-7 each sort 32 experts' keys; the 8 best of every
+// warp (64 keys) are sorted again in two rounds by warp 0.  The logit of
+// expert e is the sum of its four K-quarter partial sums in a fixed order,
+// plus the bias.  Every block computes the same result.
+__device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bias, unsigned long long *s_keys,
+                                           int *s_idx, float *s_w) {
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    if (warp < 8) {
+        unsigned long long key = 0;  // below every real key
+        if (t < a.E) {
+            float l = __ldcg(a.logits_part + t) + __ldcg(a.logits_part + a.E + t);
+            l += __ldcg(a.logits_part + 2 * a.E + t);
+            l += __ldcg(a.logits_part + 3 * a.E + t);
+            if (bias) l += __ldg(bias + t);
+            key = topk_key(l, t);
+        }
+        key = warp_sort_desc(key, lane);
+        if (lane < 8) s_keys[warp * 8 + lane] = key;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // round 1: the 32 keys of warps 0-3 and, separately, of warps 4-7
+        unsigned long long k0 = warp_sort_desc(s_keys[lane], lane);
+        unsigned long long k1 = warp_sort_desc(s_keys[32 + lane], lane);
+        // round 2: the 8 best of each
+        const unsigned long long k1s = __shfl_sync(0xffffffffu, k1, (lane - 8) & 31);
+        unsigned long long k = lane < 8 ? k0 : lane < 16 ? k1s : 0ull;
+        k = warp_sort_desc(k, lane);
+        // lane j < k: pick j
+        const uint32_t ord = static_cast<uint32_t>(k >> 32);
+        const float l = __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+        const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k));
+        const float m = __shfl_sync(0xffffffffu, l, 0);
+        const float ex = lane < a.k ? expf(l - m) : 0.f;
+        const float sum = warp_sum(ex);
+        if (lane < a.k) {
+            s_idx[lane] = e;
+            s_w[lane] = ex / sum;
+        }
+    }
+    __syncthreads();
+}
+
+// ------------------------------------------------------------------ kernel
+
+__host__ __device__ inline int decode_smem_floats(int H, int I, int k) {
+    const int x_words = vlen(H) + H / 8;                       // xs + xsum8
+    const int h_words = (k + 1) * vlen(I) + (k + 1) * (I / 8);  // hs + hsum8 (aliases the x region)
+    return x_words > h_words ? x_words : h_words;
+}
+
+template <int HMAX>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __grid_constant__ DecodeStack a) {
+    extern __shared__ __align__(16) float dsm[];
+    __shared__ int s_idx[kMaxSlots];
+    __shared__ float s_w[kMaxSlots];
+    __shared__ int s_ok;
+    __shared__ unsigned long long s_keys[64];
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int G = gridDim.x, b = blockIdx.x;
+    const int gw = b * kDecWarps + warp, NW = G * kDecWarps;
+    float *xs = dsm;                        // [vlen(H)]
+    float *xsum8 = dsm + vlen(a.H);         // [H/8]
+    const int ip = vlen(a.I);               // padded row of h
+    float *hs = dsm;                        // [slots][ip] (aliases x: used in another phase)
+    const int nslots = a.k + (a.has_shared ? 1 : 0);
+    const int n_a_units = 4 * a.E + (a.has_shared ? a.I : 0);
+    const int gshift = a.G == 64 ? 6 : 5;   // log2 of the group (32 or 64)
+    unsigned nbar = 0;  // grid barriers passed in this launch
+    const long long lim = a.wait_limit;
+
+    for (int li = 0; li < a.n_layers; ++li) {
+        const int l = a.l0 + li;
+        const DecodeLayerPtrs &P = a.L[li];
+        const __nv_bfloat16 *in = l == 0 ? a.x : a.act + ((l - 1) % 2) * a.H;
+        __nv_bfloat16 *out = l == a.n_total - 1 ? a.y : a.act + (l % 2) * a.H;
+
+        // ------------------------------------------------------------ phase A
+        // this warp's first unit: its weights do not depend on the input, so
+        // they are loaded before waiting for the previous layer
+        UnitRegs<HMAX> ur;
+        const int u0 = gw;
+        if (u0 < 4 * a.E) {
+            router_load(a, P.Wr, u0, lane, ur);
+        } else if (u0 < n_a_units) {
+            row_pair_load(a, P, static_cast<int64_t>(a.E) * a.I + (u0 - 4 * a.E), lane, ur);
+        }
+        if (tid == 0 && a.has_shared) {
+            // the shared expert's down rows are read in phase C
+            const int64_t r0 = static_cast<int64_t>(a.E) * a.H;
+            prefetch_slice(P.qd + r0 * (a.I / 8), static_cast<size_t>(a.H) * (a.I / 8) * 4, b, G);
+            prefetch_slice(P.sd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
+            prefetch_slice(P.bd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
+        }
+        if (li > 0 && !grid_wait(a.ctrl, ++nbar * G, lim, 1, &s_ok)) return;
+        stage_x(in, a.H, xs, xsum8);
+        __syncthreads();
+        for (int u = u0; u < n_a_units; u += NW) {
+            if (u < 4 * a.E) {
+                if (u != u0) router_load(a, P.Wr, u, lane, ur);
+                const float acc = warp_sum(router_dot(a, u, lane, ur, xs));
+                if (lane == 0) a.logits_part[(u & 3) * a.E + (u >> 2)] = acc;
+            } else {
+                const int f = u - 4 * a.E;
+                const int64_t row = static_cast<int64_t>(a.E) * a.I + f;
+                if (u != u0) row_pair_load(a, P, row, lane, ur);
+                float g = 0.f, up = 0.f;
+                row_pair_dot(a, P, row, lane, ur, xs, xsum8, g, up);
+                g = warp_sum(g);
+                up = warp_sum(up);
+                if (lane == 0) a.h[static_cast<int64_t>(a.k) * a.I + f] = g / (1.0f + expf(-g)) * up;
+            }
+        }
+        grid_arrive(a.ctrl);
+
+        // ------------------------------------------------------------ phase B
+        // this block's contiguous range of (slot, feature) pairs of the routed
+        // gate/up rows; warp w takes pairs f_lo + w, f_lo + w + 16, ... two at a time
+        const int F = a.k * a.I;
+        const int f_lo = static_cast<int>((static_cast<int64_t>(b) * F) / G);
+        const int f_hi = static_cast<int>((static_cast<int64_t>(b + 1) * F) / G);
+        if (!grid_wait(a.ctrl, ++nbar * G, lim, 2, &s_ok)) return;
+        topk_block(a, P.bias, s_keys, s_idx, s_w);
+        if (b == 0 && tid < a.k) {
+            a.topk_idx[tid] = s_idx[tid];
+            a.topk_w[tid] = s_w[tid];
+        }
+        if (tid < a.k) {
+            // this block's share of the picked experts' down rows, read in phase C
+            const int64_t r0 = static_cast<int64_t>(s_idx[tid]) * a.H;
+            prefetch_slice(P.qd + r0 * (a.I / 8), static_cast<size_t>(a.H) * (a.I / 8) * 4, b, G);
+            prefetch_slice(P.sd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
+            prefetch_slice(P.bd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
+        }
+        for (int f0 = f_lo + warp; f0 < f_hi; f0 += 2 * kDecWarps) {
+            UnitRegs<HMAX> r2[2];
+            int64_t rows[2];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int f = f0 + i * kDecWarps;
+                if (f < f_hi) {
+                    const int j = f / a.I;
+                    rows[i] = static_cast<int64_t>(s_idx[j]) * a.I + (f - j * a.I);
+                    row_pair_load(a, P, rows[i], lane, r2[i]);
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int f = f0 + i * kDecWarps;
+                if (f < f_hi) {
+                    float g = 0.f, up = 0.f;
+                    row_pair_dot(a, P, rows[i], lane, r2[i], xs, xsum8, g, up);
+                    g = warp_sum(g);
+                    up = warp_sum(up);
+                    if (lane == 0) a.h[f] = g / (1.0f + expf(-g)) * up;  // slot f / I, feature f % I
+                }
+            }
+        }
+        grid_arrive(a.ctrl);
+
+        // ------------------------------------------------------------ phase C
+        // slot tables in shared memory: slot k is the shared expert, weight 1
+        if (tid == 0) {
+            s_idx[a.k] = a.E;
+            s_w[a.k] = 1.0f;
+        }
+        __syncthreads();
+        const int *e_j = s_idx;
+        const float *w_j = s_w;
+        const int y_lo = static_cast<int>((static_cast<int64_t>(b) * a.H) / G);
+        const int y_hi = static_cast<int>((static_cast<int64_t>(b + 1) * a.H) / G);
+        const bool preload = a.I <= 512;  // the whole row is one 8-byte load per lane
+        DownLoad dl;
+        if (preload && y_lo + warp < y_hi) down_load(a, P, e_j, nslots, y_lo + warp, lane, gshift, dl);
+        if (tid == 0) {
+            // the next layer's router and shared gate/up rows do not depend on
+            // this layer: start moving this block's share into L2
+            const float *nWr = li + 1 < a.n_layers ? a.L[li + 1].Wr : a.next_Wr;
+            if (nWr) prefetch_slice(nWr, static_cast<size_t>(a.E) * a.H * 4, b, G);
+            if (li + 1 < a.n_layers && a.has_shared) {
+                const DecodeLayerPtrs &N = a.L[li + 1];
+                const int64_t r0 = static_cast<int64_t>(a.E) * a.I;
+                prefetch_slice(N.qg + r0 * (a.H / 8), static_cast<size_t>(a.I) * (a.H / 8) * 4, b, G);
+                prefetch_slice(N.qu + r0 * (a.H / 8), static_cast<size_t>(a.I) * (a.H / 8) * 4, b, G);
+            }
+        }
+        if (!grid_wait(a.ctrl, ++nbar * G, lim, 3, &s_ok)) return;
+        {
+            // h of every slot into shared memory (written by other blocks: read from L2)
+            const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
+            const int n4 = nslots * a.I / 4;
+            const int r4 = a.I / 4;  // float4 per slot
+            for (int i = tid; i < n4; i += kDecThreads) {
+                const float4 v = __ldcg(h4 + i);
+                *reinterpret_cast<float4 *>(hs + (i / r4) * ip + vpos((i % r4) * 4)) = v;
+            }
+        }
+        __syncthreads();
+        float *hsum8 = hs + nslots * ip;
+        const int nw8 = a.I / 8;
+        for (int w = tid; w < nslots * nw8; w += kDecThreads) {
+            const float4 *src = reinterpret_cast<const float4 *>(hs + (w / nw8) * ip + vpos((w % nw8) * 8));
+            const float4 u0v = src[0], u1v = src[1];
+            hsum8[w] = ((u0v.x + u0v.y) + (u0v.z + u0v.w)) + ((u1v.x + u1v.y) + (u1v.z + u1v.w));
+        }
+        __syncthreads();
+        for (int f = y_lo + warp; f < y_hi; f += kDecWarps) {
+            const bool pre = preload && f == y_lo + warp;
+            const float y = warp_sum(down_dot(a, P, e_j, w_j, nslots, f, lane, gshift, dl, pre, hs, hsum8, ip));
+            if (lane == 0) out[f] = __float2bfloat16_rn(y);
+        }
+        if (li + 1 < a.n_layers) grid_arrive(a.ctrl);
+        __syncthreads();  // hs is overwritten by the next layer's staging
+    }
+}
+
+size_t decode_smem_bytes(int E, int k, int H, int I, int grid) {
+    (void)E;
+    (void)grid;
+    return sizeof(float) * static_cast<size_t>(decode_smem_floats(H, I, k));
+}
+
+template <int HMAX>
+static cudaError_t launch_decode_t(const DecodeStack &a, int grid, cudaStream_t s) {
+    const size_t smem = decode_smem_bytes(a.E, a.k, a.H, a.I, grid);
+    cudaError_t e = cudaFuncSetAttribute(decode_stack_kernel<HMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    // every block must be resident at once: one per SM
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stack_kernel<HMAX>, kDecThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
+    cfg.blockDim = dim3(kDecThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, args...);
+    return cudaLaunchKernelEx(&cfg, decode_stack_kernel<HMAX>, a);
 }
 
-cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
-    const int nr = (a.E + 1) / 2;
-    const int nshared = a.has_shared ? a.I / 8 : 0;
-    cudaError_t e = launch_pdl(decode_k1_kernel, nr + nshared, 256, 0, s, a);
-    if (e != cudaSuccess) return e;
-    if ((e = launch_pdl(decode_k2_kernel, a.k * (a.I / 8), 256, 0, s, a)) != cudaSuccess) return e;
-    const int nslots = a.k + (a.has_shared ? 1 : 0);
-    const size_t sm_dn = sizeof(float) * (nslots * (a.I + a.I / 16) + nslots * a.I / 8);
-    if (sm_dn > 48 * 1024 &&
-        (e = cudaFuncSetAttribute(decode_k3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(sm_dn))) != cudaSuccess)
-        return e;
-    return launch_pdl(decode_k3_kernel, a.H / 8, 256, sm_dn, s, a);
+cudaError_t launch_decode(const DecodeStack &a, int grid, cudaStream_t s) {
+    return a.H <= 2048 ? launch_decode_t<2048>(a, grid, s) : launch_decode_t<4096>(a, grid, s);
 }
 
 }  // namespace moe

@@ -29,23 +29,35 @@ struct GemmMaps {
     CUtensorMap s0, b0, s1, b1;  // scale / bias blocks
 };
 
-constexpr int kDecodeMaxH = 4096;  // largest hidden size of the decode kernels
+constexpr int kDecodeMaxH = 4096;      // largest hidden size of the decode kernel
+constexpr int kMaxStackLayers = 64;    // layers per decode launch (longer stacks take several)
 
-struct DecodeArgs {
-    const __nv_bfloat16 *x;
-    __nv_bfloat16 *y;
+// Weights of one layer as the decode kernel reads them.
+struct DecodeLayerPtrs {
     const float *Wr;
     const float *bias;
     const uint32_t *qg, *qu, *qd;
     const uint16_t *sg, *bg, *su, *bu, *sd, *bd;
+};
+
+// One launch of the batch-1 decode kernel: layers l0 .. l0 + n_layers - 1 of
+// a stack of n_total layers of one shape.  Layer l reads x (l = 0) or act[(l-1)
+// % 2] and writes y (l = n_total - 1) or act[l % 2].
+struct DecodeStack {
     int E, k, H, I, G, has_shared;
-    int ldg_h, ldg_i;  // row pitch (in groups) of the gate/up and down scale arrays
-    Ctrl *ctrl;
-    float *logits;
-    int *topk_idx;
-    float *topk_w;
-    float *h;  // [(k+1)][I]
-    const float *next_Wr;  // router of the next layer of a stack (prefetched into L2), or NULL
+    int ldg_h, ldg_i;        // row pitch (in groups) of the gate/up and down scale arrays
+    int n_layers, l0, n_total;
+    const __nv_bfloat16 *x;
+    __nv_bfloat16 *y;
+    __nv_bfloat16 *act;      // [2][H] (stacks of more than one layer)
+    Ctrl *ctrl;              // status, grid-barrier counter, abort flag
+    float *logits_part;      // [4][E]: router partial sums over K quarters
+    int *topk_idx;           // [8]
+    float *topk_w;           // [8]
+    float *h;                // [k + 1][I] fp32 (slot k = shared expert)
+    const float *next_Wr;    // router of the layer after this launch (L2 prefetch), or NULL
+    long long wait_limit;
+    DecodeLayerPtrs L[kMaxStackLayers];
 };
 
 cudaError_t launch_pack_int4(const float *w, int64_t rows, int K, int G, uint32_t *q, uint16_t *scale,
@@ -61,6 +73,7 @@ cudaError_t launch_zero_i32(int *p, int64_t n, cudaStream_t s);
 cudaError_t launch_xperm(const __nv_bfloat16 *x, __nv_bfloat16 *xp, const int *row_token, int rows, int H,
                          int num_sms, cudaStream_t s);
 cudaError_t launch_convert(const float *y_acc, __nv_bfloat16 *y, int64_t n, int num_sms, cudaStream_t s);
-cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+size_t decode_smem_bytes(int E, int k, int H, int I, int grid);
+cudaError_t launch_decode(const DecodeStack &a, int grid, cudaStream_t s);
 
 }  // namespace moe

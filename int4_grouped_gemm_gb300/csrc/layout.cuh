@@ -16,8 +16,10 @@ inline int ld_groups(int K, int G) { return (K / G + 7) / 8 * 8; }
 // Control block at the start of every workspace.
 struct Ctrl {
     int status;         // first device-side error (0 = none)
-    unsigned ticket;    // decode: blocks of the router kernel that finished
-    int pad[62];
+    unsigned ticket;    // spare counter
+    unsigned bar;       // decode: arrivals at the kernel's grid barriers
+    int abort;          // decode: set by a block whose bounded wait ran out
+    int pad[60];
 };
 
 struct RoutingBufs {
@@ -102,7 +104,7 @@ inline DecodeLayout decode_layout(int E, int k, int I) {
         return at;
     };
     L.ctrl = take(kCtrlBytes);
-    L.logits = take(sizeof(float) * (size_t)E);
+    L.logits = take(sizeof(float) * 4 * (size_t)E);  // partial sums over 4 K quarters
     L.topk_idx = take(sizeof(int) * 8);
     L.topk_w = take(sizeof(float) * 8);
     L.h = take(sizeof(float) * (size_t)(k + 1) * I);
