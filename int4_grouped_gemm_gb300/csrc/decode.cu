@@ -11,19 +11,18 @@
 // launched cooperatively so that every block is resident).  Each layer is
 // three phases separated by grid barriers (a counter in the workspace,
 // bounded waits):
-//   A  router partial sums over K quarters (one warp per expert and quarter)
-//      and the shared expert's gate/up rows (one warp per feature; it needs
-//      no routing); every block stages the layer input in shared memory
-//   B  every block computes the same top-k from the partial sums, prefetches
-//      its share of the picked experts' down rows into L2, then the gate/up
-//      rows of the k routed experts: a block owns a contiguous range of
-//      (slot, feature) pairs, its warps take K quarters, h = silu(g) * u
+//   A  router partial sums over K quarters (one warp per expert and
+//      quarter); every block stages the layer input in shared memory
+//   B  every block computes the same top-k from the partial sums (a bitonic
+//      sort of 64-bit keys in registers), prefetches its share of the picked
+//      experts' down rows into L2, then the gate/up rows of the k routed
+//      experts and of the shared expert: a block owns a contiguous range of
+//      (slot, feature) pairs, one warp per pair, h = silu(g) * u
 //   C  one warp per output feature over the down rows of all k + 1 experts,
 //      weighted combine fused, bf16 out; the next layer's router and shared
 //      expert are prefetched into L2 meanwhile
-// Loads that do not depend on the previous phase (router rows, shared rows,
-// down rows) are issued before the barrier wait, so their latency overlaps
-// it.  Only the router and the k + 1 touched experts are read.  The int4 dot
+// Loads that do not depend on the previous phase (router rows, down rows)
+// are issued before the barrier wait, so their latency overlaps it.  Only the router and the k + 1 touched experts are read.  The int4 dot
 // products use sum_i x_i (s q_i + b) = s sum_i x_i q_i + b sum_i x_i per
 // 8-element word, with the per-word input sums computed once per block.
 #include "kernels.cuh"
@@ -255,11 +254,11 @@ __device__ __forceinline__ void row_pair_dot(const DecodeStack &a, const DecodeL
 // ------------------------------------------------------------ phase C parts
 
 // Down rows of one output feature f: lane holds words 2*lane, 2*lane + 1 of
-// every slot's row (I = 512: the whole row; wider rows are read in place) and
-// the group's scale and bias (G >= 16, so both words share a group).
+// every slot's row (I <= 512: the whole row; wider rows are read in place).
+// Both words share a quantisation group (G >= 16); scales and biases are
+// read when the row is used (they were prefetched into L2 with the rows).
 struct DownLoad {
     uint2 q[kMaxSlots];
-    uint16_t s[kMaxSlots], b[kMaxSlots];
 };
 
 __device__ __forceinline__ void down_load(const DecodeStack &a, const DecodeLayerPtrs &P, const int *e_j, int nslots,
@@ -272,8 +271,6 @@ __device__ __forceinline__ void down_load(const DecodeStack &a, const DecodeLaye
         if (j < nslots && w < nw) {
             const int64_t row = static_cast<int64_t>(e_j[j]) * a.H + f;
             d.q[j] = __ldg(reinterpret_cast<const uint2 *>(P.qd + row * nw + w));
-            d.s[j] = __ldg(P.sd + row * a.ldg_i + ((w * 8) >> gshift));
-            d.b[j] = __ldg(P.bd + row * a.ldg_i + ((w * 8) >> gshift));
         }
     }
 }
@@ -292,17 +289,9 @@ __device__ __forceinline__ float down_dot(const DecodeStack &a, const DecodeLaye
             const float *hv = hs + j * ip;
             float acc = 0.f;
             for (int w = 2 * lane; w < nw; w += 64) {
-                uint2 qv;
-                uint16_t sb, bb;
-                if (preloaded) {
-                    qv = d.q[j];
-                    sb = d.s[j];
-                    bb = d.b[j];
-                } else {
-                    qv = __ldg(reinterpret_cast<const uint2 *>(P.qd + row * nw + w));
-                    sb = __ldg(P.sd + row * a.ldg_i + ((w * 8) >> gshift));
-                    bb = __ldg(P.bd + row * a.ldg_i + ((w * 8) >> gshift));
-                }
+                const uint2 qv = preloaded ? d.q[j] : __ldg(reinterpret_cast<const uint2 *>(P.qd + row * nw + w));
+                const uint16_t sb = __ldg(P.sd + row * a.ldg_i + ((w * 8) >> gshift));
+                const uint16_t bb = __ldg(P.bd + row * a.ldg_i + ((w * 8) >> gshift));
                 const float s = bf16_bits_to_float(sb), b = bf16_bits_to_float(bb);
                 const float dsum = dot8_codes128(qv.x, hv + vpos(w * 8)) + dot8_codes128(qv.y, hv + vpos(w * 8 + 8));
                 const float hsum = hsum8[j * nw + w] + hsum8[j * nw + w + 1];
@@ -408,7 +397,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     const int ip = vlen(a.I);               // padded row of h
     float *hs = dsm;                        // [slots][ip] (aliases x: used in another phase)
     const int nslots = a.k + (a.has_shared ? 1 : 0);
-    const int n_a_units = 4 * a.E + (a.has_shared ? a.I : 0);
+    const int n_a_units = 4 * a.E;
     const int gshift = a.G == 64 ? 6 : 5;   // log2 of the group (32 or 64)
     unsigned nbar = 0;  // grid barriers passed in this launch
     const long long lim = a.wait_limit;
@@ -424,11 +413,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         // they are loaded before waiting for the previous layer
         UnitRegs<HMAX> ur;
         const int u0 = gw;
-        if (u0 < 4 * a.E) {
-            router_load(a, P.Wr, u0, lane, ur);
-        } else if (u0 < n_a_units) {
-            row_pair_load(a, P, static_cast<int64_t>(a.E) * a.I + (u0 - 4 * a.E), lane, ur);
-        }
+        if (u0 < n_a_units) router_load(a, P.Wr, u0, lane, ur);
         if (tid == 0 && a.has_shared) {
             // the shared expert's down rows are read in phase C
             const int64_t r0 = static_cast<int64_t>(a.E) * a.H;
@@ -440,27 +425,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         stage_x(in, a.H, xs, xsum8);
         __syncthreads();
         for (int u = u0; u < n_a_units; u += NW) {
-            if (u < 4 * a.E) {
-                if (u != u0) router_load(a, P.Wr, u, lane, ur);
-                const float acc = warp_sum(router_dot(a, u, lane, ur, xs));
-                if (lane == 0) a.logits_part[(u & 3) * a.E + (u >> 2)] = acc;
-            } else {
-                const int f = u - 4 * a.E;
-                const int64_t row = static_cast<int64_t>(a.E) * a.I + f;
-                if (u != u0) row_pair_load(a, P, row, lane, ur);
-                float g = 0.f, up = 0.f;
-                row_pair_dot(a, P, row, lane, ur, xs, xsum8, g, up);
-                g = warp_sum(g);
-                up = warp_sum(up);
-                if (lane == 0) a.h[static_cast<int64_t>(a.k) * a.I + f] = g / (1.0f + expf(-g)) * up;
-            }
+            if (u != u0) router_load(a, P.Wr, u, lane, ur);
+            const float acc = warp_sum(router_dot(a, u, lane, ur, xs));
+            if (lane == 0) a.logits_part[(u & 3) * a.E + (u >> 2)] = acc;
         }
         grid_arrive(a.ctrl);
 
         // ------------------------------------------------------------ phase B
-        // this block's contiguous range of (slot, feature) pairs of the routed
-        // gate/up rows; warp w takes pairs f_lo + w, f_lo + w + 16, ... two at a time
-        const int F = a.k * a.I;
+        // this block's contiguous range of (slot, feature) pairs of the gate/up
+        // rows, slot k being the shared expert; warp w takes pairs f_lo + w,
+        // f_lo + w + kDecWarps, ... two at a time
+        const int F = nslots * a.I;
         const int f_lo = static_cast<int>((static_cast<int64_t>(b) * F) / G);
         const int f_hi = static_cast<int>((static_cast<int64_t>(b + 1) * F) / G);
         if (!grid_wait(a.ctrl, ++nbar * G, lim, 2, &s_ok)) return;
@@ -477,6 +452,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             prefetch_slice(P.bd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
         }
         for (int f0 = f_lo + warp; f0 < f_hi; f0 += 2 * kDecWarps) {
+            // both pairs' rows are requested before either is used
             UnitRegs<HMAX> r2[2];
             int64_t rows[2];
 #pragma unroll
@@ -484,7 +460,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                 const int f = f0 + i * kDecWarps;
                 if (f < f_hi) {
                     const int j = f / a.I;
-                    rows[i] = static_cast<int64_t>(s_idx[j]) * a.I + (f - j * a.I);
+                    rows[i] = static_cast<int64_t>(j < a.k ? s_idx[j] : a.E) * a.I + (f - j * a.I);
                     row_pair_load(a, P, rows[i], lane, r2[i]);
                 }
             }
