@@ -381,9 +381,9 @@ def oracle_time(cfg, s, toks):
 
 def cpu_baseline(cfg, target_s=15.0):
     import oracle
-    s = oracle_sample(cfg, 256)
+    s = oracle_sample(cfg, 2048)
     t = oracle_time(cfg, s, s["toks"][:4])
-    n = int(max(4, min(256, 4 * target_s / max(t, 1e-3))))
+    n = int(max(4, min(2048, 4 * target_s / max(t, 1e-3))))
     t = oracle_time(cfg, s, s["toks"][:n])
     return {"value": round(n / t, 3), "unit": "tok/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{n} of the {cfg.T} tokens of the {cfg.name} layer (router, top-8, 8 routed + shared "
