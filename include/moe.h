@@ -111,7 +111,6 @@ typedef struct {
                           * the group has an odd count); units of 2 full tiles
                           * first, then by rows descending, ties lower group */
     int64_t num_tiles;   /* int32 [2]: tiles, work units */
-    int64_t xperm;       /* bf16 [T*k][H]: x rows in routed-row order */
     int64_t h;           /* bf16 [T*k + T][I]: SwiGLU output per routed/shared row */
     int64_t y_acc;       /* fp32 [T][H]: combine accumulator */
     int32_t max_tiles;

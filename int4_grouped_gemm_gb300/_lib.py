@@ -39,7 +39,7 @@ class moe_layer_desc(ctypes.Structure):
 class moe_routing_views(ctypes.Structure):
     _fields_ = [(n, c_i64) for n in ("logits", "topk_idx", "topk_w", "counts", "offsets", "perm",
                                       "inv_perm", "tile_group", "tile_row", "tile_rows", "tile_sched",
-                                      "num_tiles", "xperm", "h", "y_acc")] + \
+                                      "num_tiles", "h", "y_acc")] + \
         [("max_tiles", c_i32), ("tile_size", c_i32)]
 
 

@@ -180,7 +180,6 @@ int moe_routing_views_for(const moe_layer_desc *desc, int32_t T, moe_routing_vie
     v->tile_rows = L.tile_rows;
     v->tile_sched = L.tile_sched;
     v->num_tiles = L.num_tiles;
-    v->xperm = L.xperm;
     v->h = L.h;
     v->y_acc = L.y_acc;
     v->max_tiles = L.max_tiles;
@@ -226,7 +225,6 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     const int nexp = E + 1;
 
     __nv_bfloat16 *wr3 = reinterpret_cast<__nv_bfloat16 *>(w + L.wr3);
-    __nv_bfloat16 *xperm = reinterpret_cast<__nv_bfloat16 *>(w + L.xperm);
     float *logits_part = reinterpret_cast<float *>(w + L.logits_part);
     const int routed = T * k;
     const int ldg_h = ld_groups(H, G), ldg_i = ld_groups(I, G);
@@ -242,10 +240,10 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
         return rc;
     mr.a1 = mr.a0;
     mr.w1 = mr.s0 = mr.b0 = mr.s1 = mr.b1 = mr.w0;
-    // gate/up: A = permuted x (routed rows) or x (shared rows); B = gate rows
-    // f0..f0+127 and up rows f0..f0+127 of one expert
-    if ((rc = encode_2d(&m1.a0, BF16, 2, routed > 0 ? static_cast<const void *>(xperm) : x, H,
-                        routed > 0 ? routed : T, 64, 128, SW128)) ||
+    // gate/up: A = token rows gathered from x by the kernel itself (the maps
+    // below are unused placeholders); B = gate rows f0..f0+127 and up rows
+    // f0..f0+127 of one expert
+    if ((rc = encode_2d(&m1.a0, BF16, 2, x, H, T, 64, 128, SW128)) ||
         (rc = encode_2d(&m1.a1, BF16, 2, x, H, T, 64, 128, SW128)) ||
         (rc = encode_2d(&m1.w0, U32, 4, desc->gate.q, H / 8, gu_rows, 4, 128, SW0)) ||
         (rc = encode_2d(&m1.w1, U32, 4, desc->up.q, H / 8, gu_rows, 4, 128, SW0)) ||
@@ -275,6 +273,7 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     ga.E_pad16 = L.E_pad16;
     ga.rb = rb;
     ga.h = h;
+    ga.x = static_cast<const __nv_bfloat16 *>(x);
     ga.y_acc = y_acc;
     ga.logits_part = logits_part;
     ga.status = &ctrl->status;
@@ -292,12 +291,9 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     ga.K = H;
     if (launch_gemm(2, mr, ga, grid_for(router_units(T)), stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(events, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    // routing tables and the permuted copy of x
+    // routing tables
     if (launch_routing_tables(logits_part, L.E_pad16, nullptr, desc->router_bias, T, E, k, desc->has_shared, rb,
-                              stream) !=
-            cudaSuccess ||
-        launch_xperm(static_cast<const __nv_bfloat16 *>(x), xperm, rb.row_token, routed, H, dev->num_sms, stream) !=
-            cudaSuccess)
+                              stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (mark(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
     // gate/up + SwiGLU

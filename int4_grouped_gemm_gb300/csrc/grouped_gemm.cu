@@ -20,9 +20,10 @@
 // token tile per unit.  Units run on a persistent grid of one CTA per SM in a
 // largest-first order.
 //
-//   warp 10     A producer: TMA loads of both token tiles (2 x 16 KB boxes per
-//               stage) from the permuted copy of x (gate/up), from x itself
-//               (shared expert, router) or from h (down)
+//   warps 27-30 gate/up A producers: 16-byte cp.async gathers of the unit's
+//               token rows straight from x (no permuted copy of x)
+//   warp 10     down/router A producer: TMA loads of both token tiles (2 x 16 KB
+//               boxes per stage) from h (down) or from x (router)
 //   warp 8      W producer: TMA loads of packed nibbles (8 KB per stage, two
 //               16-byte halves per row so that each dequant thread reads 16
 //               contiguous bytes) and of scale/bias blocks (8 groups x 256
@@ -54,10 +55,15 @@ constexpr int BN = 256;                          // weight rows per tile (MMA N)
 constexpr int GK = 64;                           // K elements per stage
 constexpr int SG = 8;                            // quantisation groups per scale block
 constexpr int NS_A = 3, NS_B = 2, NS_S = 2;      // ring depths
+static_assert(NS_A >= 2, "the gate/up copy producer hands a stage over one stage late");
 constexpr int kMaxNsQ = 4;
 __host__ __device__ constexpr int ns_q(int mode) { return mode == 1 ? 3 : 4; }
 constexpr int kEpiWarps = 8, kWProdWarp = 8, kMmaWarp = 9, kAProdWarp = 10, kDeqWarp0 = 11, kDeqWarps = 16;
-constexpr int kGemmThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 864
+constexpr int kLsuWarp0 = kDeqWarp0 + kDeqWarps, kLsuWarps = 4;  // gate/up: token-row copiers
+constexpr int kLsuThreads = kLsuWarps * 32;
+__host__ __device__ constexpr int gemm_threads(int mode) {
+    return (kLsuWarp0 + (mode == 0 ? kLsuWarps : 0)) * 32;  // 992 (gate/up) or 864
+}
 constexpr int TILE_A = BM * 128;                 // 16 KB: 128 token rows x 64 bf16
 constexpr int A_STAGE = TPU * TILE_A;            // 32 KB: both token tiles
 constexpr int B_STAGE = BN * 128;                // 32 KB: 256 weight rows x 64 bf16
@@ -167,7 +173,7 @@ __device__ __forceinline__ void drain_ring(uint64_t *full, int depth, uint32_t i
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(gemm_threads(MODE), 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
                         const __grid_constant__ CUtensorMap tm_w0, const __grid_constant__ CUtensorMap tm_w1,
                         const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_b0,
@@ -187,7 +193,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (tid == 0) {
         for (int i = 0; i < NS_A; ++i) {
-            mbar_init(&s->a_full[i], 1);
+            mbar_init(&s->a_full[i], MODE == 0 ? kLsuThreads : 1);
             mbar_init(&s->a_empty[i], 1);
         }
         for (int i = 0; i < NS_B; ++i) {
@@ -210,10 +216,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         s->abort = 0;
         fence_mbar_init();
     }
-    if (warp == kAProdWarp && lane == 0) {
-        prefetch_tmap(&tm_a0);
-        if (MODE == 0) prefetch_tmap(&tm_a1);
-    }
+    if (MODE != 0 && warp == kAProdWarp && lane == 0) prefetch_tmap(&tm_a0);
     if (warp == kWProdWarp && lane == 0) {
         prefetch_tmap(&tm_w0);
         if (MODE != 2) {
@@ -240,9 +243,59 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int ks_per_sblock = SG * a.G / GK;            // stages per scale block
     const int nb = MODE == 2 ? a.E_pad16 : BN;          // MMA N
 
-    if (warp == kAProdWarp) {
+    if (MODE == 0 && warp >= kLsuWarp0) {
+        // -------------------------------------------- token rows (gate/up)
+        // The unit's 256 token rows are gathered straight from x (it fits in
+        // L2) with 16-byte cp.async: 8 threads per 128-byte row segment, a
+        // warp covers 4 whole rows per instruction, and each chunk lands at
+        // its 128-byte-swizzle position.  A stage is handed to the MMA once
+        // its copies have landed and been made visible to the async proxy;
+        // one stage stays in flight behind the one being issued.  Before the
+        // wait for a free slot (stage it - NS_A consumed), every stage up to
+        // it - 2 has been handed over, so that wait always ends.
+        const int pt = tid - kLsuWarp0 * 32;  // 0..127
+        const int chunk = pt & 7;             // 16-byte chunk of the row segment
+        const int rsub = pt >> 3;             // rows rsub, rsub + 16, ... of the unit
+        uint32_t it = 0, sig = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+            const Unit t = load_unit<MODE>(a, u);
+            const bool shared = t.g == a.E;
+            int tok[TPU * BM / 16];
+#pragma unroll
+            for (int i = 0; i < TPU * BM / 16; ++i) {
+                const int rr = min(rsub + 16 * i, t.n - 1);  // rows past the unit repeat its last row
+                tok[i] = shared ? t.row0 + rr - a.routed_rows : a.rb.row_token[t.row0 + rr];
+            }
+            for (int ks = 0; ks < ksteps && ok; ++ks, ++it) {
+                const int st = it % NS_A;
+                ok = wait_or_abort(&s->a_empty[st], ((it / NS_A) & 1) ^ 1, a, s, 1);
+                if (!ok) break;
+                uint8_t *stage = sA + st * A_STAGE;
+#pragma unroll
+                for (int i = 0; i < TPU * BM / 16; ++i) {
+                    const int rr = rsub + 16 * i;  // row of the unit: tile rr / 128
+                    if (rr < t.ntiles * BM) {
+                        const int r = rr & (BM - 1);
+                        cp_async<16>(stage + (rr / BM) * TILE_A + r * 128 + ((chunk ^ (r & 7)) << 4),
+                                     a.x + static_cast<int64_t>(tok[i]) * a.K + ks * GK + chunk * 8);
+                    }
+                }
+                cp_async_commit();
+                if (sig < it) {  // the previous stage has landed
+                    cp_async_wait<1>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&s->a_full[sig % NS_A]);
+                    ++sig;
+                }
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        for (; sig < it; ++sig) mbar_arrive(&s->a_full[sig % NS_A]);
+    } else if (warp == kAProdWarp) {
         // ------------------------------------------------------- token tiles
-        if (lane == 0) {
+        if (MODE != 0 && lane == 0) {
             uint32_t it = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
@@ -378,7 +431,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             mbar_wait(&s->drain, 0, a.wait_limit);
         }
         __syncwarp();
-    } else if (warp >= kDeqWarp0 && MODE != 2) {
+    } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps && MODE != 2) {
         // ---------------------------------------------------------- dequantise
         const int dt = tid - kDeqWarp0 * 32;
         const int hf = dt / BN;  // 32-element half of the stage
@@ -564,7 +617,8 @@ cudaError_t launch_gemm_t(const GemmMaps &m, const GemmArgs &a, int grid, cudaSt
     const int smem = gemm_smem_bytes(MODE);
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<MODE><<<grid, kGemmThreads, smem, s>>>(m.a0, m.a1, m.w0, m.w1, m.s0, m.b0, m.s1, m.b1, a);
+    grouped_gemm_kernel<MODE><<<grid, gemm_threads(MODE), smem, s>>>(m.a0, m.a1, m.w0, m.w1, m.s0, m.b0, m.s1,
+                                                                     m.b1, a);
     return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ struct GemmArgs {
     int routed_rows;  // T * k: first permuted row of the shared expert
     int E_pad16;      // router: experts rounded up to 16 (MMA N)
     RoutingBufs rb;
+    const __nv_bfloat16 *x;    // [T][H]: layer input (gate/up gathers its token rows from it)
     __nv_bfloat16 *h;          // [R][I]
     float *y_acc;              // [T][H]
     float *logits_part;        // router: [4][T][E_pad16] (parts x K halves)
@@ -70,8 +71,6 @@ cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 
                         int *counts_blk, int64_t n_counts, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm(int mode, const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_zero_i32(int *p, int64_t n, cudaStream_t s);
-cudaError_t launch_xperm(const __nv_bfloat16 *x, __nv_bfloat16 *xp, const int *row_token, int rows, int H,
-                         int num_sms, cudaStream_t s);
 cudaError_t launch_convert(const float *y_acc, __nv_bfloat16 *y, int64_t n, int num_sms, cudaStream_t s);
 size_t decode_smem_bytes(int E, int k, int H, int I, int grid);
 cudaError_t launch_decode(const DecodeStack &a, int grid, cudaStream_t s);

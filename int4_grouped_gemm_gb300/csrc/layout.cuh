@@ -45,7 +45,7 @@ struct RoutingBufs {
 
 struct PrefillLayout {
     size_t ctrl, logits, topk_idx, topk_w, counts_blk, base_blk, counts, offsets, perm, inv_perm, row_token,
-        row_weight, tile_group, tile_row, tile_rows, tile_sched, num_tiles, h, y_acc, wr3, logits_part, xperm,
+        row_weight, tile_group, tile_row, tile_rows, tile_sched, num_tiles, h, y_acc, wr3, logits_part,
         total;
     int max_tiles, nblk, R, E_pad16;
 };
@@ -90,7 +90,6 @@ inline PrefillLayout prefill_layout(int T, int E, int k, int H, int I) {
     L.E_pad16 = (E + 15) / 16 * 16;
     L.wr3 = take(sizeof(uint16_t) * 2 * (size_t)L.E_pad16 * H);
     L.logits_part = take(sizeof(float) * 4 * (size_t)T * L.E_pad16);
-    L.xperm = take(sizeof(uint16_t) * (size_t)T * k * H);
     L.total = o;
     return L;
 }

@@ -14,8 +14,6 @@
 //                         (offsets), canonical tile map, launch schedule
 //   permute_kernel        stable (expert, token) permutation, its inverse and
 //                         the per-row token / combine weight tables
-//   xperm_kernel          the permuted copy of x that the gate/up GEMM reads
-//                         in whole tiles
 // Every table is deterministic: counts and ranks come from per-block counts
 // scanned in token order, never from the order in which atomics land.
 #include "kernels.cuh"
@@ -272,32 +270,6 @@ __global__ void __launch_bounds__(32) permute_kernel(int T, int E, int k, Routin
     }
 }
 
-// x_perm[r] = x[row_token[r]] for the routed rows: one warp per row, every
-// lane issues all its 16-byte loads before its stores.
-__global__ void __launch_bounds__(256) xperm_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ xp,
-                                                    const int *__restrict__ row_token, int rows, int n16) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    const int nwarps = (gridDim.x * blockDim.x) >> 5;
-    for (int r = warp; r < rows; r += nwarps) {
-        const uint4 *src = x + static_cast<int64_t>(row_token[r]) * n16;
-        uint4 *dst = xp + static_cast<int64_t>(r) * n16;
-        constexpr int U = 8;
-        for (int i0 = 0; i0 < n16; i0 += 32 * U) {
-            uint4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = i0 + u * 32 + lane;
-                if (i < n16) v[u] = src[i];
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = i0 + u * 32 + lane;
-                if (i < n16) dst[i] = v[u];
-            }
-        }
-    }
-}
-
 __global__ void zero_i32_kernel(int *__restrict__ p, int64_t n) {
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x)
@@ -319,17 +291,6 @@ cudaError_t launch_routing_tables(const float *logits_part, int ld, const float 
     topk_hist_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits_part, ld, given, bias, T, E, k, has_shared, rb);
     scan_tiles_kernel<<<1, 512, 0, s>>>(T, E, k, has_shared, rb);
     permute_kernel<<<rb.nblk, 32, 0, s>>>(T, E, k, rb);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_xperm(const __nv_bfloat16 *x, __nv_bfloat16 *xp, const int *row_token, int rows, int H,
-                         int num_sms, cudaStream_t s) {
-    if (rows <= 0) return cudaSuccess;
-    const int n16 = H * 2 / 16;
-    int blocks = (rows + 7) / 8;
-    if (blocks > 8 * num_sms) blocks = 8 * num_sms;
-    xperm_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const uint4 *>(x), reinterpret_cast<uint4 *>(xp), row_token,
-                                        rows, n16);
     return cudaGetLastError();
 }
 

@@ -123,7 +123,6 @@ class Workspace:
             tile_rows=self.view(v.tile_rows, torch.int32, n_tiles),
             tile_sched=self.view(v.tile_sched, torch.int32, n_units),
             tile_size=v.tile_size,
-            xperm=self.view(v.xperm, torch.bfloat16, T * k * desc.H).view(T * k, desc.H),
             h=self.view(v.h, torch.bfloat16, (T * k + T) * desc.I).view(T * k + T, desc.I),
             y_acc=self.view(v.y_acc, torch.float32, T * desc.H).view(T, desc.H),
         )
