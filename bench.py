@@ -57,14 +57,19 @@ def parse():
 
 
 def dist_setup(n_gpus):
+    """One process per GPU under torchrun (NCCL); gloo when there is no GPU
+    (the host-side multi-rank logic runs that way in the CPU tests)."""
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl")
+        else:
+            dist.init_process_group("gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(0)
     return rank, world
@@ -76,24 +81,25 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(v, world):
+def _reduce(v, world, op):
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=op)
     return float(t.item())
+
+
+def max_over_ranks(v, world):
+    import torch.distributed as dist
+    return _reduce(v, world, dist.ReduceOp.MAX)
 
 
 def sum_over_ranks(v, world):
-    if world == 1:
-        return v
-    import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.SUM)
-    return float(t.item())
+    return _reduce(v, world, dist.ReduceOp.SUM)
 
 
 def peaks():
