@@ -55,7 +55,6 @@ constexpr int BN = 256;                          // weight rows per tile (MMA N)
 constexpr int GK = 64;                           // K elements per stage
 constexpr int SG = 8;                            // quantisation groups per scale block
 constexpr int NS_A = 3, NS_B = 2, NS_S = 2;      // ring depths
-static_assert(NS_A >= 2, "the gate/up copy producer hands a stage over one stage late");
 constexpr int kMaxNsQ = 4;
 __host__ __device__ constexpr int ns_q(int mode) { return mode == 1 ? 3 : 4; }
 constexpr int kEpiWarps = 8, kWProdWarp = 8, kMmaWarp = 9, kAProdWarp = 10, kDeqWarp0 = 11, kDeqWarps = 16;
@@ -248,15 +247,13 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         // The unit's 256 token rows are gathered straight from x (it fits in
         // L2) with 16-byte cp.async: 8 threads per 128-byte row segment, a
         // warp covers 4 whole rows per instruction, and each chunk lands at
-        // its 128-byte-swizzle position.  A stage is handed to the MMA once
-        // its copies have landed and been made visible to the async proxy;
-        // one stage stays in flight behind the one being issued.  Before the
-        // wait for a free slot (stage it - NS_A consumed), every stage up to
-        // it - 2 has been handed over, so that wait always ends.
+        // its 128-byte-swizzle position.  Every copying thread arrives on the
+        // stage's barrier when its copies have landed (no waiting here), so
+        // the copier runs up to NS_A stages ahead of the MMA.
         const int pt = tid - kLsuWarp0 * 32;  // 0..127
         const int chunk = pt & 7;             // 16-byte chunk of the row segment
         const int rsub = pt >> 3;             // rows rsub, rsub + 16, ... of the unit
-        uint32_t it = 0, sig = 0;
+        uint32_t it = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
             const Unit t = load_unit<MODE>(a, u);
@@ -281,18 +278,14 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                                      a.x + static_cast<int64_t>(tok[i]) * a.K + ks * GK + chunk * 8);
                     }
                 }
-                cp_async_commit();
-                if (sig < it) {  // the previous stage has landed
-                    cp_async_wait<1>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(&s->a_full[sig % NS_A]);
-                    ++sig;
-                }
+                // this thread's arrival on the stage's barrier happens once its
+                // copies have landed; the MMA thread orders them before its
+                // tensor-core reads with a proxy fence after the wait
+                cp_async_arrive_noinc(&s->a_full[st]);
             }
         }
+        cp_async_commit();  // nothing of this thread's may still be landing when the block exits
         cp_async_wait<0>();
-        fence_proxy_async_smem();
-        for (; sig < it; ++sig) mbar_arrive(&s->a_full[sig % NS_A]);
     } else if (warp == kAProdWarp) {
         // ------------------------------------------------------- token tiles
         if (MODE != 0 && lane == 0) {
@@ -399,6 +392,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                     ok = wait_or_abort(&s->a_full[as], (ait / NS_A) & 1, a, s, 6) &&
                          wait_or_abort(&s->b_full[bs], (bit / NS_B) & 1, a, s, 7);
                     if (!ok) break;
+                    if (MODE == 0) fence_proxy_async_smem();  // token rows written by cp.async
                     tc_fence_after();
                     const uint32_t a_addr = smem_u32(sA + as * A_STAGE);
                     const uint32_t b_addr = smem_u32(sB + bs * B_STAGE);
