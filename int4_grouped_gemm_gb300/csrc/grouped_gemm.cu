@@ -515,25 +515,41 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                     }
                 } else if (MODE == 1) {
                     const int f0 = t.nt * BN;
-                    for (int c0 = chalf * 16; c0 < BN; c0 += 32) {
-                        float v[16];
-                        tmem_ld16(tbase + c0, v);
+                    // the 4 rows whose values this lane adds (and whether they are
+                    // real rows) are the same for every column chunk of the tile
+                    int tks[4];
+                    bool vvs[4];
 #pragma unroll
-                        for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4 *>(tbuf + lane * T_PITCH + j) =
-                                make_float4(wgt * v[j], wgt * v[j + 1], wgt * v[j + 2], wgt * v[j + 3]);
-                        __syncwarp();
+                    for (int q = 0; q < 4; ++q) {
+                        tks[q] = __shfl_sync(0xffffffffu, tok, 8 * q + lane / 4);
+                        vvs[q] = __shfl_sync(0xffffffffu, valid, 8 * q + lane / 4);
+                    }
+                    // two column chunks per pass: both TMEM loads are in flight together
+                    for (int c0 = chalf * 16; c0 < BN; c0 += 64) {
+                        uint32_t r2[2][16];
+                        tmem_ld16_issue(tbase + c0, r2[0]);
+                        tmem_ld16_issue(tbase + c0 + 32, r2[1]);
+                        tmem_ld_wait();
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int src = 8 * q + lane / 4;  // row of the warp whose values this lane adds
-                            const int tk = __shfl_sync(0xffffffffu, tok, src);
-                            const bool vv = __shfl_sync(0xffffffffu, valid, src);
-                            const float4 val =
-                                *reinterpret_cast<const float4 *>(tbuf + src * T_PITCH + 4 * (lane % 4));
-                            if (vv)
-                                red_add_v4(a.y_acc + static_cast<int64_t>(tk) * a.H + f0 + c0 + 4 * (lane % 4), val);
+                        for (int h = 0; h < 2; ++h) {
+                            const int cc = c0 + 32 * h;
+#pragma unroll
+                            for (int j = 0; j < 16; j += 4)
+                                *reinterpret_cast<float4 *>(tbuf + lane * T_PITCH + j) =
+                                    make_float4(wgt * __uint_as_float(r2[h][j]), wgt * __uint_as_float(r2[h][j + 1]),
+                                                wgt * __uint_as_float(r2[h][j + 2]), wgt * __uint_as_float(r2[h][j + 3]));
+                            __syncwarp();
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int src = 8 * q + lane / 4;  // row of the warp whose values this lane adds
+                                const float4 val =
+                                    *reinterpret_cast<const float4 *>(tbuf + src * T_PITCH + 4 * (lane % 4));
+                                if (vvs[q])
+                                    red_add_v4(a.y_acc + static_cast<int64_t>(tks[q]) * a.H + f0 + cc + 4 * (lane % 4),
+                                               val);
+                            }
+                            __syncwarp();
                         }
-                        __syncwarp();
                     }
                 } else {
                     float *lrow = a.logits_part +
