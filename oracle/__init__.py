@@ -50,10 +50,16 @@ _i64 = ctypes.c_int64
 
 
 def lib():
+    """The compiled oracle.  MOE_ORACLE_LIB names another build of the same
+    source to load instead (the mutation tests load deliberately broken
+    copies that way, to show that the pins catch them)."""
     global _lib
     if _lib is None:
-        build()
-        L = ctypes.CDLL(_LIB)
+        path = os.environ.get("MOE_ORACLE_LIB")
+        if not path:
+            build()
+            path = _LIB
+        L = ctypes.CDLL(path)
         L.oracle_bf16_round.argtypes = [_p, _i64, _p]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_quantize.argtypes = [_p, _i64, _i32, _i32, _p, _p, _p]
