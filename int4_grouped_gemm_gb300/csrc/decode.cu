@@ -19,8 +19,10 @@
 //      experts and of the shared expert: a block owns a contiguous range of
 //      (slot, feature) pairs, one warp per pair, h = silu(g) * u
 //   C  one warp per output feature over the down rows of all k + 1 experts,
-//      weighted combine fused, bf16 out; the next layer's router and shared
-//      expert are prefetched into L2 meanwhile
+//      weighted combine fused, bf16 out; each block then adds its output
+//      features' share of the next layer's router logits (fp64 atomics), so
+//      that later layers skip phase A and its barrier; the next layer's
+//      router and shared expert are prefetched into L2 meanwhile
 // Loads that do not depend on the previous phase (router rows, down rows)
 // are issued before the barrier wait, so their latency overlaps it.  Only the router and the k + 1 touched experts are read.  The int4 dot
 // products use sum_i x_i (s q_i + b) = s sum_i x_i q_i + b sum_i x_i per
@@ -32,6 +34,7 @@ namespace moe {
 constexpr int kDecThreads = 512;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMaxSlots = 9;        // k <= 8 routed + 1 shared
+constexpr int kMaxYSlice = 64;      // output features per block: H / grid (4096 / 64 at least)
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -333,17 +336,23 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
 // Top-k of E <= 256 logits (ties -> lower expert index) and the softmax over
 // the picked ones.  Warps 0-7 each sort 32 experts' keys; the 8 best of every
 // warp (64 keys) are sorted again in two rounds by warp 0.  The logit of
-// expert e is the sum of its four K-quarter partial sums in a fixed order,
-// plus the bias.  Every block computes the same result.
-__device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bias, unsigned long long *s_keys,
-                                           int *s_idx, float *s_w) {
+// expert e is the sum of its four K-quarter partial sums in a fixed order
+// (first layer of a launch) or the fp64 sum that the previous layer's blocks
+// accumulated, plus the bias.  Every block computes the same result.
+__device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bias, const double *racc,
+                                           unsigned long long *s_keys, int *s_idx, float *s_w) {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     if (warp < 8) {
         unsigned long long key = 0;  // below every real key
         if (t < a.E) {
-            float l = __ldcg(a.logits_part + t) + __ldcg(a.logits_part + a.E + t);
-            l += __ldcg(a.logits_part + 2 * a.E + t);
-            l += __ldcg(a.logits_part + 3 * a.E + t);
+            float l;
+            if (racc) {
+                l = static_cast<float>(__ldcg(racc + t));  // summed by the previous layer's blocks
+            } else {
+                l = __ldcg(a.logits_part + t) + __ldcg(a.logits_part + a.E + t);
+                l += __ldcg(a.logits_part + 2 * a.E + t);
+                l += __ldcg(a.logits_part + 3 * a.E + t);
+            }
             if (bias) l += __ldg(bias + t);
             key = topk_key(l, t);
         }
@@ -389,6 +398,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     __shared__ float s_w[kMaxSlots];
     __shared__ int s_ok;
     __shared__ unsigned long long s_keys[64];
+    __shared__ float s_y[kMaxYSlice];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int G = gridDim.x, b = blockIdx.x;
     const int gw = b * kDecWarps + warp, NW = G * kDecWarps;
@@ -409,11 +419,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         __nv_bfloat16 *out = l == a.n_total - 1 ? a.y : a.act + (l % 2) * a.H;
 
         // ------------------------------------------------------------ phase A
-        // this warp's first unit: its weights do not depend on the input, so
-        // they are loaded before waiting for the previous layer
-        UnitRegs<HMAX> ur;
-        const int u0 = gw;
-        if (u0 < n_a_units) router_load(a, P.Wr, u0, lane, ur);
+        // Only the first layer of a launch: later layers' router logits are
+        // summed by the previous layer's phase C.
         if (tid == 0 && a.has_shared) {
             // the shared expert's down rows are read in phase C
             const int64_t r0 = static_cast<int64_t>(a.E) * a.H;
@@ -421,15 +428,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             prefetch_slice(P.sd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
             prefetch_slice(P.bd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
         }
-        if (li > 0 && !grid_wait(a.ctrl, ++nbar * G, lim, 1, &s_ok)) return;
-        stage_x(in, a.H, xs, xsum8);
-        __syncthreads();
-        for (int u = u0; u < n_a_units; u += NW) {
-            if (u != u0) router_load(a, P.Wr, u, lane, ur);
-            const float acc = warp_sum(router_dot(a, u, lane, ur, xs));
-            if (lane == 0) a.logits_part[(u & 3) * a.E + (u >> 2)] = acc;
+        if (li == 0) {
+            UnitRegs<HMAX> ur;
+            const int u0 = gw;
+            if (u0 < n_a_units) router_load(a, P.Wr, u0, lane, ur);
+            stage_x(in, a.H, xs, xsum8);
+            __syncthreads();
+            for (int u = u0; u < n_a_units; u += NW) {
+                if (u != u0) router_load(a, P.Wr, u, lane, ur);
+                const float acc = warp_sum(router_dot(a, u, lane, ur, xs));
+                if (lane == 0) a.logits_part[(u & 3) * a.E + (u >> 2)] = acc;
+            }
+            grid_arrive(a.ctrl);
         }
-        grid_arrive(a.ctrl);
 
         // ------------------------------------------------------------ phase B
         // this block's contiguous range of (slot, feature) pairs of the gate/up
@@ -439,7 +450,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         const int f_lo = static_cast<int>((static_cast<int64_t>(b) * F) / G);
         const int f_hi = static_cast<int>((static_cast<int64_t>(b + 1) * F) / G);
         if (!grid_wait(a.ctrl, ++nbar * G, lim, 2, &s_ok)) return;
-        topk_block(a, P.bias, s_keys, s_idx, s_w);
+        if (li > 0) {
+            // the layer input, complete once every block passed the barrier
+            stage_x(in, a.H, xs, xsum8);
+        }
+        topk_block(a, P.bias, li == 0 ? nullptr : a.racc + (l % 2) * a.E, s_keys, s_idx, s_w);
+        if (b == 0 && li + 1 < a.n_layers) {
+            // the next layer's logit sums start from zero; this buffer was last
+            // read by the previous layer's top-k, before the previous barrier
+            for (int e = tid; e < a.E; e += kDecThreads) a.racc[((l + 1) % 2) * a.E + e] = 0.0;
+        }
         if (b == 0 && tid < a.k) {
             a.topk_idx[tid] = s_idx[tid];
             a.topk_w[tid] = s_w[tid];
@@ -527,9 +547,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         for (int f = y_lo + warp; f < y_hi; f += kDecWarps) {
             const bool pre = preload && f == y_lo + warp;
             const float y = warp_sum(down_dot(a, P, e_j, w_j, nslots, f, lane, gshift, dl, pre, hs, hsum8, ip));
-            if (lane == 0) out[f] = __float2bfloat16_rn(y);
+            if (lane == 0) {
+                const __nv_bfloat16 yb = __float2bfloat16_rn(y);
+                out[f] = yb;
+                s_y[f - y_lo] = __bfloat162float(yb);
+            }
         }
-        if (li + 1 < a.n_layers) grid_arrive(a.ctrl);
+        if (li + 1 < a.n_layers) {
+            // this block's share of the next layer's router logits: its output
+            // features times the matching router columns, two threads per
+            // expert, added into the next layer's buffer in fp64
+            __syncthreads();
+            const float *nWr = a.L[li + 1].Wr;
+            const int e = tid >> 1, half = tid & 1;
+            float part = 0.f;
+            if (e < a.E)
+                for (int f = y_lo + half; f < y_hi; f += 2)
+                    part = fmaf(__ldg(nWr + static_cast<int64_t>(e) * a.H + f), s_y[f - y_lo], part);
+            part += __shfl_xor_sync(0xffffffffu, part, 1);
+            if (half == 0 && e < a.E) atomicAdd(a.racc + ((l + 1) % 2) * a.E + e, static_cast<double>(part));
+            grid_arrive(a.ctrl);
+        }
         __syncthreads();  // hs is overwritten by the next layer's staging
     }
 }
@@ -542,6 +580,7 @@ size_t decode_smem_bytes(int E, int k, int H, int I, int grid) {
 
 template <int HMAX>
 static cudaError_t launch_decode_t(const DecodeStack &a, int grid, cudaStream_t s) {
+    if ((a.H + grid - 1) / grid > kMaxYSlice) return cudaErrorInvalidConfiguration;  // too few SMs for H
     const size_t smem = decode_smem_bytes(a.E, a.k, a.H, a.I, grid);
     cudaError_t e = cudaFuncSetAttribute(decode_stack_kernel<HMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));

@@ -51,7 +51,7 @@ struct PrefillLayout {
 };
 
 struct DecodeLayout {
-    size_t ctrl, logits, topk_idx, topk_w, h, act, total;
+    size_t ctrl, logits, topk_idx, topk_w, h, racc, act, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -107,6 +107,7 @@ inline DecodeLayout decode_layout(int E, int k, int I) {
     L.topk_idx = take(sizeof(int) * 8);
     L.topk_w = take(sizeof(float) * 8);
     L.h = take(sizeof(float) * (size_t)(k + 1) * I);
+    L.racc = take(sizeof(double) * 2 * (size_t)E);
     L.act = 0;
     L.total = o;
     return L;
