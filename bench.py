@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer prefill tok/s @T=4096; batch-1 decode tok/s; % of roofline"
 PREFILL_CFG = "prefill4096"
 DECODE_CFG = "decode40"
-KERNELS_PER_PREFILL = 9      # prep, router GEMM, top-k, scan, permute, x copy, gate/up GEMM, down GEMM, convert
+KERNELS_PER_PREFILL = 8      # prep, router GEMM, top-k, scan, permute, gate/up GEMM, down GEMM, convert
 DECODE_LAYERS_PER_KERNEL = 64  # one persistent decode kernel runs up to 64 layers of a step
 
 
@@ -401,8 +401,9 @@ def oracle_time(cfg, s, toks):
 def cpu_baseline(cfg, target_s=15.0):
     import oracle
     s = oracle_sample(cfg, 2048)
-    t = oracle_time(cfg, s, s["toks"][:4])
-    n = int(max(4, min(2048, 4 * target_s / max(t, 1e-3))))
+    oracle_time(cfg, s, s["toks"][:4])           # first call: thread start-up, page-in
+    t = oracle_time(cfg, s, s["toks"][:32])
+    n = int(max(32, min(2048, 32 * target_s / max(t, 1e-3))))
     t = oracle_time(cfg, s, s["toks"][:n])
     return {"value": round(n / t, 3), "unit": "tok/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{n} of the {cfg.T} tokens of the {cfg.name} layer (router, top-8, 8 routed + shared "
