@@ -132,10 +132,13 @@ __device__ __forceinline__ int vpos(int k) { return k + ((k >> 5) << 2); }
 __host__ __device__ constexpr int vlen(int n) { return n + n / 8; }  // padded length (n % 32 == 0)
 
 // Layer input to shared memory as fp32 (padded positions) plus the sum of
-// every 8-element word; it was written by other blocks, so it is read from L2.
-__device__ __forceinline__ void stage_x(const __nv_bfloat16 *x, int H, float *xs, float *xsum8) {
+// every 8-element word, by threads t0 .. t0 + nthreads - 1; it was written by
+// other blocks, so it is read from L2.
+__device__ __forceinline__ void stage_x(const __nv_bfloat16 *x, int H, float *xs, float *xsum8, int t0 = 0,
+                                        int nthreads = 0) {
     const int nw = H / 8;
-    for (int w = threadIdx.x; w < nw; w += blockDim.x) {
+    if (nthreads == 0) nthreads = blockDim.x;
+    for (int w = static_cast<int>(threadIdx.x) - t0; w >= 0 && w < nw; w += nthreads) {
         const uint4 raw = __ldcg(reinterpret_cast<const uint4 *>(x) + w);
         const uint32_t p[4] = {raw.x, raw.y, raw.z, raw.w};
         float sum = 0.f;
@@ -451,8 +454,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         const int f_hi = static_cast<int>((static_cast<int64_t>(b + 1) * F) / G);
         if (!grid_wait(a.ctrl, ++nbar * G, lim, 2, &s_ok)) return;
         if (li > 0) {
-            // the layer input, complete once every block passed the barrier
-            stage_x(in, a.H, xs, xsum8);
+            // the layer input, complete once every block passed the barrier:
+            // warps 8-15 stage it while warps 0-7 start the top-k below
+            stage_x(in, a.H, xs, xsum8, 256, kDecThreads - 256);
         }
         topk_block(a, P.bias, li == 0 ? nullptr : a.racc + (l % 2) * a.E, s_keys, s_idx, s_w);
         if (b == 0 && li + 1 < a.n_layers) {

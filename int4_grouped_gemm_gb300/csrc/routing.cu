@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(512) scan_tiles_kernel(int T, int E, int k, in
         // running sum over the token chunks; loads batched so that many are
         // in flight at once
         int run = 0;
-        constexpr int BATCH = 16;
+        constexpr int BATCH = 64;  // every chunk of a 4096-token call in one round of loads
         for (int b0 = 0; b0 < rb.nblk; b0 += BATCH) {
             int c[BATCH];
 #pragma unroll
