@@ -28,8 +28,11 @@
  *
  * Weight format (int4 asymmetric, groups of `group` consecutive K elements):
  *   value = scale * q + bias, q unsigned in 0..15, scale and bias bf16.
- *   q:      uint32 [rows][K/8]; element k of a row is in word k/8 at bits
- *           4*(k%8) .. 4*(k%8)+3 (low nibble first).
+ *   q:      uint32 [rows][K/8]; element k of a row is in word k/8, in
+ *           nibble n(k%8) = (k%8)/2 + 4*((k%8)%2), i.e. bits 4n .. 4n+3:
+ *           the even elements of the word fill nibbles 0-3 and the odd ones
+ *           nibbles 4-7, so that nibbles j and j+4 are the adjacent pair
+ *           (2j, 2j+1).
  *   scale, bias: bf16 bit patterns, uint16 [rows][ldg] with the row pitch
  *           ldg = K/group rounded up to a multiple of 8 (16 bytes, so that
  *           8-group blocks can be moved by TMA); entries past K/group are 0.

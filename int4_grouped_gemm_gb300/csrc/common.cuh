@@ -242,18 +242,18 @@ __device__ __forceinline__ __nv_bfloat162 u32_as_bf162(uint32_t u) {
     return *reinterpret_cast<__nv_bfloat162 *>(&u);
 }
 
-// Eight int4 codes (element i at bits 4i) -> eight bf16 weights s*q + b, each
-// rounded once (round to nearest even) from the exact value: 128 + q is built
-// by bit insertion into the bf16 pattern of 128, 128 is subtracted exactly,
-// and one fused multiply-add applies scale and bias.
+// Eight int4 codes (element 2j in nibble j, 2j + 1 in nibble j + 4) -> eight
+// bf16 weights s*q + b in element order, each rounded once (round to nearest
+// even) from the exact value: one mask of the word shifted by 4j lifts the
+// pair (2j, 2j + 1) into the two halves of a bf16x2 as 128 + q, 128 is
+// subtracted exactly, and one fused multiply-add applies scale and bias.
 __device__ __forceinline__ uint4 dequant8_bf16(uint32_t word, __nv_bfloat162 s2, __nv_bfloat162 b2) {
-    const uint32_t hi = word >> 4;
     const __nv_bfloat162 c128 = u32_as_bf162(0x43004300u);
     uint32_t p[4];
-    p[0] = __byte_perm(word, hi, 0x0400);
-    p[1] = __byte_perm(word, hi, 0x0501);
-    p[2] = __byte_perm(word, hi, 0x0602);
-    p[3] = __byte_perm(word, hi, 0x0703);
+    p[0] = word;
+    p[1] = word >> 4;
+    p[2] = word >> 8;
+    p[3] = word >> 12;
     uint4 out;
     uint32_t *o = reinterpret_cast<uint32_t *>(&out);
 #pragma unroll

@@ -106,14 +106,15 @@ __device__ __forceinline__ bool grid_wait(Ctrl *c, unsigned target, long long li
 }
 
 // 8 int4 codes -> sum_i x_i * (128 + q_i) (x: 8 consecutive fp32 in shared
-// memory, 16-byte aligned).  Codes j and j + 4 are lifted together into the
-// two bf16 halves of one register as 128 + q (exact), and each half widens to
-// fp32 with one shift or mask; callers subtract 128 * sum_i x_i (folded into
-// the bias term).  Two accumulators halve the dependent FMA chain.
+// memory, 16-byte aligned).  Nibbles j and j + 4 hold elements 2j and 2j + 1:
+// they are lifted together into the two bf16 halves of one register as
+// 128 + q (exact), and each half widens to fp32 with one shift or mask;
+// callers subtract 128 * sum_i x_i (folded into the bias term).  Two
+// accumulators halve the dependent FMA chain.
 __device__ __forceinline__ float dot8_codes128(uint32_t word, const float *xv) {
     const float4 x0 = *reinterpret_cast<const float4 *>(xv);
     const float4 x1 = *reinterpret_cast<const float4 *>(xv + 4);
-    const float xl[4] = {x0.x, x0.y, x0.z, x0.w}, xh[4] = {x1.x, x1.y, x1.z, x1.w};
+    const float xl[4] = {x0.x, x0.z, x1.x, x1.z}, xh[4] = {x0.y, x0.w, x1.y, x1.w};  // elements 2j, 2j + 1
     float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {

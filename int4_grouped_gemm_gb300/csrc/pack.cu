@@ -7,7 +7,8 @@
 // values wins), rounds scale and bias to bf16 (nearest even) and codes every
 // element in fp32 with IEEE subtraction and division, round half to even.
 // Scale and bias rows have a pitch of K/G rounded up to 8 groups (16 bytes);
-// the padding is written as zero.
+// the padding is written as zero.  Inside a word, element 2j goes to nibble j
+// and element 2j + 1 to nibble j + 4 (the order include/moe.h states).
 #include "kernels.cuh"
 
 namespace moe {
@@ -53,7 +54,7 @@ __global__ void __launch_bounds__(256) pack_int4_kernel(const float *__restrict_
                 const float rq = rintf(t);
                 code = rq < 0.0f ? 0 : (rq > 15.0f ? 15 : static_cast<int>(rq));
             }
-            word |= static_cast<uint32_t>(code) << (4 * i);
+            word |= static_cast<uint32_t>(code) << (4 * (i / 2 + 4 * (i % 2)));  // even elements low
         }
         qrow[w8] = word;
     }

@@ -36,9 +36,10 @@
  * Build without -ffast-math and with -ffp-contract=off so that every fp32
  * operation is one IEEE operation in the written order.
  *
- * Packed layout (little end first): the code of element k of a row lives in
- * 32-bit word k/8 of that row, bits 4*(k%8) .. 4*(k%8)+3.  Scale and bias are
- * bf16 bit patterns, one per (row, group), row-major [rows][K/G].
+ * Packed layout: the code of element k of a row lives in 32-bit word k/8 of
+ * that row, in nibble n = p/2 + 4*(p%2) with p = k%8 (bits 4n .. 4n+3): the
+ * word's even elements fill nibbles 0-3, its odd ones nibbles 4-7.  Scale and
+ * bias are bf16 bit patterns, one per (row, group), row-major [rows][K/G].
  */
 #include <math.h>
 #include <stdint.h>
@@ -87,9 +88,16 @@ int oracle_num_threads(void)
 
 /* ------------------------------------------------------- int4 quantiser */
 
+/* Nibble of element p (0..7) inside its word: even elements in nibbles 0-3,
+ * odd ones in nibbles 4-7 (element 2j in nibble j, 2j + 1 in nibble j + 4). */
+static int nibble_of(int32_t p)
+{
+    return p / 2 + 4 * (p % 2);
+}
+
 static int get_code(const uint32_t *row_words, int32_t k)
 {
-    return (int)((row_words[k / 8] >> (4 * (k % 8))) & 0xFu);
+    return (int)((row_words[k / 8] >> (4 * nibble_of(k % 8))) & 0xFu);
 }
 
 /*
@@ -137,7 +145,7 @@ void oracle_quantize(const float *w, int64_t rows, int32_t K, int32_t G,
                     else code = (int)rq;
                 }
                 int32_t k = g * G + i;
-                qrow[k / 8] |= (uint32_t)code << (4 * (k % 8));
+                qrow[k / 8] |= (uint32_t)code << (4 * nibble_of(k % 8));
             }
         }
     }

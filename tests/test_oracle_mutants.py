@@ -16,8 +16,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "moe_oracle.c")
 
 MUTANTS = [
-    ("nibble_order_high_first", "return (int)((row_words[k / 8] >> (4 * (k % 8))) & 0xFu);",
-     "return (int)((row_words[k / 8] >> (4 * (7 - k % 8))) & 0xFu);"),
+    ("nibble_order_plain", "return p / 2 + 4 * (p % 2);", "return p;"),
     ("scale_over_16", "float s_exact = range / 15.0f;", "float s_exact = range / 16.0f;"),
     ("code_rounds_down", "float rq = nearbyintf(t);", "float rq = floorf(t);"),
     ("bias_subtracted", "return s * (double)code + b;", "return s * (double)code - b;"),

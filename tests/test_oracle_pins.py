@@ -48,13 +48,15 @@ def test_quantize_hand_packed(fixture_loader):
     np.testing.assert_array_equal(deq, np.array([fx["deq_row0"], fx["deq_row1"]], np.float64))
 
 
-def test_nibble_order_low_first():
-    # codes 0..7 and 15..8 in one row: word k/8 holds element k at bits 4*(k%8)
+def test_nibble_order_even_elements_low():
+    # word k/8 holds element 2j of the word in nibble j and 2j+1 in nibble j+4
     s_bits = 0x3F80  # scale 1, bias 0 -> w == code
     w = np.array([[0, 15, 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14]], np.float32)
     q, s, b = oracle.quantize(w, 16)
     assert s[0, 0] == s_bits and b[0, 0] == 0
-    assert q[0, 0] == 0x6543_21F0 and q[0, 1] == 0xEDCB_A987
+    # word 0: elements 0 15 1 2 3 4 5 6 -> nibbles (low to high) 0 1 3 5 | 15 2 4 6
+    # word 1: elements 7 .. 14            -> nibbles 7 9 11 13 | 8 10 12 14
+    assert q[0, 0] == 0x642F_5310 and q[0, 1] == 0xECA8_DB97
 
 
 def _bf16_of(x):
