@@ -14,19 +14,21 @@
 //   A  router partial sums over K quarters (one warp per expert and
 //      quarter); every block stages the layer input in shared memory
 //   B  every block computes the same top-k from the partial sums (a bitonic
-//      sort of 64-bit keys in registers), prefetches its share of the picked
-//      experts' down rows into L2, then the gate/up rows of the k routed
-//      experts and of the shared expert: a block owns a contiguous range of
-//      (slot, feature) pairs, one warp per pair, h = silu(g) * u
+//      sort of 64-bit keys in registers), then the gate/up rows of the k
+//      routed experts and of the shared expert: a block owns a contiguous
+//      range of (slot, feature) pairs, one warp per pair, h = silu(g) * u
 //   C  one warp per output feature over the down rows of all k + 1 experts,
 //      weighted combine fused, bf16 out; each block then adds its output
 //      features' share of the next layer's router logits (fp64 atomics), so
-//      that later layers skip phase A and its barrier; the next layer's
-//      router and shared expert are prefetched into L2 meanwhile
-// Loads that do not depend on the previous phase (router rows, down rows)
-// are issued before the barrier wait, so their latency overlaps it.  Only the router and the k + 1 touched experts are read.  The int4 dot
-// products use sum_i x_i (s q_i + b) = s sum_i x_i q_i + b sum_i x_i per
-// 8-element word, with the per-word input sums computed once per block.
+//      that later layers skip phase A and its barrier
+// A block's output features are fixed, so what phase C reads is copied into
+// shared memory with cp.async as soon as it is known, while the earlier
+// phases run: the shared expert's down rows and the next layer's router
+// columns at the start of the layer, the picked experts' down rows right
+// after the gate/up rows have been requested.  Only the router and the k + 1
+// touched experts are read.  The int4 dot products use
+// sum_i x_i (s q_i + b) = s sum_i x_i q_i + b sum_i x_i per 8-element word,
+// with the per-word input sums computed once per block.
 #include "kernels.cuh"
 
 namespace moe {
@@ -48,17 +50,18 @@ __device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
 }
 
 // Slice `part` of `parts` of [p, p + bytes) into L2 (16-byte granules, at
-// most 64 KB per instruction); p is 16-byte aligned.
+// most 64 KB per instruction); p is 16-byte aligned, bytes < 2^36 (32-bit
+// arithmetic on granules keeps the issuing thread short).
 __device__ __forceinline__ void prefetch_slice(const void *p, size_t bytes, int part, int parts) {
-    const size_t granules = bytes / 16;
-    const size_t per = (granules + parts - 1) / parts;
-    size_t g0 = per * part, g1 = g0 + per;
+    const uint32_t granules = static_cast<uint32_t>(bytes / 16);
+    const uint32_t per = (granules + parts - 1) / static_cast<uint32_t>(parts);
+    uint32_t g0 = per * part, g1 = g0 + per;
     if (g1 > granules) g1 = granules;
-    const char *c = static_cast<const char *>(p) + g0 * 16;
+    const char *c = static_cast<const char *>(p) + static_cast<size_t>(g0) * 16;
     while (g0 < g1) {
-        const size_t n = (g1 - g0) > 4096 ? 4096 : (g1 - g0);
-        prefetch_l2(c, static_cast<uint32_t>(n * 16));
-        c += n * 16;
+        const uint32_t n = (g1 - g0) > 4096 ? 4096 : (g1 - g0);
+        prefetch_l2(c, n * 16);
+        c += static_cast<size_t>(n) * 16;
         g0 += n;
     }
 }
@@ -260,49 +263,99 @@ __device__ __forceinline__ void row_pair_dot(const DecodeStack &a, const DecodeL
 
 // ------------------------------------------------------------ phase C parts
 
-// Down rows of one output feature f: lane holds words 2*lane, 2*lane + 1 of
-// every slot's row (I <= 512: the whole row; wider rows are read in place).
-// Both words share a quantisation group (G >= 16); scales and biases are
-// read when the row is used (they were prefetched into L2 with the rows).
-struct DownLoad {
-    uint2 q[kMaxSlots];
+// Shared-memory staging of what a block's output features need in phase C,
+// copied with cp.async while earlier phases run: the down rows of every slot
+// for features [y_lo, y_lo + ys) (row r of slot j at dq + (j * ys_cap + r) *
+// I/8 words, its scales and biases at ds / db + (j * ys_cap + r) * ldg_i) and
+// the next layer's router columns [c0, c0 + wr_ld) of every expert (c0 = y_lo
+// rounded down to 4 floats).  All sources are 16-byte aligned: a down row is
+// I/2 bytes (I % 32 == 0), a scale row ldg_i * 2 bytes (ldg_i % 8 == 0) and a
+// router row H * 4 bytes.
+struct DownStage {
+    uint32_t *dq;
+    uint16_t *ds, *db;
+    float *wr;
+    int ys_cap, wr_ld;
 };
 
-__device__ __forceinline__ void down_load(const DecodeStack &a, const DecodeLayerPtrs &P, const int *e_j, int nslots,
-                                          int f, int lane, int gshift, DownLoad &d) {
-    // e_j: expert of each slot (shared memory)
+// Slots j0 .. j1 - 1 (experts e_j) of this block's down rows, by threads
+// t .. in steps of nt.
+__device__ __forceinline__ void stage_down_rows(const DecodeStack &a, const DecodeLayerPtrs &P, const int *e_j, int j0,
+                                                int j1, int y_lo, int ys, const DownStage &st, int t, int nt) {
     const int nw = a.I / 8;
-    const int w = 2 * lane;
-#pragma unroll
-    for (int j = 0; j < kMaxSlots; ++j) {
-        if (j < nslots && w < nw) {
-            const int64_t row = static_cast<int64_t>(e_j[j]) * a.H + f;
-            d.q[j] = __ldg(reinterpret_cast<const uint2 *>(P.qd + row * nw + w));
+    const int qc = ys * nw / 4;        // 16-byte chunks of one slot's rows
+    const int sc = ys * a.ldg_i / 8;   // ... of its scales (and of its biases)
+    const int per = qc + 2 * sc;
+    for (int c = t; c < (j1 - j0) * per; c += nt) {
+        const int j = j0 + c / per, r = c % per;
+        const int64_t row0 = static_cast<int64_t>(e_j[j]) * a.H + y_lo;
+        const int srow = j * st.ys_cap;
+        if (r < qc) {
+            cp_async<16>(reinterpret_cast<uint4 *>(st.dq + static_cast<int64_t>(srow) * nw) + r,
+                         reinterpret_cast<const uint4 *>(P.qd + row0 * nw) + r);
+        } else {
+            const int rs = r - qc < sc ? r - qc : r - qc - sc;
+            const uint16_t *src = (r - qc < sc ? P.sd : P.bd) + row0 * a.ldg_i;
+            uint16_t *dst = (r - qc < sc ? st.ds : st.db) + srow * a.ldg_i;
+            cp_async<16>(reinterpret_cast<uint4 *>(dst) + rs, reinterpret_cast<const uint4 *>(src) + rs);
         }
     }
 }
 
-// This lane's share of y[f]: sum over slots of w_j (s * h.(128+q) + (b - 128 s) * sum h).
+// Router columns c0 .. c0 + wr_ld - 1 (clipped to H) of every expert.
+__device__ __forceinline__ void stage_router_cols(const DecodeStack &a, const float *Wr, int c0, const DownStage &st,
+                                                  int t, int nt) {
+    const int n4 = st.wr_ld / 4;
+    for (int c = t; c < a.E * n4; c += nt) {
+        const int e = c / n4, v = c % n4;
+        if (c0 + 4 * v < a.H)
+            cp_async<16>(st.wr + e * st.wr_ld + 4 * v, Wr + static_cast<int64_t>(e) * a.H + c0 + 4 * v);
+    }
+}
+
+// This lane's share of y[f]: sum over slots of w_j (s * h.(128+q) + (b - 128 s) * sum h);
+// lane holds words 2*lane, 2*lane + 1 (+ 64 i) of every slot's row, which
+// share a quantisation group (G >= 16).  Rows come from the staged copy
+// (fl = f - y_lo) or, when it did not fit in shared memory, from global memory.
+template <bool kStaged>
 __device__ __forceinline__ float down_dot(const DecodeStack &a, const DecodeLayerPtrs &P, const int *e_j,
-                                          const float *w_j, int nslots, int f, int lane, int gshift,
-                                          const DownLoad &d, bool preloaded, const float *hs, const float *hsum8,
-                                          int ip) {
+                                          const float *w_j, int nslots, int f, int fl, int lane, int gshift,
+                                          const DownStage &st, const float *hs, const float *hsum8, int ip) {
     const int nw = a.I / 8;
     float y = 0.f;
 #pragma unroll
     for (int j = 0; j < kMaxSlots; ++j) {
         if (j < nslots) {
-            const int64_t row = static_cast<int64_t>(e_j[j]) * a.H + f;
+            const uint32_t *qrow;
+            const uint16_t *srow, *brow;
+            if (kStaged) {
+                const int r = j * st.ys_cap + fl;
+                qrow = st.dq + static_cast<int64_t>(r) * nw;
+                srow = st.ds + r * a.ldg_i;
+                brow = st.db + r * a.ldg_i;
+            } else {
+                const int64_t row = static_cast<int64_t>(e_j[j]) * a.H + f;
+                qrow = P.qd + row * nw;
+                srow = P.sd + row * a.ldg_i;
+                brow = P.bd + row * a.ldg_i;
+            }
             const float *hv = hs + j * ip;
             float acc = 0.f;
             for (int w = 2 * lane; w < nw; w += 64) {
-                const uint2 qv = preloaded ? d.q[j] : __ldg(reinterpret_cast<const uint2 *>(P.qd + row * nw + w));
-                const uint16_t sb = __ldg(P.sd + row * a.ldg_i + ((w * 8) >> gshift));
-                const uint16_t bb = __ldg(P.bd + row * a.ldg_i + ((w * 8) >> gshift));
-                const float s = bf16_bits_to_float(sb), b = bf16_bits_to_float(bb);
+                uint2 qv;
+                float sv, bv;
+                if (kStaged) {
+                    qv = *reinterpret_cast<const uint2 *>(qrow + w);
+                    sv = bf16_bits_to_float(srow[(w * 8) >> gshift]);
+                    bv = bf16_bits_to_float(brow[(w * 8) >> gshift]);
+                } else {
+                    qv = __ldg(reinterpret_cast<const uint2 *>(qrow + w));
+                    sv = bf16_bits_to_float(__ldg(srow + ((w * 8) >> gshift)));
+                    bv = bf16_bits_to_float(__ldg(brow + ((w * 8) >> gshift)));
+                }
                 const float dsum = dot8_codes128(qv.x, hv + vpos(w * 8)) + dot8_codes128(qv.y, hv + vpos(w * 8 + 8));
                 const float hsum = hsum8[j * nw + w] + hsum8[j * nw + w + 1];
-                acc += s * dsum + (b - 128.0f * s) * hsum;
+                acc += sv * dsum + (bv - 128.0f * sv) * hsum;
             }
             y += w_j[j] * acc;
         }
@@ -395,6 +448,16 @@ __host__ __device__ inline int decode_smem_floats(int H, int I, int k) {
     return x_words > h_words ? x_words : h_words;
 }
 
+// Shared memory beyond the x / h region: the staged down rows (when
+// stage_down) and router columns (when stage_router), in 4-byte words.
+__host__ __device__ inline int decode_stage_words(const DecodeStack &a, bool down, bool router) {
+    const int slots = a.k + 1;
+    int w = 0;
+    if (down) w += slots * a.ys_cap * (a.I / 8) + slots * a.ys_cap * a.ldg_i;  // q words + scales and biases (u16)
+    if (router) w += a.E * a.wr_ld;
+    return w;
+}
+
 template <int HMAX>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __grid_constant__ DecodeStack a) {
     extern __shared__ __align__(16) float dsm[];
@@ -416,22 +479,47 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     unsigned nbar = 0;  // grid barriers passed in this launch
     const long long lim = a.wait_limit;
 
+    // this block's output features and the staging buffers behind the x / h region
+    const int y_lo = static_cast<int>((static_cast<int64_t>(b) * a.H) / G);
+    const int y_hi = static_cast<int>((static_cast<int64_t>(b + 1) * a.H) / G);
+    const int ys = y_hi - y_lo;
+    const int c0 = y_lo & ~3;
+    DownStage st;
+    {
+        float *p = dsm + decode_smem_floats(a.H, a.I, a.k);
+        st.ys_cap = a.ys_cap;
+        st.wr_ld = a.wr_ld;
+        st.wr = p;
+        if (a.stage_router) p += a.E * a.wr_ld;
+        st.dq = reinterpret_cast<uint32_t *>(p);
+        st.ds = reinterpret_cast<uint16_t *>(st.dq + (a.k + 1) * a.ys_cap * (a.I / 8));
+        st.db = st.ds + (a.k + 1) * a.ys_cap * a.ldg_i;
+    }
+    if (tid == 0) {
+        s_idx[a.k] = a.E;  // slot k: the shared expert, weight 1 (the top-k fills slots 0 .. k-1)
+        s_w[a.k] = 1.0f;
+    }
+    __syncthreads();
+
     for (int li = 0; li < a.n_layers; ++li) {
         const int l = a.l0 + li;
         const DecodeLayerPtrs &P = a.L[li];
         const __nv_bfloat16 *in = l == 0 ? a.x : a.act + ((l - 1) % 2) * a.H;
         __nv_bfloat16 *out = l == a.n_total - 1 ? a.y : a.act + (l % 2) * a.H;
 
+        // What this layer needs later and does not depend on its routing
+        // starts moving now: the shared expert's down rows and the next
+        // layer's router columns (phase C).
+        if (a.stage_down && a.has_shared) stage_down_rows(a, P, s_idx, a.k, a.k + 1, y_lo, ys, st, tid, kDecThreads);
+        if (a.stage_router && li + 1 < a.n_layers) stage_router_cols(a, a.L[li + 1].Wr, c0, st, tid, kDecThreads);
+        if (!a.stage_down && tid == kDecThreads - 1 && a.has_shared) {
+            const int64_t r0 = static_cast<int64_t>(a.E) * a.H;
+            prefetch_slice(P.qd + r0 * (a.I / 8), static_cast<size_t>(a.H) * (a.I / 8) * 4, b, G);
+        }
+
         // ------------------------------------------------------------ phase A
         // Only the first layer of a launch: later layers' router logits are
         // summed by the previous layer's phase C.
-        if (tid == 0 && a.has_shared) {
-            // the shared expert's down rows are read in phase C
-            const int64_t r0 = static_cast<int64_t>(a.E) * a.H;
-            prefetch_slice(P.qd + r0 * (a.I / 8), static_cast<size_t>(a.H) * (a.I / 8) * 4, b, G);
-            prefetch_slice(P.sd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
-            prefetch_slice(P.bd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
-        }
         if (li == 0) {
             UnitRegs<HMAX> ur;
             const int u0 = gw;
@@ -469,13 +557,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             a.topk_idx[tid] = s_idx[tid];
             a.topk_w[tid] = s_w[tid];
         }
-        if (tid < a.k) {
-            // this block's share of the picked experts' down rows, read in phase C
-            const int64_t r0 = static_cast<int64_t>(s_idx[tid]) * a.H;
-            prefetch_slice(P.qd + r0 * (a.I / 8), static_cast<size_t>(a.H) * (a.I / 8) * 4, b, G);
-            prefetch_slice(P.sd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
-            prefetch_slice(P.bd + r0 * a.ldg_i, static_cast<size_t>(a.H) * a.ldg_i * 2, b, G);
-        }
+        // the picked experts' down rows for this block's output features are
+        // requested right after the gate/up rows, which are needed first
+        bool down_requested = false;
+        auto request_down = [&]() {
+            if (a.stage_down) {
+                stage_down_rows(a, P, s_idx, 0, a.k, y_lo, ys, st, tid, kDecThreads);
+            } else if (tid < a.k) {
+                const int64_t r0 = static_cast<int64_t>(s_idx[tid]) * a.H;
+                prefetch_slice(P.qd + r0 * (a.I / 8), static_cast<size_t>(a.H) * (a.I / 8) * 4, b, G);
+            }
+            down_requested = true;
+        };
         for (int f0 = f_lo + warp; f0 < f_hi; f0 += 2 * kDecWarps) {
             // both pairs' rows are requested before either is used
             UnitRegs<HMAX> r2[2];
@@ -489,6 +582,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                     row_pair_load(a, P, rows[i], lane, r2[i]);
                 }
             }
+            if (!down_requested) request_down();
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int f = f0 + i * kDecWarps;
@@ -501,33 +595,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                 }
             }
         }
+        if (!down_requested) request_down();
         grid_arrive(a.ctrl);
 
         // ------------------------------------------------------------ phase C
-        // slot tables in shared memory: slot k is the shared expert, weight 1
-        if (tid == 0) {
-            s_idx[a.k] = a.E;
-            s_w[a.k] = 1.0f;
-        }
-        __syncthreads();
         const int *e_j = s_idx;
         const float *w_j = s_w;
-        const int y_lo = static_cast<int>((static_cast<int64_t>(b) * a.H) / G);
-        const int y_hi = static_cast<int>((static_cast<int64_t>(b + 1) * a.H) / G);
-        const bool preload = a.I <= 512;  // the whole row is one 8-byte load per lane
-        DownLoad dl;
-        if (preload && y_lo + warp < y_hi) down_load(a, P, e_j, nslots, y_lo + warp, lane, gshift, dl);
-        if (tid == 0) {
-            // the next layer's router and shared gate/up rows do not depend on
-            // this layer: start moving this block's share into L2
-            const float *nWr = li + 1 < a.n_layers ? a.L[li + 1].Wr : a.next_Wr;
+        if (tid == kDecThreads - 1 && li + 1 < a.n_layers && a.has_shared) {
+            // the next layer's shared gate/up rows do not depend on this
+            // layer: start moving this block's share into L2
+            const DecodeLayerPtrs &N = a.L[li + 1];
+            const int64_t r0 = static_cast<int64_t>(a.E) * a.I;
+            prefetch_slice(N.qg + r0 * (a.H / 8), static_cast<size_t>(a.I) * (a.H / 8) * 4, b, G);
+            prefetch_slice(N.qu + r0 * (a.H / 8), static_cast<size_t>(a.I) * (a.H / 8) * 4, b, G);
+        }
+        if (tid == kDecThreads - 2) {
+            // the router of the next launch's first layer is read whole there
+            const float *nWr = li + 1 < a.n_layers ? (a.stage_router ? nullptr : a.L[li + 1].Wr) : a.next_Wr;
             if (nWr) prefetch_slice(nWr, static_cast<size_t>(a.E) * a.H * 4, b, G);
-            if (li + 1 < a.n_layers && a.has_shared) {
-                const DecodeLayerPtrs &N = a.L[li + 1];
-                const int64_t r0 = static_cast<int64_t>(a.E) * a.I;
-                prefetch_slice(N.qg + r0 * (a.H / 8), static_cast<size_t>(a.I) * (a.H / 8) * 4, b, G);
-                prefetch_slice(N.qu + r0 * (a.H / 8), static_cast<size_t>(a.I) * (a.H / 8) * 4, b, G);
-            }
         }
         if (!grid_wait(a.ctrl, ++nbar * G, lim, 3, &s_ok)) return;
         {
@@ -548,10 +633,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             const float4 u0v = src[0], u1v = src[1];
             hsum8[w] = ((u0v.x + u0v.y) + (u0v.z + u0v.w)) + ((u1v.x + u1v.y) + (u1v.z + u1v.w));
         }
+        cp_async_wait_all();  // this thread's staged rows and router columns
         __syncthreads();
         for (int f = y_lo + warp; f < y_hi; f += kDecWarps) {
-            const bool pre = preload && f == y_lo + warp;
-            const float y = warp_sum(down_dot(a, P, e_j, w_j, nslots, f, lane, gshift, dl, pre, hs, hsum8, ip));
+            const float y = warp_sum(a.stage_down
+                                         ? down_dot<true>(a, P, e_j, w_j, nslots, f, f - y_lo, lane, gshift, st, hs,
+                                                          hsum8, ip)
+                                         : down_dot<false>(a, P, e_j, w_j, nslots, f, f - y_lo, lane, gshift, st, hs,
+                                                           hsum8, ip));
             if (lane == 0) {
                 const __nv_bfloat16 yb = __float2bfloat16_rn(y);
                 out[f] = yb;
@@ -563,30 +652,47 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             // features times the matching router columns, two threads per
             // expert, added into the next layer's buffer in fp64
             __syncthreads();
-            const float *nWr = a.L[li + 1].Wr;
             const int e = tid >> 1, half = tid & 1;
             float part = 0.f;
-            if (e < a.E)
-                for (int f = y_lo + half; f < y_hi; f += 2)
-                    part = fmaf(__ldg(nWr + static_cast<int64_t>(e) * a.H + f), s_y[f - y_lo], part);
+            if (e < a.E) {
+                if (a.stage_router) {
+                    const float *wr = st.wr + e * st.wr_ld - c0;
+                    for (int f = y_lo + half; f < y_hi; f += 2) part = fmaf(wr[f], s_y[f - y_lo], part);
+                } else {
+                    const float *nWr = a.L[li + 1].Wr + static_cast<int64_t>(e) * a.H;
+                    for (int f = y_lo + half; f < y_hi; f += 2) part = fmaf(__ldg(nWr + f), s_y[f - y_lo], part);
+                }
+            }
             part += __shfl_xor_sync(0xffffffffu, part, 1);
             if (half == 0 && e < a.E) atomicAdd(a.racc + ((l + 1) % 2) * a.E + e, static_cast<double>(part));
             grid_arrive(a.ctrl);
         }
-        __syncthreads();  // hs is overwritten by the next layer's staging
+        __syncthreads();  // hs and the staging buffers are refilled by the next layer
     }
 }
 
-size_t decode_smem_bytes(int E, int k, int H, int I, int grid) {
-    (void)E;
-    (void)grid;
-    return sizeof(float) * static_cast<size_t>(decode_smem_floats(H, I, k));
+// Shared-memory limit of one block that the staging buffers may grow to.
+constexpr size_t kDecSmemLimit = 220 * 1024;
+
+static void decode_plan(DecodeStack &a, int grid) {
+    a.ys_cap = (a.H + grid - 1) / grid;
+    int ld = (a.ys_cap + 3 + 3) & ~3;      // covers [y_lo & ~3, y_hi) for any y_lo
+    if (ld % 8 == 0) ld += 4;              // odd multiple of 4 floats: fewer bank conflicts
+    a.wr_ld = ld;
+    const size_t base = sizeof(float) * static_cast<size_t>(decode_smem_floats(a.H, a.I, a.k));
+    a.stage_router = base + 4 * static_cast<size_t>(decode_stage_words(a, false, true)) <= kDecSmemLimit;
+    a.stage_down = base + 4 * static_cast<size_t>(decode_stage_words(a, true, a.stage_router)) <= kDecSmemLimit;
+}
+
+size_t decode_smem_bytes(const DecodeStack &a) {
+    return sizeof(float) * (static_cast<size_t>(decode_smem_floats(a.H, a.I, a.k)) +
+                            static_cast<size_t>(decode_stage_words(a, a.stage_down, a.stage_router)));
 }
 
 template <int HMAX>
 static cudaError_t launch_decode_t(const DecodeStack &a, int grid, cudaStream_t s) {
     if ((a.H + grid - 1) / grid > kMaxYSlice) return cudaErrorInvalidConfiguration;  // too few SMs for H
-    const size_t smem = decode_smem_bytes(a.E, a.k, a.H, a.I, grid);
+    const size_t smem = decode_smem_bytes(a);
     cudaError_t e = cudaFuncSetAttribute(decode_stack_kernel<HMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -608,7 +714,9 @@ static cudaError_t launch_decode_t(const DecodeStack &a, int grid, cudaStream_t 
     return cudaLaunchKernelEx(&cfg, decode_stack_kernel<HMAX>, a);
 }
 
-cudaError_t launch_decode(const DecodeStack &a, int grid, cudaStream_t s) {
+cudaError_t launch_decode(const DecodeStack &a0, int grid, cudaStream_t s) {
+    DecodeStack a = a0;
+    decode_plan(a, grid);
     return a.H <= 2048 ? launch_decode_t<2048>(a, grid, s) : launch_decode_t<4096>(a, grid, s);
 }
 

@@ -59,6 +59,10 @@ struct DecodeStack {
     double *racc;            // [2][E]: next layer's router logits, summed over blocks (alternating buffers)
     const float *next_Wr;    // router of the layer after this launch (L2 prefetch), or NULL
     long long wait_limit;
+    // set by the launcher from the shape and grid: output features per block
+    // (at most), pitch of the staged router columns, and which of the down
+    // rows / router columns are staged in shared memory
+    int ys_cap, wr_ld, stage_down, stage_router;
     DecodeLayerPtrs L[kMaxStackLayers];
 };
 
@@ -73,7 +77,6 @@ cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 
 cudaError_t launch_gemm(int mode, const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t s);
 cudaError_t launch_zero_i32(int *p, int64_t n, cudaStream_t s);
 cudaError_t launch_convert(const float *y_acc, __nv_bfloat16 *y, int64_t n, int num_sms, cudaStream_t s);
-size_t decode_smem_bytes(int E, int k, int H, int I, int grid);
 cudaError_t launch_decode(const DecodeStack &a, int grid, cudaStream_t s);
 
 }  // namespace moe
