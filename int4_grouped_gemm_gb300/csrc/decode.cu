@@ -108,24 +108,38 @@ __device__ __forceinline__ bool grid_wait(Ctrl *c, unsigned target, long long li
     return *s_ok != 0;
 }
 
+// Two fp32 lanes in one 64-bit register pair, and their fused multiply-add
+// (one packed instruction; each lane rounds like fmaf).
+__device__ __forceinline__ unsigned long long f32x2(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // 8 int4 codes -> sum_i x_i * (128 + q_i) (x: 8 consecutive fp32 in shared
 // memory, 16-byte aligned).  Nibbles j and j + 4 hold elements 2j and 2j + 1:
 // they are lifted together into the two bf16 halves of one register as
 // 128 + q (exact), and each half widens to fp32 with one shift or mask;
-// callers subtract 128 * sum_i x_i (folded into the bias term).  Two
-// accumulators halve the dependent FMA chain.
+// callers subtract 128 * sum_i x_i (folded into the bias term).  The even
+// and the odd elements accumulate in the two lanes of a packed fp32 pair,
+// which also halves the dependent FMA chain.
 __device__ __forceinline__ float dot8_codes128(uint32_t word, const float *xv) {
     const float4 x0 = *reinterpret_cast<const float4 *>(xv);
     const float4 x1 = *reinterpret_cast<const float4 *>(xv + 4);
-    const float xl[4] = {x0.x, x0.z, x1.x, x1.z}, xh[4] = {x0.y, x0.w, x1.y, x1.w};  // elements 2j, 2j + 1
-    float acc0 = 0.f, acc1 = 0.f;
+    const unsigned long long xp[4] = {f32x2(x0.x, x0.y), f32x2(x0.z, x0.w), f32x2(x1.x, x1.y), f32x2(x1.z, x1.w)};
+    unsigned long long acc = 0;  // (+0, +0)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const uint32_t p = ((word >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
-        acc0 = fmaf(xl[j], __uint_as_float(p << 16), acc0);
-        acc1 = fmaf(xh[j], __uint_as_float(p & 0xFFFF0000u), acc1);
+        acc = fma_f32x2(xp[j], f32x2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u)), acc);
     }
-    return acc0 + acc1;
+    return __uint_as_float(static_cast<uint32_t>(acc)) + __uint_as_float(static_cast<uint32_t>(acc >> 32));
 }
 
 // Shared-memory position of element k of a staged vector: four padding
@@ -392,7 +406,10 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
 
 // Top-k of E <= 256 logits (ties -> lower expert index) and the softmax over
 // the picked ones.  Warps 0-7 each sort 32 experts' keys; the 8 best of every
-// warp (64 keys) are sorted again in two rounds by warp 0.  The logit of
+// warp (64 candidates, which hold the top k <= 8) are then placed by rank:
+// thread i < 64 counts the candidates above candidate i, and a rank below k
+// is its slot (real keys are distinct; padding keys are 0 and rank after
+// every real one).  s_keys holds 64 candidates + 8 picked keys.  The logit of
 // expert e is the sum of its four K-quarter partial sums in a fixed order
 // (first layer of a launch) or the fp64 sum that the previous layer's blocks
 // accumulated, plus the bias.  Every block computes the same result.
@@ -404,7 +421,15 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
         if (t < a.E) {
             float l;
             if (racc) {
-                l = static_cast<float>(__ldcg(racc + t));  // summed by the previous layer's blocks
+                // summed by the previous layer's blocks into kRaccCopies copies,
+                // added here in a fixed order
+                double v[kRaccCopies];
+#pragma unroll
+                for (int r = 0; r < kRaccCopies; ++r) v[r] = __ldcg(racc + r * a.E + t);
+                double sum = v[0];
+#pragma unroll
+                for (int r = 1; r < kRaccCopies; ++r) sum += v[r];
+                l = static_cast<float>(sum);
             } else {
                 l = __ldcg(a.logits_part + t) + __ldcg(a.logits_part + a.E + t);
                 l += __ldcg(a.logits_part + 2 * a.E + t);
@@ -417,15 +442,17 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
         if (lane < 8) s_keys[warp * 8 + lane] = key;
     }
     __syncthreads();
+    if (t < 64) {
+        const unsigned long long mine = s_keys[t];
+        int rank = 0;
+#pragma unroll 16
+        for (int i = 0; i < 64; ++i) rank += s_keys[i] > mine ? 1 : 0;
+        if (rank < a.k) s_keys[64 + rank] = mine;
+        named_barrier(1, 64);
+    }
     if (warp == 0) {
-        // round 1: the 32 keys of warps 0-3 and, separately, of warps 4-7
-        unsigned long long k0 = warp_sort_desc(s_keys[lane], lane);
-        unsigned long long k1 = warp_sort_desc(s_keys[32 + lane], lane);
-        // round 2: the 8 best of each
-        const unsigned long long k1s = __shfl_sync(0xffffffffu, k1, (lane - 8) & 31);
-        unsigned long long k = lane < 8 ? k0 : lane < 16 ? k1s : 0ull;
-        k = warp_sort_desc(k, lane);
         // lane j < k: pick j
+        const unsigned long long k = lane < a.k ? s_keys[64 + lane] : 0ull;
         const uint32_t ord = static_cast<uint32_t>(k >> 32);
         const float l = __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
         const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k));
@@ -464,7 +491,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     __shared__ int s_idx[kMaxSlots];
     __shared__ float s_w[kMaxSlots];
     __shared__ int s_ok;
-    __shared__ unsigned long long s_keys[64];
+    __shared__ unsigned long long s_keys[64 + 8];
     __shared__ float s_y[kMaxYSlice];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int G = gridDim.x, b = blockIdx.x;
@@ -547,11 +574,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             // warps 8-15 stage it while warps 0-7 start the top-k below
             stage_x(in, a.H, xs, xsum8, 256, kDecThreads - 256);
         }
-        topk_block(a, P.bias, li == 0 ? nullptr : a.racc + (l % 2) * a.E, s_keys, s_idx, s_w);
+        topk_block(a, P.bias, li == 0 ? nullptr : a.racc + (l % 2) * kRaccCopies * a.E, s_keys, s_idx, s_w);
         if (b == 0 && li + 1 < a.n_layers) {
             // the next layer's logit sums start from zero; this buffer was last
             // read by the previous layer's top-k, before the previous barrier
-            for (int e = tid; e < a.E; e += kDecThreads) a.racc[((l + 1) % 2) * a.E + e] = 0.0;
+            double *nr = a.racc + ((l + 1) % 2) * kRaccCopies * a.E;
+            for (int e = tid; e < kRaccCopies * a.E; e += kDecThreads) nr[e] = 0.0;
         }
         if (b == 0 && tid < a.k) {
             a.topk_idx[tid] = s_idx[tid];
@@ -650,7 +678,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         if (li + 1 < a.n_layers) {
             // this block's share of the next layer's router logits: its output
             // features times the matching router columns, two threads per
-            // expert, added into the next layer's buffer in fp64
+            // expert, added in fp64 into copy b % kRaccCopies of the next
+            // layer's buffer (fewer blocks contend for one address)
             __syncthreads();
             const int e = tid >> 1, half = tid & 1;
             float part = 0.f;
@@ -664,7 +693,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                 }
             }
             part += __shfl_xor_sync(0xffffffffu, part, 1);
-            if (half == 0 && e < a.E) atomicAdd(a.racc + ((l + 1) % 2) * a.E + e, static_cast<double>(part));
+            if (half == 0 && e < a.E)
+                atomicAdd(a.racc + (((l + 1) % 2) * kRaccCopies + b % kRaccCopies) * a.E + e, static_cast<double>(part));
             grid_arrive(a.ctrl);
         }
         __syncthreads();  // hs and the staging buffers are refilled by the next layer

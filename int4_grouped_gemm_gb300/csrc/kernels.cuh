@@ -56,7 +56,7 @@ struct DecodeStack {
     int *topk_idx;           // [8]
     float *topk_w;           // [8]
     float *h;                // [k + 1][I] fp32 (slot k = shared expert)
-    double *racc;            // [2][E]: next layer's router logits, summed over blocks (alternating buffers)
+    double *racc;            // [2][kRaccCopies][E]: next layer's router logits, summed over blocks (alternating buffers)
     const float *next_Wr;    // router of the layer after this launch (L2 prefetch), or NULL
     long long wait_limit;
     // set by the launcher from the shape and grid: output features per block

@@ -9,6 +9,7 @@ namespace moe {
 constexpr int kTileRows = 128;      // token rows per grouped-GEMM tile (MMA M)
 constexpr int kRouteChunk = 64;     // tokens per routing block (histogram granularity)
 constexpr int kCtrlBytes = 256;     // status word, decode ticket, ...
+constexpr int kRaccCopies = 8;      // decode: copies of the next layer's logit sums (block b adds to copy b % 8)
 
 // Scale/bias row pitch in groups: K/G rounded up to a multiple of 8 (16 bytes).
 inline int ld_groups(int K, int G) { return (K / G + 7) / 8 * 8; }
@@ -107,16 +108,19 @@ inline DecodeLayout decode_layout(int E, int k, int I) {
     L.topk_idx = take(sizeof(int) * 8);
     L.topk_w = take(sizeof(float) * 8);
     L.h = take(sizeof(float) * (size_t)(k + 1) * I);
-    L.racc = take(sizeof(double) * 2 * (size_t)E);
+    L.racc = 0;  // stacks only
     L.act = 0;
     L.total = o;
     return L;
 }
 
-// decode workspace plus two bf16 activation rows for a stack of layers
+// decode workspace plus, for a stack of layers, the next layer's router
+// logit sums ([2][kRaccCopies][E] fp64, alternating buffers) and two bf16
+// activation rows
 inline DecodeLayout decode_stack_layout(int E, int k, int H, int I) {
     DecodeLayout L = decode_layout(E, k, I);
-    L.act = L.total;
+    L.racc = L.total;
+    L.act = align_up(L.racc + sizeof(double) * 2 * kRaccCopies * (size_t)E, 256);
     L.total = align_up(L.act + 2 * sizeof(uint16_t) * (size_t)H, 256);
     return L;
 }
