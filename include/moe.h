@@ -200,7 +200,7 @@ int pack_int4(const float *w, int64_t rows, int32_t K, int32_t group, uint32_t *
  * may synchronise the device) is not allowed.
  *
  * Limit: the layer's decode scratch must fit the 64 KiB (E = 256, k = 8
- * fits up to I = 1664); larger layers return MOE_ERR_WORKSPACE before
+ * fits up to I = 3328); larger layers return MOE_ERR_WORKSPACE before
  * anything is launched.  Other requirements are those of moe_decode.
  * Set-up: the first call on each device, with that device current, looks up
  * the array's address; make that first call before any stream capture

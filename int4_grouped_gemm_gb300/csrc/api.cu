@@ -125,7 +125,7 @@ using namespace moe;
 // Fixed decode scratch for moe_decode_static_scratch: one array per device,
 // zero when the module loads, and from then on holding whatever the last call
 // left in it.  64 KiB holds the decode scratch (control block, router sums,
-// top-k, k + 1 fp32 rows of I) of E = 256, k = 8 layers up to I = 1664.
+// top-k, k + 1 bf16 rows of I) of E = 256, k = 8 layers up to I = 3328.
 static constexpr size_t kStaticScratchBytes = 64 * 1024;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
@@ -371,7 +371,7 @@ static int decode_run(const moe_layer_desc *descs, int n, const void *x, void *y
     a.logits_part = reinterpret_cast<float *>(w + L.logits);
     a.topk_idx = reinterpret_cast<int *>(w + L.topk_idx);
     a.topk_w = reinterpret_cast<float *>(w + L.topk_w);
-    a.h = reinterpret_cast<float *>(w + L.h);
+    a.h = reinterpret_cast<__nv_bfloat16 *>(w + L.h);
     a.racc = n > 1 ? reinterpret_cast<double *>(w + L.racc) : nullptr;  // read and written only between layers
     a.wait_limit = g_wait_limit;
     for (int l0 = 0; l0 < n; l0 += kMaxStackLayers) {

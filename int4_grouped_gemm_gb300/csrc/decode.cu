@@ -108,67 +108,88 @@ __device__ __forceinline__ bool grid_wait(Ctrl *c, unsigned target, long long li
     return *s_ok != 0;
 }
 
-// Two fp32 lanes in one 64-bit register pair, and their fused multiply-add
-// (one packed instruction; each lane rounds like fmaf).
-__device__ __forceinline__ unsigned long long f32x2(float lo, float hi) {
-    unsigned long long r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
-                                                        unsigned long long c) {
-    unsigned long long d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+// acc + a * b for the low (H = 0) or high (H = 1) bf16 halves of a and b,
+// multiplied exactly and added in fp32 with one rounding, like fmaf on the
+// widened values (the mixed-precision form of fma: bf16 sources, f32
+// accumulator and result).
+template <int H>
+__device__ __forceinline__ float fma_bf16_half(uint32_t a, uint32_t b, float acc) {
+    float d;
+    if (H == 0)
+        asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, al, bl, %3;}"
+            : "=f"(d) : "r"(a), "r"(b), "f"(acc));
+    else
+        asm("{.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+            "fma.rn.f32.bf16 %0, ah, bh, %3;}"
+            : "=f"(d) : "r"(a), "r"(b), "f"(acc));
     return d;
 }
 
-// 8 int4 codes -> sum_i x_i * (128 + q_i) (x: 8 consecutive fp32 in shared
-// memory, 16-byte aligned).  Nibbles j and j + 4 hold elements 2j and 2j + 1:
-// they are lifted together into the two bf16 halves of one register as
-// 128 + q (exact), and each half widens to fp32 with one shift or mask;
-// callers subtract 128 * sum_i x_i (folded into the bias term).  The even
-// and the odd elements accumulate in the two lanes of a packed fp32 pair,
-// which also halves the dependent FMA chain.
-__device__ __forceinline__ float dot8_codes128(uint32_t word, const float *xv) {
-    const float4 x0 = *reinterpret_cast<const float4 *>(xv);
-    const float4 x1 = *reinterpret_cast<const float4 *>(xv + 4);
-    const unsigned long long xp[4] = {f32x2(x0.x, x0.y), f32x2(x0.z, x0.w), f32x2(x1.x, x1.y), f32x2(x1.z, x1.w)};
-    unsigned long long acc = 0;  // (+0, +0)
+// 8 int4 codes -> sum_i v_i * (128 + q_i), v: the word's 8 bf16 inputs as
+// four bf16 pairs (2j, 2j + 1).  Nibbles j and j + 4 hold elements 2j and
+// 2j + 1: they are lifted together into the two bf16 halves of one register
+// as 128 + q (exact), which meet the matching input pair half by half;
+// every product is exact and the even and odd elements accumulate in two
+// fp32 sums.  Callers subtract 128 * sum_i v_i (folded into the bias term).
+__device__ __forceinline__ float dot8_codes128(uint32_t word, const uint4 v) {
+    const uint32_t vp[4] = {v.x, v.y, v.z, v.w};
+    float acc0 = 0.f, acc1 = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const uint32_t p = ((word >> (4 * j)) & 0x000F000Fu) | 0x43004300u;
-        acc = fma_f32x2(xp[j], f32x2(__uint_as_float(p << 16), __uint_as_float(p & 0xFFFF0000u)), acc);
+        acc0 = fma_bf16_half<0>(vp[j], p, acc0);
+        acc1 = fma_bf16_half<1>(vp[j], p, acc1);
     }
-    return __uint_as_float(static_cast<uint32_t>(acc)) + __uint_as_float(static_cast<uint32_t>(acc >> 32));
+    return acc0 + acc1;
 }
 
-// Shared-memory position of element k of a staged vector: four padding
-// floats after every 32 elements.  Blocks of 32 consecutive elements stay
-// contiguous and 16-byte aligned, and lanes reading blocks one apart start
-// four banks apart, so eight lanes' 16-byte reads never collide.
+// Sum of the 8 bf16 values of a word, in fp32 (fixed order).
+__device__ __forceinline__ float sum8_bf16(const uint4 v) {
+    const uint32_t p[4] = {v.x, v.y, v.z, v.w};
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sum += __uint_as_float(p[i] << 16) + __uint_as_float(p[i] & 0xFFFF0000u);
+    return sum;
+}
+
+// Shared-memory position of element k of the fp32 layer input (phase A):
+// four padding floats after every 32 elements.  Blocks of 32 consecutive
+// elements stay contiguous and 16-byte aligned, and lanes reading blocks one
+// apart start four banks apart, so eight lanes' 16-byte reads never collide.
 __device__ __forceinline__ int vpos(int k) { return k + ((k >> 5) << 2); }
 __host__ __device__ constexpr int vlen(int n) { return n + n / 8; }  // padded length (n % 32 == 0)
 
-// Layer input to shared memory as fp32 (padded positions) plus the sum of
-// every 8-element word, by threads t0 .. t0 + nthreads - 1; it was written by
-// other blocks, so it is read from L2.
-__device__ __forceinline__ void stage_x(const __nv_bfloat16 *x, int H, float *xs, float *xsum8, int t0 = 0,
-                                        int nthreads = 0) {
+// Positions (in 16-byte units) of word w of the bf16 layer input and of a
+// bf16 h row in shared memory: one padding unit after every 4 (input) or 8
+// (h) words.  Phase B's lanes read words 4 apart (lane * 4 + i) and phase C's
+// lanes words 2 apart (2 * lane, 2 * lane + 1): with these pads any eight
+// consecutive lanes hit eight different 4-bank groups.
+__device__ __forceinline__ int xpos(int w) { return w + (w >> 2); }
+__device__ __forceinline__ int hpos(int w) { return w + (w >> 3); }
+__host__ __device__ constexpr int xunits(int H) { return H / 8 + H / 32; }
+__host__ __device__ constexpr int hunits(int I) { return I / 8 + I / 64; }
+
+// Layer input to shared memory: bf16 words (padded positions), the sum of
+// every 8-element word, and, when xs is not null, fp32 values for phase A;
+// by threads t0 .. t0 + nthreads - 1.  It was written by other blocks, so it
+// is read from L2.
+__device__ __forceinline__ void stage_x(const __nv_bfloat16 *x, int H, uint4 *xb, float *xsum8, float *xs,
+                                        int t0 = 0, int nthreads = 0) {
     const int nw = H / 8;
     if (nthreads == 0) nthreads = blockDim.x;
     for (int w = static_cast<int>(threadIdx.x) - t0; w >= 0 && w < nw; w += nthreads) {
         const uint4 raw = __ldcg(reinterpret_cast<const uint4 *>(x) + w);
-        const uint32_t p[4] = {raw.x, raw.y, raw.z, raw.w};
-        float sum = 0.f;
+        xb[xpos(w)] = raw;
+        xsum8[w] = sum8_bf16(raw);
+        if (xs) {
+            const uint32_t p[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const __nv_bfloat162 v = u32_as_bf162(p[i]);
-            const float lo = __low2float(v), hi = __high2float(v);
-            xs[vpos(w * 8) + 2 * i] = lo;  // the 8 elements of a word never straddle a pad
-            xs[vpos(w * 8) + 2 * i + 1] = hi;
-            sum += lo + hi;
+            for (int i = 0; i < 4; ++i) {
+                xs[vpos(w * 8) + 2 * i] = __uint_as_float(p[i] << 16);  // a word never straddles a pad
+                xs[vpos(w * 8) + 2 * i + 1] = __uint_as_float(p[i] & 0xFFFF0000u);
+            }
         }
-        xsum8[w] = sum;
     }
 }
 
@@ -226,7 +247,7 @@ __device__ __forceinline__ float router_dot(const DecodeStack &a, int unit, int 
 
 template <int HMAX>
 __device__ __forceinline__ void row_pair_load(const DecodeStack &a, const DecodeLayerPtrs &P, int64_t row, int lane,
-                                              UnitRegs<HMAX> &rp) {
+                                              int gshift, UnitRegs<HMAX> &rp) {
     constexpr int kMaxRowVec = UnitRegs<HMAX>::V / 2;  // gate words in r[0..V/2), up words in r[V/2..V)
     const int nwords = a.H / 8;
     const uint32_t *qg = P.qg + row * nwords;
@@ -237,7 +258,7 @@ __device__ __forceinline__ void row_pair_load(const DecodeStack &a, const Decode
         if (w0 < nwords) {
             rp.r[v] = __ldg(reinterpret_cast<const uint4 *>(qg + w0));
             rp.r[kMaxRowVec + v] = __ldg(reinterpret_cast<const uint4 *>(qu + w0));
-            const int grp = (w0 * 8) / a.G;  // the 4 words (32 elements) share a group (G >= 32)
+            const int grp = (w0 * 8) >> gshift;  // the 4 words (32 elements) share a group (G >= 32)
             rp.sb[4 * v + 0] = __ldg(P.sg + row * a.ldg_h + grp);
             rp.sb[4 * v + 1] = __ldg(P.bg + row * a.ldg_h + grp);
             rp.sb[4 * v + 2] = __ldg(P.su + row * a.ldg_h + grp);
@@ -246,31 +267,41 @@ __device__ __forceinline__ void row_pair_load(const DecodeStack &a, const Decode
     }
 }
 
-template <int HMAX>
-__device__ __forceinline__ void row_pair_dot(const DecodeStack &a, const DecodeLayerPtrs &P, int64_t row, int lane,
-                                             const UnitRegs<HMAX> &rp, const float *xs, const float *xsum8,
-                                             float &gacc, float &uacc) {
+// NP gate/up row pairs against the staged input: each input word is read
+// once for all of them, and the 2 * NP dot products form independent chains.
+template <int HMAX, int NP>
+__device__ __forceinline__ void row_pairs_dot(const DecodeStack &a, int lane, const UnitRegs<HMAX> *rp,
+                                              const uint4 *xb, const float *xsum8, float *gacc, float *uacc) {
     constexpr int kMaxRowVec = UnitRegs<HMAX>::V / 2;
     const int nwords = a.H / 8;
 #pragma unroll
     for (int v = 0; v < kMaxRowVec; ++v) {
         const int w0 = lane * 4 + v * 128;
         if (w0 < nwords) {
-            const uint4 gv = rp.r[v], uv = rp.r[kMaxRowVec + v];
-            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-            const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
-            const float sgv = bf16_bits_to_float(rp.sb[4 * v + 0]), bgv = bf16_bits_to_float(rp.sb[4 * v + 1]);
-            const float suv = bf16_bits_to_float(rp.sb[4 * v + 2]), buv = bf16_bits_to_float(rp.sb[4 * v + 3]);
-            float dg = 0.f, du = 0.f, xs4 = 0.f;
+            float dg[NP], du[NP], xs4 = 0.f;
+#pragma unroll
+            for (int p = 0; p < NP; ++p) dg[p] = du[p] = 0.f;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int w = w0 + i;
-                dg += dot8_codes128(gw[i], xs + vpos(w * 8));
-                du += dot8_codes128(uw[i], xs + vpos(w * 8));
+                const uint4 xv = xb[xpos(w)];
+#pragma unroll
+                for (int p = 0; p < NP; ++p) {
+                    const uint4 gv = rp[p].r[v], uv = rp[p].r[kMaxRowVec + v];
+                    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+                    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w};
+                    dg[p] += dot8_codes128(gw[i], xv);
+                    du[p] += dot8_codes128(uw[i], xv);
+                }
                 xs4 += xsum8[w];
             }
-            gacc += sgv * dg + (bgv - 128.0f * sgv) * xs4;
-            uacc += suv * du + (buv - 128.0f * suv) * xs4;
+#pragma unroll
+            for (int p = 0; p < NP; ++p) {
+                const float sgv = bf16_bits_to_float(rp[p].sb[4 * v + 0]), bgv = bf16_bits_to_float(rp[p].sb[4 * v + 1]);
+                const float suv = bf16_bits_to_float(rp[p].sb[4 * v + 2]), buv = bf16_bits_to_float(rp[p].sb[4 * v + 3]);
+                gacc[p] += sgv * dg[p] + (bgv - 128.0f * sgv) * xs4;
+                uacc[p] += suv * du[p] + (buv - 128.0f * suv) * xs4;
+            }
         }
     }
 }
@@ -300,8 +331,10 @@ __device__ __forceinline__ void stage_down_rows(const DecodeStack &a, const Deco
     const int qc = ys * nw / 4;        // 16-byte chunks of one slot's rows
     const int sc = ys * a.ldg_i / 8;   // ... of its scales (and of its biases)
     const int per = qc + 2 * sc;
+    // chunk c = (j - j0) * per + r, stepped without a division per chunk
+    int j = j0 + t / per, r = t % per;
+    const int dj = nt / per, dr = nt % per;
     for (int c = t; c < (j1 - j0) * per; c += nt) {
-        const int j = j0 + c / per, r = c % per;
         const int64_t row0 = static_cast<int64_t>(e_j[j]) * a.H + y_lo;
         const int srow = j * st.ys_cap;
         if (r < qc) {
@@ -313,6 +346,12 @@ __device__ __forceinline__ void stage_down_rows(const DecodeStack &a, const Deco
             uint16_t *dst = (r - qc < sc ? st.ds : st.db) + srow * a.ldg_i;
             cp_async<16>(reinterpret_cast<uint4 *>(dst) + rs, reinterpret_cast<const uint4 *>(src) + rs);
         }
+        j += dj;
+        r += dr;
+        if (r >= per) {
+            r -= per;
+            ++j;
+        }
     }
 }
 
@@ -320,10 +359,17 @@ __device__ __forceinline__ void stage_down_rows(const DecodeStack &a, const Deco
 __device__ __forceinline__ void stage_router_cols(const DecodeStack &a, const float *Wr, int c0, const DownStage &st,
                                                   int t, int nt) {
     const int n4 = st.wr_ld / 4;
+    int e = t / n4, v = t % n4;
+    const int de = nt / n4, dv = nt % n4;
     for (int c = t; c < a.E * n4; c += nt) {
-        const int e = c / n4, v = c % n4;
         if (c0 + 4 * v < a.H)
             cp_async<16>(st.wr + e * st.wr_ld + 4 * v, Wr + static_cast<int64_t>(e) * a.H + c0 + 4 * v);
+        e += de;
+        v += dv;
+        if (v >= n4) {
+            v -= n4;
+            ++e;
+        }
     }
 }
 
@@ -334,7 +380,7 @@ __device__ __forceinline__ void stage_router_cols(const DecodeStack &a, const fl
 template <bool kStaged>
 __device__ __forceinline__ float down_dot(const DecodeStack &a, const DecodeLayerPtrs &P, const int *e_j,
                                           const float *w_j, int nslots, int f, int fl, int lane, int gshift,
-                                          const DownStage &st, const float *hs, const float *hsum8, int ip) {
+                                          const DownStage &st, const uint4 *hb, const float *hsum8, int hp) {
     const int nw = a.I / 8;
     float y = 0.f;
 #pragma unroll
@@ -353,7 +399,7 @@ __device__ __forceinline__ float down_dot(const DecodeStack &a, const DecodeLaye
                 srow = P.sd + row * a.ldg_i;
                 brow = P.bd + row * a.ldg_i;
             }
-            const float *hv = hs + j * ip;
+            const uint4 *hv = hb + j * hp;  // slot j's h row (bf16 words at hpos)
             float acc = 0.f;
             for (int w = 2 * lane; w < nw; w += 64) {
                 uint2 qv;
@@ -367,7 +413,7 @@ __device__ __forceinline__ float down_dot(const DecodeStack &a, const DecodeLaye
                     sv = bf16_bits_to_float(__ldg(srow + ((w * 8) >> gshift)));
                     bv = bf16_bits_to_float(__ldg(brow + ((w * 8) >> gshift)));
                 }
-                const float dsum = dot8_codes128(qv.x, hv + vpos(w * 8)) + dot8_codes128(qv.y, hv + vpos(w * 8 + 8));
+                const float dsum = dot8_codes128(qv.x, hv[hpos(w)]) + dot8_codes128(qv.y, hv[hpos(w + 1)]);
                 const float hsum = hsum8[j * nw + w] + hsum8[j * nw + w + 1];
                 acc += sv * dsum + (bv - 128.0f * sv) * hsum;
             }
@@ -469,9 +515,12 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
 
 // ------------------------------------------------------------------ kernel
 
+// Shared memory of the x / h region, in 4-byte words: phase A/B hold the
+// fp32 input (phase A only), the bf16 input and its word sums; phase C holds
+// the k + 1 bf16 h rows and their word sums in the same space.
 __host__ __device__ inline int decode_smem_floats(int H, int I, int k) {
-    const int x_words = vlen(H) + H / 8;                       // xs + xsum8
-    const int h_words = (k + 1) * vlen(I) + (k + 1) * (I / 8);  // hs + hsum8 (aliases the x region)
+    const int x_words = vlen(H) + 4 * xunits(H) + H / 8;                  // xs + xb + xsum8
+    const int h_words = (k + 1) * 4 * hunits(I) + (k + 1) * (I / 8);    // hb + hsum8
     return x_words > h_words ? x_words : h_words;
 }
 
@@ -496,10 +545,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int G = gridDim.x, b = blockIdx.x;
     const int gw = b * kDecWarps + warp, NW = G * kDecWarps;
-    float *xs = dsm;                        // [vlen(H)]
-    float *xsum8 = dsm + vlen(a.H);         // [H/8]
-    const int ip = vlen(a.I);               // padded row of h
-    float *hs = dsm;                        // [slots][ip] (aliases x: used in another phase)
+    float *xs = dsm;                                                       // [vlen(H)] fp32 (phase A)
+    uint4 *xb = reinterpret_cast<uint4 *>(dsm + vlen(a.H));                // [xunits(H)] bf16 words
+    float *xsum8 = dsm + vlen(a.H) + 4 * xunits(a.H);                      // [H/8]
+    const int hp = hunits(a.I);                                            // 16-byte units per h row
+    uint4 *hb = reinterpret_cast<uint4 *>(dsm);  // [slots][hp] bf16 (aliases x: used in another phase)
+    float *hsum8 = dsm + (a.k + 1) * 4 * hp;     // [slots][I/8]
     const int nslots = a.k + (a.has_shared ? 1 : 0);
     const int n_a_units = 4 * a.E;
     const int gshift = a.G == 64 ? 6 : 5;   // log2 of the group (32 or 64)
@@ -511,6 +562,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     const int y_hi = static_cast<int>((static_cast<int64_t>(b + 1) * a.H) / G);
     const int ys = y_hi - y_lo;
     const int c0 = y_lo & ~3;
+    const int f_lo = static_cast<int>((static_cast<int64_t>(b) * (nslots * a.I)) / G);
+    const int f_hi = static_cast<int>((static_cast<int64_t>(b + 1) * (nslots * a.I)) / G);
     DownStage st;
     {
         float *p = dsm + decode_smem_floats(a.H, a.I, a.k);
@@ -551,7 +604,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             UnitRegs<HMAX> ur;
             const int u0 = gw;
             if (u0 < n_a_units) router_load(a, P.Wr, u0, lane, ur);
-            stage_x(in, a.H, xs, xsum8);
+            stage_x(in, a.H, xb, xsum8, xs);
             __syncthreads();
             for (int u = u0; u < n_a_units; u += NW) {
                 if (u != u0) router_load(a, P.Wr, u, lane, ur);
@@ -562,17 +615,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         }
 
         // ------------------------------------------------------------ phase B
-        // this block's contiguous range of (slot, feature) pairs of the gate/up
-        // rows, slot k being the shared expert; warp w takes pairs f_lo + w,
-        // f_lo + w + kDecWarps, ... two at a time
-        const int F = nslots * a.I;
-        const int f_lo = static_cast<int>((static_cast<int64_t>(b) * F) / G);
-        const int f_hi = static_cast<int>((static_cast<int64_t>(b + 1) * F) / G);
+        // this block's contiguous range [f_lo, f_hi) of (slot, feature) pairs
+        // of the gate/up rows, slot k being the shared expert; warp w takes
+        // pairs f_lo + w, f_lo + w + kDecWarps, ... two at a time
         if (!grid_wait(a.ctrl, ++nbar * G, lim, 2, &s_ok)) return;
         if (li > 0) {
             // the layer input, complete once every block passed the barrier:
             // warps 8-15 stage it while warps 0-7 start the top-k below
-            stage_x(in, a.H, xs, xsum8, 256, kDecThreads - 256);
+            stage_x(in, a.H, xb, xsum8, nullptr, 256, kDecThreads - 256);
         }
         topk_block(a, P.bias, li == 0 ? nullptr : a.racc + (l % 2) * kRaccCopies * a.E, s_keys, s_idx, s_w);
         if (b == 0 && li + 1 < a.n_layers) {
@@ -607,19 +657,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                 if (f < f_hi) {
                     const int j = f / a.I;
                     rows[i] = static_cast<int64_t>(j < a.k ? s_idx[j] : a.E) * a.I + (f - j * a.I);
-                    row_pair_load(a, P, rows[i], lane, r2[i]);
+                    row_pair_load(a, P, rows[i], lane, gshift, r2[i]);
                 }
             }
             if (!down_requested) request_down();
+            float g[2] = {0.f, 0.f}, up[2] = {0.f, 0.f};
+            if (f0 + kDecWarps < f_hi)
+                row_pairs_dot<HMAX, 2>(a, lane, r2, xb, xsum8, g, up);
+            else
+                row_pairs_dot<HMAX, 1>(a, lane, r2, xb, xsum8, g, up);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int f = f0 + i * kDecWarps;
                 if (f < f_hi) {
-                    float g = 0.f, up = 0.f;
-                    row_pair_dot(a, P, rows[i], lane, r2[i], xs, xsum8, g, up);
-                    g = warp_sum(g);
-                    up = warp_sum(up);
-                    if (lane == 0) a.h[f] = g / (1.0f + expf(-g)) * up;  // slot f / I, feature f % I
+                    const float gs = warp_sum(g[i]), us = warp_sum(up[i]);
+                    if (lane == 0) a.h[f] = __float2bfloat16_rn(gs / (1.0f + expf(-gs)) * us);  // slot f / I, feature f % I
                 }
             }
         }
@@ -644,31 +696,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         }
         if (!grid_wait(a.ctrl, ++nbar * G, lim, 3, &s_ok)) return;
         {
-            // h of every slot into shared memory (written by other blocks: read from L2)
-            const float4 *h4 = reinterpret_cast<const float4 *>(a.h);
-            const int n4 = nslots * a.I / 4;
-            const int r4 = a.I / 4;  // float4 per slot
-            for (int i = tid; i < n4; i += kDecThreads) {
-                const float4 v = __ldcg(h4 + i);
-                *reinterpret_cast<float4 *>(hs + (i / r4) * ip + vpos((i % r4) * 4)) = v;
+            // h of every slot (bf16 words) and the sums of its words into shared
+            // memory; h was written by other blocks, so it is read from L2
+            const uint4 *h4 = reinterpret_cast<const uint4 *>(a.h);
+            const int nw8 = a.I / 8;  // words per slot
+            for (int i = tid; i < nslots * nw8; i += kDecThreads) {
+                const uint4 v = __ldcg(h4 + i);
+                const int j = i / nw8;
+                hb[j * hp + hpos(i - j * nw8)] = v;
+                hsum8[i] = sum8_bf16(v);
             }
-        }
-        __syncthreads();
-        float *hsum8 = hs + nslots * ip;
-        const int nw8 = a.I / 8;
-        for (int w = tid; w < nslots * nw8; w += kDecThreads) {
-            const float4 *src = reinterpret_cast<const float4 *>(hs + (w / nw8) * ip + vpos((w % nw8) * 8));
-            const float4 u0v = src[0], u1v = src[1];
-            hsum8[w] = ((u0v.x + u0v.y) + (u0v.z + u0v.w)) + ((u1v.x + u1v.y) + (u1v.z + u1v.w));
         }
         cp_async_wait_all();  // this thread's staged rows and router columns
         __syncthreads();
         for (int f = y_lo + warp; f < y_hi; f += kDecWarps) {
             const float y = warp_sum(a.stage_down
-                                         ? down_dot<true>(a, P, e_j, w_j, nslots, f, f - y_lo, lane, gshift, st, hs,
-                                                          hsum8, ip)
-                                         : down_dot<false>(a, P, e_j, w_j, nslots, f, f - y_lo, lane, gshift, st, hs,
-                                                           hsum8, ip));
+                                         ? down_dot<true>(a, P, e_j, w_j, nslots, f, f - y_lo, lane, gshift, st, hb,
+                                                          hsum8, hp)
+                                         : down_dot<false>(a, P, e_j, w_j, nslots, f, f - y_lo, lane, gshift, st, hb,
+                                                           hsum8, hp));
             if (lane == 0) {
                 const __nv_bfloat16 yb = __float2bfloat16_rn(y);
                 out[f] = yb;
@@ -697,7 +743,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                 atomicAdd(a.racc + (((l + 1) % 2) * kRaccCopies + b % kRaccCopies) * a.E + e, static_cast<double>(part));
             grid_arrive(a.ctrl);
         }
-        __syncthreads();  // hs and the staging buffers are refilled by the next layer
+        __syncthreads();  // hb and the staging buffers are refilled by the next layer
     }
 }
 

@@ -55,7 +55,7 @@ struct DecodeStack {
     float *logits_part;      // [4][E]: router partial sums over K quarters
     int *topk_idx;           // [8]
     float *topk_w;           // [8]
-    float *h;                // [k + 1][I] fp32 (slot k = shared expert)
+    __nv_bfloat16 *h;        // [k + 1][I] (slot k = shared expert)
     double *racc;            // [2][kRaccCopies][E]: next layer's router logits, summed over blocks (alternating buffers)
     const float *next_Wr;    // router of the layer after this launch (L2 prefetch), or NULL
     long long wait_limit;

@@ -107,7 +107,7 @@ inline DecodeLayout decode_layout(int E, int k, int I) {
     L.logits = take(sizeof(float) * 4 * (size_t)E);  // partial sums over 4 K quarters
     L.topk_idx = take(sizeof(int) * 8);
     L.topk_w = take(sizeof(float) * 8);
-    L.h = take(sizeof(float) * (size_t)(k + 1) * I);
+    L.h = take(sizeof(uint16_t) * (size_t)(k + 1) * I);  // bf16 SwiGLU rows
     L.racc = 0;  // stacks only
     L.act = 0;
     L.total = o;

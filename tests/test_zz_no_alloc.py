@@ -26,8 +26,8 @@ def test_oversized_layer_rejected_on_host():
     from int4_grouped_gemm_gb300 import build
     build.build()
     lib = _lib.load()
-    # at E=256, k=8 the 64 KiB array holds I <= 1664; each of these needs more
-    for E, k, H, I, G in [(256, 8, 2048, 1792, 64), (256, 8, 4096, 4096, 32), (128, 8, 2048, 2048, 64)]:
+    # at E=256, k=8 the 64 KiB array holds I <= 3328; each of these needs more
+    for E, k, H, I, G in [(256, 8, 2048, 3456, 64), (256, 8, 4096, 4096, 32), (128, 8, 2048, 4096, 64)]:
         d = _fake_desc(E, k, H, I, G)
         rc = lib.moe_decode_static_scratch(ctypes.byref(d), ctypes.c_void_p(2048), ctypes.c_void_p(4096), None)
         assert rc == _lib.MOE_ERR_WORKSPACE, (E, k, H, I, G, rc)
