@@ -428,6 +428,7 @@ __device__ __forceinline__ float down_dot(const DecodeStack &a, const DecodeLaye
 // Order-preserving 64-bit key of (logit, expert): larger logit first, then
 // lower expert index first; distinct for distinct experts.
 __device__ __forceinline__ unsigned long long topk_key(float l, int e) {
+    if (l == 0.0f) l = 0.0f;  // -0 ties with +0, as in a comparison of values
     uint32_t u = __float_as_uint(l);
     u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
     return (static_cast<unsigned long long>(u) << 32) | static_cast<uint32_t>(0xFFFFFFFFu - e);
@@ -589,9 +590,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
 
         // What this layer needs later and does not depend on its routing
         // starts moving now: the shared expert's down rows and the next
-        // layer's router columns (phase C).
-        if (a.stage_down && a.has_shared) stage_down_rows(a, P, s_idx, a.k, a.k + 1, y_lo, ys, st, tid, kDecThreads);
-        if (a.stage_router && li + 1 < a.n_layers) stage_router_cols(a, a.L[li + 1].Wr, c0, st, tid, kDecThreads);
+        // layer's router columns (phase C).  Warp 0, whose thread 0 polls the
+        // grid barriers, issues none of these copies (here or in phase B):
+        // its barrier polls then run without copies of its own in flight.
+        if (warp > 0) {
+            if (a.stage_down && a.has_shared)
+                stage_down_rows(a, P, s_idx, a.k, a.k + 1, y_lo, ys, st, tid - 32, kDecThreads - 32);
+            if (a.stage_router && li + 1 < a.n_layers)
+                stage_router_cols(a, a.L[li + 1].Wr, c0, st, tid - 32, kDecThreads - 32);
+        }
         if (!a.stage_down && tid == kDecThreads - 1 && a.has_shared) {
             const int64_t r0 = static_cast<int64_t>(a.E) * a.H;
             prefetch_slice(P.qd + r0 * (a.I / 8), static_cast<size_t>(a.H) * (a.I / 8) * 4, b, G);
@@ -640,7 +647,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         bool down_requested = false;
         auto request_down = [&]() {
             if (a.stage_down) {
-                stage_down_rows(a, P, s_idx, 0, a.k, y_lo, ys, st, tid, kDecThreads);
+                if (warp > 0) stage_down_rows(a, P, s_idx, 0, a.k, y_lo, ys, st, tid - 32, kDecThreads - 32);
             } else if (tid < a.k) {
                 const int64_t r0 = static_cast<int64_t>(s_idx[tid]) * a.H;
                 prefetch_slice(P.qd + r0 * (a.I / 8), static_cast<size_t>(a.H) * (a.I / 8) * 4, b, G);

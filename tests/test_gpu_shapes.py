@@ -1,8 +1,8 @@
 """Parity at shapes the benchmark does not exercise: the widest hidden size
 the decode kernel serves (4096, its second register-tile instance), a wide
-expert (I = 1024: longer down rows, read in place by decode), group 32 along
-a long K, and decode stacks longer than one kernel launch (more than 64
-layers)."""
+expert (I = 1024: longer down rows), both at once with k = 8 (the decode
+kernel's register fallback for the gate/up rows), group 32 along a long K,
+and decode stacks longer than one kernel launch (more than 64 layers)."""
 import pytest
 import torch
 
@@ -16,6 +16,10 @@ pytestmark = pytest.mark.gpu
 
 WIDE_H = synthetic.MoEConfig("wideH", T=300, H=4096, E=8, k=2, I=256, group=32, seed=21)
 WIDE_I = synthetic.MoEConfig("wideI", T=200, H=512, E=8, k=2, I=1024, group=64, seed=22)
+# widest hidden and expert sizes with k = 8: the decode kernel's gate/up rows
+# no longer fit in shared memory (they go through registers) and its down rows
+# are wider than one 16-element span per lane
+WIDE_HI = synthetic.MoEConfig("wideHI", T=6, H=4096, E=8, k=8, I=1024, group=64, seed=23)
 
 
 @pytest.mark.parametrize("cfg", [WIDE_H, WIDE_I], ids=lambda c: c.name)
@@ -24,7 +28,7 @@ def test_prefill_wide_shapes(cfg):
     check_layer(L, L.x)
 
 
-@pytest.mark.parametrize("cfg", [WIDE_H, WIDE_I], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", [WIDE_H, WIDE_I, WIDE_HI], ids=lambda c: c.name)
 def test_decode_wide_shapes(cfg):
     L = synthetic.make_layer(cfg, T=6)
     layer = PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down)
