@@ -254,16 +254,16 @@ __device__ __forceinline__ void row_pair_load(const DecodeStack &a, const Decode
     const uint32_t *qu = P.qu + row * nwords;
 #pragma unroll
     for (int v = 0; v < kMaxRowVec; ++v) {
-        const int w0 = lane * 4 + v * 128;
-        if (w0 < nwords) {
-            rp.r[v] = __ldg(reinterpret_cast<const uint4 *>(qg + w0));
-            rp.r[kMaxRowVec + v] = __ldg(reinterpret_cast<const uint4 *>(qu + w0));
-            const int grp = (w0 * 8) >> gshift;  // the 4 words (32 elements) share a group (G >= 32)
-            rp.sb[4 * v + 0] = __ldg(P.sg + row * a.ldg_h + grp);
-            rp.sb[4 * v + 1] = __ldg(P.bg + row * a.ldg_h + grp);
-            rp.sb[4 * v + 2] = __ldg(P.su + row * a.ldg_h + grp);
-            rp.sb[4 * v + 3] = __ldg(P.bu + row * a.ldg_h + grp);
-        }
+        // spans past the row (H < HMAX) re-read the row's first span; the dot
+        // product drops them
+        const int w0 = lane * 4 + v * 128 < nwords ? lane * 4 + v * 128 : 0;
+        rp.r[v] = __ldg(reinterpret_cast<const uint4 *>(qg + w0));
+        rp.r[kMaxRowVec + v] = __ldg(reinterpret_cast<const uint4 *>(qu + w0));
+        const int grp = (w0 * 8) >> gshift;  // the 4 words (32 elements) share a group (G >= 32)
+        rp.sb[4 * v + 0] = __ldg(P.sg + row * a.ldg_h + grp);
+        rp.sb[4 * v + 1] = __ldg(P.bg + row * a.ldg_h + grp);
+        rp.sb[4 * v + 2] = __ldg(P.su + row * a.ldg_h + grp);
+        rp.sb[4 * v + 3] = __ldg(P.bu + row * a.ldg_h + grp);
     }
 }
 
@@ -276,8 +276,9 @@ __device__ __forceinline__ void row_pairs_dot(const DecodeStack &a, int lane, co
     const int nwords = a.H / 8;
 #pragma unroll
     for (int v = 0; v < kMaxRowVec; ++v) {
-        const int w0 = lane * 4 + v * 128;
-        if (w0 < nwords) {
+        const bool valid = lane * 4 + v * 128 < nwords;
+        const int w0 = valid ? lane * 4 + v * 128 : 0;
+        {
             float dg[NP], du[NP], xs4 = 0.f;
 #pragma unroll
             for (int p = 0; p < NP; ++p) dg[p] = du[p] = 0.f;
@@ -299,8 +300,8 @@ __device__ __forceinline__ void row_pairs_dot(const DecodeStack &a, int lane, co
             for (int p = 0; p < NP; ++p) {
                 const float sgv = bf16_bits_to_float(rp[p].sb[4 * v + 0]), bgv = bf16_bits_to_float(rp[p].sb[4 * v + 1]);
                 const float suv = bf16_bits_to_float(rp[p].sb[4 * v + 2]), buv = bf16_bits_to_float(rp[p].sb[4 * v + 3]);
-                gacc[p] += sgv * dg[p] + (bgv - 128.0f * sgv) * xs4;
-                uacc[p] += suv * du[p] + (buv - 128.0f * suv) * xs4;
+                gacc[p] += valid ? sgv * dg[p] + (bgv - 128.0f * sgv) * xs4 : 0.f;
+                uacc[p] += valid ? suv * du[p] + (buv - 128.0f * suv) * xs4 : 0.f;
             }
         }
     }
@@ -420,6 +421,36 @@ __device__ __forceinline__ float down_dot(const DecodeStack &a, const DecodeLaye
             y += w_j[j] * acc;
         }
     }
+    return y;
+}
+
+// down_dot for staged rows at most 512 wide (one 16-element span per lane):
+// straight-line code over all kMaxSlots slots (slots past nslots re-read the
+// last slot and are weighted out by a select), so the slots' loads and
+// arithmetic interleave freely.
+__device__ __forceinline__ float down_dot_flat(const DecodeStack &a, const float *w_j, int nslots, int fl, int lane,
+                                               int gshift, const DownStage &st, const uint4 *hb, const float *hsum8,
+                                               int hp) {
+    const int nw = a.I / 8;
+    const bool act = 2 * lane < nw;
+    const int w = act ? 2 * lane : 0;  // lanes past the row re-read word 0 and are weighted out
+    const int g = (w * 8) >> gshift;
+    float t[kMaxSlots];
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j) {
+        const int jj = j < nslots ? j : nslots - 1;
+        const int r = jj * st.ys_cap + fl;
+        const uint2 qv = *reinterpret_cast<const uint2 *>(st.dq + r * nw + w);
+        const float sc = bf16_bits_to_float(st.ds[r * a.ldg_i + g]);
+        const float bi = bf16_bits_to_float(st.db[r * a.ldg_i + g]);
+        const uint4 *hv = hb + jj * hp;
+        const float dsum = dot8_codes128(qv.x, hv[hpos(w)]) + dot8_codes128(qv.y, hv[hpos(w + 1)]);
+        const float hsum = hsum8[jj * nw + w] + hsum8[jj * nw + w + 1];
+        t[j] = sc * dsum + (bi - 128.0f * sc) * hsum;
+    }
+    float y = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxSlots; ++j) y += (act && j < nslots ? w_j[j] : 0.f) * (act && j < nslots ? t[j] : 0.f);
     return y;
 }
 
@@ -660,19 +691,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             int64_t rows[2];
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
-                const int f = f0 + i * kDecWarps;
-                if (f < f_hi) {
-                    const int j = f / a.I;
-                    rows[i] = static_cast<int64_t>(j < a.k ? s_idx[j] : a.E) * a.I + (f - j * a.I);
-                    row_pair_load(a, P, rows[i], lane, gshift, r2[i]);
-                }
+                // a missing second pair re-reads the first; its result is dropped
+                const int f = f0 + i * kDecWarps < f_hi ? f0 + i * kDecWarps : f0;
+                const int j = f / a.I;
+                rows[i] = static_cast<int64_t>(j < a.k ? s_idx[j] : a.E) * a.I + (f - j * a.I);
+                row_pair_load(a, P, rows[i], lane, gshift, r2[i]);
             }
             if (!down_requested) request_down();
             float g[2] = {0.f, 0.f}, up[2] = {0.f, 0.f};
-            if (f0 + kDecWarps < f_hi)
-                row_pairs_dot<HMAX, 2>(a, lane, r2, xb, xsum8, g, up);
-            else
-                row_pairs_dot<HMAX, 1>(a, lane, r2, xb, xsum8, g, up);
+            row_pairs_dot<HMAX, 2>(a, lane, r2, xb, xsum8, g, up);
 #pragma unroll
             for (int i = 0; i < 2; ++i) {
                 const int f = f0 + i * kDecWarps;
@@ -718,8 +745,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         __syncthreads();
         for (int f = y_lo + warp; f < y_hi; f += kDecWarps) {
             const float y = warp_sum(a.stage_down
-                                         ? down_dot<true>(a, P, e_j, w_j, nslots, f, f - y_lo, lane, gshift, st, hb,
-                                                          hsum8, hp)
+                                         ? (a.I <= 512 ? down_dot_flat(a, w_j, nslots, f - y_lo, lane, gshift, st, hb,
+                                                                       hsum8, hp)
+                                                       : down_dot<true>(a, P, e_j, w_j, nslots, f, f - y_lo, lane, gshift, st, hb,
+                                                          hsum8, hp))
                                          : down_dot<false>(a, P, e_j, w_j, nslots, f, f - y_lo, lane, gshift, st, hb,
                                                            hsum8, hp));
             if (lane == 0) {
