@@ -499,15 +499,20 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
         if (t < a.E) {
             float l;
             if (racc) {
-                // summed by the previous layer's blocks into kRaccCopies copies,
-                // added here in a fixed order
+                // summed by the previous layer's blocks into kRaccCopies copies
+                // (fp64, exact for so few terms), rounded to fp32 and added
+                // pairwise here in a fixed order
                 double v[kRaccCopies];
 #pragma unroll
                 for (int r = 0; r < kRaccCopies; ++r) v[r] = __ldcg(racc + r * a.E + t);
-                double sum = v[0];
+                float vf[kRaccCopies];
 #pragma unroll
-                for (int r = 1; r < kRaccCopies; ++r) sum += v[r];
-                l = static_cast<float>(sum);
+                for (int r = 0; r < kRaccCopies; ++r) vf[r] = static_cast<float>(v[r]);
+#pragma unroll
+                for (int w = 1; w < kRaccCopies; w *= 2)
+#pragma unroll
+                    for (int r = 0; r + w < kRaccCopies; r += 2 * w) vf[r] += vf[r + w];
+                l = vf[0];
             } else {
                 l = __ldcg(a.logits_part + t) + __ldcg(a.logits_part + a.E + t);
                 l += __ldcg(a.logits_part + 2 * a.E + t);
