@@ -484,10 +484,11 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
 
 // Top-k of E <= 256 logits (ties -> lower expert index) and the softmax over
 // the picked ones.  Warps 0-7 each sort 32 experts' keys; the 8 best of every
-// warp (64 candidates, which hold the top k <= 8) are then placed by rank:
-// thread i < 64 counts the candidates above candidate i, and a rank below k
-// is its slot (real keys are distinct; padding keys are 0 and rank after
-// every real one).  s_keys holds 64 candidates + 8 picked keys.  The logit of
+// warp (64 candidates in 8 lists, which hold the top k <= 8) are then placed
+// by rank: the number of candidates above one, counted by 8 threads (one per
+// list), and a rank below k is its slot (real keys are distinct; padding
+// keys are 0 and rank after every real one).  s_keys holds the 64
+// candidates + 8 picked keys.  The logit of
 // expert e is the sum of its four K-quarter partial sums in a fixed order
 // (first layer of a launch) or the fp64 sum that the previous layer's blocks
 // accumulated, plus the bias.  Every block computes the same result.
@@ -522,17 +523,24 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
             key = topk_key(l, t);
         }
         key = warp_sort_desc(key, lane);
-        if (lane < 8) s_keys[warp * 8 + lane] = key;
+        if (lane < 8) s_keys[lane * 8 + warp] = key;  // list `warp`, i-th best at i * 8 + warp
     }
     __syncthreads();
-    if (t < 64) {
-        const unsigned long long mine = s_keys[t];
-        int rank = 0;
-#pragma unroll 16
-        for (int i = 0; i < 64; ++i) rank += s_keys[i] > mine ? 1 : 0;
-        if (rank < a.k) s_keys[64 + rank] = mine;
-        named_barrier(1, 64);
+    {
+        // candidate c = t / 8: thread t counts the keys of list t % 8 above
+        // it, and the 8 threads of a candidate add their counts
+        static_assert(kDecThreads == 64 * 8, "one thread per candidate and list");
+        const int c = t >> 3, list = t & 7;
+        const unsigned long long mine = s_keys[c];
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cnt += s_keys[i * 8 + list] > mine ? 1 : 0;
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, 4);
+        if (list == 0 && cnt < a.k) s_keys[64 + cnt] = mine;
     }
+    __syncthreads();
     if (warp == 0) {
         // lane j < k: pick j
         const unsigned long long k = lane < a.k ? s_keys[64 + lane] : 0ull;
@@ -541,7 +549,10 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
         const int e = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>(k));
         const float m = __shfl_sync(0xffffffffu, l, 0);
         const float ex = lane < a.k ? expf(l - m) : 0.f;
-        const float sum = warp_sum(ex);
+        float sum = ex;  // lanes 0-7 hold the picks
+        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+        sum += __shfl_xor_sync(0xffffffffu, sum, 1);
         if (lane < a.k) {
             s_idx[lane] = e;
             s_w[lane] = ex / sum;

@@ -9,7 +9,7 @@ namespace moe {
 constexpr int kTileRows = 128;      // token rows per grouped-GEMM tile (MMA M)
 constexpr int kRouteChunk = 64;     // tokens per routing block (histogram granularity)
 constexpr int kCtrlBytes = 256;     // status word, decode ticket, ...
-constexpr int kRaccCopies = 8;      // decode: copies of the next layer's logit sums (block b adds to copy b % 8)
+constexpr int kRaccCopies = 4;      // decode: copies of the next layer's logit sums (block b adds to copy b % 4)
 
 // Scale/bias row pitch in groups: K/G rounded up to a multiple of 8 (16 bytes).
 inline int ld_groups(int K, int G) { return (K / G + 7) / 8 * 8; }
