@@ -283,7 +283,7 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     cudaError_t e = mark(events, 0, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     // router: bf16 split of the weights (and clearing of the combine
-    // accumulator and histogram), then the four partial router GEMMs on the
+    // accumulator and histogram), then the eight partial router GEMMs on the
     // tensor cores
     if (launch_prep(desc->router_w, E, L.E_pad16, H, wr3, y_acc, static_cast<int64_t>(T) * H, rb.counts_blk,
                     static_cast<int64_t>(rb.nblk) * E, dev->num_sms, stream) != cudaSuccess)

@@ -39,7 +39,7 @@
 //               MODE 0 (gate/up): h = silu(gate) * up -> bf16 h rows
 //               MODE 1 (down):    y_acc[token] += w * o  (fp32 v4 reductions
 //                                 after a transpose through shared memory)
-//               MODE 2 (router):  partial logits of one bf16 part and K half
+//               MODE 2 (router):  partial logits of one bf16 part and K quarter
 //               Tile 0's accumulator is handed back first, so that the next
 //               unit's tile-0 MMAs overlap the draining of tile 1.
 //
@@ -72,7 +72,8 @@ constexpr int S_STAGE = 2 * BN * SG * 2;         // 8 KB: [scale|bias][256 rows]
 constexpr int T_PITCH = 20;                      // fp32 pitch of the epilogue transpose rows
 constexpr uint32_t kTmemCols = 512;              // two 256-column fp32 accumulators
 constexpr int kRouterParts = 2;                  // bf16 parts of the fp32 router weights
-constexpr int kRouterUnits = 2 * kRouterParts;   // router units per token-tile pair (parts x K halves)
+constexpr int kRouterKSplit = 4;                 // K quarters of the router GEMM
+constexpr int kRouterUnits = kRouterParts * kRouterKSplit;  // router units per token-tile pair (parts x K quarters)
 
 struct Smem {
     uint64_t a_full[NS_A], a_empty[NS_A];
@@ -109,8 +110,8 @@ struct Unit {
     int row0;    // first token row: permuted row (MODE 0/1) or token (MODE 2)
     int n;       // valid rows of the unit (<= TPU * BM)
     int ntiles;  // token tiles holding them (1 or 2)
-    int part;    // MODE 2: bf16 part (0 hi, 1 lo) and K half
-    int khalf;
+    int part;    // MODE 2: bf16 part (0 hi, 1 lo) and K quarter
+    int kq;
 };
 
 // A unit of MODE 0/1 is tiles t0 and t0 + 1 of one group when the scheduled
@@ -122,8 +123,8 @@ __device__ __forceinline__ Unit load_unit(const GemmArgs &a, int u) {
     Unit t{};
     if (MODE == 2) {
         const int pair = u / kRouterUnits, rem = u % kRouterUnits;
-        t.part = rem / 2;
-        t.khalf = rem % 2;
+        t.part = rem / kRouterKSplit;
+        t.kq = rem % kRouterKSplit;
         t.row0 = pair * TPU * BM;
         t.n = min(TPU * BM, a.T - t.row0);
     } else {
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     const uint32_t tmem_base = s->tmem_base;
 
     const int nunits = num_units<MODE>(a);
-    const int ksteps = MODE == 2 ? (a.K / 2) / GK : a.K / GK;
+    const int ksteps = MODE == 2 ? (a.K / kRouterKSplit) / GK : a.K / GK;
     const int ks_per_sblock = SG * a.G / GK;            // stages per scale block
     const int nb = MODE == 2 ? a.E_pad16 : BN;          // MMA N
 
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 const bool shared = MODE == 0 && t.g == a.E;
                 const CUtensorMap *map_a = shared ? &tm_a1 : &tm_a0;
                 const int arow = shared ? t.row0 - a.routed_rows : t.row0;
-                const int kcol0 = MODE == 2 ? t.khalf * (a.K / 2) : 0;
+                const int kcol0 = MODE == 2 ? t.kq * (a.K / kRouterKSplit) : 0;
                 for (int ks = 0; ks < ksteps; ++ks, ++it) {
                     const int st = it % NS_A;
                     ok = wait_or_abort(&s->a_empty[st], ((it / NS_A) & 1) ^ 1, a, s, 1);
@@ -318,7 +319,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
                 const Unit t = load_unit<MODE>(a, u);
                 if (MODE == 2) {
-                    const int kcol0 = t.khalf * (a.K / 2);
+                    const int kcol0 = t.kq * (a.K / kRouterKSplit);
                     for (int ks = 0; ks < ksteps; ++ks, ++bit) {
                         const int st = bit % NS_B;
                         ok = wait_or_abort(&s->b_empty[st], ((bit / NS_B) & 1) ^ 1, a, s, 2);
@@ -553,7 +554,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                     }
                 } else {
                     float *lrow = a.logits_part +
-                                  (static_cast<int64_t>(t.part * 2 + t.khalf) * a.T + t.row0 + rr) * a.E_pad16;
+                                  (static_cast<int64_t>(t.part * kRouterKSplit + t.kq) * a.T + t.row0 + rr) * a.E_pad16;
                     for (int c0 = chalf * 16; c0 < nb; c0 += 32) {
                         float v[16];
                         tmem_ld16(tbase + c0, v);

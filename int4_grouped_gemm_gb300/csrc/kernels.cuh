@@ -18,7 +18,7 @@ struct GemmArgs {
     const __nv_bfloat16 *x;    // [T][H]: layer input (gate/up gathers its token rows from it)
     __nv_bfloat16 *h;          // [R][I]
     float *y_acc;              // [T][H]
-    float *logits_part;        // router: [4][T][E_pad16] (parts x K halves)
+    float *logits_part;        // router: [8][T][E_pad16] (parts x K quarters)
     int *status;
     long long wait_limit;
 };

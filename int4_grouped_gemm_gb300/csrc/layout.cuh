@@ -90,7 +90,7 @@ inline PrefillLayout prefill_layout(int T, int E, int k, int H, int I) {
     L.y_acc = take(sizeof(float) * (size_t)T * H);
     L.E_pad16 = (E + 15) / 16 * 16;
     L.wr3 = take(sizeof(uint16_t) * 2 * (size_t)L.E_pad16 * H);
-    L.logits_part = take(sizeof(float) * 4 * (size_t)T * L.E_pad16);
+    L.logits_part = take(sizeof(float) * 8 * (size_t)T * L.E_pad16);  // 2 bf16 parts x 4 K quarters
     L.total = o;
     return L;
 }

@@ -48,11 +48,12 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
             if (e < E) {
                 if (logits_part) {
                     // partial sums: hi and lo bf16 parts of the router weights,
-                    // two K halves each; the small part first
+                    // four K quarters each, added pairwise in a fixed order;
+                    // the small part first
                     const int64_t pstride = static_cast<int64_t>(T) * ld;
                     const float *p = logits_part + static_cast<int64_t>(t) * ld + e;
-                    const float lo = p[2 * pstride] + p[3 * pstride];
-                    const float hi = p[0] + p[pstride];
+                    const float lo = (p[4 * pstride] + p[5 * pstride]) + (p[6 * pstride] + p[7 * pstride]);
+                    const float hi = (p[0] + p[pstride]) + (p[2 * pstride] + p[3 * pstride]);
                     l = lo + hi;
                     if (bias) l += bias[e];
                     rb.logits[static_cast<int64_t>(t) * E + e] = l;
