@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--decode-steps", type=int, default=256)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other", action="store_true", help="skip the T=512 and T=16384 secondary prefill layers")
     ap.add_argument("--profile", action="store_true",
                     help="only run warmup + steps prefill calls of the headline layer (for ncu captures)")
     ap.add_argument("--profile-decode", action="store_true",
@@ -386,6 +387,54 @@ def run_decode(args, pk):
                 clocks=clk.summary(), launches=-(-cfg.layers // DECODE_LAYERS_PER_KERNEL) * steps)
 
 
+def run_prefill_other(name, pk, steps=10):
+    """Secondary prefill layers (not the headline): graph-replayed calls with an
+    L2 flush before each, expert FLOP/s against the bf16 peak and the bytes
+    of the touched experts' weights (+ router) against HBM."""
+    import torch
+    from int4_grouped_gemm_gb300 import _lib, synthetic
+    cfg = synthetic.CONFIGS[name]
+    layer, x = build_prefill(cfg)
+    ws = layer.workspace(cfg.T)
+    y = torch.empty_like(x)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        _lib.moe_prefill(layer.desc, x, cfg.T, y, ws.buf)
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        _lib.moe_prefill(layer.desc, x, cfg.T, y, ws.buf)
+    torch.cuda.current_stream().wait_stream(side)
+    with torch.cuda.graph(graph):
+        _lib.moe_prefill(layer.desc, x, cfg.T, y, ws.buf)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        ev[i][0].record()
+        graph.replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    st = _lib.moe_read_device_status(ws.buf)
+    if st != 0:
+        raise RuntimeError(f"{name}: device status {st}")
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    counts = ws.routing(layer.desc, cfg.T)["counts"].cpu()
+    rows = int(counts.sum().item())
+    touched = int((counts > 0).sum().item())  # routed experts with rows + the shared one (its count is T)
+    per_expert = 3 * cfg.H * cfg.I // 2 + 3 * cfg.H * cfg.I // cfg.group * 4
+    wbytes = touched * per_expert + cfg.E * cfg.H * 4
+    tflops = expert_flops(rows, cfg.H, cfg.I) / (ms * 1e-3) / 1e12
+    gbs = wbytes / (ms * 1e-3) / 1e9
+    del flush, graph, ws, layer, x, y
+    torch.cuda.empty_cache()
+    return {"T": cfg.T, "ms_per_call": round(ms, 4), "tok_s": round(cfg.T / (ms * 1e-3), 1),
+            "expert_tflops": round(tflops, 1), "frac_of_bf16_peak": round(tflops / pk["bf16"], 4),
+            "weight_bytes": wbytes, "hbm_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
+            "experts_touched": touched, "note": cfg.name}
+
+
 # ------------------------------------------------------------ CPU oracle
 
 
@@ -513,6 +562,9 @@ def main():
     D = None
     if not args.no_decode and rank == 0:
         D = run_decode(args, pk)
+    other = None
+    if rank == 0 and not args.no_other:
+        other = {n: run_prefill_other(n, pk) for n in ("prefill512", "skew16384")}
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg)
@@ -547,6 +599,8 @@ def main():
                               "value": round(D["tok_s"], 1), "unit": "tok/s", "ms_per_step": round(D["ms_per_step"], 4),
                               "steps": D["steps"], "roofline": D["roofline"], "clocks": D["clocks"],
                               "gpu_launches": D["launches"], "fresh_token_per_step": D["fresh"]}
+        if other is not None:
+            line["other_prefill"] = other
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
