@@ -92,3 +92,46 @@ def test_graph_step_equals_eager_and_first_layers_match_oracle(chain40):
         ref = _oracle_touched(L, xb, cfg)
         assert_close(eager[l].float().cpu().numpy(), ref, f"chain layer {l}")
         xb = oracle.bf16_round(ref.astype(np.float32))
+
+
+# Routing shapes of the decode kernel beyond the benchmark's: no shared expert
+# (8 slots, not 9), a single pick, and expert counts that fill the top-k
+# kernel's 32-key warps only partly (padding keys must never be picked).
+DECODE_SHAPES = [
+    synthetic.MoEConfig("dec_noshared", T=5, H=256, E=16, k=2, I=128, group=32, seed=31, has_shared=False),
+    synthetic.MoEConfig("dec_k1", T=5, H=512, E=8, k=1, I=256, group=64, seed=32),
+    synthetic.MoEConfig("dec_e40_k3", T=5, H=256, E=40, k=3, I=128, group=32, seed=33),
+    synthetic.MoEConfig("dec_e200_k8_noshared", T=4, H=512, E=200, k=8, I=128, group=64, seed=34,
+                        has_shared=False),
+]
+
+
+@pytest.mark.parametrize("cfg", DECODE_SHAPES, ids=lambda c: c.name)
+def test_decode_routing_shapes(cfg):
+    L = synthetic.make_layer(cfg)
+    layer = PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down)
+    ws = layer.workspace(1)
+    ref = oracle_layer(L, L.x)
+    for t in range(cfg.T):
+        y = layer.decode(L.x[t:t + 1].cuda().contiguous(), ws)
+        torch.cuda.synchronize()
+        assert_close(y.float().cpu().numpy(), ref["y"][t:t + 1], f"{cfg.name} token {t}")
+    assert _lib.moe_read_device_status(ws.buf) == 0
+
+
+def test_decode_stack_without_shared_expert():
+    """A 3-layer stack of the no-shared shape: one launch runs all three and
+    equals three single-layer calls."""
+    cfg = DECODE_SHAPES[0]
+    layers = []
+    for l in range(3):
+        L = synthetic.make_layer(cfg, layer=l, with_x=False)
+        layers.append(PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down))
+    chain = DecodeChain(layers)
+    x0 = synthetic.make_tokens(cfg.H, 1, seed=35).cuda() * 4
+    eager = chain.layer_outputs_eager(x0)
+    chain.set_input(x0)
+    chain.step_eager()
+    torch.cuda.synchronize()
+    assert torch.equal(chain.output(), eager[-1])
+    assert _lib.moe_read_device_status(chain.ws.buf) == 0
