@@ -69,6 +69,17 @@ def test_no_shared_expert():
     check_layer(L, L.x)
 
 
+@pytest.mark.parametrize("cfg", [
+    synthetic.MoEConfig("e40_k3", T=150, H=256, E=40, k=3, I=128, group=32, seed=36),
+    synthetic.MoEConfig("e200_k8", T=90, H=512, E=200, k=8, I=128, group=64, seed=37),
+], ids=lambda c: c.name)
+def test_expert_counts_not_a_multiple_of_16(cfg):
+    """The router GEMM pads the expert rows to 16 (zero rows) and the top-k
+    must never pick a padding column."""
+    L = synthetic.make_layer(cfg)
+    check_layer(L, L.x)
+
+
 def test_one_expert_takes_all_tokens_and_empty_experts():
     cfg = synthetic.MoEConfig("skewtiny", T=300, H=256, E=16, k=2, I=128, group=32, seed=9)
     L = synthetic.make_layer(cfg)
