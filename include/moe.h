@@ -233,6 +233,25 @@ int moe_selftest_wait_timeout(void *ws, size_t ws_bytes, long long limit_cycles,
 int moe_forward_host(const moe_layer_desc *desc, const void *x_host, int32_t T, void *y_host, void *x_dev,
                      void *y_dev, void *ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * n layer calls from host memory, pipelined: call i copies x_host[i] (T x H
+ * bf16) to the device, runs the layer like moe_forward_host and copies the
+ * result to y_host[i].  The copies in run on a second stream and the copies
+ * out on a third (both created and destroyed inside the call), so that call
+ * i + 1's input and call i - 1's output move while call i computes on
+ * `stream`; two device staging sets alternate: x_dev[i % 2], y_dev[i % 2]
+ * (caller-owned, T x H bf16 each, 16-byte aligned).  The workspace is shared
+ * by the calls, which run one after the other on `stream`.  Returns when
+ * every result is in host memory.  Host buffers should be pinned (else the
+ * copies are synchronous and nothing overlaps); the same host buffer may be
+ * given to several calls.  Errors: as moe_forward_host, and MOE_ERR_NULL for
+ * a NULL array or element; n < 1 is MOE_ERR_TOKENS.  The pages describe no
+ * such call: it is the host side of a serving loop.
+ */
+int moe_forward_host_stream(const moe_layer_desc *desc, const void *const *x_host, void *const *y_host, int32_t n,
+                            int32_t T, void *const *x_dev, void *const *y_dev, void *ws, size_t ws_bytes,
+                            cudaStream_t stream);
+
 /* Human-readable text for a status code. */
 const char *moe_status_string(int code);
 

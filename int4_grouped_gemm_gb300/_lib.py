@@ -67,6 +67,7 @@ SIGNATURES = {
     "moe_set_wait_limit": (c_ll, [c_ll]),
     "moe_selftest_wait_timeout": (ctypes.c_int, [c_p, c_sz, c_ll, c_p]),
     "moe_forward_host": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_sz, c_p]),
+    "moe_forward_host_stream": (ctypes.c_int, [c_p, c_p, c_p, c_i32, c_i32, c_p, c_p, c_p, c_sz, c_p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -183,3 +184,19 @@ def moe_forward_host(desc: moe_layer_desc, x_host, T: int, y_host, x_dev, y_dev,
     _check(load().moe_forward_host(ctypes.byref(desc), _ptr(x_host), T, _ptr(y_host), _ptr(x_dev), _ptr(y_dev),
                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "moe_forward_host")
+
+
+def moe_forward_host_stream(desc: moe_layer_desc, x_hosts, T: int, y_hosts, x_devs, y_devs, ws, stream=None):
+    """len(x_hosts) pipelined calls; x_devs / y_devs: two device staging tensors each."""
+    n = len(x_hosts)
+    if len(y_hosts) != n or len(x_devs) != 2 or len(y_devs) != 2:
+        raise ValueError("moe_forward_host_stream: n host inputs and outputs, two device staging buffers each")
+    arr = ctypes.c_void_p * n
+    pair = ctypes.c_void_p * 2
+    xs = arr(*[_ptr(t) for t in x_hosts])
+    ys = arr(*[_ptr(t) for t in y_hosts])
+    xd = pair(*[_ptr(t) for t in x_devs])
+    yd = pair(*[_ptr(t) for t in y_devs])
+    _check(load().moe_forward_host_stream(ctypes.byref(desc), xs, ys, n, T, xd, yd, _ptr(ws),
+                                          ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_forward_host_stream")

@@ -471,6 +471,63 @@ int moe_forward_host(const moe_layer_desc *desc, const void *x_host, int32_t T, 
     return cuda_rc(cudaStreamSynchronize(stream));
 }
 
+int moe_forward_host_stream(const moe_layer_desc *desc, const void *const *x_host, void *const *y_host, int32_t n,
+                            int32_t T, void *const *x_dev, void *const *y_dev, void *ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+    int rc = check_shape(desc);
+    if (rc) return rc;
+    if (n < 1) return MOE_ERR_TOKENS;
+    if (!x_host || !y_host || !x_dev || !y_dev) return MOE_ERR_NULL;
+    for (int i = 0; i < n; ++i)
+        if (!x_host[i] || !y_host[i]) return MOE_ERR_NULL;
+    for (int s = 0; s < 2; ++s)
+        if ((rc = check_ptr(x_dev[s])) || (rc = check_ptr(y_dev[s]))) return rc;
+    if ((rc = check_tokens(desc, T))) return rc;
+    const size_t bytes = static_cast<size_t>(T) * desc->H * 2;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t in_done[2] = {}, comp_done[2] = {}, out_done[2] = {};
+    bool made = cudaStreamCreateWithFlags(&h2d, cudaStreamNonBlocking) == cudaSuccess &&
+                cudaStreamCreateWithFlags(&d2h, cudaStreamNonBlocking) == cudaSuccess;
+    for (int s = 0; s < 2 && made; ++s)
+        made = cudaEventCreateWithFlags(&in_done[s], cudaEventDisableTiming) == cudaSuccess &&
+               cudaEventCreateWithFlags(&comp_done[s], cudaEventDisableTiming) == cudaSuccess &&
+               cudaEventCreateWithFlags(&out_done[s], cudaEventDisableTiming) == cudaSuccess;
+    rc = made ? MOE_OK : MOE_ERR_CUDA;
+    for (int i = 0; i < n && rc == MOE_OK; ++i) {
+        const int s = i % 2;
+        // x_dev[s] was last read by call i - 2's layer; y_dev[s] last copied out by its d2h
+        if (i >= 2 && (cudaStreamWaitEvent(h2d, comp_done[s], 0) != cudaSuccess ||
+                       cudaStreamWaitEvent(stream, out_done[s], 0) != cudaSuccess)) {
+            rc = MOE_ERR_CUDA;
+            break;
+        }
+        if (cudaMemcpyAsync(x_dev[s], x_host[i], bytes, cudaMemcpyHostToDevice, h2d) != cudaSuccess ||
+            cudaEventRecord(in_done[s], h2d) != cudaSuccess || cudaStreamWaitEvent(stream, in_done[s], 0) != cudaSuccess) {
+            rc = MOE_ERR_CUDA;
+            break;
+        }
+        rc = T == 1 ? moe_decode(desc, x_dev[s], y_dev[s], ws, ws_bytes, stream)
+                    : moe_prefill(desc, x_dev[s], T, y_dev[s], ws, ws_bytes, stream);
+        if (rc) break;
+        if (cudaEventRecord(comp_done[s], stream) != cudaSuccess || cudaStreamWaitEvent(d2h, comp_done[s], 0) != cudaSuccess ||
+            cudaMemcpyAsync(y_host[i], y_dev[s], bytes, cudaMemcpyDeviceToHost, d2h) != cudaSuccess ||
+            cudaEventRecord(out_done[s], d2h) != cudaSuccess)
+            rc = MOE_ERR_CUDA;
+    }
+    // everything enqueued so far finishes before the streams and events go away
+    if (h2d && cudaStreamSynchronize(h2d) != cudaSuccess) rc = rc ? rc : MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) rc = rc ? rc : MOE_ERR_CUDA;
+    if (d2h && cudaStreamSynchronize(d2h) != cudaSuccess) rc = rc ? rc : MOE_ERR_CUDA;
+    for (int s = 0; s < 2; ++s) {
+        if (in_done[s]) cudaEventDestroy(in_done[s]);
+        if (comp_done[s]) cudaEventDestroy(comp_done[s]);
+        if (out_done[s]) cudaEventDestroy(out_done[s]);
+    }
+    if (h2d) cudaStreamDestroy(h2d);
+    if (d2h) cudaStreamDestroy(d2h);
+    return rc;
+}
+
 const char *moe_status_string(int code) {
     switch (code) {
         case MOE_OK: return "ok";
