@@ -84,6 +84,24 @@ def test_argument_errors_are_caught_on_the_host(lib):
     assert lib.moe_read_device_status(None, None) == _lib.MOE_ERR_NULL
 
 
+def test_pipelined_host_call_rejects_bad_arguments_on_the_host(lib):
+    from int4_grouped_gemm_gb300 import _lib
+    d = _desc()
+    two = (ctypes.c_void_p * 2)(16, 32)
+    one = (ctypes.c_void_p * 1)(64)
+    none = (ctypes.c_void_p * 1)(None)
+    f = lib.moe_forward_host_stream
+    # no calls, no arrays, a NULL host buffer, a misaligned staging buffer
+    assert f(ctypes.byref(d), one, one, 0, 16, two, two, None, 0, None) == _lib.MOE_ERR_TOKENS
+    assert f(ctypes.byref(d), None, one, 1, 16, two, two, None, 0, None) == _lib.MOE_ERR_NULL
+    assert f(ctypes.byref(d), none, one, 1, 16, two, two, None, 0, None) == _lib.MOE_ERR_NULL
+    assert f(ctypes.byref(d), one, one, 1, 16, (ctypes.c_void_p * 2)(16, 40), two, None, 0, None) == \
+        _lib.MOE_ERR_ALIGN
+    assert f(ctypes.byref(d), one, one, 1, 0, two, two, None, 0, None) == _lib.MOE_ERR_TOKENS
+    bad = _desc(k=9)
+    assert f(ctypes.byref(bad), one, one, 1, 16, two, two, None, 0, None) == _lib.MOE_ERR_SHAPE
+
+
 def test_routing_views_layout(lib):
     from int4_grouped_gemm_gb300 import _lib
     d = _desc()
