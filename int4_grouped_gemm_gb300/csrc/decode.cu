@@ -672,7 +672,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         // this block's contiguous range [f_lo, f_hi) of (slot, feature) pairs
         // of the gate/up rows, slot k being the shared expert; warp w takes
         // pairs f_lo + w, f_lo + w + kDecWarps, ... two at a time
-        if (!grid_wait(a.ctrl, ++nbar * G, lim, 2, &s_ok)) return;
+        if (!grid_wait(a.ctrl, ++nbar * G, lim, 2, &s_ok)) {
+            cp_async_wait_all();  // this thread's staging copies land before the block exits
+            return;
+        }
         if (li > 0) {
             // the layer input, complete once every block passed the barrier:
             // warps 8-15 stage it while warps 0-7 start the top-k below
@@ -744,7 +747,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             const float *nWr = li + 1 < a.n_layers ? (a.stage_router ? nullptr : a.L[li + 1].Wr) : a.next_Wr;
             if (nWr) prefetch_slice(nWr, static_cast<size_t>(a.E) * a.H * 4, b, G);
         }
-        if (!grid_wait(a.ctrl, ++nbar * G, lim, 3, &s_ok)) return;
+        if (!grid_wait(a.ctrl, ++nbar * G, lim, 3, &s_ok)) {
+            cp_async_wait_all();
+            return;
+        }
         {
             // h of every slot (bf16 words) and the sums of its words into shared
             // memory; h was written by other blocks, so it is read from L2
