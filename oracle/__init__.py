@@ -66,10 +66,14 @@ def lib():
         L.oracle_dequant.argtypes = [_p, _p, _p, _i64, _i32, _i32, _p]
         L.oracle_router_logits.argtypes = [_p, _i32, _i32, _p, _p, _i32, _p]
         L.oracle_topk.argtypes = [_p, _i32, _i32, _i32, _p, _p]
+        L.oracle_topk_opt.argtypes = [_p, _i32, _i32, _i32, _i32, _p, _p]
+        L.oracle_shared_gate.argtypes = [_p, _i32, _i32, _p, _p]
         L.oracle_route.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _p, _i32]
         L.oracle_route.restype = _i32
         L.oracle_moe_layer.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p] + [_p] * 9 + \
             [_p, _i32, _p, _p, _p, _p]
+        L.oracle_moe_layer_opt.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p] + \
+            [_p] * 9 + [_p, _i32, _p, _p, _p, _p, _p]
         L.oracle_experts_given_routing.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _i32, _i32] + [_p] * 9 + \
             [_p, _p, _p]
         L.oracle_dispatch_combine_identity.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _p, _p, _p]
@@ -132,13 +136,25 @@ def router_logits(x_bits: np.ndarray, Wr: np.ndarray, bias: Optional[np.ndarray]
     return out
 
 
-def topk(logits: np.ndarray, k: int):
+def topk(logits: np.ndarray, k: int, renorm: bool = True):
+    """Top-k of every row; weights renormalised over the picked (default) or
+    the picked softmax probabilities as they are (renorm=False)."""
     logits = _c(logits, np.float32)
     T, E = logits.shape
     idx = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float64)
-    lib().oracle_topk(_ptr(logits), T, E, k, _ptr(idx), _ptr(w))
+    lib().oracle_topk_opt(_ptr(logits), T, E, k, int(renorm), _ptr(idx), _ptr(w))
     return idx, w
+
+
+def shared_gate(x_bits: np.ndarray, gate: np.ndarray) -> np.ndarray:
+    """Per-token weight of a gated shared expert: sigmoid(x . gate)."""
+    x_bits = _c(x_bits, np.uint16)
+    T, H = x_bits.shape
+    gate = _c(gate, np.float32)
+    out = np.empty(T, np.float64)
+    lib().oracle_shared_gate(_ptr(x_bits), T, H, _ptr(gate), _ptr(out))
+    return out
 
 
 def route(idx: np.ndarray, E: int, has_shared: bool, BN: int) -> dict:
@@ -178,8 +194,11 @@ def quantize_stack(w: np.ndarray, group: int) -> QWeights:
 
 def moe_layer(x_bits: np.ndarray, Wr: np.ndarray, bias: Optional[np.ndarray], gate: QWeights,
               up: QWeights, down: QWeights, E: int, k: int, has_shared: bool,
-              tokens: Optional[np.ndarray] = None) -> dict:
-    """Full layer for the listed tokens (all by default); y is fp64 [n, H]."""
+              tokens: Optional[np.ndarray] = None, renorm: bool = True,
+              shared_gate_w: Optional[np.ndarray] = None) -> dict:
+    """Full layer for the listed tokens (all by default); y is fp64 [n, H].
+    Routing variants: renorm=False keeps the picked softmax probabilities;
+    shared_gate_w ([H] fp32) gates the shared expert per token."""
     x_bits = _c(x_bits, np.uint16)
     T, H = x_bits.shape
     I = gate.rows
@@ -196,10 +215,12 @@ def moe_layer(x_bits: np.ndarray, Wr: np.ndarray, bias: Optional[np.ndarray], ga
     y = np.empty((n, H), np.float64)
     arrays = [gate.q, gate.s, gate.b, up.q, up.s, up.b, down.q, down.s, down.b]
     arrays = [_c(a, a.dtype) for a in arrays]
-    lib().oracle_moe_layer(_ptr(x_bits), T, H, I, E, k, G, int(has_shared), _ptr(Wr), _ptr(bias),
-                           *[_ptr(a) for a in arrays], _ptr(tokens), n,
-                           _ptr(logits), _ptr(idx), _ptr(w), _ptr(y))
-    return dict(logits=logits, idx=idx, w=w, y=y, tokens=tokens)
+    sw = np.empty(n, np.float64)
+    sg = None if shared_gate_w is None else _c(shared_gate_w, np.float32)
+    lib().oracle_moe_layer_opt(_ptr(x_bits), T, H, I, E, k, G, int(has_shared), int(renorm), _ptr(Wr),
+                               _ptr(bias), _ptr(sg), *[_ptr(a) for a in arrays], _ptr(tokens), n,
+                               _ptr(logits), _ptr(idx), _ptr(w), _ptr(y), _ptr(sw))
+    return dict(logits=logits, idx=idx, w=w, y=y, tokens=tokens, shared_w=sw)
 
 
 def experts_given_routing(x_bits, gate: QWeights, up: QWeights, down: QWeights, E, has_shared,

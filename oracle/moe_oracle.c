@@ -215,9 +215,10 @@ static int by_logit_then_index(const void *pa, const void *pb)
 /*
  * Full sort of one token's E logits, keep the first k ([MoE]: "picks 8").
  * Weights: p = softmax over all E (fp64, max subtracted), then
- * w_j = p_{e_j} / sum over the picked p.
+ * w_j = p_{e_j} / sum over the picked p (renorm), or w_j = p_{e_j} (no
+ * renormalisation: the routing variant whose picked weights sum below 1).
  */
-static void topk_one(const float *l, int32_t E, int32_t k, int32_t *idx, double *w)
+static void topk_one(const float *l, int32_t E, int32_t k, int32_t renorm, int32_t *idx, double *w)
 {
     scored *s = (scored *)malloc(sizeof(scored) * (size_t)E);
     for (int32_t e = 0; e < E; ++e) {
@@ -235,15 +236,35 @@ static void topk_one(const float *l, int32_t E, int32_t k, int32_t *idx, double 
         picked += exp((double)s[j].logit - mx) / total;
     }
     for (int32_t j = 0; j < k; ++j)
-        w[j] = (exp((double)s[j].logit - mx) / total) / picked;
+        w[j] = renorm ? (exp((double)s[j].logit - mx) / total) / picked : exp((double)s[j].logit - mx) / total;
     free(s);
+}
+
+void oracle_topk_opt(const float *logits, int32_t T, int32_t E, int32_t k, int32_t renorm, int32_t *idx,
+                     double *w)
+{
+#pragma omp parallel for schedule(static)
+    for (int32_t t = 0; t < T; ++t)
+        topk_one(logits + (int64_t)t * E, E, k, renorm, idx + (int64_t)t * k, w + (int64_t)t * k);
 }
 
 void oracle_topk(const float *logits, int32_t T, int32_t E, int32_t k, int32_t *idx, double *w)
 {
-#pragma omp parallel for schedule(static)
+    oracle_topk_opt(logits, T, E, k, 1, idx, w);
+}
+
+/*
+ * Shared-expert gate of the routing variant with a gated shared expert: one
+ * more router-like score per token, l = sum_h x[t][h] * g[h] (fp32, in
+ * increasing h, as the router logits), weight = 1 / (1 + exp(-l)) in fp64.
+ */
+void oracle_shared_gate(const uint16_t *x, int32_t T, int32_t H, const float *gate, double *w)
+{
+    float *l = (float *)malloc(sizeof(float) * (size_t)T);
+    oracle_router_logits(x, T, H, gate, NULL, 1, l);
     for (int32_t t = 0; t < T; ++t)
-        topk_one(logits + (int64_t)t * E, E, k, idx + (int64_t)t * k, w + (int64_t)t * k);
+        w[t] = 1.0 / (1.0 + exp(-(double)l[t]));
+    free(l);
 }
 
 /* ------------------------------------------- histogram, scan, permutation */
@@ -347,12 +368,14 @@ static void swiglu_expert(const void *ctx, int32_t e, const double *xv, double *
 
 /*
  * Dispatch and combine for the listed tokens:
- *   y_t = sum_j w_{t,j} * expert(e_{t,j}, x_t) + shared(x_t)   (fp64)
- * The expert is a callable so that the tests can plug in an identity expert.
+ *   y_t = sum_j w_{t,j} * expert(e_{t,j}, x_t) + c_t * shared(x_t)   (fp64)
+ * with c_t = 1, or the shared gate's weight of token n when shared_w is
+ * given.  The expert is a callable so that the tests can plug in an identity
+ * expert.
  */
 static void dispatch_combine(const uint16_t *x, int32_t H, int32_t k, int32_t E,
                              int32_t has_shared, const int32_t *idx, const double *w,
-                             const int32_t *tokens, int32_t n_tokens,
+                             const int32_t *tokens, int32_t n_tokens, const double *shared_w,
                              expert_fn fn, const void *ctx, double *y)
 {
 #pragma omp parallel for schedule(dynamic, 1)
@@ -371,9 +394,10 @@ static void dispatch_combine(const uint16_t *x, int32_t H, int32_t k, int32_t E,
                 yt[h] += w[(int64_t)n * k + j] * o[h];
         }
         if (has_shared) {
+            const double c = shared_w ? shared_w[n] : 1.0;
             fn(ctx, E, xv, o);
             for (int32_t h = 0; h < H; ++h)
-                yt[h] += o[h];
+                yt[h] += c * o[h];
         }
         free(xv);
         free(o);
@@ -383,16 +407,19 @@ static void dispatch_combine(const uint16_t *x, int32_t H, int32_t k, int32_t E,
 /*
  * Whole layer for the listed tokens (tokens == NULL: all T tokens, in order):
  * router logits, top-k and weights, experts, combine.  Outputs are per listed
- * token: logits [n][E] fp32, idx [n][k], w [n][k] fp64, y [n][H] fp64.
+ * token: logits [n][E] fp32, idx [n][k], w [n][k] fp64, y [n][H] fp64, and,
+ * when shared_w is not NULL, the shared expert's weight [n] (1, or the gate's).
+ * Routing variants: renorm = 0 keeps the picked softmax probabilities as they
+ * are; shared_gate ([H] fp32, or NULL) gates the shared expert per token.
  */
-void oracle_moe_layer(const uint16_t *x, int32_t T, int32_t H, int32_t I, int32_t E,
-                      int32_t k, int32_t G, int32_t has_shared,
-                      const float *Wr, const float *router_bias,
-                      const uint32_t *qg, const uint16_t *sg, const uint16_t *bg,
-                      const uint32_t *qu, const uint16_t *su, const uint16_t *bu,
-                      const uint32_t *qd, const uint16_t *sd, const uint16_t *bd,
-                      const int32_t *tokens, int32_t n_tokens,
-                      float *logits, int32_t *idx, double *w, double *y)
+void oracle_moe_layer_opt(const uint16_t *x, int32_t T, int32_t H, int32_t I, int32_t E,
+                          int32_t k, int32_t G, int32_t has_shared, int32_t renorm,
+                          const float *Wr, const float *router_bias, const float *shared_gate,
+                          const uint32_t *qg, const uint16_t *sg, const uint16_t *bg,
+                          const uint32_t *qu, const uint16_t *su, const uint16_t *bu,
+                          const uint32_t *qd, const uint16_t *sd, const uint16_t *bd,
+                          const int32_t *tokens, int32_t n_tokens,
+                          float *logits, int32_t *idx, double *w, double *y, double *shared_w)
 {
     int32_t *all = NULL;
     if (!tokens) {
@@ -407,16 +434,38 @@ void oracle_moe_layer(const uint16_t *x, int32_t T, int32_t H, int32_t I, int32_
     for (int32_t n = 0; n < n_tokens; ++n)
         memcpy(xs + (int64_t)n * H, x + (int64_t)tokens[n] * H, sizeof(uint16_t) * (size_t)H);
     oracle_router_logits(xs, n_tokens, H, Wr, router_bias, E, logits);
-    oracle_topk(logits, n_tokens, E, k, idx, w);
+    oracle_topk_opt(logits, n_tokens, E, k, renorm, idx, w);
+    double *cw = NULL;
+    if (shared_gate) {
+        cw = (double *)malloc(sizeof(double) * (size_t)n_tokens);
+        oracle_shared_gate(xs, n_tokens, H, shared_gate, cw);
+    }
+    if (shared_w)
+        for (int32_t n = 0; n < n_tokens; ++n)
+            shared_w[n] = cw ? cw[n] : 1.0;
 
     int32_t *seq = (int32_t *)malloc(sizeof(int32_t) * (size_t)n_tokens);
     for (int32_t n = 0; n < n_tokens; ++n)
         seq[n] = n;
     expert_weights W = {H, I, G, qg, qu, qd, sg, bg, su, bu, sd, bd};
-    dispatch_combine(xs, H, k, E, has_shared, idx, w, seq, n_tokens, swiglu_expert, &W, y);
+    dispatch_combine(xs, H, k, E, has_shared, idx, w, seq, n_tokens, cw, swiglu_expert, &W, y);
+    free(cw);
     free(seq);
     free(xs);
     free(all);
+}
+
+void oracle_moe_layer(const uint16_t *x, int32_t T, int32_t H, int32_t I, int32_t E,
+                      int32_t k, int32_t G, int32_t has_shared,
+                      const float *Wr, const float *router_bias,
+                      const uint32_t *qg, const uint16_t *sg, const uint16_t *bg,
+                      const uint32_t *qu, const uint16_t *su, const uint16_t *bu,
+                      const uint32_t *qd, const uint16_t *sd, const uint16_t *bd,
+                      const int32_t *tokens, int32_t n_tokens,
+                      float *logits, int32_t *idx, double *w, double *y)
+{
+    oracle_moe_layer_opt(x, T, H, I, E, k, G, has_shared, 1, Wr, router_bias, NULL, qg, sg, bg, qu, su, bu,
+                         qd, sd, bd, tokens, n_tokens, logits, idx, w, y, NULL);
 }
 
 /* Experts only, with routing given (used for the single-expert dense pin). */
@@ -431,7 +480,7 @@ void oracle_experts_given_routing(const uint16_t *x, int32_t T, int32_t H, int32
     for (int32_t t = 0; t < T; ++t)
         seq[t] = t;
     expert_weights W = {H, I, G, qg, qu, qd, sg, bg, su, bu, sd, bd};
-    dispatch_combine(x, H, k, E, has_shared, idx, w, seq, T, swiglu_expert, &W, y);
+    dispatch_combine(x, H, k, E, has_shared, idx, w, seq, T, NULL, swiglu_expert, &W, y);
     free(seq);
 }
 
@@ -451,6 +500,6 @@ void oracle_dispatch_combine_identity(const uint16_t *x, int32_t T, int32_t H, i
     for (int32_t t = 0; t < T; ++t)
         seq[t] = t;
     int32_t dims[2] = {H, E};
-    dispatch_combine(x, H, k, E, has_shared, idx, w, seq, T, identity_expert, dims, y);
+    dispatch_combine(x, H, k, E, has_shared, idx, w, seq, T, NULL, identity_expert, dims, y);
     free(seq);
 }

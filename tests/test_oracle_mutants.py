@@ -25,13 +25,18 @@ MUTANTS = [
      "for (int32_t h = 0; h < H - 1; ++h) {\n                float prod"),
     ("ties_to_higher_index", "return (a->expert > b->expert) - (a->expert < b->expert);",
      "return (a->expert < b->expert) - (a->expert > b->expert);"),
-    ("weights_not_renormalised", "w[j] = (exp((double)s[j].logit - mx) / total) / picked;",
+    ("weights_not_renormalised",
+     "w[j] = renorm ? (exp((double)s[j].logit - mx) / total) / picked : exp((double)s[j].logit - mx) / total;",
      "w[j] = exp((double)s[j].logit - mx) / total;"),
+    ("renorm_flag_ignored",
+     "w[j] = renorm ? (exp((double)s[j].logit - mx) / total) / picked : exp((double)s[j].logit - mx) / total;",
+     "w[j] = (exp((double)s[j].logit - mx) / total) / picked;"),
+    ("shared_gate_not_applied", "const double c = shared_w ? shared_w[n] : 1.0;", "const double c = 1.0;"),
     ("silu_of_up", "hbuf[i] = gsum / (1.0 + exp(-gsum)) * usum;", "hbuf[i] = usum / (1.0 + exp(-usum)) * gsum;"),
     ("tokens_reversed_in_expert", "for (int32_t t = 0; t < T; ++t) {\n        for (int32_t j = 0; j < k; ++j) {\n            int32_t e = idx",
      "for (int32_t t = T - 1; t >= 0; --t) {\n        for (int32_t j = 0; j < k; ++j) {\n            int32_t e = idx"),
-    ("shared_expert_dropped", "        if (has_shared) {\n            fn(ctx, E, xv, o);",
-     "        if (0) {\n            fn(ctx, E, xv, o);"),
+    ("shared_expert_dropped", "        if (has_shared) {\n            const double c",
+     "        if (0) {\n            const double c"),
     ("down_reads_gate_scales", "osum += hbuf[i] * dequant_one(W->qd, W->sd, W->bd, row, I, G, i);",
      "osum += hbuf[i] * dequant_one(W->qd, W->sd, W->sd, row, I, G, i);"),
 ]

@@ -274,3 +274,59 @@ def test_tiny_layer_against_numpy_evaluation():
     # the oracle's router is fp32 (weights move by ~1e-7 relative), the numpy
     # evaluation's is fp64
     np.testing.assert_allclose(out["y"], y, rtol=1e-5, atol=1e-6 * np.abs(y).max())
+
+
+# ------------------------------------------------------- routing variants
+
+
+def test_topk_without_renormalisation_keeps_full_softmax_probabilities():
+    """renorm=False: the picked weights are the softmax over all E as they
+    are (scipy), so they sum below 1; the picks themselves do not change."""
+    rng = np.random.default_rng(41)
+    logits = rng.normal(size=(40, 24)).astype(np.float32)
+    idx_r, _ = oracle.topk(logits, 5)
+    idx, w = oracle.topk(logits, 5, renorm=False)
+    np.testing.assert_array_equal(idx, idx_r)
+    p = scipy.special.softmax(logits.astype(np.float64), axis=1)
+    np.testing.assert_allclose(w, np.take_along_axis(p, idx.astype(np.int64), axis=1), rtol=1e-12)
+    assert np.all(w.sum(axis=1) < 1.0)
+
+
+def _gated_inputs(seed=43):
+    cfg = synthetic.MoEConfig("gated", T=7, H=128, E=6, k=2, I=64, group=32, seed=seed)
+    L = synthetic.make_layer(cfg)
+    stacks = [oracle.quantize_stack(w.numpy(), 32) for w in (L.w_gate, L.w_up, L.w_down)]
+    xb = synthetic.bf16_bits(L.x).numpy().view(np.uint16)
+    g = torch.Generator().manual_seed(seed)
+    sg = (torch.randn(cfg.H, generator=g) * 0.05).numpy().astype(np.float32)
+    return cfg, L, stacks, xb, sg
+
+
+def test_shared_gate_weight_is_the_sigmoid_of_the_gate_score():
+    """sigmoid(x . g) with the dot in float64 (numpy): the oracle's fp32 sum
+    differs by at most a few fp32 roundings of the terms."""
+    cfg, L, stacks, xb, sg = _gated_inputs()
+    out = oracle.moe_layer(xb, L.router_w.numpy(), None, *stacks, cfg.E, cfg.k, True, shared_gate_w=sg)
+    xf = L.x.float().numpy().astype(np.float64)
+    s = xf @ sg.astype(np.float64)
+    bound = cfg.H * 2.0 ** -23 * (np.abs(xf) @ np.abs(sg.astype(np.float64)))
+    ref_lo, ref_hi = 1.0 / (1.0 + np.exp(-(s - bound))), 1.0 / (1.0 + np.exp(-(s + bound)))
+    assert np.all((out["shared_w"] >= ref_lo - 1e-15) & (out["shared_w"] <= ref_hi + 1e-15))
+    np.testing.assert_array_equal(oracle.shared_gate(xb, sg), out["shared_w"])
+    ungated = oracle.moe_layer(xb, L.router_w.numpy(), None, *stacks, cfg.E, cfg.k, True)
+    assert np.all(ungated["shared_w"] == 1.0)
+
+
+def test_gated_shared_expert_scales_only_the_shared_part():
+    """y(gated) = y(no shared) + c * (y(shared, weight 1) - y(no shared)) per
+    token: the gate multiplies the shared expert's output and nothing else.
+    A zero gate vector gives c = 1/2 exactly."""
+    cfg, L, stacks, xb, sg = _gated_inputs(44)
+    Wr = L.router_w.numpy()
+    none = oracle.moe_layer(xb, Wr, None, *stacks, cfg.E, cfg.k, False)["y"]
+    one = oracle.moe_layer(xb, Wr, None, *stacks, cfg.E, cfg.k, True)["y"]
+    for vec in (sg, np.zeros_like(sg)):
+        out = oracle.moe_layer(xb, Wr, None, *stacks, cfg.E, cfg.k, True, shared_gate_w=vec)
+        c = out["shared_w"][:, None]
+        np.testing.assert_allclose(out["y"], none + c * (one - none), rtol=1e-9, atol=1e-12)
+    assert np.all(out["shared_w"] == 0.5)
