@@ -87,12 +87,25 @@ typedef struct {
  * One MoE layer.  Supported: 1 <= E <= 256, 1 <= k <= min(8, E),
  * 256 <= H <= 16384 with H % 256 == 0, 128 <= I <= 4096 with I % 128 == 0,
  * group in {32, 64}.  has_shared is 0 or 1.
+ *
+ * Routing variants (zero / NULL give the layer described above: weights
+ * renormalised over the k picked, shared expert with weight 1):
+ *   no_renorm    1: each picked expert keeps its softmax probability over all
+ *                E (the k weights sum below 1); 0: renormalised over the k.
+ *   shared_gate  [H] fp32, 16-byte aligned, or NULL: the shared expert's
+ *                output is weighed per token by sigmoid(sum_h x[h] g[h]) (the
+ *                score summed in fp32 like a router logit) instead of 1;
+ *                requires has_shared.  moe_route_logits ignores it (it has
+ *                no x).
+ * The pages fix neither; both are members of the model family's routing.
  */
 typedef struct {
     int32_t E, k, H, I, group, has_shared;
     const float *router_w;    /* [E][H] fp32 */
     const float *router_bias; /* [E] fp32, or NULL for none */
     moe_qweight gate, up, down;
+    int32_t no_renorm;
+    const float *shared_gate; /* [H] fp32 or NULL */
 } moe_layer_desc;
 
 /* Byte offsets, inside the workspace, of the routing tables that the last

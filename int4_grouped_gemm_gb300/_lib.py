@@ -33,7 +33,8 @@ class moe_qweight(ctypes.Structure):
 class moe_layer_desc(ctypes.Structure):
     _fields_ = [("E", c_i32), ("k", c_i32), ("H", c_i32), ("I", c_i32), ("group", c_i32),
                 ("has_shared", c_i32), ("router_w", c_p), ("router_bias", c_p),
-                ("gate", moe_qweight), ("up", moe_qweight), ("down", moe_qweight)]
+                ("gate", moe_qweight), ("up", moe_qweight), ("down", moe_qweight),
+                ("no_renorm", c_i32), ("shared_gate", c_p)]
 
 
 class moe_routing_views(ctypes.Structure):

@@ -70,6 +70,8 @@ static int check_shape(const moe_layer_desc *d) {
     if (d->E < 1 || d->E > 256) return MOE_ERR_SHAPE;
     if (d->k < 1 || d->k > 8 || d->k > d->E) return MOE_ERR_SHAPE;
     if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_SHAPE;
+    if (d->no_renorm != 0 && d->no_renorm != 1) return MOE_ERR_SHAPE;
+    if (d->shared_gate && !d->has_shared) return MOE_ERR_SHAPE;
     if (d->group != 32 && d->group != 64) return MOE_ERR_SHAPE;
     if (d->H < 256 || d->H % 256 != 0 || d->H > 16384) return MOE_ERR_SHAPE;
     if (d->I < 128 || d->I % 128 != 0 || d->I > 4096) return MOE_ERR_SHAPE;
@@ -80,6 +82,7 @@ static int check_weights(const moe_layer_desc *d) {
     int rc;
     if ((rc = check_ptr(d->router_w))) return rc;
     if (d->router_bias && !aligned16(d->router_bias)) return MOE_ERR_ALIGN;
+    if (d->shared_gate && !aligned16(d->shared_gate)) return MOE_ERR_ALIGN;
     const moe_qweight *ws[3] = {&d->gate, &d->up, &d->down};
     for (const moe_qweight *w : ws) {
         if ((rc = check_ptr(w->q))) return rc;
@@ -201,7 +204,8 @@ int moe_route_logits(const moe_layer_desc *desc, const float *logits, int32_t T,
     if (launch_zero_i32(rb.counts_blk, static_cast<int64_t>(rb.nblk) * desc->E, stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     return cuda_rc(
-        launch_routing_tables(nullptr, 0, logits, nullptr, T, desc->E, desc->k, desc->has_shared, rb, stream));
+        launch_routing_tables(nullptr, 0, logits, nullptr, T, desc->E, desc->k, desc->has_shared,
+                              RouteOpts{nullptr, nullptr, desc->H, desc->no_renorm}, rb, stream));
 }
 
 static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
@@ -292,7 +296,8 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     if (launch_gemm(2, mr, ga, grid_for(router_units(T)), stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(events, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
     // routing tables
-    if (launch_routing_tables(logits_part, L.E_pad16, nullptr, desc->router_bias, T, E, k, desc->has_shared, rb,
+    const RouteOpts ropts{static_cast<const __nv_bfloat16 *>(x), desc->shared_gate, H, desc->no_renorm};
+    if (launch_routing_tables(logits_part, L.E_pad16, nullptr, desc->router_bias, T, E, k, desc->has_shared, ropts, rb,
                               stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (mark(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -344,6 +349,7 @@ static DecodeLayerPtrs decode_ptrs(const moe_layer_desc &d) {
     P.bu = d.up.bias;
     P.sd = d.down.scale;
     P.bd = d.down.bias;
+    P.shg = d.shared_gate;
     return P;
 }
 
@@ -362,6 +368,7 @@ static int decode_run(const moe_layer_desc *descs, int n, const void *x, void *y
     a.has_shared = d0.has_shared;
     a.ldg_h = ld_groups(d0.H, d0.group);
     a.ldg_i = ld_groups(d0.I, d0.group);
+    a.no_renorm = d0.no_renorm;
     a.n_total = n;
     a.x = static_cast<const __nv_bfloat16 *>(x);
     a.y = static_cast<__nv_bfloat16 *>(y);
@@ -406,7 +413,7 @@ int moe_decode_layers(const moe_layer_desc *descs, int32_t n_layers, const void 
         if ((rc = decode_check(&descs[l]))) return rc;
         const moe_layer_desc &a = descs[0], &b = descs[l];
         if (a.E != b.E || a.k != b.k || a.H != b.H || a.I != b.I || a.group != b.group ||
-            a.has_shared != b.has_shared)
+            a.has_shared != b.has_shared || a.no_renorm != b.no_renorm)
             return MOE_ERR_SHAPE;
     }
     if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;

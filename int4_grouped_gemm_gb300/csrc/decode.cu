@@ -208,12 +208,13 @@ struct UnitRegs {
 };
 
 template <int HMAX>
-__device__ __forceinline__ void router_load(const DecodeStack &a, const float *Wr, int unit, int lane,
-                                            UnitRegs<HMAX> &r) {
+__device__ __forceinline__ void router_load(const DecodeStack &a, const float *Wr, const float *shg, int unit,
+                                            int lane, UnitRegs<HMAX> &r) {
     constexpr int kMaxRouterVec = UnitRegs<HMAX>::V;
     const int e = unit >> 2, q = unit & 3;
     const int span = a.H / 4;
-    const float *wrow = Wr + static_cast<int64_t>(e) * a.H + q * span;
+    // row E: the shared-expert gate vector (a gated layer's extra score)
+    const float *wrow = (e < a.E ? Wr + static_cast<int64_t>(e) * a.H : shg) + q * span;
 #pragma unroll
     for (int v = 0; v < kMaxRouterVec; ++v) {
         const int c = lane * 4 + v * 128;
@@ -493,8 +494,10 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
 // (first layer of a launch) or the fp64 sum that the previous layer's blocks
 // accumulated, plus the bias.  Every block computes the same result.
 __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bias, const double *racc,
-                                           unsigned long long *s_keys, int *s_idx, float *s_w) {
+                                           unsigned long long *s_keys, int *s_idx, float *s_w, float *s_red) {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int Es = a.E + 1;  // stride of the partial and summed logits (entry E: shared gate)
+    float lt = 0.f;          // this thread's expert logit (t < E)
     if (warp < 8) {
         unsigned long long key = 0;  // below every real key
         if (t < a.E) {
@@ -505,7 +508,7 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
                 // pairwise here in a fixed order
                 double v[kRaccCopies];
 #pragma unroll
-                for (int r = 0; r < kRaccCopies; ++r) v[r] = __ldcg(racc + r * a.E + t);
+                for (int r = 0; r < kRaccCopies; ++r) v[r] = __ldcg(racc + r * Es + t);
                 float vf[kRaccCopies];
 #pragma unroll
                 for (int r = 0; r < kRaccCopies; ++r) vf[r] = static_cast<float>(v[r]);
@@ -515,11 +518,12 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
                     for (int r = 0; r + w < kRaccCopies; r += 2 * w) vf[r] += vf[r + w];
                 l = vf[0];
             } else {
-                l = __ldcg(a.logits_part + t) + __ldcg(a.logits_part + a.E + t);
-                l += __ldcg(a.logits_part + 2 * a.E + t);
-                l += __ldcg(a.logits_part + 3 * a.E + t);
+                l = __ldcg(a.logits_part + t) + __ldcg(a.logits_part + Es + t);
+                l += __ldcg(a.logits_part + 2 * Es + t);
+                l += __ldcg(a.logits_part + 3 * Es + t);
             }
             if (bias) l += __ldg(bias + t);
+            lt = l;
             key = topk_key(l, t);
         }
         key = warp_sort_desc(key, lane);
@@ -541,6 +545,16 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
         if (list == 0 && cnt < a.k) s_keys[64 + cnt] = mine;
     }
     __syncthreads();
+    if (a.no_renorm) {
+        // weights without renormalisation: the softmax denominator runs over
+        // all E logits (max = the first pick), summed per warp, then 8 warps
+        const uint32_t ord = static_cast<uint32_t>(s_keys[64] >> 32);
+        const float m = __uint_as_float((ord & 0x80000000u) ? (ord & 0x7FFFFFFFu) : ~ord);
+        float ex = warp < 8 && t < a.E ? expf(lt - m) : 0.f;
+        ex = warp_sum(ex);
+        if (lane == 0 && warp < 8) s_red[warp] = ex;
+        __syncthreads();
+    }
     if (warp == 0) {
         // lane j < k: pick j
         const unsigned long long k = lane < a.k ? s_keys[64 + lane] : 0ull;
@@ -553,6 +567,7 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
         sum += __shfl_xor_sync(0xffffffffu, sum, 4);
         sum += __shfl_xor_sync(0xffffffffu, sum, 2);
         sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+        if (a.no_renorm) sum = ((s_red[0] + s_red[1]) + (s_red[2] + s_red[3])) + ((s_red[4] + s_red[5]) + (s_red[6] + s_red[7]));
         if (lane < a.k) {
             s_idx[lane] = e;
             s_w[lane] = ex / sum;
@@ -589,6 +604,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     __shared__ float s_w[kMaxSlots];
     __shared__ int s_ok;
     __shared__ unsigned long long s_keys[64 + 8];
+    __shared__ float s_red[8];
     __shared__ float s_y[kMaxYSlice];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int G = gridDim.x, b = blockIdx.x;
@@ -600,7 +616,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     uint4 *hb = reinterpret_cast<uint4 *>(dsm);  // [slots][hp] bf16 (aliases x: used in another phase)
     float *hsum8 = dsm + (a.k + 1) * 4 * hp;     // [slots][I/8]
     const int nslots = a.k + (a.has_shared ? 1 : 0);
-    const int n_a_units = 4 * a.E;
+    const int Es = a.E + 1;  // stride of the partial and summed logits (entry E: shared gate)
     const int gshift = a.G == 64 ? 6 : 5;   // log2 of the group (32 or 64)
     unsigned nbar = 0;  // grid barriers passed in this launch
     const long long lim = a.wait_limit;
@@ -656,14 +672,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         // summed by the previous layer's phase C.
         if (li == 0) {
             UnitRegs<HMAX> ur;
+            const int n_a_units = 4 * (a.E + (P.shg ? 1 : 0));  // + the shared gate's score
             const int u0 = gw;
-            if (u0 < n_a_units) router_load(a, P.Wr, u0, lane, ur);
+            if (u0 < n_a_units) router_load(a, P.Wr, P.shg, u0, lane, ur);
             stage_x(in, a.H, xb, xsum8, xs);
             __syncthreads();
             for (int u = u0; u < n_a_units; u += NW) {
-                if (u != u0) router_load(a, P.Wr, u, lane, ur);
+                if (u != u0) router_load(a, P.Wr, P.shg, u, lane, ur);
                 const float acc = warp_sum(router_dot(a, u, lane, ur, xs));
-                if (lane == 0) a.logits_part[(u & 3) * a.E + (u >> 2)] = acc;
+                if (lane == 0) a.logits_part[(u & 3) * Es + (u >> 2)] = acc;
             }
             grid_arrive(a.ctrl);
         }
@@ -681,12 +698,37 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             // warps 8-15 stage it while warps 0-7 start the top-k below
             stage_x(in, a.H, xb, xsum8, nullptr, 256, kDecThreads - 256);
         }
-        topk_block(a, P.bias, li == 0 ? nullptr : a.racc + (l % 2) * kRaccCopies * a.E, s_keys, s_idx, s_w);
+        if (tid == kDecThreads - 1) {
+            // the shared expert's weight: 1, or sigmoid of the gate's score,
+            // summed like an expert's logit
+            float cw = 1.0f;
+            if (P.shg) {
+                float lg;
+                if (li == 0) {
+                    lg = __ldcg(a.logits_part + a.E) + __ldcg(a.logits_part + Es + a.E);
+                    lg += __ldcg(a.logits_part + 2 * Es + a.E);
+                    lg += __ldcg(a.logits_part + 3 * Es + a.E);
+                } else {
+                    const double *rc = a.racc + (l % 2) * kRaccCopies * Es + a.E;
+                    float vf[kRaccCopies];
+#pragma unroll
+                    for (int r = 0; r < kRaccCopies; ++r) vf[r] = static_cast<float>(__ldcg(rc + r * Es));
+#pragma unroll
+                    for (int w = 1; w < kRaccCopies; w *= 2)
+#pragma unroll
+                        for (int r = 0; r + w < kRaccCopies; r += 2 * w) vf[r] += vf[r + w];
+                    lg = vf[0];
+                }
+                cw = 1.0f / (1.0f + expf(-lg));
+            }
+            s_w[a.k] = cw;
+        }
+        topk_block(a, P.bias, li == 0 ? nullptr : a.racc + (l % 2) * kRaccCopies * Es, s_keys, s_idx, s_w, s_red);
         if (b == 0 && li + 1 < a.n_layers) {
             // the next layer's logit sums start from zero; this buffer was last
             // read by the previous layer's top-k, before the previous barrier
-            double *nr = a.racc + ((l + 1) % 2) * kRaccCopies * a.E;
-            for (int e = tid; e < kRaccCopies * a.E; e += kDecThreads) nr[e] = 0.0;
+            double *nr = a.racc + ((l + 1) % 2) * kRaccCopies * Es;
+            for (int e = tid; e < kRaccCopies * Es; e += kDecThreads) nr[e] = 0.0;
         }
         if (b == 0 && tid < a.k) {
             a.topk_idx[tid] = s_idx[tid];
@@ -797,8 +839,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                 }
             }
             part += __shfl_xor_sync(0xffffffffu, part, 1);
-            if (half == 0 && e < a.E)
-                atomicAdd(a.racc + (((l + 1) % 2) * kRaccCopies + b % kRaccCopies) * a.E + e, static_cast<double>(part));
+            double *nr = a.racc + (((l + 1) % 2) * kRaccCopies + b % kRaccCopies) * Es;
+            if (half == 0 && e < a.E) atomicAdd(nr + e, static_cast<double>(part));
+            const float *nshg = a.L[li + 1].shg;
+            if (nshg && warp == kDecWarps - 1) {
+                // the next layer's shared gate: its score's share over this block's features
+                float pg = 0.f;
+                for (int f = y_lo + lane; f < y_hi; f += 32) pg = fmaf(__ldg(nshg + f), s_y[f - y_lo], pg);
+                pg = warp_sum(pg);
+                if (lane == 0) atomicAdd(nr + a.E, static_cast<double>(pg));
+            }
             grid_arrive(a.ctrl);
         }
         __syncthreads();  // hb and the staging buffers are refilled by the next layer

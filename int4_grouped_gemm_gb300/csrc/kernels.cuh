@@ -39,6 +39,7 @@ struct DecodeLayerPtrs {
     const float *bias;
     const uint32_t *qg, *qu, *qd;
     const uint16_t *sg, *bg, *su, *bu, *sd, *bd;
+    const float *shg;  // shared-expert gate vector [H], or NULL (weight 1)
 };
 
 // One launch of the batch-1 decode kernel: layers l0 .. l0 + n_layers - 1 of
@@ -52,24 +53,34 @@ struct DecodeStack {
     __nv_bfloat16 *y;
     __nv_bfloat16 *act;      // [2][H] (stacks of more than one layer)
     Ctrl *ctrl;              // status, grid-barrier counter, abort flag
-    float *logits_part;      // [4][E]: router partial sums over K quarters
+    float *logits_part;      // [4][E + 1]: router partial sums over K quarters (entry E: shared gate)
     int *topk_idx;           // [8]
     float *topk_w;           // [8]
     __nv_bfloat16 *h;        // [k + 1][I] (slot k = shared expert)
-    double *racc;            // [2][kRaccCopies][E]: next layer's router logits, summed over blocks (alternating buffers)
+    double *racc;            // [2][kRaccCopies][E + 1]: next layer's router logits (+ shared gate), summed over blocks
     const float *next_Wr;    // router of the layer after this launch (L2 prefetch), or NULL
     long long wait_limit;
     // set by the launcher from the shape and grid: output features per block
     // (at most), pitch of the staged router columns, and which of the down
     // rows / router columns are staged in shared memory
     int ys_cap, wr_ld, stage_down, stage_router;
+    int no_renorm;           // weights: picked softmax probabilities as they are (1) or renormalised (0)
     DecodeLayerPtrs L[kMaxStackLayers];
 };
 
 cudaError_t launch_pack_int4(const float *w, int64_t rows, int K, int G, uint32_t *q, uint16_t *scale,
                              uint16_t *bias, cudaStream_t stream);
+// Routing variants of the top-k kernel: weights without renormalisation, and
+// the per-token weight of a gated shared expert (needs x).
+struct RouteOpts {
+    const __nv_bfloat16 *x;    // [T][H], or NULL (no gate)
+    const float *shared_gate;  // [H], or NULL
+    int H;
+    int no_renorm;
+};
 cudaError_t launch_routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
-                                  int E, int k, int has_shared, const RoutingBufs &rb, cudaStream_t s);
+                                  int E, int k, int has_shared, const RouteOpts &opts, const RoutingBufs &rb,
+                                  cudaStream_t s);
 int gemm_smem_bytes(int mode);
 int router_units(int T);
 cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 *wr2, float *y_acc, int64_t y_elems,

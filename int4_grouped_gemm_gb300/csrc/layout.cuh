@@ -104,7 +104,7 @@ inline DecodeLayout decode_layout(int E, int k, int I) {
         return at;
     };
     L.ctrl = take(kCtrlBytes);
-    L.logits = take(sizeof(float) * 4 * (size_t)E);  // partial sums over 4 K quarters
+    L.logits = take(sizeof(float) * 4 * (size_t)(E + 1));  // partial sums over 4 K quarters (+ shared gate)
     L.topk_idx = take(sizeof(int) * 8);
     L.topk_w = take(sizeof(float) * 8);
     L.h = take(sizeof(uint16_t) * (size_t)(k + 1) * I);  // bf16 SwiGLU rows
@@ -115,12 +115,12 @@ inline DecodeLayout decode_layout(int E, int k, int I) {
 }
 
 // decode workspace plus, for a stack of layers, the next layer's router
-// logit sums ([2][kRaccCopies][E] fp64, alternating buffers) and two bf16
-// activation rows
+// logit sums ([2][kRaccCopies][E + 1] fp64, alternating buffers; entry E is
+// the shared-expert gate's score) and two bf16 activation rows
 inline DecodeLayout decode_stack_layout(int E, int k, int H, int I) {
     DecodeLayout L = decode_layout(E, k, I);
     L.racc = L.total;
-    L.act = align_up(L.racc + sizeof(double) * 2 * kRaccCopies * (size_t)E, 256);
+    L.act = align_up(L.racc + sizeof(double) * 2 * kRaccCopies * (size_t)(E + 1), 256);  // + shared gate
     L.total = align_up(L.act + 2 * sizeof(uint16_t) * (size_t)H, 256);
     return L;
 }

@@ -32,7 +32,7 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict__ logits_part, int ld,
                                                         const float *__restrict__ given,
                                                         const float *__restrict__ bias, int T, int E, int k,
-                                                        int has_shared, RoutingBufs rb) {
+                                                        int has_shared, RouteOpts opts, RoutingBufs rb) {
     __shared__ int hist[256];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     for (int e = tid; e < 256; e += blockDim.x) hist[e] = 0;
@@ -95,12 +95,21 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
                 sel_i[j] = bi;
             }
         }
-        // softmax over all E renormalised over the picked k == softmax over the picked k
+        // softmax over all E renormalised over the picked k == softmax over the picked k;
+        // without renormalisation the denominator runs over all E
         const float m = sel_v[0];
         float sum = 0.f;
+        if (opts.no_renorm) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-            if (j < k) sum += expf(sel_v[j] - m);
+            for (int i = 0; i < 8; ++i)
+                if (lane + 32 * i < E) sum += expf(v[i] - m);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                if (j < k) sum += expf(sel_v[j] - m);
+        }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             if (j < k && lane == j) {
@@ -109,10 +118,34 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
                 atomicAdd(&hist[sel_i[j]], 1);
             }
         }
-        if (has_shared && lane == 0) {
-            const int64_t r = static_cast<int64_t>(T) * k + t;
-            rb.row_token[r] = t;
-            rb.row_weight[r] = 1.0f;
+        if (has_shared) {
+            float cw = 1.0f;
+            if (opts.shared_gate && opts.x) {
+                // gated shared expert: sigmoid of x . g (fp32), the lane's 8-element
+                // words in order, then the lanes in a fixed tree
+                float acc = 0.f;
+                const uint4 *xr = reinterpret_cast<const uint4 *>(opts.x + static_cast<int64_t>(t) * opts.H);
+                const float4 *gr = reinterpret_cast<const float4 *>(opts.shared_gate);
+                for (int w = lane; w < opts.H / 8; w += 32) {
+                    const uint4 xv = xr[w];
+                    const float4 g0 = gr[2 * w], g1 = gr[2 * w + 1];
+                    const uint32_t xp[4] = {xv.x, xv.y, xv.z, xv.w};
+                    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        acc = fmaf(__uint_as_float(xp[i] << 16), gv[2 * i], acc);
+                        acc = fmaf(__uint_as_float(xp[i] & 0xFFFF0000u), gv[2 * i + 1], acc);
+                    }
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+                cw = 1.0f / (1.0f + expf(-acc));
+            }
+            if (lane == 0) {
+                const int64_t r = static_cast<int64_t>(T) * k + t;
+                rb.row_token[r] = t;
+                rb.row_weight[r] = cw;
+            }
         }
     }
     __syncthreads();
@@ -288,8 +321,9 @@ cudaError_t launch_zero_i32(int *p, int64_t n, cudaStream_t s) {
 }
 
 cudaError_t launch_routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
-                                  int E, int k, int has_shared, const RoutingBufs &rb, cudaStream_t s) {
-    topk_hist_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits_part, ld, given, bias, T, E, k, has_shared, rb);
+                                  int E, int k, int has_shared, const RouteOpts &opts, const RoutingBufs &rb,
+                                  cudaStream_t s) {
+    topk_hist_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits_part, ld, given, bias, T, E, k, has_shared, opts, rb);
     scan_tiles_kernel<<<1, 512, 0, s>>>(T, E, k, has_shared, rb);
     permute_kernel<<<rb.nblk, 32, 0, s>>>(T, E, k, rb);
     return cudaGetLastError();

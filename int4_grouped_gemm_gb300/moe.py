@@ -51,26 +51,32 @@ def pack_matrix(w: torch.Tensor, group: int, stream=None) -> QMatrix:
 class PackedLayer:
     def __init__(self, E: int, k: int, H: int, I: int, group: int, has_shared: bool,
                  router_w: torch.Tensor, router_bias: Optional[torch.Tensor],
-                 gate: QMatrix, up: QMatrix, down: QMatrix):
+                 gate: QMatrix, up: QMatrix, down: QMatrix, no_renorm: bool = False,
+                 shared_gate: Optional[torch.Tensor] = None):
         self.E, self.k, self.H, self.I, self.group, self.has_shared = E, k, H, I, group, bool(has_shared)
         self.router_w = router_w.contiguous()
         self.router_bias = None if router_bias is None else router_bias.contiguous()
+        self.shared_gate = None if shared_gate is None else shared_gate.contiguous()
         self.gate, self.up, self.down = gate, up, down
         self.desc = moe_layer_desc(E, k, H, I, group, int(has_shared), self.router_w.data_ptr(),
                                    None if self.router_bias is None else self.router_bias.data_ptr(),
-                                   gate.as_c(), up.as_c(), down.as_c())
+                                   gate.as_c(), up.as_c(), down.as_c(), int(no_renorm),
+                                   None if self.shared_gate is None else self.shared_gate.data_ptr())
 
     @classmethod
-    def from_fp32(cls, cfg, router_w, router_bias, w_gate, w_up, w_down, stream=None) -> "PackedLayer":
-        """Pack fp32 expert weights (on the GPU) into a device-resident layer."""
+    def from_fp32(cls, cfg, router_w, router_bias, w_gate, w_up, w_down, stream=None, no_renorm: bool = False,
+                  shared_gate: Optional[torch.Tensor] = None) -> "PackedLayer":
+        """Pack fp32 expert weights (on the GPU) into a device-resident layer
+        (routing variants: no_renorm, shared_gate [H] fp32)."""
         dev = torch.device("cuda")
         router_w = router_w.to(dev, torch.float32)
         router_bias = None if router_bias is None else router_bias.to(dev, torch.float32)
+        shared_gate = None if shared_gate is None else shared_gate.to(dev, torch.float32)
         gate = pack_matrix(w_gate.to(dev), cfg.group, stream)
         up = pack_matrix(w_up.to(dev), cfg.group, stream)
         down = pack_matrix(w_down.to(dev), cfg.group, stream)
         return cls(cfg.E, cfg.k, cfg.H, cfg.I, cfg.group, cfg.has_shared, router_w, router_bias,
-                   gate, up, down)
+                   gate, up, down, no_renorm, shared_gate)
 
     def workspace(self, T_max: int) -> "Workspace":
         return Workspace(self.desc, T_max)
