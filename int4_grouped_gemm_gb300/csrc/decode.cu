@@ -496,7 +496,7 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
 __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bias, const double *racc,
                                            unsigned long long *s_keys, int *s_idx, float *s_w, float *s_red) {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int Es = a.E + 1;  // stride of the partial and summed logits (entry E: shared gate)
+    const int Es = decode_logit_stride(a.E);  // stride of the partial and summed logits (entry E: shared gate)
     float lt = 0.f;          // this thread's expert logit (t < E)
     if (warp < 8) {
         unsigned long long key = 0;  // below every real key
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     uint4 *hb = reinterpret_cast<uint4 *>(dsm);  // [slots][hp] bf16 (aliases x: used in another phase)
     float *hsum8 = dsm + (a.k + 1) * 4 * hp;     // [slots][I/8]
     const int nslots = a.k + (a.has_shared ? 1 : 0);
-    const int Es = a.E + 1;  // stride of the partial and summed logits (entry E: shared gate)
+    const int Es = decode_logit_stride(a.E);  // stride of the partial and summed logits (entry E: shared gate)
     const int gshift = a.G == 64 ? 6 : 5;   // log2 of the group (32 or 64)
     unsigned nbar = 0;  // grid barriers passed in this launch
     const long long lim = a.wait_limit;

@@ -53,11 +53,11 @@ struct DecodeStack {
     __nv_bfloat16 *y;
     __nv_bfloat16 *act;      // [2][H] (stacks of more than one layer)
     Ctrl *ctrl;              // status, grid-barrier counter, abort flag
-    float *logits_part;      // [4][E + 1]: router partial sums over K quarters (entry E: shared gate)
+    float *logits_part;      // [4][decode_logit_stride(E)]: router partial sums over K quarters (entry E: shared gate)
     int *topk_idx;           // [8]
     float *topk_w;           // [8]
     __nv_bfloat16 *h;        // [k + 1][I] (slot k = shared expert)
-    double *racc;            // [2][kRaccCopies][E + 1]: next layer's router logits (+ shared gate), summed over blocks
+    double *racc;            // [2][kRaccCopies][decode_logit_stride(E)]: next layer's logits (+ shared gate), block sums
     const float *next_Wr;    // router of the layer after this launch (L2 prefetch), or NULL
     long long wait_limit;
     // set by the launcher from the shape and grid: output features per block

@@ -10,6 +10,10 @@ constexpr int kTileRows = 128;      // token rows per grouped-GEMM tile (MMA M)
 constexpr int kRouteChunk = 64;     // tokens per routing block (histogram granularity)
 constexpr int kCtrlBytes = 256;     // status word, decode ticket, ...
 constexpr int kRaccCopies = 4;      // decode: copies of the next layer's logit sums (block b adds to copy b % 4)
+// decode: entries per row of the router partial and summed logits: E experts,
+// the shared gate's score, padded to 16 (each copy of the sums starts on a
+// 128-byte line)
+__host__ __device__ constexpr int decode_logit_stride(int E) { return (E + 16) & ~15; }
 
 // Scale/bias row pitch in groups: K/G rounded up to a multiple of 8 (16 bytes).
 inline int ld_groups(int K, int G) { return (K / G + 7) / 8 * 8; }
@@ -104,7 +108,7 @@ inline DecodeLayout decode_layout(int E, int k, int I) {
         return at;
     };
     L.ctrl = take(kCtrlBytes);
-    L.logits = take(sizeof(float) * 4 * (size_t)(E + 1));  // partial sums over 4 K quarters (+ shared gate)
+    L.logits = take(sizeof(float) * 4 * (size_t)decode_logit_stride(E));  // partial sums over 4 K quarters (+ shared gate)
     L.topk_idx = take(sizeof(int) * 8);
     L.topk_w = take(sizeof(float) * 8);
     L.h = take(sizeof(uint16_t) * (size_t)(k + 1) * I);  // bf16 SwiGLU rows
@@ -115,12 +119,13 @@ inline DecodeLayout decode_layout(int E, int k, int I) {
 }
 
 // decode workspace plus, for a stack of layers, the next layer's router
-// logit sums ([2][kRaccCopies][E + 1] fp64, alternating buffers; entry E is
-// the shared-expert gate's score) and two bf16 activation rows
+// logit sums ([2][kRaccCopies][decode_logit_stride(E)] fp64, alternating
+// buffers; entry E is the shared-expert gate's score) and two bf16 activation
+// rows
 inline DecodeLayout decode_stack_layout(int E, int k, int H, int I) {
     DecodeLayout L = decode_layout(E, k, I);
     L.racc = L.total;
-    L.act = align_up(L.racc + sizeof(double) * 2 * kRaccCopies * (size_t)(E + 1), 256);  // + shared gate
+    L.act = align_up(L.racc + sizeof(double) * 2 * kRaccCopies * (size_t)decode_logit_stride(E), 256);
     L.total = align_up(L.act + 2 * sizeof(uint16_t) * (size_t)H, 256);
     return L;
 }
