@@ -26,7 +26,11 @@
 // phases run: the shared expert's down rows and the next layer's router
 // columns at the start of the layer, the picked experts' down rows right
 // after the gate/up rows have been requested.  Only the router and the k + 1
-// touched experts are read.  The int4 dot products use
+// touched experts are read.  Routing variants of the layer descriptor: the
+// score of a shared-expert gate is one more router row (phase A, and the
+// next-layer sums of phase C), its sigmoid the shared slot's weight; without
+// renormalisation the top-k divides by the softmax sum over all E.  The int4
+// dot products use
 // sum_i x_i (s q_i + b) = s sum_i x_i q_i + b sum_i x_i per 8-element word,
 // with the per-word input sums computed once per block.
 #include "kernels.cuh"
