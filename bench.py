@@ -388,6 +388,52 @@ def run_decode(args, pk):
                 clocks=clk.summary(), launches=-(-cfg.layers // DECODE_LAYERS_PER_KERNEL) * steps)
 
 
+def run_small_batches(pk, sizes=(1, 2, 4, 8), steps=10):
+    """Small token batches (the speculative-verify shape) through moe_prefill
+    on one layer of the T=512 shapes: graph-replayed calls, L2 flushed before
+    each; bytes = the touched experts' weights + router."""
+    import torch
+    from int4_grouped_gemm_gb300 import _lib, synthetic
+    cfg = synthetic.CONFIGS["prefill512"]
+    layer, x = build_prefill(cfg)
+    ws = layer.workspace(max(sizes))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    per_expert = 3 * cfg.H * cfg.I // 2 + 3 * cfg.H * cfg.I // cfg.group * 4
+    out = {}
+    for T in sizes:
+        xt = x[:T].contiguous()
+        y = torch.empty_like(xt)
+        for _ in range(3):
+            _lib.moe_prefill(layer.desc, xt, T, y, ws.buf)
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            _lib.moe_prefill(layer.desc, xt, T, y, ws.buf)
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(graph):
+            _lib.moe_prefill(layer.desc, xt, T, y, ws.buf)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record()
+            graph.replay()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        if _lib.moe_read_device_status(ws.buf) != 0:
+            raise RuntimeError(f"small batch T={T}: device status")
+        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+        touched = int((ws.routing(layer.desc, T)["counts"].cpu() > 0).sum().item())
+        wbytes = touched * per_expert + cfg.E * cfg.H * 4
+        out[f"T{T}"] = {"ms_per_call": round(ms, 4), "tok_s": round(T / (ms * 1e-3), 1), "experts_touched": touched,
+                        "frac_of_hbm": round(wbytes / (ms * 1e-3) / 1e9 / pk["hbm"], 4)}
+        del graph
+    del flush, ws, layer, x
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_prefill_other(name, pk, steps=10):
     """Secondary prefill layers (not the headline): graph-replayed calls with an
     L2 flush before each, expert FLOP/s against the bf16 peak and the bytes
@@ -566,6 +612,7 @@ def main():
     other = None
     if rank == 0 and not args.no_other:
         other = {n: run_prefill_other(n, pk) for n in ("prefill512", "skew16384")}
+        other["small_batches_through_moe_prefill"] = run_small_batches(pk)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg)

@@ -91,6 +91,15 @@ def test_one_expert_takes_all_tokens_and_empty_experts():
     check_layer(L, L.x)
 
 
+@pytest.mark.parametrize("T", [1, 2, 8])
+def test_full_shapes_small_batches(T):
+    """The speculative-verify shape: a few tokens through the full-size
+    layer (most experts empty, one short tile per touched expert)."""
+    cfg = dataclasses.replace(synthetic.CONFIGS["prefill512"], T=T, seed=70 + T)
+    L = synthetic.make_layer(cfg, device="cuda")
+    check_layer(L, L.x)
+
+
 @pytest.mark.parametrize("name,n", [("prefill512", 40), ("prefill4096", 40)])
 def test_full_size_sampled(name, n):
     cfg = synthetic.CONFIGS[name]
