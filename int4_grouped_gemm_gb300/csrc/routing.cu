@@ -13,16 +13,24 @@
 //   scan_tiles_kernel     per-expert block bases, counts, exclusive scan
 //                         (offsets), canonical tile map, launch schedule
 //   permute_kernel        stable (expert, token) permutation, its inverse and
-//                         the per-row token / combine weight tables
+//                         the per-row token / combine weight tables (one
+//                         thread per pick of a chunk)
 // Every table is deterministic: counts and ranks come from per-block counts
 // scanned in token order, never from the order in which atomics land.
 #include "kernels.cuh"
 
 namespace moe {
 
-// Better candidate: larger logit, or equal logit and lower expert index.
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-    return v > bv || (v == bv && i < bi);
+// Order-preserving map of an fp32 logit to an unsigned key (a larger logit
+// gives a larger key; -0 and +0 give the same key), and its inverse.  Key 0
+// lies below every finite logit and marks an entry out of the running.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    uint32_t b = __float_as_uint(v);
+    if ((b << 1) == 0u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
 // One warp per token.  logits_part == nullptr: the fp32 logits are given in
@@ -63,6 +71,12 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
             }
             v[i] = l;
         }
+        // k rounds of a warp-wide arg-max: each lane's best remaining key (its
+        // lowest expert on equal keys), the warp maximum of those keys, then
+        // the lowest expert among the lanes holding it
+        uint32_t key[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) key[i] = (lane + 32 * i < E) ? order_key(v[i]) : 0u;
         unsigned taken = 0;
         float sel_v[8];
         int sel_i[8];
@@ -71,28 +85,22 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
             sel_v[j] = 0.f;
             sel_i[j] = 0;
             if (j < k) {
-                float bv = -INFINITY;
-                int bi = 0x7fffffff;
+                uint32_t bk = 0u;
+                int bi = 0;
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    const int e = lane + 32 * i;
-                    if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
-                        bv = v[i];
-                        bi = e;
+                    const uint32_t kk = ((taken >> i) & 1u) ? 0u : key[i];
+                    if (kk > bk) {
+                        bk = kk;
+                        bi = i;
                     }
                 }
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                    const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-                    if (better(ov, oi, bv, bi)) {
-                        bv = ov;
-                        bi = oi;
-                    }
-                }
-                if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-                sel_v[j] = bv;
-                sel_i[j] = bi;
+                const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+                const uint32_t cand = bk == m ? static_cast<uint32_t>(lane + 32 * bi) : 0xffffffffu;
+                const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
+                if ((win & 31u) == static_cast<uint32_t>(lane)) taken |= 1u << (win >> 5);
+                sel_v[j] = key_logit(m);
+                sel_i[j] = static_cast<int>(win);
             }
         }
         // softmax over all E renormalised over the picked k == softmax over the picked k;
@@ -187,7 +195,7 @@ __device__ int block_exclusive_scan_512(int v, int *out_excl, int *warp_tot) {
 
 __global__ void __launch_bounds__(512) scan_tiles_kernel(int T, int E, int k, int has_shared, RoutingBufs rb) {
     __shared__ int warp_tot[40];
-    __shared__ int s_key[512];
+    __shared__ __align__(16) int s_key[512];
     const int g = threadIdx.x;
     const int G = E + (has_shared ? 1 : 0);
 
@@ -242,65 +250,72 @@ __global__ void __launch_bounds__(512) scan_tiles_kernel(int T, int E, int k, in
     int fbase = 0;
     const int total_full = block_exclusive_scan_512(full, &fbase, warp_tot);
     for (int i = 0; i < full; ++i) rb.tile_sched[fbase + i] = tbase + 2 * i;
-    s_key[g] = part_rows;  // 0 = no smaller unit
+    // rank of the smaller unit = the groups whose unit comes before it; the
+    // key (rows, then lower group first) is one integer per group, unique,
+    // and below 512 for a group without a smaller unit
+    const int my_key = part_rows * 512 + (511 - g);
+    s_key[g] = my_key;
     __syncthreads();
     int nparts = 0;
     if (part_rows > 0) {
         int rank = 0;
-        for (int o = 0; o < G; ++o) {
-            const int ko = s_key[o];
-            rank += (ko > part_rows) || (ko == part_rows && o < g);
+        const int4 *key4 = reinterpret_cast<const int4 *>(s_key);
+        const int n16 = (G + 15) / 16;  // whole 16-key blocks; the keys past G are below 512
+#pragma unroll 2
+        for (int b = 0; b < n16; ++b) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int4 o = key4[4 * b + q];
+                rank += (o.x > my_key) + (o.y > my_key) + (o.z > my_key) + (o.w > my_key);
+            }
         }
         rb.tile_sched[total_full + rank] = tbase + 2 * full;
         nparts = 1;
     }
-    int pbase = 0;
-    const int total_parts = block_exclusive_scan_512(nparts, &pbase, warp_tot);
+    const int total_parts = __syncthreads_count(nparts);
     if (g == 0) rb.num_tiles[1] = total_full + total_parts;
 }
 
 // ------------------------------------------------------------- permutation
 
-// One warp per chunk of kRouteChunk tokens: the chunk's expert picks and the
-// experts' first rows are loaded first, then ranks follow token order
-// (match_any within a pass of 32/k tokens, a counter per expert across passes).
-__global__ void __launch_bounds__(32) permute_kernel(int T, int E, int k, RoutingBufs rb) {
+// One block per chunk of kRouteChunk tokens, one thread per (token, pick)
+// slot in slot order (t * k + j).  A slot's row = its expert's first row for
+// the chunk + the slots of that expert in earlier warps of the block + its
+// rank among the lanes of its own warp with the same expert (match_any), so
+// the rows follow slot order within every expert.
+constexpr int kPermThreads = kRouteChunk * 8;
+constexpr int kPermWarps = kPermThreads / 32;
+
+__global__ void __launch_bounds__(kPermThreads) permute_kernel(int T, int E, int k, RoutingBufs rb) {
     __shared__ int base[256];
-    __shared__ int pick[kRouteChunk * 8];
-    __shared__ float pw[kRouteChunk * 8];
-    const int lane = threadIdx.x;
+    __shared__ int wcnt[kPermWarps][256];  // per warp, per expert: slots picking it
+    const int s = threadIdx.x, lane = s % 32, warp = s / 32;
     const int blk = blockIdx.x;
     const int t_begin = blk * kRouteChunk;
-    const int t_end = min(T, t_begin + kRouteChunk);
-    const int nslots = (t_end - t_begin) * k;
-    for (int e = lane; e < E; e += 32)
+    const int nslots = (min(T, t_begin + kRouteChunk) - t_begin) * k;
+    for (int e = s; e < E; e += kPermThreads)
         base[e] = rb.offsets[e] + rb.base_blk[static_cast<int64_t>(blk) * E + e];
-    for (int i = lane; i < nslots; i += 32) {
-        pick[i] = rb.topk_idx[static_cast<int64_t>(t_begin) * k + i];
-        pw[i] = rb.topk_w[static_cast<int64_t>(t_begin) * k + i];
+    for (int i = s; i < kPermWarps * 256; i += kPermThreads) (&wcnt[0][0])[i] = 0;
+    const bool active = s < nslots;
+    const int slot = t_begin * k + s;
+    int e = -1 - s;  // inactive lanes: a value no other lane holds
+    float w = 0.f;
+    if (active) {
+        e = rb.topk_idx[slot];
+        w = rb.topk_w[slot];
     }
-    __syncwarp();
-    const int per_pass = 32 / k;
-    const unsigned lt_mask = (1u << lane) - 1u;
-    for (int t0 = t_begin; t0 < t_end; t0 += per_pass) {
-        const int tt = lane / k, j = lane % k;
-        const int t = t0 + tt;
-        const bool active = tt < per_pass && t < t_end;
-        const int e = active ? pick[(t - t_begin) * k + j] : -1 - lane;
-        const unsigned same = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(same & lt_mask);
-        const int before = active ? base[e] : 0;
-        __syncwarp();
-        if (active) {
-            if (rank == 0) base[e] = before + __popc(same);
-            const int pos = before + rank;
-            const int slot = t * k + j;
-            rb.perm[pos] = slot;
-            rb.inv_perm[slot] = pos;
-            rb.row_token[pos] = t;
-            rb.row_weight[pos] = pw[slot - t_begin * k];
-        }
-        __syncwarp();
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(same & ((1u << lane) - 1u));
+    __syncthreads();
+    if (active && rank == 0) wcnt[warp][e] = __popc(same);
+    __syncthreads();
+    if (active) {
+        int pos = base[e] + rank;
+        for (int w2 = 0; w2 < warp; ++w2) pos += wcnt[w2][e];
+        rb.perm[pos] = slot;
+        rb.inv_perm[slot] = pos;
+        rb.row_token[pos] = t_begin + s / k;
+        rb.row_weight[pos] = w;
     }
 }
 
@@ -325,7 +340,7 @@ cudaError_t launch_routing_tables(const float *logits_part, int ld, const float 
                                   cudaStream_t s) {
     topk_hist_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits_part, ld, given, bias, T, E, k, has_shared, opts, rb);
     scan_tiles_kernel<<<1, 512, 0, s>>>(T, E, k, has_shared, rb);
-    permute_kernel<<<rb.nblk, 32, 0, s>>>(T, E, k, rb);
+    permute_kernel<<<rb.nblk, kPermThreads, 0, s>>>(T, E, k, rb);
     return cudaGetLastError();
 }
 
