@@ -106,7 +106,10 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
         // softmax over all E renormalised over the picked k == softmax over the picked k;
         // without renormalisation the denominator runs over all E
         const float m = sel_v[0];
+        float ex[8];
         float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ex[j] = j < k ? expf(sel_v[j] - m) : 0.f;
         if (opts.no_renorm) {
 #pragma unroll
             for (int i = 0; i < 8; ++i)
@@ -116,15 +119,22 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
         } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                if (j < k) sum += expf(sel_v[j] - m);
+                if (j < k) sum += ex[j];
         }
+        // lane j writes pick j
+        int my_i = 0;
+        float my_ex = 0.f;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            if (j < k && lane == j) {
-                rb.topk_idx[static_cast<int64_t>(t) * k + j] = sel_i[j];
-                rb.topk_w[static_cast<int64_t>(t) * k + j] = expf(sel_v[j] - m) / sum;
-                atomicAdd(&hist[sel_i[j]], 1);
+            if (lane == j) {
+                my_i = sel_i[j];
+                my_ex = ex[j];
             }
+        }
+        if (lane < k) {
+            rb.topk_idx[static_cast<int64_t>(t) * k + lane] = my_i;
+            rb.topk_w[static_cast<int64_t>(t) * k + lane] = my_ex / sum;
+            atomicAdd(&hist[my_i], 1);
         }
         if (has_shared) {
             float cw = 1.0f;
@@ -164,40 +174,68 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
 
 // ------------------------------------------------------- scan and tile map
 
-// Exclusive scan of v over 512 threads (one value each); returns the total.
-__device__ int block_exclusive_scan_512(int v, int *out_excl, int *warp_tot) {
+// Exclusive scans of four values per thread over a 512-thread block in one
+// pass (one shuffle ladder per warp, one over the 16 warp totals); `sh`
+// holds 2 x 4 x 17 ints.  Returns the exclusive prefixes and the totals.
+__device__ __forceinline__ void block_scan4_512(const int (&v)[4], int (&excl)[4], int (&total)[4], int *sh) {
     const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
-    int incl = v;
+    int incl[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) incl[c] = v[c];
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const int o = __shfl_up_sync(0xffffffffu, incl[c], off);
+            if (lane >= off) incl[c] += o;
+        }
     }
-    if (lane == 31) warp_tot[warp] = incl;
+    if (lane == 31) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sh[c * 17 + warp] = incl[c];
+    }
     __syncthreads();
     if (warp == 0) {
-        int w = lane < 16 ? warp_tot[lane] : 0;
-        int wi = w;
+        int w[4], wi[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            w[c] = lane < 16 ? sh[c * 17 + lane] : 0;
+            wi[c] = w[c];
+        }
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, wi, off);
-            if (lane >= off) wi += o;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int o = __shfl_up_sync(0xffffffffu, wi[c], off);
+                if (lane >= off) wi[c] += o;
+            }
         }
-        if (lane < 16) warp_tot[16 + lane] = wi - w;  // exclusive warp bases
-        if (lane == 15) warp_tot[32] = wi;           // grand total
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (lane < 16) sh[68 + c * 17 + lane] = wi[c] - w[c];  // exclusive warp bases
+            if (lane == 15) sh[68 + c * 17 + 16] = wi[c];         // grand total
+        }
     }
     __syncthreads();
-    *out_excl = warp_tot[16 + warp] + incl - v;
-    const int total = warp_tot[32];
-    __syncthreads();
-    return total;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        excl[c] = sh[68 + c * 17 + warp] + incl[c] - v[c];
+        total[c] = sh[68 + c * 17 + 16];
+    }
 }
 
+// One thread per group (expert, then the shared expert).
 __global__ void __launch_bounds__(512) scan_tiles_kernel(int T, int E, int k, int has_shared, RoutingBufs rb) {
-    __shared__ int warp_tot[40];
-    __shared__ __align__(16) int s_key[512];
-    const int g = threadIdx.x;
+    constexpr int kUnitRows = 2 * kTileRows;
+    static_assert(kUnitRows <= 256, "row counts of a smaller unit index 256-entry tables");
+    __shared__ int sh[2 * 4 * 17];
+    __shared__ int s_hist[kUnitRows];     // groups per row count of their smaller unit
+    __shared__ int s_gt[kUnitRows];       // groups whose smaller unit has more rows
+    __shared__ int s_wc[16][kUnitRows];   // the same counts per warp
+    const int g = threadIdx.x, lane = g % 32, warp = g / 32;
     const int G = E + (has_shared ? 1 : 0);
+    for (int i = g; i < kUnitRows; i += 512) s_hist[i] = 0;
+    for (int i = g; i < 16 * kUnitRows; i += 512) (&s_wc[0][0])[i] = 0;
 
     int cnt = 0;
     if (g < E) {
@@ -220,60 +258,53 @@ __global__ void __launch_bounds__(512) scan_tiles_kernel(int T, int E, int k, in
     } else if (g == E && has_shared) {
         cnt = T;
     }
-    int off = 0;
-    const int total_rows = block_exclusive_scan_512(cnt, &off, warp_tot);
+
+    // Work units of the grouped GEMMs: a group's tiles in pairs (0-1, 2-3,
+    // ...; the last one alone when the count is odd); tile_sched holds each
+    // unit's first tile.  Launch order: units of 2 full tiles in canonical
+    // order, then each group's last, smaller unit by row count descending
+    // (ties: lower group first).  A smaller unit's place among those = the
+    // groups with more rows (a histogram over row counts, scanned from the
+    // top) + the lower groups with as many rows (ranks within the warp from
+    // match_any, per-warp counts for the warps before).
+    const int nt = (cnt + kTileRows - 1) / kTileRows;
+    const int full = cnt / kUnitRows;
+    const int part_rows = cnt % kUnitRows;
+    const unsigned same = __match_any_sync(0xffffffffu, part_rows > 0 ? part_rows : -1 - g);
+    const int rank_in_warp = __popc(same & ((1u << lane) - 1u));
+    __syncthreads();
+    if (part_rows > 0) {
+        atomicAdd(&s_hist[part_rows], 1);
+        if (rank_in_warp == 0) s_wc[warp][part_rows] = __popc(same);
+    }
+    __syncthreads();
+    const int v[4] = {cnt, nt, full, g < kUnitRows ? s_hist[kUnitRows - 1 - g] : 0};
+    int ex[4], tot[4];
+    block_scan4_512(v, ex, tot, sh);
+    const int off = ex[0], tbase = ex[1], fbase = ex[2];
+    if (g < kUnitRows) s_gt[kUnitRows - 1 - g] = ex[3];
     if (g < G) {
         rb.counts[g] = cnt;
         rb.offsets[g] = off;
     }
-    if (g == 0) rb.offsets[G] = total_rows;
-
-    const int nt = (cnt + kTileRows - 1) / kTileRows;
-    int tbase = 0;
-    const int total_tiles = block_exclusive_scan_512(nt, &tbase, warp_tot);
+    if (g == 0) {
+        rb.offsets[G] = tot[0];
+        rb.num_tiles[0] = tot[1];
+        rb.num_tiles[1] = tot[2] + tot[3];
+    }
     for (int i = 0; i < nt; ++i) {
         const int at = tbase + i;
         rb.tile_group[at] = g;
         rb.tile_row[at] = off + i * kTileRows;
         rb.tile_rows[at] = min(kTileRows, cnt - i * kTileRows);
     }
-    if (g == 0) rb.num_tiles[0] = total_tiles;
-
-    // Work units of the grouped GEMMs: a group's tiles in pairs (0-1, 2-3,
-    // ...; the last one alone when the count is odd); tile_sched holds each
-    // unit's first tile.  Launch order: units of 2 full tiles in canonical
-    // order, then each group's last, smaller unit by row count descending
-    // (ties: lower group first).
-    constexpr int kUnitRows = 2 * kTileRows;
-    const int full = cnt / kUnitRows;
-    const int part_rows = cnt % kUnitRows;
-    int fbase = 0;
-    const int total_full = block_exclusive_scan_512(full, &fbase, warp_tot);
     for (int i = 0; i < full; ++i) rb.tile_sched[fbase + i] = tbase + 2 * i;
-    // rank of the smaller unit = the groups whose unit comes before it; the
-    // key (rows, then lower group first) is one integer per group, unique,
-    // and below 512 for a group without a smaller unit
-    const int my_key = part_rows * 512 + (511 - g);
-    s_key[g] = my_key;
     __syncthreads();
-    int nparts = 0;
     if (part_rows > 0) {
-        int rank = 0;
-        const int4 *key4 = reinterpret_cast<const int4 *>(s_key);
-        const int n16 = (G + 15) / 16;  // whole 16-key blocks; the keys past G are below 512
-#pragma unroll 2
-        for (int b = 0; b < n16; ++b) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int4 o = key4[4 * b + q];
-                rank += (o.x > my_key) + (o.y > my_key) + (o.z > my_key) + (o.w > my_key);
-            }
-        }
-        rb.tile_sched[total_full + rank] = tbase + 2 * full;
-        nparts = 1;
+        int rank = s_gt[part_rows] + rank_in_warp;
+        for (int w2 = 0; w2 < warp; ++w2) rank += s_wc[w2][part_rows];
+        rb.tile_sched[tot[2] + rank] = tbase + 2 * full;
     }
-    const int total_parts = __syncthreads_count(nparts);
-    if (g == 0) rb.num_tiles[1] = total_full + total_parts;
 }
 
 // ------------------------------------------------------------- permutation
