@@ -33,20 +33,25 @@ __device__ __forceinline__ float key_logit(uint32_t key) {
     return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// One warp per token.  logits_part == nullptr: the fp32 logits are given in
-// `given` instead of being summed from the router's partial products.  The
-// chunk histogram counts_blk (cleared beforehand) receives the block's counts
-// with atomic adds: a sum, so its value does not depend on their order.
-__global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict__ logits_part, int ld,
-                                                        const float *__restrict__ given,
-                                                        const float *__restrict__ bias, int T, int E, int k,
-                                                        int has_shared, RouteOpts opts, RoutingBufs rb) {
+// One warp per token, kTopkWarps tokens per block (small blocks: about seven
+// per SM at T = 4096, so the SMs end together).  logits_part == nullptr: the
+// fp32 logits are given in `given` instead of being summed from the router's
+// partial products.  The chunk histogram counts_blk (cleared beforehand)
+// receives the block's counts with atomic adds: a sum, so its value does not
+// depend on their order.
+constexpr int kTopkWarps = 4;
+static_assert(kRouteChunk % kTopkWarps == 0, "a top-k block stays within one chunk");
+
+__global__ void __launch_bounds__(kTopkWarps * 32)
+    topk_hist_kernel(const float *__restrict__ logits_part, int ld, const float *__restrict__ given,
+                     const float *__restrict__ bias, int T, int E, int k, int has_shared, RouteOpts opts,
+                     RoutingBufs rb) {
     __shared__ int hist[256];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     for (int e = tid; e < 256; e += blockDim.x) hist[e] = 0;
     __syncthreads();
 
-    const int t = blockIdx.x * 8 + warp;  // 8 tokens per block, all in one chunk
+    const int t = blockIdx.x * kTopkWarps + warp;
     if (t < T) {
         float v[8];
 #pragma unroll
@@ -77,7 +82,6 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
         uint32_t key[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) key[i] = (lane + 32 * i < E) ? order_key(v[i]) : 0u;
-        unsigned taken = 0;
         float sel_v[8];
         int sel_i[8];
 #pragma unroll
@@ -85,20 +89,33 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
             sel_v[j] = 0.f;
             sel_i[j] = 0;
             if (j < k) {
-                uint32_t bk = 0u;
-                int bi = 0;
+                // the lane's best remaining key, lower slot on equal keys (a
+                // pairwise tree: the right operand wins only when larger)
+                uint32_t k1[4], k2[2];
+                int i1[4], i2[2];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint32_t kk = ((taken >> i) & 1u) ? 0u : key[i];
-                    if (kk > bk) {
-                        bk = kk;
-                        bi = i;
-                    }
+                for (int q = 0; q < 4; ++q) {
+                    const bool r = key[2 * q + 1] > key[2 * q];
+                    k1[q] = r ? key[2 * q + 1] : key[2 * q];
+                    i1[q] = r ? 2 * q + 1 : 2 * q;
                 }
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const bool r = k1[2 * q + 1] > k1[2 * q];
+                    k2[q] = r ? k1[2 * q + 1] : k1[2 * q];
+                    i2[q] = r ? i1[2 * q + 1] : i1[2 * q];
+                }
+                const bool r = k2[1] > k2[0];
+                const uint32_t bk = r ? k2[1] : k2[0];
+                const int bi = r ? i2[1] : i2[0];
                 const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
                 const uint32_t cand = bk == m ? static_cast<uint32_t>(lane + 32 * bi) : 0xffffffffu;
                 const uint32_t win = __reduce_min_sync(0xffffffffu, cand);
-                if ((win & 31u) == static_cast<uint32_t>(lane)) taken |= 1u << (win >> 5);
+                // the winner leaves the running
+                const int out = (win & 31u) == static_cast<uint32_t>(lane) ? static_cast<int>(win >> 5) : -1;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i == out) key[i] = 0u;
                 sel_v[j] = key_logit(m);
                 sel_i[j] = static_cast<int>(win);
             }
@@ -167,7 +184,7 @@ __global__ void __launch_bounds__(256) topk_hist_kernel(const float *__restrict_
         }
     }
     __syncthreads();
-    const int chunk = (blockIdx.x * 8) / kRouteChunk;
+    const int chunk = (blockIdx.x * kTopkWarps) / kRouteChunk;
     for (int e = tid; e < E; e += blockDim.x)
         if (hist[e]) atomicAdd(&rb.counts_blk[static_cast<int64_t>(chunk) * E + e], hist[e]);
 }
@@ -369,7 +386,7 @@ cudaError_t launch_zero_i32(int *p, int64_t n, cudaStream_t s) {
 cudaError_t launch_routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
                                   int E, int k, int has_shared, const RouteOpts &opts, const RoutingBufs &rb,
                                   cudaStream_t s) {
-    topk_hist_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits_part, ld, given, bias, T, E, k, has_shared, opts, rb);
+    topk_hist_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(logits_part, ld, given, bias, T, E, k, has_shared, opts, rb);
     scan_tiles_kernel<<<1, 512, 0, s>>>(T, E, k, has_shared, rb);
     permute_kernel<<<rb.nblk, kPermThreads, 0, s>>>(T, E, k, rb);
     return cudaGetLastError();
