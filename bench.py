@@ -389,9 +389,10 @@ def run_decode(args, pk):
 
 
 def run_small_batches(pk, sizes=(1, 2, 4, 8), steps=10):
-    """Small token batches (the speculative-verify shape) through moe_prefill
-    on one layer of the T=512 shapes: graph-replayed calls, L2 flushed before
-    each; bytes = the touched experts' weights + router."""
+    """Small token batches (the speculative-verify shape) on one layer of the
+    T=512 shapes, through moe_prefill and through moe_decode_batch (each
+    picked expert read once for the batch): graph-replayed calls, L2 flushed
+    before each; bytes = the touched experts' weights + router."""
     import torch
     from int4_grouped_gemm_gb300 import _lib, synthetic
     cfg = synthetic.CONFIGS["prefill512"]
@@ -399,20 +400,18 @@ def run_small_batches(pk, sizes=(1, 2, 4, 8), steps=10):
     ws = layer.workspace(max(sizes))
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
     per_expert = 3 * cfg.H * cfg.I // 2 + 3 * cfg.H * cfg.I // cfg.group * 4
-    out = {}
-    for T in sizes:
-        xt = x[:T].contiguous()
-        y = torch.empty_like(xt)
+
+    def time_graph(call, tag):
         for _ in range(3):
-            _lib.moe_prefill(layer.desc, xt, T, y, ws.buf)
+            call()
         graph = torch.cuda.CUDAGraph()
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):
-            _lib.moe_prefill(layer.desc, xt, T, y, ws.buf)
+            call()
         torch.cuda.current_stream().wait_stream(side)
         with torch.cuda.graph(graph):
-            _lib.moe_prefill(layer.desc, xt, T, y, ws.buf)
+            call()
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for i in range(steps):
@@ -422,16 +421,31 @@ def run_small_batches(pk, sizes=(1, 2, 4, 8), steps=10):
             ev[i][1].record()
         torch.cuda.synchronize()
         if _lib.moe_read_device_status(ws.buf) != 0:
-            raise RuntimeError(f"small batch T={T}: device status")
-        ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+            raise RuntimeError(f"small batch {tag}: device status")
+        del graph
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    via_prefill, via_batch = {}, {}
+    for T in sizes:
+        xt = x[:T].contiguous()
+        y = torch.empty_like(xt)
+        ms = time_graph(lambda: _lib.moe_prefill(layer.desc, xt, T, y, ws.buf), f"prefill T={T}")
         touched = int((ws.routing(layer.desc, T)["counts"].cpu() > 0).sum().item())
         wbytes = touched * per_expert + cfg.E * cfg.H * 4
-        out[f"T{T}"] = {"ms_per_call": round(ms, 4), "tok_s": round(T / (ms * 1e-3), 1), "experts_touched": touched,
-                        "frac_of_hbm": round(wbytes / (ms * 1e-3) / 1e9 / pk["hbm"], 4)}
-        del graph
+        via_prefill[f"T{T}"] = {"ms_per_call": round(ms, 4), "tok_s": round(T / (ms * 1e-3), 1),
+                                "experts_touched": touched,
+                                "frac_of_hbm": round(wbytes / (ms * 1e-3) / 1e9 / pk["hbm"], 4)}
+        ms_b = time_graph(lambda: _lib.moe_decode_batch(layer.desc, xt, y, ws.buf), f"decode_batch B={T}")
+        via_batch[f"B{T}"] = {"ms_per_call": round(ms_b, 4), "tok_s": round(T / (ms_b * 1e-3), 1),
+                              "experts_touched": touched,
+                              "hbm_gbs": round(wbytes / (ms_b * 1e-3) / 1e9, 1),
+                              "frac_of_hbm": round(wbytes / (ms_b * 1e-3) / 1e9 / pk["hbm"], 4),
+                              "speedup_vs_moe_prefill": round(ms / ms_b, 2)}
+    via_batch["note"] = ("moe_decode_batch on the same layer and tokens; experts touched counted from the same "
+                         "tokens' moe_prefill routing")
     del flush, ws, layer, x
     torch.cuda.empty_cache()
-    return out
+    return via_prefill, via_batch
 
 
 def run_prefill_other(name, pk, steps=10):
@@ -612,7 +626,7 @@ def main():
     other = None
     if rank == 0 and not args.no_other:
         other = {n: run_prefill_other(n, pk) for n in ("prefill512", "skew16384")}
-        other["small_batches_through_moe_prefill"] = run_small_batches(pk)
+        other["small_batches_through_moe_prefill"], other["small_batch_decode"] = run_small_batches(pk)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg)

@@ -61,6 +61,7 @@ SIGNATURES = {
     "moe_prefill_profiled": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_sz, c_p, c_p]),
     "moe_decode": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_sz, c_p]),
     "moe_decode_layers": (ctypes.c_int, [c_p, c_i32, c_p, c_p, c_p, c_sz, c_p]),
+    "moe_decode_batch": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_sz, c_p]),
     "moe_decode_static_scratch": (ctypes.c_int, [c_p, c_p, c_p, c_p]),
     "moe_route_logits": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_sz, c_p]),
     "pack_int4": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_p]),
@@ -144,6 +145,12 @@ def moe_prefill_profiled(desc: moe_layer_desc, x, T: int, y, ws, events, stream=
 def moe_decode(desc: moe_layer_desc, x, y, ws, stream=None):
     _check(load().moe_decode(ctypes.byref(desc), _ptr(x), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(),
                              _stream(stream)), "moe_decode")
+
+
+def moe_decode_batch(desc: moe_layer_desc, x, y, ws, stream=None):
+    """x, y: [B][H] bf16 with 1 <= B <= 8."""
+    _check(load().moe_decode_batch(ctypes.byref(desc), _ptr(x), x.shape[0], _ptr(y), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream)), "moe_decode_batch")
 
 
 def moe_decode_layers(descs, x, y, ws, stream=None):

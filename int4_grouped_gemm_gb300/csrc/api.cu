@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "kernels.cuh"
+#include "small_batch.cuh"
 
 
 namespace moe {
@@ -155,7 +156,9 @@ size_t moe_workspace_bytes(const moe_layer_desc *desc, int32_t T_max) {
     if (check_shape(desc) != MOE_OK || check_tokens(desc, T_max) != MOE_OK) return 0;
     const PrefillLayout P = prefill_layout(T_max, desc->E, desc->k, desc->H, desc->I);
     const DecodeLayout D = decode_stack_layout(desc->E, desc->k, desc->H, desc->I);
-    return P.total > D.total ? P.total : D.total;
+    const BatchLayout Bt = batch_layout(desc->E, desc->k, desc->H, desc->I);
+    size_t total = P.total > D.total ? P.total : D.total;
+    return total > Bt.total ? total : Bt.total;
 }
 
 int moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
@@ -402,6 +405,52 @@ int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, siz
     DeviceInfo *dev = nullptr;
     if ((rc = current_device(dev))) return rc;
     return decode_run(desc, 1, x, y, static_cast<char *>(ws), L, dev->num_sms, stream);
+}
+
+int moe_decode_batch(const moe_layer_desc *desc, const void *x, int32_t B, void *y, void *ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+    int rc = decode_check(desc);
+    if (rc) return rc;
+    if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
+    if (B < 1 || B > kBatchMax) return MOE_ERR_TOKENS;
+    const BatchLayout L = batch_layout(desc->E, desc->k, desc->H, desc->I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    char *w = static_cast<char *>(ws);
+    BatchArgs a{};
+    a.E = desc->E;
+    a.k = desc->k;
+    a.H = desc->H;
+    a.I = desc->I;
+    a.G = desc->group;
+    a.B = B;
+    a.has_shared = desc->has_shared;
+    a.no_renorm = desc->no_renorm;
+    a.ldg_h = ld_groups(desc->H, desc->group);
+    a.ldg_i = ld_groups(desc->I, desc->group);
+    a.S_max = L.S_max;
+    a.x = static_cast<const __nv_bfloat16 *>(x);
+    a.y = static_cast<__nv_bfloat16 *>(y);
+    a.Wr = desc->router_w;
+    a.bias = desc->router_bias;
+    a.shg = desc->shared_gate;
+    a.qg = desc->gate.q;
+    a.qu = desc->up.q;
+    a.qd = desc->down.q;
+    a.sg = desc->gate.scale;
+    a.bg = desc->gate.bias;
+    a.su = desc->up.scale;
+    a.bu = desc->up.bias;
+    a.sd = desc->down.scale;
+    a.bd = desc->down.bias;
+    a.ticket = &reinterpret_cast<Ctrl *>(w + L.ctrl)->ticket;
+    a.logits = reinterpret_cast<float *>(w + L.logits);
+    a.slots = reinterpret_cast<int *>(w + L.slots);
+    a.slot_w = reinterpret_cast<float *>(w + L.slot_w);
+    a.h = reinterpret_cast<__nv_bfloat16 *>(w + L.h);
+    a.o = reinterpret_cast<float *>(w + L.o);
+    return cuda_rc(launch_batch(a, dev->num_sms, stream));
 }
 
 int moe_decode_layers(const moe_layer_desc *descs, int32_t n_layers, const void *x, void *y, void *ws,

@@ -94,6 +94,13 @@ class PackedLayer:
         _lib.moe_decode(self.desc, x, y, ws.buf, stream)
         return y
 
+    def decode_batch(self, x: torch.Tensor, ws: "Workspace", y: Optional[torch.Tensor] = None, stream=None):
+        """1 to 8 tokens: each picked expert is read once for all of them."""
+        if y is None:
+            y = torch.empty_like(x)
+        _lib.moe_decode_batch(self.desc, x, y, ws.buf, stream)
+        return y
+
 
 class Workspace:
     """Scratch memory for one layer call (routing tables, h, fp32 combine)."""

@@ -111,3 +111,27 @@ def test_routing_views_layout(lib):
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert v.tile_size == 128
     assert v.max_tiles >= (4096 * 9) // 128 + 257
+
+
+def test_small_batch_decode_checks_on_the_host(lib):
+    from int4_grouped_gemm_gb300 import _lib
+    # 16-byte aligned stand-in pointers: every case below must be rejected on
+    # the host, before a device or any of the pointers is touched
+    q = _lib.moe_qweight(256, 512, 768)
+    d = _lib.moe_layer_desc(256, 8, 2048, 512, 64, 1, 1024, None, q, q, q)
+    f = lib.moe_decode_batch
+    x, y, ws = ctypes.c_void_p(2048), ctypes.c_void_p(4096), ctypes.c_void_p(8192)
+    n = _lib.moe_workspace_bytes(d, 1)
+    # the union of 8 tokens' picks (at most 64 experts) + the shared expert:
+    # per-slot SwiGLU rows [8][I] bf16, and per group of slots (one slot per
+    # group at most) the weighted outputs [8][H] fp32
+    assert n >= 65 * 8 * (512 * 2 + 2048 * 4)
+    assert f(ctypes.byref(d), x, 0, y, ws, n, None) == _lib.MOE_ERR_TOKENS
+    assert f(ctypes.byref(d), x, 9, y, ws, n, None) == _lib.MOE_ERR_TOKENS
+    assert f(ctypes.byref(d), x, 4, y, ws, 4096, None) == _lib.MOE_ERR_WORKSPACE
+    assert f(ctypes.byref(d), ctypes.c_void_p(2056), 4, y, ws, n, None) == _lib.MOE_ERR_ALIGN
+    assert f(ctypes.byref(d), None, 4, y, ws, n, None) == _lib.MOE_ERR_NULL
+    wide = _lib.moe_layer_desc(256, 8, 8192, 512, 64, 1, 1024, None, q, q, q)   # above the decode limit
+    assert f(ctypes.byref(wide), x, 4, y, ws, 1 << 30, None) == _lib.MOE_ERR_SHAPE
+    bad = _lib.moe_layer_desc(256, 9, 2048, 512, 64, 1, 1024, None, q, q, q)
+    assert f(ctypes.byref(bad), x, 4, y, ws, n, None) == _lib.MOE_ERR_SHAPE
