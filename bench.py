@@ -51,6 +51,9 @@ def parse():
                     help="only run warmup + steps prefill calls of the headline layer (for ncu captures)")
     ap.add_argument("--profile-decode", action="store_true",
                     help="only run warmup + steps eager decode passes through 4 layers (for ncu captures)")
+    ap.add_argument("--profile-batch", action="store_true",
+                    help="only run warmup + steps moe_decode_batch calls with 1 and then 8 tokens on one layer of "
+                         "the T=512 shapes (for ncu captures)")
     return ap.parse_args()
 
 
@@ -578,6 +581,15 @@ def profile_only(args):
         y = torch.empty_like(x)
         for _ in range(args.warmup + args.steps):
             _lib.moe_prefill(layer.desc, x, cfg.T, y, ws.buf)
+    elif args.profile_batch:
+        cfg = synthetic.CONFIGS["prefill512"]
+        layer, x = build_prefill(cfg)
+        ws = layer.workspace(8)
+        for B in (1, 8):
+            xb = x[:B].contiguous()
+            y = torch.empty_like(xb)
+            for _ in range(args.warmup + args.steps):
+                _lib.moe_decode_batch(layer.desc, xb, y, ws.buf)
     else:
         cfg = synthetic.CONFIGS[DECODE_CFG]
         layers = []
@@ -612,7 +624,7 @@ def main():
     rank, world = dist_setup(args.gpus)
     from int4_grouped_gemm_gb300 import _lib
     _lib.load()
-    if args.profile or args.profile_decode:
+    if args.profile or args.profile_decode or args.profile_batch:
         profile_only(args)
         return
     pk = peaks()
