@@ -5,8 +5,9 @@ the CPU-baseline leg of ``bench.py``; never by the library.  It shares no code
 with the CUDA path.  Every function here only marshals numpy arrays; the
 arithmetic is in ``moe_oracle.c`` (whose header cites the passages it follows).
 
-Parity status: quantiser, dequant, router, top-k, routing tables and the
-dense single-expert case are pinned by ``tests/test_oracle_pins.py``; the
+Parity status: quantiser, dequant, router, top-k, routing tables, the
+dense single-expert case and the residual add / RMS norm steps around the
+layer are pinned by ``tests/test_oracle_pins.py``; the
 whole layer beyond those pins is "parity unpinned" (the pages print no worked
 example or output value).
 """
@@ -77,6 +78,8 @@ def lib():
         L.oracle_experts_given_routing.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _i32, _i32] + [_p] * 9 + \
             [_p, _p, _p]
         L.oracle_dispatch_combine_identity.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _p, _p, _p]
+        L.oracle_residual_rmsnorm.argtypes = [_p, _p, _i32, _i32, _p, ctypes.c_double, _p, _p]
+        L.oracle_residual_out.argtypes = [_p, _p, _i64, _p]
         _lib = L
     return _lib
 
@@ -221,6 +224,40 @@ def moe_layer(x_bits: np.ndarray, Wr: np.ndarray, bias: Optional[np.ndarray], ga
                                _ptr(bias), _ptr(sg), *[_ptr(a) for a in arrays], _ptr(tokens), n,
                                _ptr(logits), _ptr(idx), _ptr(w), _ptr(y), _ptr(sw))
     return dict(logits=logits, idx=idx, w=w, y=y, tokens=tokens, shared_w=sw)
+
+
+def residual_rmsnorm(a_bits: np.ndarray, r_bits: np.ndarray, norm_w: np.ndarray, eps: float):
+    """Residual add and RMS norm before the layer: (h, x) as bf16 bit patterns."""
+    a_bits = _c(a_bits, np.uint16)
+    r_bits = _c(r_bits, np.uint16)
+    T, H = a_bits.shape
+    assert r_bits.shape == (T, H)
+    norm_w = _c(norm_w, np.float32)
+    h = np.empty((T, H), np.uint16)
+    x = np.empty((T, H), np.uint16)
+    lib().oracle_residual_rmsnorm(_ptr(a_bits), _ptr(r_bits), T, H, _ptr(norm_w), float(eps), _ptr(h), _ptr(x))
+    return h, x
+
+
+def residual_out(h_bits: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """The residual add after the layer: bf16(h + y), y fp64, as bf16 bits."""
+    h_bits = _c(h_bits, np.uint16)
+    y = _c(y, np.float64)
+    assert y.shape == h_bits.shape
+    out = np.empty(h_bits.shape, np.uint16)
+    lib().oracle_residual_out(_ptr(h_bits), _ptr(y), h_bits.size, _ptr(out))
+    return out
+
+
+def moe_block(a_bits, r_bits, norm_w, eps, Wr, bias, gate: QWeights, up: QWeights, down: QWeights, E: int, k: int,
+              has_shared: bool, **kw) -> dict:
+    """The layer with the steps either side of it: h = a + r, x = RMSNorm(h) w,
+    out = bf16(h + MoE(x)); returns the layer's dict plus h, x and out (bits)."""
+    h, x = residual_rmsnorm(a_bits, r_bits, norm_w, eps)
+    r = moe_layer(x, Wr, bias, gate, up, down, E, k, has_shared, **kw)
+    tok = r["tokens"]
+    r.update(h=h, x=x, out=residual_out(h[tok], r["y"]))
+    return r
 
 
 def experts_given_routing(x_bits, gate: QWeights, up: QWeights, down: QWeights, E, has_shared,

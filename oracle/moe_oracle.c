@@ -28,7 +28,12 @@
  *     holds the j-th largest; weights = softmax over all E logits,
  *     renormalised over the k picked ones;
  *   - expert = SwiGLU MLP: h = silu(x Wg^T) * (x Wu^T), o = h Wd^T;
- *   - y = sum_j w_j o_{e_j} + o_shared (shared expert weight 1, no gate).
+ *   - y = sum_j w_j o_{e_j} + o_shared (shared expert weight 1, no gate);
+ *   - the steps either side of the layer (a pre-norm decoder block of the
+ *     model family; the pages name the model but not its norm): residual
+ *     add h = a + r, x = RMSNorm(h) * w as the layer's input, and the
+ *     residual add out = h + y after it (oracle_residual_rmsnorm,
+ *     oracle_residual_out).
  *
  * Precision: quantisation and the router run in fp32 (they decide integers
  * that the GPU must reproduce bit for bit: codes and expert indices);
@@ -502,4 +507,51 @@ void oracle_dispatch_combine_identity(const uint16_t *x, int32_t T, int32_t H, i
     int32_t dims[2] = {H, E};
     dispatch_combine(x, H, k, E, has_shared, idx, w, seq, T, NULL, identity_expert, dims, y);
     free(seq);
+}
+
+/* ------------------------------------------- steps either side of the layer */
+
+/* Round a double to bf16 in one step (round to nearest, ties to even): the
+ * significand is brought to 8 bits with nearbyint (default rounding mode),
+ * which a float then holds exactly.  Normal range only (no subnormals here). */
+static uint16_t bf16_from_double(double v)
+{
+    if (v == 0.0 || !isfinite(v))
+        return bf16_from_float((float)v);
+    int e;
+    const double m = frexp(v, &e);                 /* |m| in [0.5, 1) */
+    const double r = nearbyint(ldexp(m, 8));       /* 8 significant bits */
+    return bf16_from_float((float)ldexp(r, e - 8)); /* exact in float and bf16 */
+}
+
+/* Residual add and RMS norm before the layer, per token t (reading: the MoE
+ * sub-layer of a pre-norm decoder block; the pages name the model, not its
+ * norm):
+ *   h[t]   = bf16(fp32(a[t] + r[t]))                      (the residual stream)
+ *   x[t]   = bf16(h[t] / sqrt(mean_k h[t][k]^2 + eps) * w) (fp64 statistics)
+ * a, r, h, x: bf16 bit patterns [T][H]; w: [H] fp32. */
+void oracle_residual_rmsnorm(const uint16_t *a, const uint16_t *r, int32_t T, int32_t H, const float *w,
+                             double eps, uint16_t *h, uint16_t *x)
+{
+    for (int32_t t = 0; t < T; ++t) {
+        const int64_t o = (int64_t)t * H;
+        double ss = 0.0;
+        for (int32_t k = 0; k < H; ++k) {
+            const float s = float_from_bf16(a[o + k]) + float_from_bf16(r[o + k]);
+            h[o + k] = bf16_from_float(s);
+            const double hv = (double)float_from_bf16(h[o + k]);
+            ss += hv * hv;
+        }
+        const double inv = 1.0 / sqrt(ss / (double)H + eps);
+        for (int32_t k = 0; k < H; ++k)
+            x[o + k] = bf16_from_double((double)float_from_bf16(h[o + k]) * inv * (double)w[k]);
+    }
+}
+
+/* The residual add after the layer: out[t] = bf16(h[t] + y[t]), y the
+ * layer's output in fp64 (rounded once). */
+void oracle_residual_out(const uint16_t *h, const double *y, int64_t n, uint16_t *out)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = bf16_from_double((double)float_from_bf16(h[i]) + y[i]);
 }

@@ -2,7 +2,8 @@
 below plants one mistake in a copy of the oracle's C source (nibble order,
 scale, rounding, sign of the bias, router bias or K range, tie-break,
 renormalisation, SwiGLU operand order, stable token order, shared expert,
-down projection index), builds it, and runs the pins against it; at least
+down projection index, the RMS norm's mean, eps and weight, the residual add
+after the layer), builds it, and runs the pins against it; at least
 one pin must fail.  The shipped oracle is never modified."""
 import os
 import subprocess
@@ -39,6 +40,16 @@ MUTANTS = [
      "        if (0) {\n            const double c"),
     ("down_reads_gate_scales", "osum += hbuf[i] * dequant_one(W->qd, W->sd, W->bd, row, I, G, i);",
      "osum += hbuf[i] * dequant_one(W->qd, W->sd, W->sd, row, I, G, i);"),
+    ("rms_mean_over_h_minus_1", "const double inv = 1.0 / sqrt(ss / (double)H + eps);",
+     "const double inv = 1.0 / sqrt(ss / (double)(H - 1) + eps);"),
+    ("rms_eps_dropped", "const double inv = 1.0 / sqrt(ss / (double)H + eps);",
+     "const double inv = 1.0 / sqrt(ss / (double)H);"),
+    ("norm_weight_ignored", "x[o + k] = bf16_from_double((double)float_from_bf16(h[o + k]) * inv * (double)w[k]);",
+     "x[o + k] = bf16_from_double((double)float_from_bf16(h[o + k]) * inv);"),
+    ("residual_out_drops_h", "out[i] = bf16_from_double((double)float_from_bf16(h[i]) + y[i]);",
+     "out[i] = bf16_from_double(y[i]);"),
+    ("double_rounding_to_bf16", "return bf16_from_float((float)ldexp(r, e - 8));",
+     "return bf16_from_float((float)v);"),
 ]
 
 

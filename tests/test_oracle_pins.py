@@ -330,3 +330,100 @@ def test_gated_shared_expert_scales_only_the_shared_part():
         c = out["shared_w"][:, None]
         np.testing.assert_allclose(out["y"], none + c * (one - none), rtol=1e-9, atol=1e-12)
     assert np.all(out["shared_w"] == 0.5)
+
+
+# ------------------------------------------- steps either side of the layer
+
+def _bits(vals):
+    return torch.tensor(vals, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _floats(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).float().numpy()
+
+
+def test_residual_add_rounds_to_nearest_even():
+    # 1 + 2^-9 (a quarter ulp) and 1 + 2^-8 (a tie, even neighbour below) stay
+    # 1; (1 + 2^-7) + 2^-8 is a tie whose even neighbour is 1 + 2^-6
+    a = np.array([[0x3F80, 0x3F80, 0x3F81]], np.uint16)
+    r = np.array([[0x3B00, 0x3B80, 0x3B80]], np.uint16)
+    h, _ = oracle.residual_rmsnorm(a, r, np.ones(3, np.float32), 0.0)
+    assert h.tolist() == [[0x3F80, 0x3F80, 0x3F82]]
+
+
+def test_rmsnorm_worked_example():
+    # h = (3, 4): mean square 12.5, x = (3, 4) / sqrt(12.5) = (0.84853, 1.13137),
+    # to bf16: 0.84765625 (0x3F59) and 1.1328125 (0x3F91)
+    h, x = oracle.residual_rmsnorm(_bits([[3.0, 4.0]]), _bits([[0.0, 0.0]]), np.ones(2, np.float32), 0.0)
+    assert h.tolist() == [[0x4040, 0x4080]]
+    assert x.tolist() == [[0x3F59, 0x3F91]]
+    # alternating signs of one magnitude: the RMS is that magnitude, x = w
+    w = np.array([0.5, -2.0, 3.0, 0.25], np.float32)
+    _, x = oracle.residual_rmsnorm(_bits([[6.0, -6.0, 6.0, -6.0]]), _bits([[0.0] * 4]), w, 0.0)
+    assert np.array_equal(_floats(x)[0], w * np.array([1, -1, 1, -1], np.float32))
+
+
+def test_rmsnorm_against_torch_and_invariants():
+    g = torch.Generator().manual_seed(41)
+    T, H = 6, 512
+    a = _bits(torch.randn(T, H, generator=g).numpy())
+    r = _bits((torch.randn(T, H, generator=g) * 0.5).numpy())
+    w = (torch.rand(H, generator=g) + 0.5).numpy().astype(np.float32)
+    eps = 1e-6
+    h, x = oracle.residual_rmsnorm(a, r, w, eps)
+    # residual: the fp32 sum of the two bf16 values, rounded by torch
+    hv = torch.from_numpy(_floats(a)) + torch.from_numpy(_floats(r))
+    assert np.array_equal(h, hv.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16))
+    # norm: float64 torch reference (its bf16 cast goes through fp32, so a rare
+    # element may differ by one ulp from the oracle's single rounding)
+    hd = torch.from_numpy(_floats(h)).double()
+    ref = hd / torch.sqrt((hd * hd).mean(dim=1, keepdim=True) + eps) * torch.from_numpy(w).double()
+    ref_bits = ref.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    diff = np.abs(x.astype(np.int32) - ref_bits.astype(np.int32))
+    assert diff.max() <= 1 and (diff > 0).mean() < 1e-3
+    # doubling h changes nothing (eps = 0); doubling w doubles x exactly
+    _, x1 = oracle.residual_rmsnorm(h, np.zeros_like(h), w, 0.0)
+    _, x2 = oracle.residual_rmsnorm(_bits(2 * _floats(h)), np.zeros_like(h), w, 0.0)
+    assert np.array_equal(x1, x2)
+    _, x3 = oracle.residual_rmsnorm(h, np.zeros_like(h), 2 * w, 0.0)
+    assert np.array_equal(_floats(x3), 2 * _floats(x1))
+
+
+def test_rmsnorm_eps_dominates_a_tiny_row():
+    # h = 2^-10 everywhere, eps = 1: x = 2^-10 / sqrt(1 + 2^-20), which rounds to 2^-10
+    c = np.float32(2.0 ** -10)
+    _, x = oracle.residual_rmsnorm(_bits([[c] * 8]), _bits([[0.0] * 8]), np.ones(8, np.float32), 1.0)
+    assert np.array_equal(_floats(x)[0], np.full(8, c, np.float32))
+    # without eps the same row normalises to 1
+    _, x = oracle.residual_rmsnorm(_bits([[c] * 8]), _bits([[0.0] * 8]), np.ones(8, np.float32), 0.0)
+    assert np.array_equal(_floats(x)[0], np.ones(8, np.float32))
+
+
+def test_residual_out_adds_h_and_rounds_once():
+    h = _bits([[1.0, 1.0, 1.0, -2.0]])
+    y = np.array([[2.0 ** -9, 3 * 2.0 ** -9, -1.0, 0.5]])
+    out = oracle.residual_out(h, y)
+    # 1 + 2^-9 -> 1; 1 + 3 * 2^-9 -> 1 + 2^-7; 1 - 1 -> 0; -2 + 0.5 -> -1.5
+    assert out.tolist() == [[0x3F80, 0x3F81, 0x0000, 0xBFC0]]
+    # just above a tie: 1 + 2^-8 + 2^-30 rounds up to 1 + 2^-7 when rounded
+    # once (through fp32 it would become the tie 1 + 2^-8 and then 1)
+    assert oracle.residual_out(_bits([[1.0]]), np.array([[2.0 ** -8 + 2.0 ** -30]])).tolist() == [[0x3F81]]
+
+
+def test_block_with_zero_experts_is_the_residual_stream():
+    # all expert weights zero: the layer adds nothing, out is h bit for bit
+    cfg = synthetic.CONFIGS["tiny"]
+    L = synthetic.make_layer(cfg)
+    zero = oracle.quantize_stack(np.zeros_like(L.w_gate.numpy()), cfg.group)
+    zdown = oracle.quantize_stack(np.zeros_like(L.w_down.numpy()), cfg.group)
+    g = torch.Generator().manual_seed(5)
+    a = _bits(torch.randn(cfg.T, cfg.H, generator=g).numpy())
+    r = _bits(torch.randn(cfg.T, cfg.H, generator=g).numpy())
+    w = np.ones(cfg.H, np.float32)
+    blk = oracle.moe_block(a, r, w, 1e-6, L.router_w.numpy(), None, zero, zero, zdown, cfg.E, cfg.k, True)
+    assert np.array_equal(blk["out"], blk["h"])
+    # and with the real experts, out - h is the layer on the normalised input
+    gate, up, down = (oracle.quantize_stack(m.numpy(), cfg.group) for m in (L.w_gate, L.w_up, L.w_down))
+    blk = oracle.moe_block(a, r, w, 1e-6, L.router_w.numpy(), None, gate, up, down, cfg.E, cfg.k, True)
+    plain = oracle.moe_layer(blk["x"], L.router_w.numpy(), None, gate, up, down, cfg.E, cfg.k, True)
+    assert np.array_equal(blk["out"], oracle.residual_out(blk["h"], plain["y"]))
