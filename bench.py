@@ -446,7 +446,27 @@ def run_small_batches(pk, sizes=(1, 2, 4, 8), steps=10):
                               "speedup_vs_moe_prefill": round(ms / ms_b, 2)}
     via_batch["note"] = ("moe_decode_batch on the same layer and tokens; experts touched counted from the same "
                          "tokens' moe_prefill routing")
-    del flush, ws, layer, x
+    # the decoder-block forms (residual add + RMS norm before the layer, the
+    # residual add after it) against the plain layer on the same tokens
+    g = torch.Generator(device="cuda").manual_seed(7)
+    resid = (torch.randn(x.shape, generator=g, device="cuda") * 0.5).to(torch.bfloat16)
+    norm_w = torch.rand(cfg.H, generator=g, device="cuda") + 0.5
+    wsb = layer.workspace(cfg.T)
+    yb = torch.empty_like(x)
+    block = {}
+    ms_plain = time_graph(lambda: _lib.moe_prefill(layer.desc, x, cfg.T, yb, wsb.buf), "prefill T=512")
+    ms_blk = time_graph(lambda: _lib.moe_prefill_block(layer.desc, x, resid, norm_w, 1e-6, yb, wsb.buf),
+                        "prefill block T=512")
+    block[f"prefill_T{cfg.T}"] = {"ms_plain": round(ms_plain, 4), "ms_block": round(ms_blk, 4),
+                                  "added_ms": round(ms_blk - ms_plain, 4)}
+    x8, r8, y8 = x[:8].contiguous(), resid[:8].contiguous(), torch.empty_like(x[:8])
+    ms_plain = time_graph(lambda: _lib.moe_decode_batch(layer.desc, x8, y8, wsb.buf), "decode_batch B=8")
+    ms_blk = time_graph(lambda: _lib.moe_decode_batch_block(layer.desc, x8, r8, norm_w, 1e-6, y8, wsb.buf),
+                        "decode_batch block B=8")
+    block["decode_batch_B8"] = {"ms_plain": round(ms_plain, 4), "ms_block": round(ms_blk, 4),
+                                "added_ms": round(ms_blk - ms_plain, 4)}
+    via_batch["decoder_block"] = block
+    del flush, ws, wsb, layer, x
     torch.cuda.empty_cache()
     return via_prefill, via_batch
 

@@ -133,8 +133,9 @@ typedef struct {
     int32_t tile_size;   /* rows per tile (tokens per grouped-GEMM block) */
 } moe_routing_views;
 
-/* Workspace bytes for moe_prefill with up to T_max tokens, for moe_decode
- * and for moe_decode_batch; 0 if the shape is unsupported.  The workspace must be
+/* Workspace bytes for moe_prefill (and moe_prefill_block) with up to T_max
+ * tokens, for moe_decode and for moe_decode_batch (and its block form); 0 if
+ * the shape is unsupported.  The workspace must be
  * zero-filled once before first use (moe_workspace_init does it). */
 size_t moe_workspace_bytes(const moe_layer_desc *desc, int32_t T_max);
 
@@ -202,6 +203,27 @@ int moe_decode_layers(const moe_layer_desc *descs, int32_t n_layers, const void 
  */
 int moe_decode_batch(const moe_layer_desc *desc, const void *x, int32_t B, void *y, void *ws, size_t ws_bytes,
                      cudaStream_t stream);
+
+/*
+ * The layer inside a pre-norm decoder block: the residual add and RMS norm
+ * before it and the residual add after it (the pages name the model,
+ * Qwen3.6-35B-A3B, not its norm; this is the plainest reading of the steps
+ * either side of its MoE sub-layer):
+ *   h   = bf16(attn + residual)                    residual stream, fp32 add
+ *   x   = bf16(h / sqrt(mean(h^2) + eps) * norm_w) fp32 statistics per token
+ *   out = bf16(MoE(x) + h)                         the layer's fp32 output sum
+ *                                                  and h, rounded once
+ * attn, residual, out: [T][H] bf16 (device); norm_w: [H] fp32 (device,
+ * 16-byte aligned); eps >= 0 (else MOE_ERR_SHAPE).  out may be the same
+ * buffer as attn or residual.  h and x live in the workspace after the
+ * layer's own tables (moe_workspace_bytes covers them).  The prefill form
+ * writes out in place of the layer's bf16 conversion; the small-batch form
+ * (1 <= B <= 8, H <= 4096) adds h in its combine.
+ */
+int moe_prefill_block(const moe_layer_desc *desc, const void *attn, const void *residual, const float *norm_w,
+                      float eps, int32_t T, void *out, void *ws, size_t ws_bytes, cudaStream_t stream);
+int moe_decode_batch_block(const moe_layer_desc *desc, const void *attn, const void *residual, const float *norm_w,
+                           float eps, int32_t B, void *out, void *ws, size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Routing only, from given fp32 logits [T][E]: top-k and weights, histogram,

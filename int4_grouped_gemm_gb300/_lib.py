@@ -62,6 +62,8 @@ SIGNATURES = {
     "moe_decode": (ctypes.c_int, [c_p, c_p, c_p, c_p, c_sz, c_p]),
     "moe_decode_layers": (ctypes.c_int, [c_p, c_i32, c_p, c_p, c_p, c_sz, c_p]),
     "moe_decode_batch": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_sz, c_p]),
+    "moe_prefill_block": (ctypes.c_int, [c_p, c_p, c_p, c_p, ctypes.c_float, c_i32, c_p, c_p, c_sz, c_p]),
+    "moe_decode_batch_block": (ctypes.c_int, [c_p, c_p, c_p, c_p, ctypes.c_float, c_i32, c_p, c_p, c_sz, c_p]),
     "moe_decode_static_scratch": (ctypes.c_int, [c_p, c_p, c_p, c_p]),
     "moe_route_logits": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_sz, c_p]),
     "pack_int4": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_p]),
@@ -151,6 +153,20 @@ def moe_decode_batch(desc: moe_layer_desc, x, y, ws, stream=None):
     """x, y: [B][H] bf16 with 1 <= B <= 8."""
     _check(load().moe_decode_batch(ctypes.byref(desc), _ptr(x), x.shape[0], _ptr(y), _ptr(ws),
                                    ws.numel() * ws.element_size(), _stream(stream)), "moe_decode_batch")
+
+
+def moe_prefill_block(desc: moe_layer_desc, attn, residual, norm_w, eps, out, ws, stream=None):
+    """out = bf16(MoE(RMSNorm(attn + residual) * norm_w) + (attn + residual))."""
+    _check(load().moe_prefill_block(ctypes.byref(desc), _ptr(attn), _ptr(residual), _ptr(norm_w), float(eps),
+                                    attn.shape[0], _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                    _stream(stream)), "moe_prefill_block")
+
+
+def moe_decode_batch_block(desc: moe_layer_desc, attn, residual, norm_w, eps, out, ws, stream=None):
+    """The decoder-block form of moe_decode_batch (1 to 8 tokens)."""
+    _check(load().moe_decode_batch_block(ctypes.byref(desc), _ptr(attn), _ptr(residual), _ptr(norm_w), float(eps),
+                                         attn.shape[0], _ptr(out), _ptr(ws), ws.numel() * ws.element_size(),
+                                         _stream(stream)), "moe_decode_batch_block")
 
 
 def moe_decode_layers(descs, x, y, ws, stream=None):

@@ -5,6 +5,7 @@
 
 #include <mutex>
 
+#include "block.cuh"
 #include "kernels.cuh"
 #include "small_batch.cuh"
 
@@ -150,6 +151,17 @@ static int static_scratch(char *&out) {
     return MOE_OK;
 }
 
+// The residual stream h and the normalised layer input x of a decoder-block
+// call ([T][H] bf16 each), placed after the layer's own workspace.
+static size_t block_bytes(int T, int H) { return 2 * align_up(static_cast<size_t>(T) * H * 2, 256); }
+
+static int check_block(const void *attn, const void *residual, const float *norm_w, float eps) {
+    int rc;
+    if ((rc = check_ptr(attn)) || (rc = check_ptr(residual)) || (rc = check_ptr(norm_w))) return rc;
+    if (!(eps >= 0.0f) || !(eps < 1e30f)) return MOE_ERR_SHAPE;
+    return MOE_OK;
+}
+
 extern "C" {
 
 size_t moe_workspace_bytes(const moe_layer_desc *desc, int32_t T_max) {
@@ -157,8 +169,10 @@ size_t moe_workspace_bytes(const moe_layer_desc *desc, int32_t T_max) {
     const PrefillLayout P = prefill_layout(T_max, desc->E, desc->k, desc->H, desc->I);
     const DecodeLayout D = decode_stack_layout(desc->E, desc->k, desc->H, desc->I);
     const BatchLayout Bt = batch_layout(desc->E, desc->k, desc->H, desc->I);
-    size_t total = P.total > D.total ? P.total : D.total;
-    return total > Bt.total ? total : Bt.total;
+    const size_t p = P.total + block_bytes(T_max, desc->H);
+    const size_t b = Bt.total + block_bytes(kBatchMax, desc->H);
+    size_t total = p > D.total ? p : D.total;
+    return total > b ? total : b;
 }
 
 int moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
@@ -212,7 +226,7 @@ int moe_route_logits(const moe_layer_desc *desc, const float *logits, int32_t T,
 }
 
 static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
-                        cudaEvent_t *events, cudaStream_t stream) {
+                        cudaEvent_t *events, const __nv_bfloat16 *resid, cudaStream_t stream) {
     int rc = check_shape(desc);
     if (rc) return rc;
     if ((rc = check_weights(desc))) return rc;
@@ -314,21 +328,46 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     ga.n_ntiles = H / 256;
     if (launch_gemm(1, m2, ga, grid_for(L.max_tiles * ga.n_ntiles), stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(events, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_convert(y_acc, static_cast<__nv_bfloat16 *>(y), static_cast<int64_t>(T) * H, dev->num_sms, stream) !=
-        cudaSuccess)
-        return MOE_ERR_CUDA;
+    // y = bf16 of the fp32 combine, or for a decoder block bf16(combine + h)
+    const cudaError_t ce =
+        resid ? launch_residual_out(y_acc, resid, static_cast<__nv_bfloat16 *>(y), static_cast<int64_t>(T) * H,
+                                    dev->num_sms, stream)
+              : launch_convert(y_acc, static_cast<__nv_bfloat16 *>(y), static_cast<int64_t>(T) * H, dev->num_sms,
+                               stream);
+    if (ce != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(events, 5, stream) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
 }
 
 int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
                 cudaStream_t stream) {
-    return prefill_impl(desc, x, T, y, ws, ws_bytes, nullptr, stream);
+    return prefill_impl(desc, x, T, y, ws, ws_bytes, nullptr, nullptr, stream);
 }
 
 int moe_prefill_profiled(const moe_layer_desc *desc, const void *x, int32_t T, void *y, void *ws, size_t ws_bytes,
                          cudaEvent_t *events, cudaStream_t stream) {
-    return prefill_impl(desc, x, T, y, ws, ws_bytes, events, stream);
+    return prefill_impl(desc, x, T, y, ws, ws_bytes, events, nullptr, stream);
+}
+
+int moe_prefill_block(const moe_layer_desc *desc, const void *attn, const void *residual, const float *norm_w,
+                      float eps, int32_t T, void *out, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    int rc = check_shape(desc);
+    if (rc) return rc;
+    if ((rc = check_weights(desc))) return rc;
+    if ((rc = check_block(attn, residual, norm_w, eps)) || (rc = check_ptr(out)) || (rc = check_ptr(ws))) return rc;
+    if ((rc = check_tokens(desc, T))) return rc;
+    const PrefillLayout L = prefill_layout(T, desc->E, desc->k, desc->H, desc->I);
+    const size_t off = align_up(L.total, 256);
+    if (ws_bytes < off + block_bytes(T, desc->H)) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    char *w = static_cast<char *>(ws);
+    __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(w + off);
+    __nv_bfloat16 *x = reinterpret_cast<__nv_bfloat16 *>(w + off + block_bytes(T, desc->H) / 2);
+    if (launch_residual_rmsnorm(static_cast<const __nv_bfloat16 *>(attn), static_cast<const __nv_bfloat16 *>(residual),
+                                norm_w, eps, T, desc->H, h, x, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return prefill_impl(desc, x, T, out, ws, ws_bytes, nullptr, h, stream);
 }
 
 static int decode_check(const moe_layer_desc *desc) {
@@ -407,17 +446,10 @@ int moe_decode(const moe_layer_desc *desc, const void *x, void *y, void *ws, siz
     return decode_run(desc, 1, x, y, static_cast<char *>(ws), L, dev->num_sms, stream);
 }
 
-int moe_decode_batch(const moe_layer_desc *desc, const void *x, int32_t B, void *y, void *ws, size_t ws_bytes,
-                     cudaStream_t stream) {
-    int rc = decode_check(desc);
-    if (rc) return rc;
-    if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
-    if (B < 1 || B > kBatchMax) return MOE_ERR_TOKENS;
-    const BatchLayout L = batch_layout(desc->E, desc->k, desc->H, desc->I);
-    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
-    DeviceInfo *dev = nullptr;
-    if ((rc = current_device(dev))) return rc;
-    char *w = static_cast<char *>(ws);
+// The small-batch layer on x (device, [B][H]); resid, if given, is added to
+// the output before its rounding.  Arguments already checked.
+static int batch_run(const moe_layer_desc *desc, const void *x, int32_t B, void *y, const __nv_bfloat16 *resid,
+                     char *w, const BatchLayout &L, int num_sms, cudaStream_t stream) {
     BatchArgs a{};
     a.E = desc->E;
     a.k = desc->k;
@@ -432,6 +464,7 @@ int moe_decode_batch(const moe_layer_desc *desc, const void *x, int32_t B, void 
     a.S_max = L.S_max;
     a.x = static_cast<const __nv_bfloat16 *>(x);
     a.y = static_cast<__nv_bfloat16 *>(y);
+    a.resid = resid;
     a.Wr = desc->router_w;
     a.bias = desc->router_bias;
     a.shg = desc->shared_gate;
@@ -450,7 +483,40 @@ int moe_decode_batch(const moe_layer_desc *desc, const void *x, int32_t B, void 
     a.slot_w = reinterpret_cast<float *>(w + L.slot_w);
     a.h = reinterpret_cast<__nv_bfloat16 *>(w + L.h);
     a.o = reinterpret_cast<float *>(w + L.o);
-    return cuda_rc(launch_batch(a, dev->num_sms, stream));
+    return cuda_rc(launch_batch(a, num_sms, stream));
+}
+
+int moe_decode_batch(const moe_layer_desc *desc, const void *x, int32_t B, void *y, void *ws, size_t ws_bytes,
+                     cudaStream_t stream) {
+    int rc = decode_check(desc);
+    if (rc) return rc;
+    if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
+    if (B < 1 || B > kBatchMax) return MOE_ERR_TOKENS;
+    const BatchLayout L = batch_layout(desc->E, desc->k, desc->H, desc->I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    return batch_run(desc, x, B, y, nullptr, static_cast<char *>(ws), L, dev->num_sms, stream);
+}
+
+int moe_decode_batch_block(const moe_layer_desc *desc, const void *attn, const void *residual, const float *norm_w,
+                           float eps, int32_t B, void *out, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    int rc = decode_check(desc);
+    if (rc) return rc;
+    if ((rc = check_block(attn, residual, norm_w, eps)) || (rc = check_ptr(out)) || (rc = check_ptr(ws))) return rc;
+    if (B < 1 || B > kBatchMax) return MOE_ERR_TOKENS;
+    const BatchLayout L = batch_layout(desc->E, desc->k, desc->H, desc->I);
+    const size_t off = align_up(L.total, 256);
+    if (ws_bytes < off + block_bytes(kBatchMax, desc->H)) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    char *w = static_cast<char *>(ws);
+    __nv_bfloat16 *h = reinterpret_cast<__nv_bfloat16 *>(w + off);
+    __nv_bfloat16 *x = reinterpret_cast<__nv_bfloat16 *>(w + off + block_bytes(kBatchMax, desc->H) / 2);
+    if (launch_residual_rmsnorm(static_cast<const __nv_bfloat16 *>(attn), static_cast<const __nv_bfloat16 *>(residual),
+                                norm_w, eps, B, desc->H, h, x, stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return batch_run(desc, x, B, out, h, w, L, dev->num_sms, stream);
 }
 
 int moe_decode_layers(const moe_layer_desc *descs, int32_t n_layers, const void *x, void *y, void *ws,

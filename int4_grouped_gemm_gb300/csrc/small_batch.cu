@@ -21,7 +21,8 @@
 //   batch_down_kernel     per (group of 1-4 slots, 16 rows of H): each slot's
 //                         down rows times its h, weighted by the slot's
 //                         per-token weight and summed in slot order -> fp32
-//   batch_combine_kernel  y[t] = bf16(sum of the slot groups, in order)
+//   batch_combine_kernel  y[t] = bf16(sum of the slot groups, in order, and
+//                         for a decoder block the residual stream)
 // The contraction has N = 8, so these kernels are bound by the weight bytes,
 // not by the tensor pipe: mma.sync only keeps the arithmetic off the ALUs.
 // Weights stream through a per-warp ring of cp.async stages in shared memory
@@ -592,7 +593,8 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_down_kernel(BatchArgs a) 
 
 // ----------------------------------------------------------------- combine
 
-// y[t][f] = bf16(sum over the slot groups, in order, of their partial sums)
+// y[t][f] = bf16(sum over the slot groups, in order, of their partial sums
+// [+ the residual stream's h[t][f]])
 __global__ void __launch_bounds__(256) batch_combine_kernel(BatchArgs a) {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.B * a.H) return;
@@ -604,6 +606,7 @@ __global__ void __launch_bounds__(256) batch_combine_kernel(BatchArgs a) {
     float acc = 0.f;
 #pragma unroll 4
     for (int j = 0; j < ngrp; ++j) acc += op[j * ostride];
+    if (a.resid) acc += __bfloat162float(a.resid[i]);
     a.y[i] = __float2bfloat16_rn(acc);
 }
 

@@ -52,6 +52,7 @@ struct BatchArgs {
     int E, k, H, I, G, B, has_shared, no_renorm, ldg_h, ldg_i, S_max;
     const __nv_bfloat16 *x;  // [B][H]
     __nv_bfloat16 *y;        // [B][H]
+    const __nv_bfloat16 *resid;  // [B][H] residual stream added to y before rounding, or nullptr
     const float *Wr;         // [E][H]
     const float *bias;       // [E] or nullptr
     const float *shg;        // [H] shared-expert gate or nullptr

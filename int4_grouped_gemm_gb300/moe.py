@@ -94,6 +94,22 @@ class PackedLayer:
         _lib.moe_decode(self.desc, x, y, ws.buf, stream)
         return y
 
+    def prefill_block(self, attn: torch.Tensor, residual: torch.Tensor, norm_w: torch.Tensor, ws: "Workspace",
+                      eps: float = 1e-6, out: Optional[torch.Tensor] = None, stream=None):
+        """The layer in a pre-norm decoder block: out = MoE(RMSNorm(h) w) + h, h = attn + residual."""
+        if out is None:
+            out = torch.empty_like(attn)
+        _lib.moe_prefill_block(self.desc, attn, residual, norm_w, eps, out, ws.buf, stream)
+        return out
+
+    def decode_batch_block(self, attn: torch.Tensor, residual: torch.Tensor, norm_w: torch.Tensor, ws: "Workspace",
+                           eps: float = 1e-6, out: Optional[torch.Tensor] = None, stream=None):
+        """prefill_block for 1 to 8 tokens through the small-batch path."""
+        if out is None:
+            out = torch.empty_like(attn)
+        _lib.moe_decode_batch_block(self.desc, attn, residual, norm_w, eps, out, ws.buf, stream)
+        return out
+
     def decode_batch(self, x: torch.Tensor, ws: "Workspace", y: Optional[torch.Tensor] = None, stream=None):
         """1 to 8 tokens: each picked expert is read once for all of them."""
         if y is None:

@@ -135,3 +135,26 @@ def test_small_batch_decode_checks_on_the_host(lib):
     assert f(ctypes.byref(wide), x, 4, y, ws, 1 << 30, None) == _lib.MOE_ERR_SHAPE
     bad = _lib.moe_layer_desc(256, 9, 2048, 512, 64, 1, 1024, None, q, q, q)
     assert f(ctypes.byref(bad), x, 4, y, ws, n, None) == _lib.MOE_ERR_SHAPE
+
+
+def test_decoder_block_checks_on_the_host(lib):
+    from int4_grouped_gemm_gb300 import _lib
+    q = _lib.moe_qweight(256, 512, 768)
+    d = _lib.moe_layer_desc(256, 8, 2048, 512, 64, 1, 1024, None, q, q, q)
+    a, r, w, out, ws = (ctypes.c_void_p(v) for v in (2048, 4096, 8192, 16384, 32768))
+    n = _lib.moe_workspace_bytes(d, 16)
+    # the residual stream and the normalised input ([T][H] bf16 each) come
+    # after the layer's own tables, the last of which follow y_acc
+    v = _lib.moe_routing_views_for(d, 16)
+    assert n >= v.y_acc + 16 * 2048 * 4 + 2 * 16 * 2048 * 2
+    for f, T in ((lib.moe_prefill_block, 16), (lib.moe_decode_batch_block, 4)):
+        assert f(ctypes.byref(d), a, r, w, ctypes.c_float(-1.0), T, out, ws, n, None) == _lib.MOE_ERR_SHAPE
+        assert f(ctypes.byref(d), a, r, w, ctypes.c_float(float("nan")), T, out, ws, n, None) == _lib.MOE_ERR_SHAPE
+        assert f(ctypes.byref(d), a, r, ctypes.c_void_p(8196), ctypes.c_float(1e-6), T, out, ws, n, None) == \
+            _lib.MOE_ERR_ALIGN
+        assert f(ctypes.byref(d), a, None, w, ctypes.c_float(1e-6), T, out, ws, n, None) == _lib.MOE_ERR_NULL
+        assert f(ctypes.byref(d), a, r, w, ctypes.c_float(1e-6), T, out, ws, 4096, None) == _lib.MOE_ERR_WORKSPACE
+    assert lib.moe_decode_batch_block(ctypes.byref(d), a, r, w, ctypes.c_float(1e-6), 9, out, ws, n, None) == \
+        _lib.MOE_ERR_TOKENS
+    assert lib.moe_prefill_block(ctypes.byref(d), a, r, w, ctypes.c_float(1e-6), 0, out, ws, n, None) == \
+        _lib.MOE_ERR_TOKENS
