@@ -7,6 +7,7 @@
 
 #include "block.cuh"
 #include "kernels.cuh"
+#include "routing_ext.cuh"
 #include "small_batch.cuh"
 
 
@@ -303,19 +304,19 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
 
     cudaError_t e = mark(events, 0, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    // router: bf16 split of the weights (and clearing of the combine
-    // accumulator and histogram), then the eight partial router GEMMs on the
-    // tensor cores
-    if (launch_prep(desc->router_w, E, L.E_pad16, H, wr3, y_acc, static_cast<int64_t>(T) * H, rb.counts_blk,
-                    static_cast<int64_t>(rb.nblk) * E, dev->num_sms, stream) != cudaSuccess)
+    // router: bf16 split of the weights (and clearing of the histogram), then
+    // the eight partial router GEMMs on the tensor cores
+    if (launch_prep(desc->router_w, E, L.E_pad16, H, wr3, y_acc, 0, rb.counts_blk, static_cast<int64_t>(rb.nblk) * E,
+                    dev->num_sms, stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     ga.K = H;
     if (launch_gemm(2, mr, ga, grid_for(router_units(T)), stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(events, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    // routing tables
+    // routing tables; the top-k kernel clears the fp32 combine accumulator
+    // on the side
     const RouteOpts ropts{static_cast<const __nv_bfloat16 *>(x), desc->shared_gate, H, desc->no_renorm};
-    if (launch_routing_tables(logits_part, L.E_pad16, nullptr, desc->router_bias, T, E, k, desc->has_shared, ropts, rb,
-                              stream) != cudaSuccess)
+    if (launch_routing_tables_clearing(logits_part, L.E_pad16, desc->router_bias, T, E, k, desc->has_shared, ropts, rb,
+                                       y_acc, static_cast<int64_t>(T) * H, stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (mark(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
     // gate/up + SwiGLU

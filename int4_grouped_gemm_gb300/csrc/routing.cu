@@ -18,6 +18,7 @@
 // Every table is deterministic: counts and ranks come from per-block counts
 // scanned in token order, never from the order in which atomics land.
 #include "kernels.cuh"
+#include "routing_ext.cuh"
 #include "topk.cuh"
 
 namespace moe {
@@ -31,13 +32,20 @@ namespace moe {
 constexpr int kTopkWarps = 4;
 static_assert(kRouteChunk % kTopkWarps == 0, "a top-k block stays within one chunk");
 
+//
+// clear / clear_n4: a buffer the kernel zeroes on the side (the fp32 combine
+// accumulator of the prefill, 16-byte pieces, grid-strided): the kernel waits
+// on its loads, so the stores ride along.
 __global__ void __launch_bounds__(kTopkWarps * 32)
     topk_hist_kernel(const float *__restrict__ logits_part, int ld, const float *__restrict__ given,
                      const float *__restrict__ bias, int T, int E, int k, int has_shared, RouteOpts opts,
-                     RoutingBufs rb) {
+                     RoutingBufs rb, float4 *__restrict__ clear, int64_t clear_n4) {
     __shared__ int hist[256];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     for (int e = tid; e < 256; e += blockDim.x) hist[e] = 0;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid; i < clear_n4;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        clear[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     __syncthreads();
 
     const int t = blockIdx.x * kTopkWarps + warp;
@@ -334,13 +342,27 @@ cudaError_t launch_zero_i32(int *p, int64_t n, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-cudaError_t launch_routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
+static cudaError_t routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
                                   int E, int k, int has_shared, const RouteOpts &opts, const RoutingBufs &rb,
-                                  cudaStream_t s) {
-    topk_hist_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(logits_part, ld, given, bias, T, E, k, has_shared, opts, rb);
+                                  float *clear, int64_t clear_elems, cudaStream_t s) {
+    topk_hist_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(
+        logits_part, ld, given, bias, T, E, k, has_shared, opts, rb, reinterpret_cast<float4 *>(clear),
+        clear_elems / 4);
     scan_tiles_kernel<<<1, 512, 0, s>>>(T, E, k, has_shared, rb);
     permute_kernel<<<rb.nblk, kPermThreads, 0, s>>>(T, E, k, rb);
     return cudaGetLastError();
+}
+
+cudaError_t launch_routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
+                                  int E, int k, int has_shared, const RouteOpts &opts, const RoutingBufs &rb,
+                                  cudaStream_t s) {
+    return routing_tables(logits_part, ld, given, bias, T, E, k, has_shared, opts, rb, nullptr, 0, s);
+}
+
+cudaError_t launch_routing_tables_clearing(const float *logits_part, int ld, const float *bias, int T, int E, int k,
+                                           int has_shared, const RouteOpts &opts, const RoutingBufs &rb, float *clear,
+                                           int64_t clear_elems, cudaStream_t s) {
+    return routing_tables(logits_part, ld, nullptr, bias, T, E, k, has_shared, opts, rb, clear, clear_elems, s);
 }
 
 }  // namespace moe
