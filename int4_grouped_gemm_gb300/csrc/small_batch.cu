@@ -14,12 +14,15 @@
 //                         union of the picked experts the slots, in expert
 //                         order, the shared expert last, with each slot's
 //                         per-token weight
-//   batch_gate_up_kernel  per (slot, 16 rows of I): gate and up rows
-//                         dequantised in registers as the M = 16 operand of
-//                         mma.sync m16n8k16 bf16 -> fp32, the B tokens
-//                         (zero-padded to 8) as N; h = bf16(silu(g) * u)
+//   batch_gate_up_kernel  per (slot, 16 rows of I): the codes of the gate and
+//                         up rows (128 + q, exact in bf16) as the M = 16
+//                         operand of mma.sync m16n8k16 bf16 -> fp32, the B
+//                         tokens (zero-padded to 8) as N, scale and bias
+//                         applied per group after the MMAs;
+//                         h = bf16(silu(g) * u)
 //   batch_down_kernel     per (group of 1-4 slots, 16 rows of H): each slot's
-//                         down rows times its h, weighted by the slot's
+//                         down rows, dequantised in registers, times its h
+//                         (mma.sync as above), weighted by the slot's
 //                         per-token weight and summed in slot order -> fp32
 //   batch_combine_kernel  y[t] = bf16(sum of the slot groups, in order, and
 //                         for a decoder block the residual stream)
@@ -46,12 +49,13 @@ namespace moe {
 constexpr int kSbWarps = 16;  // warps per block of the streaming kernels (one block per SM)
 constexpr int kSbThreads = kSbWarps * 32;
 constexpr int kSbStages = 8;  // cp.async stages per warp
-// gate/up stage: [2 matrices][16 rows][4 threads] x 8 B of nibbles, then
-// [2 matrices][16 rows] x (4 B scale pair, 4 B bias pair)
+// gate/up stage: [2 matrices][16 rows] x 32 B of nibbles (the chunk's 8
+// words of each row), then [2 matrices][16 rows] x (4 B scale pair, 4 B bias
+// pair)
 constexpr int kGuQ = 2 * 16 * 32;
 constexpr int kGuStage = kGuQ + 2 * 16 * 8;
-// down stage: [16 rows][4 threads] x 8 B of nibbles, [16 rows] x (scale pair,
-// bias pair), then [32 lanes] x 32 B of the slot's h (token g, K = 16c ..)
+// down stage: [16 rows] x 32 B of nibbles, [16 rows] x (scale pair, bias
+// pair), then [32 lanes] x 32 B of the slot's h (token g, K = 16c ..)
 constexpr int kDnQ = 16 * 32;
 constexpr int kDnH = kDnQ + 16 * 8;
 constexpr int kDnStage = kDnH + 32 * 32;
