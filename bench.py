@@ -526,9 +526,12 @@ def oracle_sample(cfg, n_tokens, seed=0):
     """Oracle inputs for a bounded sample of the workload: host copies of the
     seeded fp32 weights, quantised by the oracle, and n sampled tokens."""
     import numpy as np
+    import torch
     import oracle
     from int4_grouped_gemm_gb300 import synthetic
-    L = synthetic.make_layer(cfg, device="cuda")
+    # the GPU path's own draw where there is a GPU (the CPU generator draws
+    # other values of the same distributions; timing does not depend on them)
+    L = synthetic.make_layer(cfg, device="cuda" if torch.cuda.is_available() else "cpu")
     stacks = tuple(oracle.quantize_stack(getattr(L, n).cpu().numpy(), cfg.group)
                    for n in ("w_gate", "w_up", "w_down"))
     xb = synthetic.bf16_bits(L.x.cpu()).numpy().view(np.uint16)
