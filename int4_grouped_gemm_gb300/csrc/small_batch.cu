@@ -46,22 +46,7 @@
 
 namespace moe {
 
-constexpr int kSbWarps = 16;  // warps per block of the streaming kernels (one block per SM)
-constexpr int kSbThreads = kSbWarps * 32;
-constexpr int kSbStages = 8;  // cp.async stages per warp
-// gate/up stage: [2 matrices][16 rows] x 32 B of nibbles (the chunk's 8
-// words of each row), then [2 matrices][16 rows] x (4 B scale pair, 4 B bias
-// pair)
-constexpr int kGuQ = 2 * 16 * 32;
-constexpr int kGuStage = kGuQ + 2 * 16 * 8;
-// down stage: [16 rows] x 32 B of nibbles, [16 rows] x (scale pair, bias
-// pair), then [32 lanes] x 32 B of the slot's h (token g, K = 16c ..)
-constexpr int kDnQ = 16 * 32;
-constexpr int kDnH = kDnQ + 16 * 8;
-constexpr int kDnStage = kDnH + 32 * 32;
-constexpr int kSmemMax = 227 * 1024;
 
-__host__ __device__ inline int align16i(int v) { return (v + 15) & ~15; }
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -241,18 +226,6 @@ __device__ __forceinline__ uint32_t codes_pair(uint32_t word, int p) {
     return ((word >> (4 * p)) & 0x000F000Fu) | 0x43004300u;
 }
 
-// Shared memory of the gate/up kernel: the 8 token rows (bf16, pitch H + 8
-// so that the 8 rows fall on different banks), the slot experts, the
-// per-group token sums of x (fp32 [H/G][8]), the rings.
-__host__ __device__ inline int gu_xpitch(int H) { return H + 8; }
-__host__ __device__ inline int gu_exp_off(int H) { return kBatchMax * gu_xpitch(H) * 2; }
-__host__ __device__ inline int gu_xsum_off(int H, int S_max) { return align16i(gu_exp_off(H) + 4 * S_max); }
-__host__ __device__ inline int gu_ring_off(int H, int G, int S_max) {
-    return gu_xsum_off(H, S_max) + 4 * kBatchMax * (H / G);
-}
-inline int gu_smem(int H, int G, int S_max, int stages) {
-    return gu_ring_off(H, G, S_max) + kSbWarps * stages * kGuStage;
-}
 
 // Warp tasks (slot u, rows 16 rb .. 16 rb + 15 of I) over all K = H; the
 // warps of the grid take tasks round-robin, SM-major, so that few tasks still
@@ -451,9 +424,6 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_gate_up_kernel(BatchArgs 
 
 // -------------------------------------------------------------------- down
 
-// Shared memory of the down kernel: the slot weights [n_slots][8], then the rings.
-__host__ __device__ inline int dn_ring_off(int S_max) { return align16i(4 * kBatchMax * S_max); }
-inline int dn_smem(int S_max) { return dn_ring_off(S_max) + kSbWarps * kSbStages * kDnStage; }
 
 // Warp tasks (slot group j: slots sg j .. sg j + sg - 1, output rows 16 fb .. 16 fb
 // + 15 of H): for each slot of the group, all K = I of its down rows against
@@ -619,8 +589,7 @@ __global__ void __launch_bounds__(256) batch_combine_kernel(BatchArgs a) {
 cudaError_t launch_batch(const BatchArgs &a, int num_sms, cudaStream_t s) {
     const int rows = a.E + (a.shg ? 1 : 0);
     batch_router_kernel<<<rows, 256, 0, s>>>(a);
-    // eight stages per warp where they fit, else six (the widest H with group 32)
-    const bool deep = gu_smem(a.H, a.G, a.S_max, 8) <= kSmemMax;
+    const bool deep = gu_stages(a.H, a.G, a.S_max) == 8;
     const int gsm = gu_smem(a.H, a.G, a.S_max, deep ? 8 : 6), dsm = dn_smem(a.S_max);
     if (gsm > kSmemMax || dsm > kSmemMax) return cudaErrorInvalidValue;
     cudaError_t e;

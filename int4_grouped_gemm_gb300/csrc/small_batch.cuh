@@ -66,6 +66,45 @@ struct BatchArgs {
     float *o;
 };
 
+// Launch geometry and shared memory of the streaming kernels (one block of
+// kSbWarps warps per SM, a ring of cp.async stages per warp).
+constexpr int kSbWarps = 16;  // warps per block of the streaming kernels (one block per SM)
+constexpr int kSbThreads = kSbWarps * 32;
+constexpr int kSbStages = 8;  // cp.async stages per warp
+// gate/up stage: [2 matrices][16 rows] x 32 B of nibbles (the chunk's 8
+// words of each row), then [2 matrices][16 rows] x (4 B scale pair, 4 B bias
+// pair)
+constexpr int kGuQ = 2 * 16 * 32;
+constexpr int kGuStage = kGuQ + 2 * 16 * 8;
+// down stage: [16 rows] x 32 B of nibbles, [16 rows] x (scale pair, bias
+// pair), then [32 lanes] x 32 B of the slot's h (token g, K = 16c ..)
+constexpr int kDnQ = 16 * 32;
+constexpr int kDnH = kDnQ + 16 * 8;
+constexpr int kDnStage = kDnH + 32 * 32;
+constexpr int kSmemMax = 227 * 1024;
+
+__host__ __device__ inline int align16i(int v) { return (v + 15) & ~15; }
+
+// Shared memory of the gate/up kernel: the 8 token rows (bf16, pitch H + 8
+// so that the 8 rows fall on different banks), the slot experts, the
+// per-group token sums of x (fp32 [H/G][8]), the rings.
+__host__ __device__ inline int gu_xpitch(int H) { return H + 8; }
+__host__ __device__ inline int gu_exp_off(int H) { return kBatchMax * gu_xpitch(H) * 2; }
+__host__ __device__ inline int gu_xsum_off(int H, int S_max) { return align16i(gu_exp_off(H) + 4 * S_max); }
+__host__ __device__ inline int gu_ring_off(int H, int G, int S_max) {
+    return gu_xsum_off(H, S_max) + 4 * kBatchMax * (H / G);
+}
+inline int gu_smem(int H, int G, int S_max, int stages) {
+    return gu_ring_off(H, G, S_max) + kSbWarps * stages * kGuStage;
+}
+// Stages per warp of the gate/up kernel: eight where they fit, else six (the
+// widest H with group 32).
+inline int gu_stages(int H, int G, int S_max) { return gu_smem(H, G, S_max, 8) <= kSmemMax ? 8 : 6; }
+
+// Shared memory of the down kernel: the slot weights [n_slots][8], then the rings.
+__host__ __device__ inline int dn_ring_off(int S_max) { return align16i(4 * kBatchMax * S_max); }
+inline int dn_smem(int S_max) { return dn_ring_off(S_max) + kSbWarps * kSbStages * kDnStage; }
+
 cudaError_t launch_batch(const BatchArgs &a, int num_sms, cudaStream_t s);
 
 }  // namespace moe

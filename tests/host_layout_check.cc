@@ -2,7 +2,8 @@
 // the supported shapes: every region starts on a 256-byte boundary after the
 // previous one and is at least as large as the tables the kernels write into
 // it, the small-batch slot bound covers the union of 8 tokens' picks plus the
-// shared expert, and the down projection's slot groups fit the output buffer.
+// shared expert, the down projection's slot groups fit the output buffer,
+// and the small-batch kernels' shared memory fits the 227 KB of a block.
 // Built with the host compiler by tests/test_host_layouts.py; exits non-zero
 // and names the shape on the first violation.
 #include <cstdio>
@@ -50,6 +51,16 @@ int main() {
                                       4u * B.S_max * kBatchMax * H},
                                      B.total),
                            "small-batch regions", E, k, H, I, 0);
+                    // the streaming kernels' shared memory fits one block per SM
+                    // (small-batch calls take H <= 4096)
+                    if (H <= 4096) {
+                        for (int G : {32, 64}) {
+                            const int st = gu_stages(H, G, B.S_max);
+                            expect(gu_smem(H, G, B.S_max, st) <= kSmemMax, "gate/up shared memory", E, k, H, I, G);
+                            expect(st == 8 || H > 2048, "eight gate/up stages up to H = 2048", E, k, H, I, G);
+                        }
+                        expect(dn_smem(B.S_max) + 1024 <= kSmemMax, "down shared memory", E, k, H, I, 0);
+                    }
                     for (int n = 1; n <= B.S_max; ++n) {
                         const int sg = slot_group(n);
                         expect(sg == 1 || sg == 2 || sg == 4, "slot group size", E, k, H, I, n);
