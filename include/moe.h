@@ -257,12 +257,90 @@ int pack_int4(const float *w, int64_t rows, int32_t K, int32_t group, uint32_t *
  * anything is launched.  Other requirements are those of moe_decode.
  * Set-up: the first call on each device, with that device current, looks up
  * the array's address; make that first call before any stream capture
- * starts.  Every call clears the array's control block on `stream` before
- * the kernels run.  All calls on one device share the one array, so two
- * calls in flight at once (other streams or threads) race: issue them in
- * order on one stream.
+ * starts.  Every call clears the array's grid-barrier counter and abort flag
+ * on `stream` before the kernel runs (the rest of the scratch is written
+ * before it is read); its status word is kept until
+ * moe_read_static_scratch_status reads it.  All calls on one device share
+ * the one array, so two calls in flight at once (other streams or threads)
+ * race: issue them in order on one stream.
  */
 int moe_decode_static_scratch(const moe_layer_desc *desc, const void *x, void *y, cudaStream_t stream);
+/* (Errors of this call on the device: see moe_read_static_scratch_status.) */
+
+/*
+ * Read and clear the status word of moe_decode_static_scratch's array on the
+ * current device: synchronises `stream`, returns 0 or the first device-side
+ * error (MOE_ERR_TIMEOUT - site) that a call on this device recorded since
+ * the last read, and clears it.  Calls of moe_decode_static_scratch do not
+ * clear it themselves, so an error stays readable however many calls
+ * follow; a call whose bounded wait ran out leaves y undefined.  Returns 0
+ * when no call on this device has used the array yet.  The method has no
+ * counterpart of this call either.
+ */
+int moe_read_static_scratch_status(cudaStream_t stream);
+
+/* ------------------------------------------------------------ inspection
+ * Calls that expose what the kernels decided, for the parity tests and for
+ * profiling.  None of them is needed to run the layer.
+ */
+
+/* Time stamps: phases recorded per layer and block, and the most blocks a
+ * time trace holds (the decode kernel runs one block per SM). */
+#define MOE_DECODE_PHASES 8
+#define MOE_DECODE_TRACE_BLOCKS 256
+
+/*
+ * moe_decode_layers that also records, when the pointers are not NULL:
+ *   routing_trace  device, (E + 2k + 1) 32-bit words per layer, layer l at
+ *                  word l * (E + 2k + 1): the fp32 logits the decode kernel's
+ *                  top-k ranked (router sums plus bias, as rounded on the
+ *                  GPU), the k picked experts (int32, slot order), their k
+ *                  fp32 weights, and the shared expert's fp32 weight;
+ *   time_trace     device, uint64 [n_layers][MOE_DECODE_TRACE_BLOCKS]
+ *                  [MOE_DECODE_PHASES]: the GPU global timer (ns) of each
+ *                  block at the kernel's phase boundaries of each layer
+ *                  (0 layer start, 1 logits complete, 2 top-k done,
+ *                  3 gate/up rows done, 4 SwiGLU rows complete, 5 output
+ *                  features done, 6 next-layer router sums added; entries of
+ *                  blocks and phases that do not exist are not written).
+ * Both 16-byte aligned.  The layer results are those of moe_decode_layers.
+ * MOE_ERR_DEVICE if the GPU has more SMs than a time trace has room for.
+ */
+int moe_decode_layers_traced(const moe_layer_desc *descs, int32_t n_layers, const void *x, void *y, void *ws,
+                             size_t ws_bytes, float *routing_trace, unsigned long long *time_trace,
+                             cudaStream_t stream);
+
+/*
+ * The batch-1 decode kernel's own top-k (the sort, rank, softmax and
+ * lowest-index tie-break it runs on every layer) applied to n given rows of
+ * fp32 logits [n][E] (device, no bias added): one routing record per row as
+ * in moe_decode_layers_traced (the logits echoed, picks, weights, shared
+ * weight 1) into out (device, n * (E + 2k + 1) words).  desc supplies E, k
+ * and no_renorm; its pointers are not read.
+ */
+int moe_decode_topk_logits(const moe_layer_desc *desc, const float *logits, int32_t n, float *out,
+                           cudaStream_t stream);
+
+/* Byte offsets, inside the workspace, of what the last moe_decode_batch call
+ * (or its block form) decided. */
+typedef struct {
+    int64_t logits;     /* fp32 [max_tokens][logit_ld]: router logits; column E the shared gate's score */
+    int64_t slots;      /* int32 [1 + S_max]: the slot count, then each slot's expert (picked experts in
+                         * ascending order, the shared expert E last) */
+    int64_t slot_w;     /* fp32 [S_max][max_tokens]: weight of token t in slot s (0: not picked) */
+    int64_t h;          /* bf16 [S_max][max_tokens][I]: SwiGLU output of each slot for every token */
+    int32_t S_max;
+    int32_t logit_ld;
+    int32_t max_tokens;
+} moe_batch_views;
+
+int moe_batch_views_for(const moe_layer_desc *desc, moe_batch_views *views);
+
+/* Byte offsets, inside the workspace, of the residual stream h and the
+ * normalised layer input x ([T][H] bf16 each) that the last decoder-block
+ * call wrote: moe_prefill_block with T tokens (small_batch = 0) or
+ * moe_decode_batch_block (small_batch = 1, 1 <= T <= 8). */
+int moe_block_views_for(const moe_layer_desc *desc, int32_t T, int32_t small_batch, int64_t *h, int64_t *x);
 
 /* Synchronise `stream`, return the device status word of `ws` (0 = fine,
  * MOE_ERR_TIMEOUT - site after a bounded wait ran out) and clear it. */

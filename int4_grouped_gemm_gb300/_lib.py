@@ -44,6 +44,15 @@ class moe_routing_views(ctypes.Structure):
         [("max_tiles", c_i32), ("tile_size", c_i32)]
 
 
+class moe_batch_views(ctypes.Structure):
+    _fields_ = [(n, c_i64) for n in ("logits", "slots", "slot_w", "h")] + \
+        [("S_max", c_i32), ("logit_ld", c_i32), ("max_tokens", c_i32)]
+
+
+MOE_DECODE_PHASES = 8
+MOE_DECODE_TRACE_BLOCKS = 256
+
+
 class MoEError(RuntimeError):
     def __init__(self, code: int, what: str):
         self.code = code
@@ -65,6 +74,11 @@ SIGNATURES = {
     "moe_prefill_block": (ctypes.c_int, [c_p, c_p, c_p, c_p, ctypes.c_float, c_i32, c_p, c_p, c_sz, c_p]),
     "moe_decode_batch_block": (ctypes.c_int, [c_p, c_p, c_p, c_p, ctypes.c_float, c_i32, c_p, c_p, c_sz, c_p]),
     "moe_decode_static_scratch": (ctypes.c_int, [c_p, c_p, c_p, c_p]),
+    "moe_read_static_scratch_status": (ctypes.c_int, [c_p]),
+    "moe_decode_layers_traced": (ctypes.c_int, [c_p, c_i32, c_p, c_p, c_p, c_sz, c_p, c_p, c_p]),
+    "moe_decode_topk_logits": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p]),
+    "moe_batch_views_for": (ctypes.c_int, [c_p, c_p]),
+    "moe_block_views_for": (ctypes.c_int, [c_p, c_i32, c_i32, c_p, c_p]),
     "moe_route_logits": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_sz, c_p]),
     "pack_int4": (ctypes.c_int, [c_p, c_i64, c_i32, c_i32, c_p, c_p, c_p, c_p]),
     "moe_read_device_status": (ctypes.c_int, [c_p, c_p]),
@@ -179,6 +193,39 @@ def moe_decode_static_scratch(desc: moe_layer_desc, x, y, stream=None):
     """moe_decode on the library's fixed scratch array (no workspace)."""
     _check(load().moe_decode_static_scratch(ctypes.byref(desc), _ptr(x), _ptr(y), _stream(stream)),
            "moe_decode_static_scratch")
+
+
+def moe_read_static_scratch_status(stream=None) -> int:
+    """Read and clear the status word of the static-scratch decode on the current device."""
+    return int(load().moe_read_static_scratch_status(_stream(stream)))
+
+
+def moe_decode_layers_traced(descs, x, y, ws, routing_trace=None, time_trace=None, stream=None):
+    """moe_decode_layers that also records each layer's routing (routing_trace:
+    float32 [n_layers][E + 2k + 1]) and per-block phase time stamps (time_trace:
+    int64 [n_layers][MOE_DECODE_TRACE_BLOCKS][MOE_DECODE_PHASES])."""
+    _check(load().moe_decode_layers_traced(ctypes.cast(descs, c_p), len(descs), _ptr(x), _ptr(y), _ptr(ws),
+                                           ws.numel() * ws.element_size(), _ptr(routing_trace), _ptr(time_trace),
+                                           _stream(stream)), "moe_decode_layers_traced")
+
+
+def moe_decode_topk_logits(desc: moe_layer_desc, logits, out, stream=None):
+    """The decode kernel's top-k on given logits [n][E]; out float32 [n][E + 2k + 1]."""
+    _check(load().moe_decode_topk_logits(ctypes.byref(desc), _ptr(logits), logits.shape[0], _ptr(out),
+                                         _stream(stream)), "moe_decode_topk_logits")
+
+
+def moe_batch_views_for(desc: moe_layer_desc) -> moe_batch_views:
+    v = moe_batch_views()
+    _check(load().moe_batch_views_for(ctypes.byref(desc), ctypes.byref(v)), "moe_batch_views_for")
+    return v
+
+
+def moe_block_views_for(desc: moe_layer_desc, T: int, small_batch: bool):
+    h, x = c_i64(), c_i64()
+    _check(load().moe_block_views_for(ctypes.byref(desc), T, int(small_batch), ctypes.byref(h), ctypes.byref(x)),
+           "moe_block_views_for")
+    return h.value, x.value
 
 
 def moe_route_logits(desc: moe_layer_desc, logits, T: int, ws, stream=None):

@@ -400,7 +400,8 @@ static DecodeLayerPtrs decode_ptrs(const moe_layer_desc &d) {
 // share d0's shape; the workspace holds the layout L.  Each launch clears the
 // grid-barrier counter and abort flag first.
 static int decode_run(const moe_layer_desc *descs, int n, const void *x, void *y, char *w, const DecodeLayout &L,
-                      int num_sms, cudaStream_t stream) {
+                      int num_sms, cudaStream_t stream, float *trace = nullptr,
+                      unsigned long long *tstamp = nullptr) {
     const moe_layer_desc &d0 = descs[0];
     DecodeStack a{};
     a.E = d0.E;
@@ -424,6 +425,9 @@ static int decode_run(const moe_layer_desc *descs, int n, const void *x, void *y
     a.h = reinterpret_cast<__nv_bfloat16 *>(w + L.h);
     a.racc = n > 1 ? reinterpret_cast<double *>(w + L.racc) : nullptr;  // read and written only between layers
     a.wait_limit = g_wait_limit;
+    a.trace = trace;
+    a.trace_ld = decode_trace_words(d0.E, d0.k);
+    a.tstamp = tstamp;
     for (int l0 = 0; l0 < n; l0 += kMaxStackLayers) {
         const int nl = n - l0 < kMaxStackLayers ? n - l0 : kMaxStackLayers;
         a.l0 = l0;
@@ -678,11 +682,101 @@ int moe_decode_static_scratch(const moe_layer_desc *desc, const void *x, void *y
     if ((rc = current_device(dev))) return rc;
     char *w = nullptr;
     if ((rc = static_scratch(w))) return rc;
-    // The control block's counters must start at zero; a call that gave up
-    // part way may have left them set.  Logits, top-k and h are written
+    // decode_run clears the grid-barrier counter and the abort flag before
+    // the launch (a call that gave up part way may have left them set); the
+    // status word is left alone so that a device-side error stays readable
+    // by moe_read_static_scratch_status.  Logits, top-k and h are written
     // before they are read.
-    if (cudaMemsetAsync(w + L.ctrl, 0, kCtrlBytes, stream) != cudaSuccess) return MOE_ERR_CUDA;
     return decode_run(desc, 1, x, y, w, L, dev->num_sms, stream);
+}
+
+int moe_read_static_scratch_status(cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_DEVICE;
+    char *w = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        w = static_cast<char *>(g_static_scratch_ptr[dev]);
+    }
+    if (!w) return MOE_OK;  // no call on this device has used the array yet
+    return moe_read_device_status(w, stream);
+}
+
+int moe_decode_layers_traced(const moe_layer_desc *descs, int32_t n_layers, const void *x, void *y, void *ws,
+                             size_t ws_bytes, float *routing_trace, unsigned long long *time_trace,
+                             cudaStream_t stream) {
+    if (!descs) return MOE_ERR_NULL;
+    if (n_layers < 1) return MOE_ERR_SHAPE;
+    int rc;
+    for (int l = 0; l < n_layers; ++l) {
+        if ((rc = decode_check(&descs[l]))) return rc;
+        const moe_layer_desc &a = descs[0], &b = descs[l];
+        if (a.E != b.E || a.k != b.k || a.H != b.H || a.I != b.I || a.group != b.group ||
+            a.has_shared != b.has_shared || a.no_renorm != b.no_renorm)
+            return MOE_ERR_SHAPE;
+    }
+    if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
+    if (routing_trace && (rc = check_ptr(routing_trace))) return rc;
+    if (time_trace && (rc = check_ptr(time_trace))) return rc;
+    const moe_layer_desc &d0 = descs[0];
+    const DecodeLayout L = n_layers > 1 ? decode_stack_layout(d0.E, d0.k, d0.H, d0.I) : decode_layout(d0.E, d0.k, d0.I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    if (dev->num_sms > kDecodeTraceMaxBlocks) return MOE_ERR_DEVICE;
+    return decode_run(descs, n_layers, x, y, static_cast<char *>(ws), L, dev->num_sms, stream, routing_trace,
+                      time_trace);
+}
+
+int moe_decode_topk_logits(const moe_layer_desc *desc, const float *logits, int32_t n, float *out,
+                           cudaStream_t stream) {
+    int rc = check_shape(desc);
+    if (rc) return rc;
+    if ((rc = check_ptr(logits)) || (rc = check_ptr(out))) return rc;
+    if (n < 1) return MOE_ERR_TOKENS;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    DecodeStack a{};
+    a.E = desc->E;
+    a.k = desc->k;
+    a.H = desc->H;
+    a.I = desc->I;
+    a.no_renorm = desc->no_renorm;
+    return cuda_rc(launch_decode_topk_given(a, logits, n, out, stream));
+}
+
+int moe_batch_views_for(const moe_layer_desc *desc, moe_batch_views *v) {
+    int rc = check_shape(desc);
+    if (rc) return rc;
+    if (!v) return MOE_ERR_NULL;
+    const BatchLayout L = batch_layout(desc->E, desc->k, desc->H, desc->I);
+    v->logits = L.logits;
+    v->slots = L.slots;
+    v->slot_w = L.slot_w;
+    v->h = L.h;
+    v->S_max = L.S_max;
+    v->logit_ld = desc->E + 1;
+    v->max_tokens = kBatchMax;
+    return MOE_OK;
+}
+
+int moe_block_views_for(const moe_layer_desc *desc, int32_t T, int32_t small_batch, int64_t *h, int64_t *x) {
+    int rc = check_shape(desc);
+    if (rc) return rc;
+    if (!h || !x) return MOE_ERR_NULL;
+    size_t off, bytes;
+    if (small_batch) {
+        if (T < 1 || T > kBatchMax) return MOE_ERR_TOKENS;
+        off = align_up(batch_layout(desc->E, desc->k, desc->H, desc->I).total, 256);
+        bytes = block_bytes(kBatchMax, desc->H);
+    } else {
+        if ((rc = check_tokens(desc, T))) return rc;
+        off = align_up(prefill_layout(T, desc->E, desc->k, desc->H, desc->I).total, 256);
+        bytes = block_bytes(T, desc->H);
+    }
+    *h = static_cast<int64_t>(off);
+    *x = static_cast<int64_t>(off + bytes / 2);
+    return MOE_OK;
 }
 
 }  // extern "C"

@@ -112,6 +112,16 @@ __device__ __forceinline__ bool grid_wait(Ctrl *c, unsigned target, long long li
     return *s_ok != 0;
 }
 
+// Inspection: thread 0 of the block records the global timer (ns) at phase
+// boundary p of layer l, when the caller asked for time stamps.
+__device__ __forceinline__ void stamp(const DecodeStack &a, int l, int p) {
+    if (a.tstamp && threadIdx.x == 0) {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        a.tstamp[(static_cast<int64_t>(l) * kDecodeTraceMaxBlocks + blockIdx.x) * kDecodePhases + p] = t;
+    }
+}
+
 // acc + a * b for the low (H = 0) or high (H = 1) bf16 halves of a and b,
 // multiplied exactly and added in fp32 with one rounding, like fmaf on the
 // widened values (the mixed-precision form of fma: bf16 sources, f32
@@ -496,9 +506,11 @@ __device__ __forceinline__ unsigned long long warp_sort_desc(unsigned long long 
 // candidates + 8 picked keys.  The logit of
 // expert e is the sum of its four K-quarter partial sums in a fixed order
 // (first layer of a launch) or the fp64 sum that the previous layer's blocks
-// accumulated, plus the bias.  Every block computes the same result.
+// accumulated, plus the bias; or, for inspection, given logits as they are.
+// Every block computes the same result.
 __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bias, const double *racc,
-                                           unsigned long long *s_keys, int *s_idx, float *s_w, float *s_red) {
+                                           const float *given, unsigned long long *s_keys, int *s_idx, float *s_w,
+                                           float *s_red, float *trace_logits) {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int Es = decode_logit_stride(a.E);  // stride of the partial and summed logits (entry E: shared gate)
     float lt = 0.f;          // this thread's expert logit (t < E)
@@ -506,7 +518,9 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
         unsigned long long key = 0;  // below every real key
         if (t < a.E) {
             float l;
-            if (racc) {
+            if (given) {
+                l = __ldcg(given + t);  // the logits as they are (no bias)
+            } else if (racc) {
                 // summed by the previous layer's blocks into kRaccCopies copies
                 // (fp64, exact for so few terms), rounded to fp32 and added
                 // pairwise here in a fixed order
@@ -526,8 +540,9 @@ __device__ __forceinline__ void topk_block(const DecodeStack &a, const float *bi
                 l += __ldcg(a.logits_part + 2 * Es + t);
                 l += __ldcg(a.logits_part + 3 * Es + t);
             }
-            if (bias) l += __ldg(bias + t);
+            if (bias && !given) l += __ldg(bias + t);
             lt = l;
+            if (trace_logits) trace_logits[t] = l;
             key = topk_key(l, t);
         }
         key = warp_sort_desc(key, lane);
@@ -652,6 +667,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     for (int li = 0; li < a.n_layers; ++li) {
         const int l = a.l0 + li;
         const DecodeLayerPtrs &P = a.L[li];
+        stamp(a, l, 0);
         const __nv_bfloat16 *in = l == 0 ? a.x : a.act + ((l - 1) % 2) * a.H;
         __nv_bfloat16 *out = l == a.n_total - 1 ? a.y : a.act + (l % 2) * a.H;
 
@@ -697,6 +713,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             cp_async_wait_all();  // this thread's staging copies land before the block exits
             return;
         }
+        stamp(a, l, 1);
         if (li > 0) {
             // the layer input, complete once every block passed the barrier:
             // warps 8-15 stage it while warps 0-7 start the top-k below
@@ -727,7 +744,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             }
             s_w[a.k] = cw;
         }
-        topk_block(a, P.bias, li == 0 ? nullptr : a.racc + (l % 2) * kRaccCopies * Es, s_keys, s_idx, s_w, s_red);
+        float *trace = a.trace && b == 0 ? a.trace + static_cast<int64_t>(l) * a.trace_ld : nullptr;
+        topk_block(a, P.bias, li == 0 ? nullptr : a.racc + (l % 2) * kRaccCopies * Es, nullptr, s_keys, s_idx, s_w,
+                   s_red, trace);
+        stamp(a, l, 2);
+        if (trace && tid <= a.k) {
+            // the picks, their weights and the shared expert's weight
+            if (tid < a.k) {
+                reinterpret_cast<int *>(trace + a.E)[tid] = s_idx[tid];
+                trace[a.E + a.k + tid] = s_w[tid];
+            } else {
+                trace[a.E + 2 * a.k] = s_w[a.k];
+            }
+        }
         if (b == 0 && li + 1 < a.n_layers) {
             // the next layer's logit sums start from zero; this buffer was last
             // read by the previous layer's top-k, before the previous barrier
@@ -775,6 +804,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             }
         }
         if (!down_requested) request_down();
+        stamp(a, l, 3);
         grid_arrive(a.ctrl);
 
         // ------------------------------------------------------------ phase C
@@ -797,6 +827,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             cp_async_wait_all();
             return;
         }
+        stamp(a, l, 4);
         {
             // h of every slot (bf16 words) and the sums of its words into shared
             // memory; h was written by other blocks, so it is read from L2
@@ -825,6 +856,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                 s_y[f - y_lo] = __bfloat162float(yb);
             }
         }
+        stamp(a, l, 5);
         if (li + 1 < a.n_layers) {
             // this block's share of the next layer's router logits: its output
             // features times the matching router columns, two threads per
@@ -855,8 +887,35 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             }
             grid_arrive(a.ctrl);
         }
+        stamp(a, l, 6);
         __syncthreads();  // hb and the staging buffers are refilled by the next layer
     }
+}
+
+// The top-k of decode_stack_kernel on given logits, one block per row: the
+// same sort, rank and softmax, for checking them against the oracle on
+// chosen logits (ties, equal values, signed zeros).
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_topk_given_kernel(const __grid_constant__ DecodeStack a, const float *logits, float *out) {
+    __shared__ int s_idx[kMaxSlots];
+    __shared__ float s_w[kMaxSlots];
+    __shared__ unsigned long long s_keys[64 + 8];
+    __shared__ float s_red[8];
+    const int ld = decode_trace_words(a.E, a.k);
+    float *rec = out + static_cast<int64_t>(blockIdx.x) * ld;
+    topk_block(a, nullptr, nullptr, logits + static_cast<int64_t>(blockIdx.x) * a.E, s_keys, s_idx, s_w, s_red, rec);
+    if (threadIdx.x < a.k) {
+        reinterpret_cast<int *>(rec + a.E)[threadIdx.x] = s_idx[threadIdx.x];
+        rec[a.E + a.k + threadIdx.x] = s_w[threadIdx.x];
+    } else if (threadIdx.x == a.k) {
+        rec[a.E + 2 * a.k] = 1.0f;
+    }
+}
+
+cudaError_t launch_decode_topk_given(const DecodeStack &a, const float *logits, int n, float *out, cudaStream_t s) {
+    if (n < 1) return cudaSuccess;
+    decode_topk_given_kernel<<<n, kDecThreads, 0, s>>>(a, logits, out);
+    return cudaGetLastError();
 }
 
 // Shared-memory limit of one block that the staging buffers may grow to.

@@ -65,8 +65,21 @@ struct DecodeStack {
     // rows / router columns are staged in shared memory
     int ys_cap, wr_ld, stage_down, stage_router;
     int no_renorm;           // weights: picked softmax probabilities as they are (1) or renormalised (0)
+    // inspection (both NULL in normal calls): block 0 writes each layer's
+    // routing record (kDecodeTraceWords words, layer l0 + i at trace + (l0 +
+    // i) * trace_ld), and thread 0 of every block the global timer at the
+    // phase boundaries ([n_total][kDecodeTraceMaxBlocks][kDecodePhases])
+    float *trace;
+    int trace_ld;
+    unsigned long long *tstamp;
     DecodeLayerPtrs L[kMaxStackLayers];
 };
+
+// Words of one decode routing record: logits [E] fp32, then the k picked
+// experts (int32), their k weights (fp32) and the shared expert's weight.
+__host__ __device__ inline int decode_trace_words(int E, int k) { return E + 2 * k + 1; }
+constexpr int kDecodePhases = MOE_DECODE_PHASES;            // time stamps per layer and block
+constexpr int kDecodeTraceMaxBlocks = MOE_DECODE_TRACE_BLOCKS;  // blocks a time trace has room for
 
 cudaError_t launch_pack_int4(const float *w, int64_t rows, int K, int G, uint32_t *q, uint16_t *scale,
                              uint16_t *bias, cudaStream_t stream);
@@ -89,5 +102,8 @@ cudaError_t launch_gemm(int mode, const GemmMaps &m, const GemmArgs &a, int grid
 cudaError_t launch_zero_i32(int *p, int64_t n, cudaStream_t s);
 cudaError_t launch_convert(const float *y_acc, __nv_bfloat16 *y, int64_t n, int num_sms, cudaStream_t s);
 cudaError_t launch_decode(const DecodeStack &a, int grid, cudaStream_t s);
+// The decode kernel's top-k on given fp32 logits [n][E] (no bias): one
+// routing record per row into out (decode_trace_words(E, k) words each).
+cudaError_t launch_decode_topk_given(const DecodeStack &a, const float *logits, int n, float *out, cudaStream_t s);
 
 }  // namespace moe

@@ -76,7 +76,7 @@ def lib():
         L.oracle_moe_layer_opt.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p, _p] + \
             [_p] * 9 + [_p, _i32, _p, _p, _p, _p, _p]
         L.oracle_experts_given_routing.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _i32, _i32] + [_p] * 9 + \
-            [_p, _p, _p]
+            [_p, _p, _p, _p]
         L.oracle_dispatch_combine_identity.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _p, _p, _p]
         L.oracle_residual_rmsnorm.argtypes = [_p, _p, _i32, _i32, _p, ctypes.c_double, _p, _p]
         L.oracle_residual_out.argtypes = [_p, _p, _i64, _p]
@@ -261,16 +261,20 @@ def moe_block(a_bits, r_bits, norm_w, eps, Wr, bias, gate: QWeights, up: QWeight
 
 
 def experts_given_routing(x_bits, gate: QWeights, up: QWeights, down: QWeights, E, has_shared,
-                          idx: np.ndarray, w: np.ndarray) -> np.ndarray:
+                          idx: np.ndarray, w: np.ndarray, shared_w: Optional[np.ndarray] = None) -> np.ndarray:
+    """Experts and combine under a given routing (idx [T, k], w [T, k]); the
+    shared expert weighs 1, or shared_w [T] per token."""
     x_bits = _c(x_bits, np.uint16)
     T, H = x_bits.shape
     idx = _c(idx, np.int32)
     w = _c(w, np.float64)
     k = idx.shape[1]
+    sw = None if shared_w is None else _c(shared_w, np.float64)
+    assert sw is None or sw.shape == (T,)
     y = np.empty((T, H), np.float64)
     arrays = [_c(a, a.dtype) for a in [gate.q, gate.s, gate.b, up.q, up.s, up.b, down.q, down.s, down.b]]
     lib().oracle_experts_given_routing(_ptr(x_bits), T, H, gate.rows, E, k, gate.group, int(has_shared),
-                                       *[_ptr(a) for a in arrays], _ptr(idx), _ptr(w), _ptr(y))
+                                       *[_ptr(a) for a in arrays], _ptr(idx), _ptr(w), _ptr(sw), _ptr(y))
     return y
 
 

@@ -473,19 +473,21 @@ void oracle_moe_layer(const uint16_t *x, int32_t T, int32_t H, int32_t I, int32_
                          qd, sd, bd, tokens, n_tokens, logits, idx, w, y, NULL);
 }
 
-/* Experts only, with routing given (used for the single-expert dense pin). */
+/* Experts only, with routing given (the single-expert dense pin, and the
+ * rows that the tests evaluate under the routing the GPU chose): shared_w
+ * [T] is the shared expert's weight per token, or NULL for 1. */
 void oracle_experts_given_routing(const uint16_t *x, int32_t T, int32_t H, int32_t I,
                                   int32_t E, int32_t k, int32_t G, int32_t has_shared,
                                   const uint32_t *qg, const uint16_t *sg, const uint16_t *bg,
                                   const uint32_t *qu, const uint16_t *su, const uint16_t *bu,
                                   const uint32_t *qd, const uint16_t *sd, const uint16_t *bd,
-                                  const int32_t *idx, const double *w, double *y)
+                                  const int32_t *idx, const double *w, const double *shared_w, double *y)
 {
     int32_t *seq = (int32_t *)malloc(sizeof(int32_t) * (size_t)T);
     for (int32_t t = 0; t < T; ++t)
         seq[t] = t;
     expert_weights W = {H, I, G, qg, qu, qd, sg, bg, su, bu, sd, bd};
-    dispatch_combine(x, H, k, E, has_shared, idx, w, seq, T, NULL, swiglu_expert, &W, y);
+    dispatch_combine(x, H, k, E, has_shared, idx, w, seq, T, shared_w, swiglu_expert, &W, y);
     free(seq);
 }
 

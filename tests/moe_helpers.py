@@ -7,7 +7,7 @@ import numpy as np
 import torch
 
 import oracle
-from int4_grouped_gemm_gb300 import synthetic
+from int4_grouped_gemm_gb300 import _lib, synthetic
 
 # Output tolerance: max|gpu - oracle| <= 2e-2 * max|oracle| and
 # sum|gpu - oracle| / sum|oracle| <= 5e-3 (gpu output bf16, oracle fp64).
@@ -70,3 +70,71 @@ def sample_tokens(T: int, n: int, seed: int) -> np.ndarray:
     pick = set(rng.choice(T, size=min(n, T), replace=False).tolist())
     pick.update({0, T - 1})
     return np.array(sorted(pick), np.int32)
+
+
+def check_topk_exact(gpu_logits: np.ndarray, gpu_idx: np.ndarray, gpu_w: np.ndarray, k: int, renorm: bool = True,
+                     what: str = ""):
+    """The GPU's picks are bit-exact, and its weights within fp32 rounding, of
+    the oracle's top-k of the GPU's own fp32 logits; returns the oracle's
+    (idx, w) for those logits."""
+    idx, w = oracle.topk(gpu_logits, k, renorm)
+    np.testing.assert_array_equal(gpu_idx, idx, err_msg=f"{what}: picks differ from oracle.topk of the GPU logits")
+    np.testing.assert_allclose(gpu_w, w, rtol=2e-6, atol=1e-7, err_msg=f"{what}: weights")
+    return idx, w
+
+
+def flipped(ref_idx: np.ndarray, gpu_idx: np.ndarray) -> np.ndarray:
+    """Rows whose set of picked experts differs between the oracle's own
+    logits and the GPU's (a near tie at the k-th place decided the other way
+    by the fp32 summation order)."""
+    return ~np.all(np.sort(ref_idx, axis=1) == np.sort(gpu_idx, axis=1), axis=1)
+
+
+def reference_under_gpu_routing(ref_y: np.ndarray, ref_idx: np.ndarray, xb_rows: np.ndarray, stacks, E: int,
+                                has_shared: bool, idx: np.ndarray, w: np.ndarray, shared_w=None,
+                                max_flipped: float = 0.05) -> np.ndarray:
+    """Oracle outputs to compare the GPU's against: the oracle's own layer
+    where its picks agree with the GPU's, and, for the rows whose near-tied
+    picks went the other way, the oracle's experts and combine evaluated
+    under the routing that the GPU's logits give (idx, w from oracle.topk of
+    the GPU logits, already checked bit-exact against the GPU's picks)."""
+    flip = flipped(ref_idx, idx)
+    assert flip.mean() <= max_flipped, f"{flip.sum()} of {len(flip)} rows picked other experts"
+    want = np.array(ref_y, dtype=np.float64, copy=True)
+    if flip.any():
+        sw = None if shared_w is None else np.asarray(shared_w, np.float64)[flip]
+        want[flip] = oracle.experts_given_routing(xb_rows[flip], *stacks, E, has_shared, idx[flip], w[flip],
+                                                  shared_w=sw)
+    return want
+
+
+def batch_routing(layer, ws, B, renorm=True, gated=False):
+    """What the small-batch kernels decided, read from the workspace views, and
+    checked against the oracle given the GPU's own fp32 logits: the slots are
+    bit-exactly the union of oracle.topk's picks in ascending expert order
+    (then the shared expert), and each slot's per-token weight is the oracle
+    weight of that pick (0 where the token did not pick it; the shared
+    slot's 1, or the sigmoid of the gate score).  Returns the oracle's
+    (idx, w) for the GPU logits."""
+    d = layer.desc
+    E, k = d.E, d.k
+    v = _lib.moe_batch_views_for(d)
+    logits = ws.view(v.logits, torch.float32, v.max_tokens * v.logit_ld).view(v.max_tokens, v.logit_ld)
+    logits = logits[:B].cpu().numpy()
+    slots = ws.view(v.slots, torch.int32, 1 + v.S_max).cpu().numpy()
+    slot_w = ws.view(v.slot_w, torch.float32, v.S_max * v.max_tokens).view(v.S_max, v.max_tokens)
+    slot_w = slot_w[:, :B].cpu().numpy()
+    idx, w = oracle.topk(logits[:, :E], k, renorm)
+    union = sorted(set(int(e) for e in idx.ravel()))
+    expect = union + ([E] if d.has_shared else [])
+    n = int(slots[0])
+    assert n == len(expect) and slots[1:1 + n].tolist() == expect, "slot list != union of oracle.topk picks"
+    want = np.zeros((n, B))
+    pos = {e: i for i, e in enumerate(union)}
+    for t in range(B):
+        for j in range(k):
+            want[pos[int(idx[t, j])], t] = w[t, j]
+    if d.has_shared:
+        want[n - 1] = 1.0 / (1.0 + np.exp(-logits[:, E].astype(np.float64))) if gated else 1.0
+    np.testing.assert_allclose(slot_w[:n], want, rtol=2e-6, atol=1e-7, err_msg="per-slot token weights")
+    return idx, w

@@ -8,7 +8,7 @@ import oracle
 from int4_grouped_gemm_gb300 import _lib, synthetic
 from int4_grouped_gemm_gb300.moe import DecodeChain, PackedLayer
 
-from moe_helpers import assert_close, oracle_layer, x_bits
+from moe_helpers import assert_close, check_topk_exact, oracle_layer, x_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -135,3 +135,79 @@ def test_decode_stack_without_shared_expert():
     torch.cuda.synchronize()
     assert torch.equal(chain.output(), eager[-1])
     assert _lib.moe_read_device_status(chain.ws.buf) == 0
+
+
+def _trace_fields(tr: np.ndarray, E: int, k: int):
+    """Split routing records [n][E + 2k + 1] into logits, picks, weights and the shared weight."""
+    tr = np.ascontiguousarray(tr, np.float32)
+    return tr[:, :E], tr[:, E:E + k].copy().view(np.int32), tr[:, E + k:E + 2 * k], tr[:, E + 2 * k]
+
+
+def test_stack_routing_is_the_oracle_topk_of_its_logits(chain40):
+    """The routing that decode_stack_kernel itself decided on every one of
+    the 40 layers (the fp32 logits it ranked, its picks and weights, read
+    back through the traced entry point): picks bit-exact and weights within
+    fp32 rounding of oracle.topk on those logits; the logits within fp32
+    summation error of the oracle's router on each layer's actual input
+    (the chain reaches all-zero activations after a few layers, where every
+    logit is exactly 0 and the picks must be experts 0..k-1).  The time
+    stamps of every block rise through each layer's phases."""
+    cfg, chain = chain40
+    E, k = cfg.E, cfg.k
+    x0 = synthetic.make_tokens(cfg.H, 1, seed=cfg.seed).cuda()
+    eager = chain.layer_outputs_eager(x0)
+    tr = torch.zeros(cfg.layers, E + 2 * k + 1, dtype=torch.float32, device="cuda")
+    tt = torch.zeros(cfg.layers, _lib.MOE_DECODE_TRACE_BLOCKS, _lib.MOE_DECODE_PHASES, dtype=torch.int64,
+                     device="cuda")
+    chain.set_input(x0)
+    _lib.moe_decode_layers_traced(chain.descs, chain.tok, chain.tok, chain.ws.buf, tr, tt)
+    torch.cuda.synchronize()
+    assert _lib.moe_read_device_status(chain.ws.buf) == 0
+    assert torch.equal(chain.output(), eager[-1])
+    logits, idx, w, sw = _trace_fields(tr.cpu().numpy(), E, k)
+    check_topk_exact(logits, idx, w, k, what="decode stack")
+    assert np.all(sw == 1.0)
+    zero_layers = 0
+    for l in range(cfg.layers):
+        L = synthetic.make_layer(cfg, layer=l, device="cuda", with_x=False)
+        xin = x0 if l == 0 else eager[l - 1]
+        bias = None if L.router_bias is None else L.router_bias.cpu().numpy()
+        ol = oracle.router_logits(x_bits(xin.cpu()), L.router_w.cpu().numpy(), bias)[0]
+        assert np.abs(ol - logits[l]).max() <= 1e-5 * np.abs(ol).max(), f"layer {l} logits"
+        if not np.any(ol):
+            zero_layers += 1
+            assert idx[l].tolist() == list(range(k))
+        del L
+    assert zero_layers > 0  # the all-equal case occurred inside the kernel
+    t = tt.cpu().numpy()
+    blocks = np.flatnonzero(t[0, :, 0])
+    assert len(blocks) == torch.cuda.get_device_properties(0).multi_processor_count
+    for l in range(cfg.layers):
+        st = t[l][blocks][:, :7].astype(np.int64)
+        assert np.all(np.diff(st, axis=1) >= 0), f"layer {l}: phases out of order"
+        if l:
+            assert np.all(st[:, 0] >= t[l - 1][blocks][:, 6])
+
+
+def test_single_layer_trace_matches_moe_decode():
+    """One layer through the traced entry point (its logits from the router
+    phase, not from a previous layer's sums): same output as moe_decode, and
+    its routing is the oracle's top-k of its logits."""
+    cfg = synthetic.CONFIGS["tiny"]
+    L = synthetic.make_layer(cfg)
+    layer = PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down)
+    ws = layer.workspace(1)
+    descs = (_lib.moe_layer_desc * 1)(layer.desc)
+    # one record per call (a record is E + 2k + 1 words: not a multiple of 16 bytes)
+    trs = [torch.zeros(1, cfg.E + 2 * cfg.k + 1, dtype=torch.float32, device="cuda") for _ in range(cfg.T)]
+    ref = oracle_layer(L, L.x)
+    for t in range(cfg.T):
+        x = L.x[t:t + 1].cuda().contiguous()
+        y = torch.empty_like(x)
+        _lib.moe_decode_layers_traced(descs, x, y, ws.buf, trs[t])
+        yd = layer.decode(x, ws)
+        torch.cuda.synchronize()
+        assert torch.equal(y, yd)
+    logits, idx, w, _ = _trace_fields(torch.cat(trs).cpu().numpy(), cfg.E, cfg.k)
+    assert np.abs(logits - ref["logits"]).max() <= 1e-5 * np.abs(ref["logits"]).max()
+    check_topk_exact(logits, idx, w, cfg.k, what="single layer")

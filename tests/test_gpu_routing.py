@@ -67,3 +67,48 @@ def test_route_small(T, E, k, shared, kind):
                                     (16384, "equal")])
 def test_route_full_sizes(T, kind):
     run_case(T, 256, 8, True, kind, seed=T)
+
+
+def _decode_logits(T, E, k, kind, seed):
+    """Logit rows for the decode top-k: the shared kinds, plus 'signed_zero'
+    (values from {-0, +0, 0.5, -0.5}: many ties between the two zeros) and
+    'kth_tie' (normal rows in which the (k+1)-th largest value is set equal
+    to the k-th, on an expert index below or above it)."""
+    if kind in ("normal", "ties", "equal"):
+        return synthetic.make_logits(T, E, seed, kind)
+    g = torch.Generator().manual_seed(seed)
+    if kind == "signed_zero":
+        grid = torch.tensor([-0.0, 0.0, 0.5, -0.5])
+        return grid[torch.randint(0, 4, (T, E), generator=g)]
+    if kind == "kth_tie":
+        x = torch.randn(T, E, generator=g)
+        if k < E:
+            order = torch.argsort(-x, dim=1)
+            for t in range(T):
+                x[t, order[t, k]] = x[t, order[t, k - 1]]
+        return x
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("renorm", [True, False], ids=["renorm", "no_renorm"])
+@pytest.mark.parametrize("kind", ["normal", "ties", "equal", "signed_zero", "kth_tie"])
+@pytest.mark.parametrize("E,k", [(16, 1), (16, 8), (40, 3), (200, 8), (256, 8), (256, 1), (9, 8)])
+def test_decode_topk_given_logits(E, k, kind, renorm):
+    """The batch-1 decode kernel's own top-k (bitonic sort, rank, softmax)
+    on given logits: picks bit-exact with oracle.topk, weights within fp32
+    rounding, the logits echoed bit for bit."""
+    T = 64
+    logits = _decode_logits(T, E, k, kind, seed=E * 31 + k)
+    desc = moe_layer_desc(E, k, 256, 128, 32, 1, None, None)
+    desc.no_renorm = 0 if renorm else 1
+    ld = E + 2 * k + 1
+    out = torch.zeros(T, ld, dtype=torch.float32, device="cuda")
+    _lib.moe_decode_topk_logits(desc, logits.cuda().contiguous(), out)
+    rec = out.cpu().numpy()
+    assert np.array_equal(rec[:, :E].view(np.uint32), logits.numpy().view(np.uint32))
+    idx = rec[:, E:E + k].copy().view(np.int32)
+    w = rec[:, E + k:E + 2 * k]
+    oi, ow = oracle.topk(logits.numpy(), k, renorm)
+    np.testing.assert_array_equal(idx, oi)
+    np.testing.assert_allclose(w, ow, rtol=2e-6, atol=1e-7)
+    assert np.all(rec[:, E + 2 * k] == 1.0)

@@ -11,7 +11,7 @@ import oracle
 from int4_grouped_gemm_gb300 import _lib, synthetic
 from int4_grouped_gemm_gb300.moe import PackedLayer
 
-from moe_helpers import ambiguous, assert_close, oracle_layer, oracle_stacks, x_bits
+from moe_helpers import assert_close, batch_routing, oracle_layer, oracle_stacks, reference_under_gpu_routing, x_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -26,18 +26,20 @@ def _packed(L, **kw):
     return PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down, **kw)
 
 
-def _check_rows(y, ref, what):
-    """Compare the tokens whose top-k set is not ambiguous (nearly tied k-th
-    and (k+1)-th oracle logits may route the other way in fp32)."""
-    cfg_k, E = ref["k"], ref["E"]
-    ok = ~ambiguous(ref["logits"], cfg_k, E)
-    assert ok.any()
-    assert_close(y.float().cpu().numpy()[ok], ref["y"][ok], what)
+def _check_rows(y, ref, what, layer, ws, renorm=True, gated=False):
+    """Routing checked exactly against the GPU's logits, then every token's
+    output against the oracle under that routing."""
+    B = y.shape[0]
+    idx, w = batch_routing(layer, ws, B, renorm, gated)
+    want = reference_under_gpu_routing(ref["y"], ref["idx"], ref["xb"], ref["stacks"], ref["E"], ref["has_shared"],
+                                       idx, w, shared_w=ref.get("shared_w"))
+    assert_close(y.float().cpu().numpy(), want, what)
 
 
-def _oracle_full(L, x):
-    r = oracle_layer(L, x)
-    r["k"], r["E"] = L.cfg.k, L.cfg.E
+def _oracle_full(L, x, stacks=None):
+    stacks = stacks if stacks is not None else oracle_stacks(L, L.cfg.group)
+    r = oracle_layer(L, x, stacks=stacks)
+    r.update(k=L.cfg.k, E=L.cfg.E, has_shared=L.cfg.has_shared, stacks=stacks, xb=x_bits(x))
     return r
 
 
@@ -47,24 +49,27 @@ def test_every_batch_size(cfg):
     layer = _packed(L)
     ws = layer.workspace(1)
     x = L.x.cuda()
+    stacks = oracle_stacks(L, cfg.group)
     for B in range(1, 9):
         xb = x[:B].contiguous()
         y = layer.decode_batch(xb, ws)
         torch.cuda.synchronize()
-        _check_rows(y, _oracle_full(L, L.x[:B]), f"{cfg.name} B={B}")
+        _check_rows(y, _oracle_full(L, L.x[:B], stacks), f"{cfg.name} B={B}", layer, ws)
     assert _lib.moe_read_device_status(ws.buf) == 0
 
 
-def _oracle_union(L, x):
+def _oracle_union(L, x, gpu_idx=None):
     """Oracle for a few tokens of a full-size layer: the oracle's own logits
-    and top-k, then only the experts in the union of the picks (and the
-    shared expert) quantised and evaluated."""
+    and top-k, then only the experts in the union of the picks (and of the
+    GPU's picks, when given; plus the shared expert) quantised and
+    evaluated.  Expert indices in the result are local to that union."""
     cfg = L.cfg
     xb = x_bits(x)
     bias = None if L.router_bias is None else L.router_bias.cpu().numpy()
     logits = oracle.router_logits(xb, L.router_w.cpu().numpy(), bias)
     idx, w = oracle.topk(logits, cfg.k)
-    union = sorted(set(int(e) for e in idx.ravel()))
+    picked = set(int(e) for e in idx.ravel())
+    union = sorted(picked | (set(int(e) for e in gpu_idx.ravel()) if gpu_idx is not None else set()))
     pos = {e: i for i, e in enumerate(union)}
     sel = torch.tensor(union + [cfg.E], device=L.w_gate.device)
     gate = oracle.quantize_stack(L.w_gate[sel].cpu().numpy(), cfg.group)
@@ -72,7 +77,20 @@ def _oracle_union(L, x):
     down = oracle.quantize_stack(L.w_down[sel].cpu().numpy(), cfg.group)
     local = np.vectorize(pos.get)(idx).astype(np.int32)
     y = oracle.experts_given_routing(xb, gate, up, down, len(union), True, local, w)
-    return {"y": y, "logits": logits, "k": cfg.k, "E": cfg.E, "union": len(union)}
+    return {"y": y, "logits": logits, "idx": local, "k": cfg.k, "E": len(union), "has_shared": True,
+            "stacks": (gate, up, down), "xb": xb, "union": len(picked), "local": pos}
+
+
+def _check_union(y, L, x, layer, ws, what):
+    """_check_rows for a full-size layer with the oracle on the union of the
+    oracle's and the GPU's picks (GPU routing mapped into that union)."""
+    B = y.shape[0]
+    idx, w = batch_routing(layer, ws, B)
+    ref = _oracle_union(L, x, gpu_idx=idx)
+    local = np.vectorize(ref["local"].get)(idx).astype(np.int32)
+    want = reference_under_gpu_routing(ref["y"], ref["idx"], ref["xb"], ref["stacks"], ref["E"], True, local, w)
+    assert_close(y.float().cpu().numpy(), want, what)
+    return ref
 
 
 @pytest.fixture(scope="module")
@@ -89,9 +107,8 @@ def test_full_size_layer(full_layer, B):
     x = synthetic.make_tokens(L.cfg.H, B, seed=90 + B)
     y = layer.decode_batch(x.cuda().contiguous(), ws)
     torch.cuda.synchronize()
-    ref = _oracle_union(L, x)
+    ref = _check_union(y, L, x, layer, ws, f"decode40 layer B={B}")
     assert ref["union"] > L.cfg.k  # the tokens pick different experts
-    _check_rows(y, ref, f"decode40 layer B={B}")
     assert _lib.moe_read_device_status(ws.buf) == 0
 
 
@@ -99,16 +116,21 @@ def test_one_token_agrees_with_decode_and_batch_with_prefill(full_layer):
     L, layer = full_layer
     ws = layer.workspace(8)
     x = synthetic.make_tokens(L.cfg.H, 8, seed=97).cuda()
-    ref = _oracle_union(L, x.cpu())
-    ok = ~ambiguous(ref["logits"], L.cfg.k, L.cfg.E)
     y1 = layer.decode_batch(x[:1].contiguous(), ws)
+    g1 = batch_routing(layer, ws, 1)[0]
     yd = layer.decode(x[:1].contiguous(), ws)
     yb = layer.decode_batch(x, ws)
+    gb = batch_routing(layer, ws, 8)[0]
     yp = layer.prefill(x, ws)
     torch.cuda.synchronize()
-    if ok[0]:
+    gp = ws.routing(layer.desc, 8)["topk_idx"].cpu().numpy()
+    # where both paths' routings agree (no near tie decided differently by
+    # their fp32 summation orders) the outputs agree within the tolerance
+    if np.array_equal(g1[0], gb[0]):
         assert_close(y1.float().cpu().numpy(), yd.float().cpu().numpy(), "B=1 vs moe_decode")
-    assert_close(yb.float().cpu().numpy()[ok], yp.float().cpu().numpy()[ok], "batch vs prefill")
+    same = np.all(np.sort(gb, axis=1) == np.sort(gp, axis=1), axis=1)
+    assert same.mean() >= 0.75
+    assert_close(yb.float().cpu().numpy()[same], yp.float().cpu().numpy()[same], "batch vs prefill")
     # a token's row does not depend on the other tokens of the batch beyond
     # the fp32 order of the slot sums (slots are grouped by the batch's union)
     np.testing.assert_allclose(yb[:1].float().cpu().numpy(), y1.float().cpu().numpy(), rtol=1e-2, atol=1e-4)
@@ -126,17 +148,18 @@ def test_same_token_repeated_and_repeat_calls_are_identical():
     for t in range(8):
         assert torch.equal(a[t], a[0])
     assert torch.equal(a, b)
-    _check_rows(a[:1], _oracle_full(L, L.x), "repeated token")
+    _check_rows(b, _oracle_full(L, L.x.repeat(8, 1)), "repeated token", layer, ws)
 
 
 def test_wide_hidden_and_expert_group32():
     L = synthetic.make_layer(WIDE, T=8)
     layer = _packed(L)
     ws = layer.workspace(1)
+    stacks = oracle_stacks(L, WIDE.group)
     for B in (3, 8):
         y = layer.decode_batch(L.x[:B].cuda().contiguous(), ws)
         torch.cuda.synchronize()
-        _check_rows(y, _oracle_full(L, L.x[:B]), f"wide B={B}")
+        _check_rows(y, _oracle_full(L, L.x[:B], stacks), f"wide B={B}", layer, ws)
 
 
 @pytest.mark.parametrize("no_renorm,gated", [(True, False), (False, True), (True, True)],
@@ -150,8 +173,10 @@ def test_routing_variants(no_renorm, gated):
     y = layer.decode_batch(L.x.cuda(), ws)
     torch.cuda.synchronize()
     bias = None if L.router_bias is None else L.router_bias.cpu().numpy()
-    ref = oracle.moe_layer(x_bits(L.x), L.router_w.cpu().numpy(), bias, *oracle_stacks(L, cfg.group), cfg.E, cfg.k,
+    stacks = oracle_stacks(L, cfg.group)
+    ref = oracle.moe_layer(x_bits(L.x), L.router_w.cpu().numpy(), bias, *stacks, cfg.E, cfg.k,
                            cfg.has_shared, renorm=not no_renorm,
                            shared_gate_w=None if sg is None else sg.numpy())
-    ref["k"], ref["E"] = cfg.k, cfg.E
-    _check_rows(y, ref, f"variant no_renorm={no_renorm} gated={gated}")
+    ref.update(k=cfg.k, E=cfg.E, has_shared=cfg.has_shared, stacks=stacks, xb=x_bits(L.x))
+    _check_rows(y, ref, f"variant no_renorm={no_renorm} gated={gated}", layer, ws, renorm=not no_renorm,
+                gated=gated)

@@ -11,7 +11,7 @@ import oracle
 from int4_grouped_gemm_gb300 import _lib, synthetic
 from int4_grouped_gemm_gb300.moe import DecodeChain, PackedLayer
 
-from moe_helpers import ambiguous, assert_close, oracle_stacks, x_bits
+from moe_helpers import assert_close, check_topk_exact, oracle_stacks, reference_under_gpu_routing, x_bits
 
 pytestmark = pytest.mark.gpu
 
@@ -46,20 +46,20 @@ def test_prefill_variants(no_renorm, gated):
     y = layer.prefill(L.x.cuda(), ws)
     torch.cuda.synchronize()
     assert _lib.moe_read_device_status(ws.buf) == 0
-    ref = _oracle(L, L.x, oracle_stacks(L, cfg.group), no_renorm, sg)
-    ok = ~ambiguous(ref["logits"], cfg.k, cfg.E)
+    stacks = oracle_stacks(L, cfg.group)
+    ref = _oracle(L, L.x, stacks, no_renorm, sg)
     rt = ws.routing(layer.desc, cfg.T)
+    g_logits = rt["logits"].cpu().numpy()
     g_idx = rt["topk_idx"].cpu().numpy()
     g_w = rt["topk_w"].cpu().numpy()
-    # the same experts with the same weights (compared in expert order: two
-    # picks whose logits nearly tie may swap slots)
-    go, ro = np.argsort(g_idx, axis=1), np.argsort(ref["idx"], axis=1)
-    assert np.array_equal(np.take_along_axis(g_idx, go, 1)[ok], np.take_along_axis(ref["idx"], ro, 1)[ok])
-    np.testing.assert_allclose(np.take_along_axis(g_w, go, 1)[ok], np.take_along_axis(ref["w"], ro, 1)[ok],
-                               rtol=2e-5, atol=1e-7)
+    assert np.abs(g_logits - ref["logits"]).max() <= 1e-5 * np.abs(ref["logits"]).max()
+    # picks bit-exact and weights (renormalised or not) of the GPU's own logits
+    idx, w = check_topk_exact(g_logits, g_idx, g_w, cfg.k, renorm=not no_renorm, what="prefill variant")
     if no_renorm:
         assert np.all(g_w.sum(axis=1) < 1.0)
-    assert_close(y.float().cpu().numpy()[ok], ref["y"][ok], f"prefill no_renorm={no_renorm} gated={gated}")
+    want = reference_under_gpu_routing(ref["y"], ref["idx"], x_bits(L.x), stacks, cfg.E, cfg.has_shared, idx, w,
+                                       shared_w=ref["shared_w"])
+    assert_close(y.float().cpu().numpy(), want, f"prefill no_renorm={no_renorm} gated={gated}")
 
 
 @pytest.mark.parametrize("no_renorm,gated", VARIANTS, ids=["no_renorm", "gated", "both"])

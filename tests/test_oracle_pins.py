@@ -332,6 +332,24 @@ def test_gated_shared_expert_scales_only_the_shared_part():
     assert np.all(out["shared_w"] == 0.5)
 
 
+def test_experts_given_routing_equals_the_layer_under_its_own_routing():
+    """The experts-only evaluation under a given routing reproduces the whole
+    layer when handed the layer's own picks and weights (also with the gated
+    shared expert's per-token weights), and with no shared expert it drops
+    exactly the shared part: the path the GPU tests use for rows whose
+    near-tied picks the GPU decided the other way."""
+    cfg, L, stacks, xb, sg = _gated_inputs(45)
+    Wr = L.router_w.numpy()
+    for vec in (None, sg):
+        out = oracle.moe_layer(xb, Wr, None, *stacks, cfg.E, cfg.k, True, shared_gate_w=vec)
+        sw = None if vec is None else out["shared_w"]
+        y = oracle.experts_given_routing(xb, *stacks, cfg.E, True, out["idx"], out["w"], shared_w=sw)
+        np.testing.assert_array_equal(y, out["y"])
+    none = oracle.moe_layer(xb, Wr, None, *stacks, cfg.E, cfg.k, False)
+    y = oracle.experts_given_routing(xb, *stacks, cfg.E, False, none["idx"], none["w"])
+    np.testing.assert_array_equal(y, none["y"])
+
+
 # ------------------------------------------- steps either side of the layer
 
 def _bits(vals):

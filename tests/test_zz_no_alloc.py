@@ -1,7 +1,9 @@
 """moe_decode_static_scratch: batch-1 decode on the library's fixed scratch
 array, with no caller workspace.  Compared with moe_decode (caller workspace)
 on the same layer and tokens, over consecutive calls, so that whatever one
-call leaves in the shared array cannot leak into the next.  The file name
+call leaves in the shared array cannot leak into the next; compared with the
+CPU oracle; and its failure path: a device-side timeout stays readable
+through moe_read_static_scratch_status until it is read.  The file name
 keeps it last in collection order, after every other test has used the
 library; it also passes on its own in a fresh process."""
 import ctypes
@@ -81,3 +83,48 @@ def test_static_scratch_matches_workspace_decode():
     torch.cuda.synchronize()
     assert_close(b.float().cpu().numpy(), a.float().cpu().numpy(), "repeat")
     assert _lib.moe_read_device_status(ws_big.buf) == 0
+
+
+@pytest.mark.gpu
+def test_static_scratch_matches_the_oracle():
+    """The static-scratch decode against the CPU oracle itself (not only
+    against moe_decode), token by token on the small layer."""
+    from moe_helpers import oracle_layer
+    cfg = synthetic.CONFIGS["tiny"]
+    L = synthetic.make_layer(cfg)
+    layer = PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down)
+    ref = oracle_layer(L, L.x)
+    for t in range(cfg.T):
+        y = _static(layer, L.x[t:t + 1].cuda().contiguous())
+        torch.cuda.synchronize()
+        assert_close(y.float().cpu().numpy(), ref["y"][t:t + 1], f"token {t}")
+    assert _lib.moe_read_static_scratch_status() == 0
+
+
+@pytest.mark.gpu
+def test_static_scratch_timeout_is_reported_then_cleared():
+    """With a one-cycle wait limit the decode kernel's grid-barrier waits run
+    out (no block waits for the others): the call still returns MOE_OK (the
+    failure happens on the device), the status stays in the array through a
+    second failing call, moe_read_static_scratch_status reports it and
+    clears it, and the next normal call matches the oracle."""
+    from moe_helpers import oracle_layer
+    cfg = synthetic.CONFIGS["tiny"]
+    L = synthetic.make_layer(cfg)
+    layer = PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down)
+    x = L.x[0:1].cuda().contiguous()
+    _lib.moe_read_static_scratch_status()  # start from a cleared status
+    old = _lib.moe_set_wait_limit(1)
+    try:
+        _static(layer, x)
+        _static(layer, x)
+        torch.cuda.synchronize()
+    finally:
+        _lib.moe_set_wait_limit(old)
+    st = _lib.moe_read_static_scratch_status()
+    assert _lib.MOE_ERR_TIMEOUT - 100 < st <= _lib.MOE_ERR_TIMEOUT, st
+    assert _lib.moe_read_static_scratch_status() == 0   # the read cleared it
+    y = _static(layer, x)
+    torch.cuda.synchronize()
+    assert _lib.moe_read_static_scratch_status() == 0
+    assert_close(y.float().cpu().numpy(), oracle_layer(L, L.x)["y"][0:1], "after the timeout")
