@@ -187,6 +187,26 @@ int moe_decode_layers(const moe_layer_desc *descs, int32_t n_layers, const void 
                       size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * Batch-1 decode through a stack of layers in the decoder-block form: the
+ * token is the residual stream r_0 = x, and layer l takes
+ *   h_l     = bf16(r_l + 0)                        (the stream; no attention
+ *                                                   sub-layer in this stack)
+ *   x_l     = bf16(h_l / sqrt(mean(h_l^2) + eps) * norm_w[l])   fp32 statistics
+ *   r_{l+1} = bf16(MoE_l(x_l) + h_l)               (rounded once)
+ * and y = r_n.  These are the steps moe_decode_batch_block runs around one
+ * layer (the pages name the model, Qwen3.6-35B-A3B, and say that decode
+ * kernel chains are fused: "Inside Lily ...", list under "Performance Gains
+ * and Workload Patterns"; the norm is the plainest reading of the block).
+ * Unlike moe_decode_layers, every layer's router runs on its own normalised
+ * input, whose scale depends on the whole residual row: one more grid-wide
+ * step per layer.  norm_w: n_layers device pointers to [H] fp32 (16-byte
+ * aligned); eps >= 0 (else MOE_ERR_SHAPE).  Other arguments and the workspace
+ * as moe_decode_layers; x and y may be the same buffer.
+ */
+int moe_decode_layers_block(const moe_layer_desc *descs, const float *const *norm_w, float eps, int32_t n_layers,
+                            const void *x, void *y, void *ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
  * Small-batch decode: y[B][H] (bf16) = MoE layer of x[B][H] (bf16) for
  * 1 <= B <= 8 tokens, the batch a step that checks a few draft tokens at
  * once produces ("Lily: Perplexity's Custom Inference Engine for Apple
@@ -290,7 +310,8 @@ int moe_read_static_scratch_status(cudaStream_t stream);
 #define MOE_DECODE_TRACE_BLOCKS 256
 
 /*
- * moe_decode_layers that also records, when the pointers are not NULL:
+ * moe_decode_layers (norm_w NULL) or moe_decode_layers_block (norm_w and
+ * eps as there) that also records, when the pointers are not NULL:
  *   routing_trace  device, (E + 2k + 1) 32-bit words per layer, layer l at
  *                  word l * (E + 2k + 1): the fp32 logits the decode kernel's
  *                  top-k ranked (router sums plus bias, as rounded on the
@@ -306,9 +327,9 @@ int moe_read_static_scratch_status(cudaStream_t stream);
  * Both 16-byte aligned.  The layer results are those of moe_decode_layers.
  * MOE_ERR_DEVICE if the GPU has more SMs than a time trace has room for.
  */
-int moe_decode_layers_traced(const moe_layer_desc *descs, int32_t n_layers, const void *x, void *y, void *ws,
-                             size_t ws_bytes, float *routing_trace, unsigned long long *time_trace,
-                             cudaStream_t stream);
+int moe_decode_layers_traced(const moe_layer_desc *descs, const float *const *norm_w, float eps, int32_t n_layers,
+                             const void *x, void *y, void *ws, size_t ws_bytes, float *routing_trace,
+                             unsigned long long *time_trace, cudaStream_t stream);
 
 /*
  * The batch-1 decode kernel's own top-k (the sort, rank, softmax and

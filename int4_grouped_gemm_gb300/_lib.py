@@ -75,7 +75,8 @@ SIGNATURES = {
     "moe_decode_batch_block": (ctypes.c_int, [c_p, c_p, c_p, c_p, ctypes.c_float, c_i32, c_p, c_p, c_sz, c_p]),
     "moe_decode_static_scratch": (ctypes.c_int, [c_p, c_p, c_p, c_p]),
     "moe_read_static_scratch_status": (ctypes.c_int, [c_p]),
-    "moe_decode_layers_traced": (ctypes.c_int, [c_p, c_i32, c_p, c_p, c_p, c_sz, c_p, c_p, c_p]),
+    "moe_decode_layers_traced": (ctypes.c_int, [c_p, c_p, ctypes.c_float, c_i32, c_p, c_p, c_p, c_sz, c_p, c_p, c_p]),
+    "moe_decode_layers_block": (ctypes.c_int, [c_p, c_p, ctypes.c_float, c_i32, c_p, c_p, c_p, c_sz, c_p]),
     "moe_decode_topk_logits": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p]),
     "moe_batch_views_for": (ctypes.c_int, [c_p, c_p]),
     "moe_block_views_for": (ctypes.c_int, [c_p, c_i32, c_i32, c_p, c_p]),
@@ -200,13 +201,33 @@ def moe_read_static_scratch_status(stream=None) -> int:
     return int(load().moe_read_static_scratch_status(_stream(stream)))
 
 
-def moe_decode_layers_traced(descs, x, y, ws, routing_trace=None, time_trace=None, stream=None):
-    """moe_decode_layers that also records each layer's routing (routing_trace:
-    float32 [n_layers][E + 2k + 1]) and per-block phase time stamps (time_trace:
-    int64 [n_layers][MOE_DECODE_TRACE_BLOCKS][MOE_DECODE_PHASES])."""
-    _check(load().moe_decode_layers_traced(ctypes.cast(descs, c_p), len(descs), _ptr(x), _ptr(y), _ptr(ws),
-                                           ws.numel() * ws.element_size(), _ptr(routing_trace), _ptr(time_trace),
-                                           _stream(stream)), "moe_decode_layers_traced")
+def _norm_ptrs(norm_w):
+    """A ctypes array of the layers' norm-weight device pointers (or None)."""
+    if norm_w is None:
+        return None
+    return (c_p * len(norm_w))(*[_ptr(w) for w in norm_w])
+
+
+def moe_decode_layers_traced(descs, x, y, ws, routing_trace=None, time_trace=None, norm_w=None, eps=1e-6,
+                             stream=None):
+    """moe_decode_layers (or, with norm_w, moe_decode_layers_block) that also
+    records each layer's routing (routing_trace: float32 [n_layers][E + 2k + 1])
+    and per-block phase time stamps (time_trace: int64 [n_layers]
+    [MOE_DECODE_TRACE_BLOCKS][MOE_DECODE_PHASES])."""
+    nw = _norm_ptrs(norm_w)
+    _check(load().moe_decode_layers_traced(ctypes.cast(descs, c_p), nw, float(eps), len(descs), _ptr(x), _ptr(y),
+                                           _ptr(ws), ws.numel() * ws.element_size(), _ptr(routing_trace),
+                                           _ptr(time_trace), _stream(stream)), "moe_decode_layers_traced")
+
+
+def moe_decode_layers_block(descs, norm_w, eps, x, y, ws, stream=None):
+    """The decoder-block form of moe_decode_layers: norm_w holds one [H] fp32
+    device tensor per layer; the token is the residual stream."""
+    if len(norm_w) != len(descs):
+        raise ValueError("moe_decode_layers_block: one norm weight per layer")
+    _check(load().moe_decode_layers_block(ctypes.cast(descs, c_p), _norm_ptrs(norm_w), float(eps), len(descs),
+                                          _ptr(x), _ptr(y), _ptr(ws), ws.numel() * ws.element_size(),
+                                          _stream(stream)), "moe_decode_layers_block")
 
 
 def moe_decode_topk_logits(desc: moe_layer_desc, logits, out, stream=None):

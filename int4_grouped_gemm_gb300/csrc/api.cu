@@ -401,7 +401,7 @@ static DecodeLayerPtrs decode_ptrs(const moe_layer_desc &d) {
 // grid-barrier counter and abort flag first.
 static int decode_run(const moe_layer_desc *descs, int n, const void *x, void *y, char *w, const DecodeLayout &L,
                       int num_sms, cudaStream_t stream, float *trace = nullptr,
-                      unsigned long long *tstamp = nullptr) {
+                      unsigned long long *tstamp = nullptr, const float *const *norm_w = nullptr, float eps = 0.f) {
     const moe_layer_desc &d0 = descs[0];
     DecodeStack a{};
     a.E = d0.E;
@@ -428,11 +428,16 @@ static int decode_run(const moe_layer_desc *descs, int n, const void *x, void *y
     a.trace = trace;
     a.trace_ld = decode_trace_words(d0.E, d0.k);
     a.tstamp = tstamp;
+    a.block_form = norm_w ? 1 : 0;
+    a.eps = eps;
     for (int l0 = 0; l0 < n; l0 += kMaxStackLayers) {
         const int nl = n - l0 < kMaxStackLayers ? n - l0 : kMaxStackLayers;
         a.l0 = l0;
         a.n_layers = nl;
-        for (int i = 0; i < nl; ++i) a.L[i] = decode_ptrs(descs[l0 + i]);
+        for (int i = 0; i < nl; ++i) {
+            a.L[i] = decode_ptrs(descs[l0 + i]);
+            a.L[i].nw = norm_w ? norm_w[l0 + i] : nullptr;
+        }
         a.next_Wr = l0 + nl < n ? descs[l0 + nl].router_w : nullptr;
         if (cudaMemsetAsync(&ctrl->bar, 0, 2 * sizeof(unsigned), stream) != cudaSuccess) return MOE_ERR_CUDA;
         if (launch_decode(a, num_sms, stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -702,9 +707,10 @@ int moe_read_static_scratch_status(cudaStream_t stream) {
     return moe_read_device_status(w, stream);
 }
 
-int moe_decode_layers_traced(const moe_layer_desc *descs, int32_t n_layers, const void *x, void *y, void *ws,
-                             size_t ws_bytes, float *routing_trace, unsigned long long *time_trace,
-                             cudaStream_t stream) {
+// Checks shared by the stack entry points: every layer supported by the
+// decode kernel and of the first layer's shape; norm weights (if any) present
+// and 16-byte aligned, eps in range.
+static int stack_check(const moe_layer_desc *descs, int32_t n_layers, const float *const *norm_w, float eps) {
     if (!descs) return MOE_ERR_NULL;
     if (n_layers < 1) return MOE_ERR_SHAPE;
     int rc;
@@ -714,7 +720,17 @@ int moe_decode_layers_traced(const moe_layer_desc *descs, int32_t n_layers, cons
         if (a.E != b.E || a.k != b.k || a.H != b.H || a.I != b.I || a.group != b.group ||
             a.has_shared != b.has_shared || a.no_renorm != b.no_renorm)
             return MOE_ERR_SHAPE;
+        if (norm_w && (rc = check_ptr(norm_w[l]))) return rc;
     }
+    if (norm_w && (!(eps >= 0.0f) || !(eps < 1e30f))) return MOE_ERR_SHAPE;
+    return MOE_OK;
+}
+
+int moe_decode_layers_traced(const moe_layer_desc *descs, const float *const *norm_w, float eps, int32_t n_layers,
+                             const void *x, void *y, void *ws, size_t ws_bytes, float *routing_trace,
+                             unsigned long long *time_trace, cudaStream_t stream) {
+    int rc = stack_check(descs, n_layers, norm_w, eps);
+    if (rc) return rc;
     if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
     if (routing_trace && (rc = check_ptr(routing_trace))) return rc;
     if (time_trace && (rc = check_ptr(time_trace))) return rc;
@@ -725,7 +741,22 @@ int moe_decode_layers_traced(const moe_layer_desc *descs, int32_t n_layers, cons
     if ((rc = current_device(dev))) return rc;
     if (dev->num_sms > kDecodeTraceMaxBlocks) return MOE_ERR_DEVICE;
     return decode_run(descs, n_layers, x, y, static_cast<char *>(ws), L, dev->num_sms, stream, routing_trace,
-                      time_trace);
+                      time_trace, norm_w, eps);
+}
+
+int moe_decode_layers_block(const moe_layer_desc *descs, const float *const *norm_w, float eps, int32_t n_layers,
+                            const void *x, void *y, void *ws, size_t ws_bytes, cudaStream_t stream) {
+    if (!norm_w) return MOE_ERR_NULL;
+    int rc = stack_check(descs, n_layers, norm_w, eps);
+    if (rc) return rc;
+    if ((rc = check_ptr(x)) || (rc = check_ptr(y)) || (rc = check_ptr(ws))) return rc;
+    const moe_layer_desc &d0 = descs[0];
+    const DecodeLayout L = decode_stack_layout(d0.E, d0.k, d0.H, d0.I);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    return decode_run(descs, n_layers, x, y, static_cast<char *>(ws), L, dev->num_sms, stream, nullptr, nullptr,
+                      norm_w, eps);
 }
 
 int moe_decode_topk_logits(const moe_layer_desc *desc, const float *logits, int32_t n, float *out,

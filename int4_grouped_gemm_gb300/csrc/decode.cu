@@ -207,6 +207,81 @@ __device__ __forceinline__ void stage_x(const __nv_bfloat16 *x, int H, uint4 *xb
     }
 }
 
+// Decoder-block form: the layer input from the residual stream r (written by
+// other blocks, read from L2), by threads 0..255: h = bf16(r + 0) (the
+// stream after an attention sub-layer that adds nothing here), the squares of
+// each thread's h values summed in order, the threads' sums by lanes then
+// warps, inv = 1 / sqrt(mean(h^2) + eps), x = bf16((h * inv) * w), as the
+// residual-add and RMS-norm kernel of the block calls computes them; x goes
+// to shared memory like stage_x's input (bf16 words, word sums, fp32), and
+// the block's own features' h to h_own.  All 512 threads call it.
+template <int HMAX>
+__device__ __forceinline__ void stage_norm(const __nv_bfloat16 *r, int H, const float *w, float eps, uint4 *xb,
+                                           float *xsum8, float *xs, float *h_own, int y_lo, int y_hi,
+                                           float *s_part, float *s_inv) {
+    constexpr int kNT = 256;
+    const int tid = threadIdx.x;
+    const int nw = H / 8;
+    uint4 hv[HMAX / 8 / kNT];
+    float ss = 0.f;
+    if (tid < kNT) {
+#pragma unroll
+        for (int i = 0; i < HMAX / 8 / kNT; ++i) {
+            const int wd = tid + i * kNT;
+            if (wd < nw) {
+                const uint4 rv = __ldcg(reinterpret_cast<const uint4 *>(r) + wd);
+                const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+                uint32_t o[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __nv_bfloat162 v = __floats2bfloat162_rn(0.f + __uint_as_float(rw[j] << 16),
+                                                                   0.f + __uint_as_float(rw[j] & 0xFFFF0000u));
+                    o[j] = *reinterpret_cast<const uint32_t *>(&v);
+                    const float lo = __uint_as_float(o[j] << 16), hi = __uint_as_float(o[j] & 0xFFFF0000u);
+                    ss = fmaf(lo, lo, ss);
+                    ss = fmaf(hi, hi, ss);
+                }
+                hv[i] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+        ss = warp_sum(ss);
+        if ((tid & 31) == 0) s_part[tid >> 5] = ss;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float tot = 0.f;
+#pragma unroll
+        for (int i = 0; i < kNT / 32; ++i) tot += s_part[i];
+        *s_inv = 1.0f / sqrtf(tot / static_cast<float>(H) + eps);
+    }
+    __syncthreads();
+    const float inv = *s_inv;
+    if (tid < kNT) {
+#pragma unroll
+        for (int i = 0; i < HMAX / 8 / kNT; ++i) {
+            const int wd = tid + i * kNT;
+            if (wd < nw) {
+                const uint32_t hw[4] = {hv[i].x, hv[i].y, hv[i].z, hv[i].w};
+                uint32_t xo[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int k = wd * 8 + 2 * j;
+                    const float lo = __uint_as_float(hw[j] << 16), hi = __uint_as_float(hw[j] & 0xFFFF0000u);
+                    const __nv_bfloat162 v = __floats2bfloat162_rn(lo * inv * __ldg(w + k), hi * inv * __ldg(w + k + 1));
+                    xo[j] = *reinterpret_cast<const uint32_t *>(&v);
+                    if (k >= y_lo && k < y_hi) h_own[k - y_lo] = lo;
+                    if (k + 1 >= y_lo && k + 1 < y_hi) h_own[k + 1 - y_lo] = hi;
+                    xs[vpos(wd * 8) + 2 * j] = __uint_as_float(xo[j] << 16);
+                    xs[vpos(wd * 8) + 2 * j + 1] = __uint_as_float(xo[j] & 0xFFFF0000u);
+                }
+                const uint4 xv = make_uint4(xo[0], xo[1], xo[2], xo[3]);
+                xb[xpos(wd)] = xv;
+                xsum8[wd] = sum8_bf16(xv);
+            }
+        }
+    }
+}
+
 // ------------------------------------------------------------ phase A parts
 
 // Register arrays are sized for the largest hidden size a kernel instance
@@ -625,6 +700,9 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     __shared__ unsigned long long s_keys[64 + 8];
     __shared__ float s_red[8];
     __shared__ float s_y[kMaxYSlice];
+    __shared__ float s_hown[kMaxYSlice];  // block form: the residual stream at this block's output features
+    __shared__ float s_part[8];
+    __shared__ float s_inv;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int G = gridDim.x, b = blockIdx.x;
     const int gw = b * kDecWarps + warp, NW = G * kDecWarps;
@@ -689,13 +767,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
 
         // ------------------------------------------------------------ phase A
         // Only the first layer of a launch: later layers' router logits are
-        // summed by the previous layer's phase C.
-        if (li == 0) {
+        // summed by the previous layer's phase C.  In the decoder-block form
+        // every layer: its input x depends on the norm of the whole residual
+        // row, which the previous layer's blocks only complete together.
+        const bool phase_a = li == 0 || a.block_form;
+        if (phase_a) {
+            if (li > 0 && !grid_wait(a.ctrl, ++nbar * G, lim, 1, &s_ok)) {  // the residual row is complete
+                cp_async_wait_all();
+                return;
+            }
             UnitRegs<HMAX> ur;
             const int n_a_units = 4 * (a.E + (P.shg ? 1 : 0));  // + the shared gate's score
             const int u0 = gw;
             if (u0 < n_a_units) router_load(a, P.Wr, P.shg, u0, lane, ur);
-            stage_x(in, a.H, xb, xsum8, xs);
+            if (a.block_form)
+                stage_norm<HMAX>(in, a.H, P.nw, a.eps, xb, xsum8, xs, s_hown, y_lo, y_hi, s_part, &s_inv);
+            else
+                stage_x(in, a.H, xb, xsum8, xs);
             __syncthreads();
             for (int u = u0; u < n_a_units; u += NW) {
                 if (u != u0) router_load(a, P.Wr, P.shg, u, lane, ur);
@@ -714,7 +802,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             return;
         }
         stamp(a, l, 1);
-        if (li > 0) {
+        if (!phase_a) {
             // the layer input, complete once every block passed the barrier:
             // warps 8-15 stage it while warps 0-7 start the top-k below
             stage_x(in, a.H, xb, xsum8, nullptr, 256, kDecThreads - 256);
@@ -725,7 +813,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             float cw = 1.0f;
             if (P.shg) {
                 float lg;
-                if (li == 0) {
+                if (phase_a) {
                     lg = __ldcg(a.logits_part + a.E) + __ldcg(a.logits_part + Es + a.E);
                     lg += __ldcg(a.logits_part + 2 * Es + a.E);
                     lg += __ldcg(a.logits_part + 3 * Es + a.E);
@@ -745,7 +833,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             s_w[a.k] = cw;
         }
         float *trace = a.trace && b == 0 ? a.trace + static_cast<int64_t>(l) * a.trace_ld : nullptr;
-        topk_block(a, P.bias, li == 0 ? nullptr : a.racc + (l % 2) * kRaccCopies * Es, nullptr, s_keys, s_idx, s_w,
+        topk_block(a, P.bias, phase_a ? nullptr : a.racc + (l % 2) * kRaccCopies * Es, nullptr, s_keys, s_idx, s_w,
                    s_red, trace);
         stamp(a, l, 2);
         if (trace && tid <= a.k) {
@@ -757,7 +845,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                 trace[a.E + 2 * a.k] = s_w[a.k];
             }
         }
-        if (b == 0 && li + 1 < a.n_layers) {
+        if (b == 0 && li + 1 < a.n_layers && !a.block_form) {
             // the next layer's logit sums start from zero; this buffer was last
             // read by the previous layer's top-k, before the previous barrier
             double *nr = a.racc + ((l + 1) % 2) * kRaccCopies * Es;
@@ -851,13 +939,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                                          : down_dot<false>(a, P, e_j, w_j, nslots, f, f - y_lo, lane, gshift, st, hb,
                                                            hsum8, hp));
             if (lane == 0) {
-                const __nv_bfloat16 yb = __float2bfloat16_rn(y);
+                // the layer's fp32 sum, plus the residual stream in the block form, rounded once
+                const __nv_bfloat16 yb = __float2bfloat16_rn(a.block_form ? y + s_hown[f - y_lo] : y);
                 out[f] = yb;
                 s_y[f - y_lo] = __bfloat162float(yb);
             }
         }
         stamp(a, l, 5);
-        if (li + 1 < a.n_layers) {
+        if (li + 1 < a.n_layers && a.block_form) {
+            grid_arrive(a.ctrl);  // the next layer's phase A reads the whole residual row
+        } else if (li + 1 < a.n_layers) {
             // this block's share of the next layer's router logits: its output
             // features times the matching router columns, two threads per
             // expert, added in fp64 into copy b % kRaccCopies of the next
@@ -927,7 +1018,7 @@ static void decode_plan(DecodeStack &a, int grid) {
     if (ld % 8 == 0) ld += 4;              // odd multiple of 4 floats: fewer bank conflicts
     a.wr_ld = ld;
     const size_t base = sizeof(float) * static_cast<size_t>(decode_smem_floats(a.H, a.I, a.k));
-    a.stage_router = base + 4 * static_cast<size_t>(decode_stage_words(a, false, true)) <= kDecSmemLimit;
+    a.stage_router = !a.block_form && base + 4 * static_cast<size_t>(decode_stage_words(a, false, true)) <= kDecSmemLimit;
     a.stage_down = base + 4 * static_cast<size_t>(decode_stage_words(a, true, a.stage_router)) <= kDecSmemLimit;
 }
 

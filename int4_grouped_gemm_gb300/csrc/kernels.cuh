@@ -40,6 +40,7 @@ struct DecodeLayerPtrs {
     const uint32_t *qg, *qu, *qd;
     const uint16_t *sg, *bg, *su, *bu, *sd, *bd;
     const float *shg;  // shared-expert gate vector [H], or NULL (weight 1)
+    const float *nw;   // decoder-block form: RMS-norm weight [H] of the layer's input
 };
 
 // One launch of the batch-1 decode kernel: layers l0 .. l0 + n_layers - 1 of
@@ -72,6 +73,11 @@ struct DecodeStack {
     float *trace;
     int trace_ld;
     unsigned long long *tstamp;
+    // decoder-block form (1): each layer takes the residual stream r, runs on
+    // x = bf16(RMSNorm(r) * nw) and passes on bf16(MoE(x) + r); every layer
+    // then computes its router logits from its own x (phase A)
+    int block_form;
+    float eps;
     DecodeLayerPtrs L[kMaxStackLayers];
 };
 

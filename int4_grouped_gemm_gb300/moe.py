@@ -167,19 +167,26 @@ class DecodeChain:
     one step as a CUDA graph.
     """
 
-    def __init__(self, layers, device="cuda"):
+    def __init__(self, layers, device="cuda", norm_w=None, eps: float = 1e-6):
+        """norm_w: one [H] fp32 device tensor per layer for the decoder-block
+        form (residual stream and RMS norm around every layer), or None."""
         self.layers = list(layers)
         H = self.layers[0].H
         self.descs = (moe_layer_desc * len(self.layers))(*[l.desc for l in self.layers])
         self.ws = Workspace(self.layers[0].desc, 1, device=device)
         self.tok = torch.zeros(1, H, dtype=torch.bfloat16, device=device)
+        self.norm_w = None if norm_w is None else [w.contiguous() for w in norm_w]
+        self.eps = eps
         self.graph = None
 
     def set_input(self, x: torch.Tensor):
         self.tok.copy_(x.reshape(self.tok.shape))
 
     def step_eager(self, stream=None):
-        _lib.moe_decode_layers(self.descs, self.tok, self.tok, self.ws.buf, stream)
+        if self.norm_w is None:
+            _lib.moe_decode_layers(self.descs, self.tok, self.tok, self.ws.buf, stream)
+        else:
+            _lib.moe_decode_layers_block(self.descs, self.norm_w, self.eps, self.tok, self.tok, self.ws.buf, stream)
 
     def layer_outputs_eager(self, x: torch.Tensor):
         """Run the layers one moe_decode call at a time and keep every output."""

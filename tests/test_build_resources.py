@@ -15,7 +15,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CSRC = os.path.join(ROOT, "int4_grouped_gemm_gb300", "csrc")
-ALLOWED_SPILL = {"decode_stack_kernelILi4096E": 128}  # bytes of spill stores
+ALLOWED_SPILL = {"decode_stack_kernelILi4096E": 160}  # bytes of spill stores
 
 
 def _report(src):

@@ -211,3 +211,121 @@ def test_single_layer_trace_matches_moe_decode():
     logits, idx, w, _ = _trace_fields(torch.cat(trs).cpu().numpy(), cfg.E, cfg.k)
     assert np.abs(logits - ref["logits"]).max() <= 1e-5 * np.abs(ref["logits"]).max()
     check_topk_exact(logits, idx, w, cfg.k, what="single layer")
+
+
+def _norm_weights(H, n, seed):
+    g = torch.Generator().manual_seed(seed)
+    return [(torch.rand(H, generator=g) + 0.5).float().cuda() for _ in range(n)]
+
+
+def _oracle_block_touched(L, r_bits, w, eps, cfg, gpu_logits=None):
+    """Oracle for one token through one layer in the decoder-block form
+    (h = r + 0, x = RMSNorm(h) w, out = bf16(MoE(x) + h)), with only the
+    touched experts quantised; the experts run under the routing of the GPU's
+    logits when those pick another set (a near tie decided the other way)."""
+    zeros = np.zeros_like(r_bits)
+    h, x = oracle.residual_rmsnorm(zeros, r_bits, w.cpu().numpy(), eps)
+    bias = None if L.router_bias is None else L.router_bias.cpu().numpy()
+    logits = oracle.router_logits(x, L.router_w.cpu().numpy(), bias)
+    idx, wt = oracle.topk(logits, cfg.k)
+    if gpu_logits is not None:
+        gi, gw = oracle.topk(gpu_logits[None, :], cfg.k)
+        if set(gi[0].tolist()) != set(idx[0].tolist()):
+            idx, wt = gi, gw
+    sel = torch.tensor([int(e) for e in idx[0]] + [cfg.E], device=L.w_gate.device)
+    stacks = [oracle.quantize_stack(m[sel].cpu().numpy(), cfg.group) for m in (L.w_gate, L.w_up, L.w_down)]
+    local = np.arange(cfg.k, dtype=np.int32)[None, :]
+    y = oracle.experts_given_routing(x, *stacks, cfg.k, True, local, wt)
+    return oracle.residual_out(h, y), h, logits
+
+
+def _bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).float().numpy()
+
+
+def _logit_bound(r_bits, w, eps, Wr, scale):
+    """How far the GPU's logits may be from the oracle's on the same residual
+    stream: fp32 summation (1e-5 of max|logit|) plus, for every element of
+    the normalised input whose exact value h * inv * w lies within 4e-6 of a
+    bf16 rounding boundary (the GPU's fp32 norm statistics are that close to
+    the oracle's fp64 ones), the router weight times the gap between the two
+    roundings."""
+    h = _bf16(r_bits)[0].astype(np.float64) + 0.0
+    inv = 1.0 / np.sqrt((h * h).sum() / h.size + eps)
+    v = h * inv * w.cpu().numpy().astype(np.float64)
+    up = torch.from_numpy(v * (1 + 4e-6)).float().to(torch.bfloat16).float().numpy()
+    dn = torch.from_numpy(v * (1 - 4e-6)).float().to(torch.bfloat16).float().numpy()
+    gap = np.abs(up - dn).astype(np.float64)
+    return 1e-5 * scale + np.abs(Wr.astype(np.float64)) @ gap
+
+
+def test_block_stack_matches_the_oracle_layer_by_layer(chain40):
+    """The decoder-block form of the 40-layer stack (residual stream and RMS
+    norm around every layer, one launch): the stack run for its first l
+    layers gives the stream r_l; each layer's output against the oracle's
+    block applied to the GPU's own r_{l-1} (within bf16 rounding of the
+    stream plus the layer tolerance); every layer's routing bit-exact of the
+    logits it ranked (traced run of all 40), those logits near the oracle's
+    (fp32 summation, plus one bf16 step of the normalised input wherever its
+    exact value lies so near a rounding boundary that the GPU's fp32 norm
+    statistics may round it the other way); and the stream keeps its scale
+    through the 40 layers."""
+    cfg, chain = chain40
+    E, k, eps = cfg.E, cfg.k, 1e-6
+    nw = _norm_weights(cfg.H, cfg.layers, 91)
+    x0 = synthetic.make_tokens(cfg.H, 1, seed=cfg.seed).cuda()
+    rs = [x0]
+    for n in range(1, cfg.layers + 1):
+        descs = (_lib.moe_layer_desc * n)(*chain.descs[:n])
+        y = torch.empty_like(x0)
+        _lib.moe_decode_layers_block(descs, nw[:n], eps, x0, y, chain.ws.buf)
+        rs.append(y)
+    tr = torch.zeros(cfg.layers, E + 2 * k + 1, dtype=torch.float32, device="cuda")
+    yt = torch.empty_like(x0)
+    _lib.moe_decode_layers_traced(chain.descs, x0, yt, chain.ws.buf, tr, None, norm_w=nw, eps=eps)
+    torch.cuda.synchronize()
+    assert _lib.moe_read_device_status(chain.ws.buf) == 0
+    assert torch.equal(yt, rs[-1])  # the traced run is the same computation
+    logits, idx, w, sw = _trace_fields(tr.cpu().numpy(), E, k)
+    check_topk_exact(logits, idx, w, k, what="block stack")
+    for l in range(cfg.layers):
+        L = synthetic.make_layer(cfg, layer=l, device="cuda", with_x=False)
+        r_prev = x_bits(rs[l].cpu())
+        want, h, ol = _oracle_block_touched(L, r_prev, nw[l], eps, cfg, gpu_logits=logits[l])
+        bound = _logit_bound(r_prev, nw[l], eps, L.router_w.cpu().numpy(), np.abs(ol).max())
+        assert np.all(np.abs(ol[0] - logits[l]) <= bound), f"layer {l} logits"
+        got = rs[l + 1].float().cpu().numpy()
+        wantf, hf = _bf16(want), _bf16(h)
+        bound = 2.0 ** -6 * np.abs(wantf) + 2e-2 * np.abs(wantf - hf).max()
+        assert np.all(np.abs(got - wantf) <= bound), f"layer {l}: max excess {(np.abs(got - wantf) - bound).max()}"
+        del L
+    rms = [float(r.float().pow(2).mean().sqrt()) for r in (rs[0], rs[-1])]
+    assert rms[1] > 0.5 * rms[0], rms  # no collapse with the residual stream
+
+
+def test_block_stack_graph_equals_eager():
+    """A 3-layer block-form stack of small layers: the CUDA-graph replay of
+    DecodeChain equals eager launches bit for bit, and with an all-zero norm
+    weight the layers add nothing (x = 0 picks experts 0..k-1 with zero
+    input, so every expert output is 0): the stream passes through."""
+    cfg = DECODE_SHAPES[2]
+    layers = []
+    for l in range(3):
+        L = synthetic.make_layer(cfg, layer=l, with_x=False)
+        layers.append(PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down))
+    nw = _norm_weights(cfg.H, 3, 92)
+    chain = DecodeChain(layers, norm_w=nw)
+    x0 = synthetic.make_tokens(cfg.H, 1, seed=93).cuda()
+    chain.set_input(x0)
+    chain.step_eager()
+    eager = chain.output().clone()
+    chain.set_input(x0)
+    chain.step()
+    torch.cuda.synchronize()
+    assert torch.equal(chain.output(), eager)
+    zero = DecodeChain(layers, norm_w=[torch.zeros(cfg.H, device="cuda") for _ in range(3)])
+    zero.set_input(x0)
+    zero.step_eager()
+    torch.cuda.synchronize()
+    assert torch.equal(zero.output(), (x0.float() + 0.0).to(torch.bfloat16))
+    assert _lib.moe_read_device_status(chain.ws.buf) == 0
