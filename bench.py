@@ -383,9 +383,37 @@ def run_decode(args, pk):
         raise RuntimeError(f"decode device status {st}")
     bytes_step = decode_bytes_per_layer(cfg) * cfg.layers
     gbs = bytes_step / (ms * 1e-3) / 1e9
+    # the same 40 layers in the decoder-block form: residual stream and RMS
+    # norm around every layer (the stream does not collapse to zero), one
+    # graph per step, output written back into the input slot
+    g = torch.Generator().manual_seed(cfg.seed + 7)
+    norm_w = [(torch.rand(cfg.H, generator=g) + 0.5).float().cuda() for _ in range(cfg.layers)]
+    block = DecodeChain(layers, norm_w=norm_w, eps=1e-6)
+    block.set_input(x0)
+    block.capture()
+    for _ in range(3):
+        block.step()
+    block.set_input(x0)
+    torch.cuda.synchronize()
+    a.record()
+    for _ in range(steps):
+        block.step()
+    b.record()
+    torch.cuda.synchronize()
+    ms_block = a.elapsed_time(b) / steps
+    if _lib.moe_read_device_status(block.ws.buf) != 0:
+        raise RuntimeError("decode block form: device status")
+    rms = float(block.output().float().pow(2).mean().sqrt())
+    gbs_block = bytes_step / (ms_block * 1e-3) / 1e9
     return dict(tok_s=1000.0 / ms, ms_per_step=ms, steps=steps, layers=cfg.layers,
                 fresh={"tok_s": round(1000.0 / ms_fresh, 1), "ms_per_step": round(ms_fresh, 4),
                        "note": "a new seeded token each step instead of the previous step's output"},
+                block={"tok_s": round(1000.0 / ms_block, 1), "ms_per_step": round(ms_block, 4),
+                       "hbm_gbs": round(gbs_block, 1), "frac_of_hbm": round(gbs_block / pk["hbm"], 4),
+                       "output_rms_after_steps": round(rms, 4),
+                       "note": "moe_decode_layers_block: residual stream + RMS norm (weights U[0.5, 1.5), eps 1e-6) "
+                               "around each of the 40 layers; the router of every layer runs on its own "
+                               "normalised input (one more grid-wide step per layer than the plain chain)"},
                 roofline={"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
                           "frac": round(gbs / pk["hbm"], 4), "bytes_per_step": bytes_step},
                 clocks=clk.summary(), launches=-(-cfg.layers // DECODE_LAYERS_PER_KERNEL) * steps)
@@ -548,16 +576,84 @@ def oracle_time(cfg, s, toks):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(cfg, target_s=15.0):
+def _oracle_threads():
+    import oracle
+    return {"threads": oracle.num_threads(), "host_cores": len(os.sched_getaffinity(0))}
+
+
+def cpu_prefill_leg(name, n_tokens, threads=None, seed=0):
+    """The oracle on n_tokens of a prefill layer (all of them when n_tokens >=
+    T), on `threads` threads (default: all host cores)."""
+    import oracle
+    from int4_grouped_gemm_gb300 import synthetic
+    cfg = synthetic.CONFIGS[name]
+    s = oracle_sample(cfg, min(n_tokens, cfg.T), seed=seed)
+    prev = oracle.set_num_threads(threads) if threads else None
+    try:
+        oracle_time(cfg, s, s["toks"][:2])          # thread start-up, page-in
+        t = oracle_time(cfg, s, s["toks"])
+        th = oracle.num_threads()
+    finally:
+        if prev:
+            oracle.set_num_threads(prev)
+    n = len(s["toks"])
+    what = "all" if n >= cfg.T else f"{n} sampled"
+    return {"value": round(n / t, 3), "unit": "tok/s", "cores": th, "kind": "oracle",
+            "host_cores": len(os.sched_getaffinity(0)), "seconds": round(t, 2),
+            "sample": f"{what} of the {cfg.T} tokens of the {cfg.name} layer (router, top-{cfg.k}, {cfg.k} routed + "
+                      f"shared int4 SwiGLU experts, combine), fp64 C loops on {th} thread(s)"}
+
+
+def cpu_decode_leg(layers=None):
+    """The oracle's batch-1 decode: the first step of the 40-layer chain (the
+    oracle's own chain from the same start token), router, top-k and the 9
+    touched experts of every layer timed; generating, moving and quantising
+    the touched experts' weights (packing, not the layer) are not."""
+    import numpy as np
+    import torch
+    import oracle
+    from int4_grouped_gemm_gb300 import synthetic
+    cfg = synthetic.CONFIGS[DECODE_CFG]
+    n_layers = layers or cfg.layers
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    xb = synthetic.bf16_bits(synthetic.make_tokens(cfg.H, 1, seed=cfg.seed)).numpy().view(np.uint16)
+    t_total = 0.0
+    for l in range(n_layers):
+        L = synthetic.make_layer(cfg, layer=l, device=dev, with_x=False)
+        Wr = L.router_w.cpu().numpy()
+        bias = None if L.router_bias is None else L.router_bias.cpu().numpy()
+        t0 = time.perf_counter()
+        logits = oracle.router_logits(xb, Wr, bias)
+        idx, w = oracle.topk(logits, cfg.k)
+        t_total += time.perf_counter() - t0
+        sel = torch.tensor([int(e) for e in idx[0]] + [cfg.E], device=L.w_gate.device)
+        stacks = [oracle.quantize_stack(m[sel].cpu().numpy(), cfg.group) for m in (L.w_gate, L.w_up, L.w_down)]
+        del L
+        t0 = time.perf_counter()
+        y = oracle.experts_given_routing(xb, *stacks, cfg.k, True, np.arange(cfg.k, dtype=np.int32)[None, :], w)
+        xb = oracle.bf16_round(y.astype(np.float32))
+        t_total += time.perf_counter() - t0
+    return {"value": round(1.0 / t_total * n_layers / cfg.layers, 4), "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "host_cores": len(os.sched_getaffinity(0)), "seconds": round(t_total, 2),
+            "sample": f"the first decode step through {n_layers} of the {cfg.layers} layers (one token: the oracle's "
+                      f"loops run it on one thread), router + top-{cfg.k} + {cfg.k + 1} touched experts per layer; "
+                      f"weight generation, copies and quantisation excluded"}
+
+
+def cpu_baseline(cfg, target_s=12.0):
+    """The headline CPU baseline: the oracle on a sample of the T=4096 layer
+    sized to about target_s seconds on all host cores."""
     import oracle
     s = oracle_sample(cfg, 2048)
     oracle_time(cfg, s, s["toks"][:4])           # first call: thread start-up, page-in
     t = oracle_time(cfg, s, s["toks"][:32])
     n = int(max(32, min(2048, 32 * target_s / max(t, 1e-3))))
     t = oracle_time(cfg, s, s["toks"][:n])
-    return {"value": round(n / t, 3), "unit": "tok/s", "cores": oracle.num_threads(), "kind": "oracle",
+    th = oracle.num_threads()
+    return {"value": round(n / t, 3), "unit": "tok/s", "cores": th, "kind": "oracle",
+            "host_cores": len(os.sched_getaffinity(0)), "seconds": round(t, 2),
             "sample": f"{n} of the {cfg.T} tokens of the {cfg.name} layer (router, top-8, 8 routed + shared "
-                      f"int4 SwiGLU experts, combine), fp64 C loops, {t:.1f} s"}
+                      f"int4 SwiGLU experts, combine), fp64 C loops on {th} threads"}
 
 
 def run_reference(args, rank, world):
@@ -663,8 +759,15 @@ def main():
         other = {n: run_prefill_other(n, pk) for n in ("prefill512", "skew16384")}
         other["small_batches_through_moe_prefill"], other["small_batch_decode"] = run_small_batches(pk)
     cpu = None
+    cpu_legs = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(cfg)
+        cpu_legs = {
+            "prefill512_all_tokens": cpu_prefill_leg("prefill512", 512),
+            "prefill4096_one_thread": cpu_prefill_leg(PREFILL_CFG, 24, threads=1, seed=3),
+            "skew16384_sample": cpu_prefill_leg("skew16384", 768, seed=4),
+            "decode40_first_step": cpu_decode_leg(),
+        }
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
@@ -691,12 +794,15 @@ def main():
             "gpu_launches": P["launches"],
             "clocks": P["clocks"],
             "cpu_baseline": cpu,
+            "cpu_baseline_legs": cpu_legs,
         }
         if D is not None:
             line["decode"] = {"metric": "batch-1 decode tok/s, 40 stacked layers, CUDA graph per step",
                               "value": round(D["tok_s"], 1), "unit": "tok/s", "ms_per_step": round(D["ms_per_step"], 4),
                               "steps": D["steps"], "roofline": D["roofline"], "clocks": D["clocks"],
-                              "gpu_launches": D["launches"], "fresh_token_per_step": D["fresh"]}
+                              "gpu_launches": D["launches"], "fresh_token_per_step": D["fresh"],
+                              "decoder_block_form": D["block"],
+                              "cpu_baseline": None if cpu_legs is None else cpu_legs["decode40_first_step"]}
         if other is not None:
             line["other_prefill"] = other
         print(json.dumps(line), flush=True)

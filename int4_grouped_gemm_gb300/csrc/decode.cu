@@ -41,6 +41,7 @@ constexpr int kDecThreads = 512;
 constexpr int kDecWarps = kDecThreads / 32;
 constexpr int kMaxSlots = 9;        // k <= 8 routed + 1 shared
 constexpr int kMaxYSlice = 64;      // output features per block: H / grid (4096 / 64 at least)
+constexpr int kDecWaveCycles = 500; // gap between the waves of gate/up row requests
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -691,7 +692,9 @@ __host__ __device__ inline int decode_stage_words(const DecodeStack &a, bool dow
     return w;
 }
 
-template <int HMAX>
+// BLOCK: the decoder-block form (a.block_form), a separate instance so that
+// the plain stack's code is not touched by it.
+template <int HMAX, bool BLOCK>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __grid_constant__ DecodeStack a) {
     extern __shared__ __align__(16) float dsm[];
     __shared__ int s_idx[kMaxSlots];
@@ -770,7 +773,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         // summed by the previous layer's phase C.  In the decoder-block form
         // every layer: its input x depends on the norm of the whole residual
         // row, which the previous layer's blocks only complete together.
-        const bool phase_a = li == 0 || a.block_form;
+        const bool phase_a = li == 0 || BLOCK;
         if (phase_a) {
             if (li > 0 && !grid_wait(a.ctrl, ++nbar * G, lim, 1, &s_ok)) {  // the residual row is complete
                 cp_async_wait_all();
@@ -780,7 +783,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             const int n_a_units = 4 * (a.E + (P.shg ? 1 : 0));  // + the shared gate's score
             const int u0 = gw;
             if (u0 < n_a_units) router_load(a, P.Wr, P.shg, u0, lane, ur);
-            if (a.block_form)
+            if (BLOCK)
                 stage_norm<HMAX>(in, a.H, P.nw, a.eps, xb, xsum8, xs, s_hown, y_lo, y_hi, s_part, &s_inv);
             else
                 stage_x(in, a.H, xb, xsum8, xs);
@@ -845,7 +848,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                 trace[a.E + 2 * a.k] = s_w[a.k];
             }
         }
-        if (b == 0 && li + 1 < a.n_layers && !a.block_form) {
+        if (b == 0 && li + 1 < a.n_layers && !BLOCK) {
             // the next layer's logit sums start from zero; this buffer was last
             // read by the previous layer's top-k, before the previous barrier
             double *nr = a.racc + ((l + 1) % 2) * kRaccCopies * Es;
@@ -868,7 +871,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             down_requested = true;
         };
         for (int f0 = f_lo + warp; f0 < f_hi; f0 += 2 * kDecWarps) {
-            // both pairs' rows are requested before either is used
+            // both pairs' rows are requested before either is used.  The
+            // warps' first requests go out in four waves about 500 cycles
+            // apart (warps 4w .. 4w+3 in wave w): requests issued together
+            // come back interleaved, so every warp would wait for the end of
+            // the whole stream; in waves the early warps' rows arrive first
+            // and they compute while the later rows stream in (measured on
+            // the 40-layer stack: 3.7 % less time per step than one wave)
+            if (f0 == f_lo + warp && (warp >> 2)) {
+                const long long ts = clock64();
+                while (clock64() - ts < (warp >> 2) * kDecWaveCycles) {
+                }
+            }
             UnitRegs<HMAX> r2[2];
             int64_t rows[2];
 #pragma unroll
@@ -940,13 +954,13 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
                                                            hsum8, hp));
             if (lane == 0) {
                 // the layer's fp32 sum, plus the residual stream in the block form, rounded once
-                const __nv_bfloat16 yb = __float2bfloat16_rn(a.block_form ? y + s_hown[f - y_lo] : y);
+                const __nv_bfloat16 yb = __float2bfloat16_rn(BLOCK ? y + s_hown[f - y_lo] : y);
                 out[f] = yb;
                 s_y[f - y_lo] = __bfloat162float(yb);
             }
         }
         stamp(a, l, 5);
-        if (li + 1 < a.n_layers && a.block_form) {
+        if (li + 1 < a.n_layers && BLOCK) {
             grid_arrive(a.ctrl);  // the next layer's phase A reads the whole residual row
         } else if (li + 1 < a.n_layers) {
             // this block's share of the next layer's router logits: its output
@@ -1027,16 +1041,16 @@ size_t decode_smem_bytes(const DecodeStack &a) {
                             static_cast<size_t>(decode_stage_words(a, a.stage_down, a.stage_router)));
 }
 
-template <int HMAX>
+template <int HMAX, bool BLOCK>
 static cudaError_t launch_decode_t(const DecodeStack &a, int grid, cudaStream_t s) {
     if ((a.H + grid - 1) / grid > kMaxYSlice) return cudaErrorInvalidConfiguration;  // too few SMs for H
     const size_t smem = decode_smem_bytes(a);
-    cudaError_t e = cudaFuncSetAttribute(decode_stack_kernel<HMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_stack_kernel<HMAX, BLOCK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // every block must be resident at once: one per SM
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stack_kernel<HMAX>, kDecThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_stack_kernel<HMAX, BLOCK>, kDecThreads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
     cudaLaunchConfig_t cfg{};
@@ -1049,13 +1063,14 @@ static cudaError_t launch_decode_t(const DecodeStack &a, int grid, cudaStream_t 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_stack_kernel<HMAX>, a);
+    return cudaLaunchKernelEx(&cfg, decode_stack_kernel<HMAX, BLOCK>, a);
 }
 
 cudaError_t launch_decode(const DecodeStack &a0, int grid, cudaStream_t s) {
     DecodeStack a = a0;
     decode_plan(a, grid);
-    return a.H <= 2048 ? launch_decode_t<2048>(a, grid, s) : launch_decode_t<4096>(a, grid, s);
+    if (a.block_form) return a.H <= 2048 ? launch_decode_t<2048, true>(a, grid, s) : launch_decode_t<4096, true>(a, grid, s);
+    return a.H <= 2048 ? launch_decode_t<2048, false>(a, grid, s) : launch_decode_t<4096, false>(a, grid, s);
 }
 
 }  // namespace moe

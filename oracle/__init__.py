@@ -63,6 +63,8 @@ def lib():
         L = ctypes.CDLL(path)
         L.oracle_bf16_round.argtypes = [_p, _i64, _p]
         L.oracle_num_threads.restype = ctypes.c_int
+        L.oracle_set_num_threads.restype = ctypes.c_int
+        L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         L.oracle_quantize.argtypes = [_p, _i64, _i32, _i32, _p, _p, _p]
         L.oracle_dequant.argtypes = [_p, _p, _p, _i64, _i32, _i32, _p]
         L.oracle_router_logits.argtypes = [_p, _i32, _i32, _p, _p, _i32, _p]
@@ -97,6 +99,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return int(lib().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> int:
+    """Threads of the oracle's parallel loops from now on; returns the previous count."""
+    return int(lib().oracle_set_num_threads(int(n)))
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:

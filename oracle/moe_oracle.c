@@ -91,6 +91,22 @@ int oracle_num_threads(void)
 #endif
 }
 
+/* Threads of the parallel loops from now on (the CPU-baseline timing runs the
+ * oracle on all host cores and on one); returns the previous count.  The
+ * per-element arithmetic does not depend on it. */
+int oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    const int prev = omp_get_max_threads();
+    if (n > 0)
+        omp_set_num_threads(n);
+    return prev;
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 /* ------------------------------------------------------- int4 quantiser */
 
 /* Nibble of element p (0..7) inside its word: even elements in nibbles 0-3,
