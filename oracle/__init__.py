@@ -6,8 +6,9 @@ with the CUDA path.  Every function here only marshals numpy arrays; the
 arithmetic is in ``moe_oracle.c`` (whose header cites the passages it follows).
 
 Parity status: quantiser, dequant, router, top-k, routing tables, the
-dense single-expert case and the residual add / RMS norm steps around the
-layer are pinned by ``tests/test_oracle_pins.py``; the
+dense single-expert case, the residual add / RMS norm steps around the
+layer and the GQA decode attention of the second workload are pinned by
+``tests/test_oracle_pins.py``; the
 whole layer beyond those pins is "parity unpinned" (the pages print no worked
 example or output value).
 """
@@ -82,6 +83,7 @@ def lib():
         L.oracle_dispatch_combine_identity.argtypes = [_p, _i32, _i32, _i32, _i32, _i32, _p, _p, _p]
         L.oracle_residual_rmsnorm.argtypes = [_p, _p, _i32, _i32, _p, ctypes.c_double, _p, _p]
         L.oracle_residual_out.argtypes = [_p, _p, _i64, _p]
+        L.oracle_gqa_attention.argtypes = [_p, _p, _p, _i32, _i32, _i32, _i32, _i32, ctypes.c_double, _p]
         _lib = L
     return _lib
 
@@ -294,3 +296,18 @@ def dispatch_combine_identity(x_bits, E, has_shared, idx, w) -> np.ndarray:
     lib().oracle_dispatch_combine_identity(_ptr(x_bits), T, H, E, idx.shape[1], int(has_shared),
                                            _ptr(idx), _ptr(w), _ptr(y))
     return y
+
+
+def gqa_attention(q_bits: np.ndarray, k_bits: np.ndarray, v_bits: np.ndarray, L: int, scale: float) -> np.ndarray:
+    """Decode attention of one token (second workload): q [Hq, D], k / v
+    [Hkv, L_cap, D] bf16 bit patterns, the first L positions attended;
+    query head h uses key-value head h // (Hq // Hkv).  Returns fp64 [Hq, D]."""
+    q_bits = _c(q_bits, np.uint16)
+    k_bits = _c(k_bits, np.uint16)
+    v_bits = _c(v_bits, np.uint16)
+    Hq, D = q_bits.shape
+    Hkv, L_cap, D2 = k_bits.shape
+    assert D2 == D and v_bits.shape == k_bits.shape and Hq % Hkv == 0 and 1 <= L <= L_cap
+    o = np.empty((Hq, D), np.float64)
+    lib().oracle_gqa_attention(_ptr(q_bits), _ptr(k_bits), _ptr(v_bits), Hq, Hkv, D, L, L_cap, float(scale), _ptr(o))
+    return o

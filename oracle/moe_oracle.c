@@ -573,3 +573,57 @@ void oracle_residual_out(const uint16_t *h, const double *y, int64_t n, uint16_t
     for (int64_t i = 0; i < n; ++i)
         out[i] = bf16_from_double((double)float_from_bf16(h[i]) + y[i]);
 }
+
+/* ------------------------------------- GQA decode attention (second workload) */
+
+/*
+ * One new token's attention over a cache of L positions, with query heads
+ * sharing key-value heads ([MoE] page, section "The architecture that forces
+ * the issue": full-attention layers use grouped-query attention, 16 query
+ * heads sharing 2 key-value heads; same page, section "How this compares to
+ * what else is happening on Apple Silicon": GQA packing loads each shared KV
+ * row once instead of once per query head).  Readings where the pages are
+ * silent: query head h uses key-value head h / (Hq / Hkv) (consecutive query
+ * heads share one), scores are scaled by `scale` (1 / sqrt(D) in the tests
+ * and benchmark), the softmax runs over all L cached positions (the new
+ * token's own key and value are already in the cache).  For each head h:
+ *   s_t    = scale * sum_d q[h][d] k[g][t][d]          (fp64)
+ *   p_t    = exp(s_t - max_t s_t) / sum_t exp(s_t - max_t s_t)
+ *   o[h][d] = sum_t p_t v[g][t][d]
+ * q: bf16 bits [Hq][D]; k, v: bf16 bits [Hkv][L_cap][D], positions 0..L-1
+ * used; o: fp64 [Hq][D].
+ */
+void oracle_gqa_attention(const uint16_t *q, const uint16_t *k, const uint16_t *v, int32_t Hq, int32_t Hkv,
+                          int32_t D, int32_t L, int32_t L_cap, double scale, double *o)
+{
+    const int32_t group = Hq / Hkv;
+#pragma omp parallel for schedule(static)
+    for (int32_t h = 0; h < Hq; ++h) {
+        const int32_t g = h / group;
+        const uint16_t *kh = k + (int64_t)g * L_cap * D;
+        const uint16_t *vh = v + (int64_t)g * L_cap * D;
+        double *s = (double *)malloc(sizeof(double) * (size_t)L);
+        double mx = -INFINITY;
+        for (int32_t t = 0; t < L; ++t) {
+            double acc = 0.0;
+            for (int32_t d = 0; d < D; ++d)
+                acc += (double)float_from_bf16(q[(int64_t)h * D + d]) *
+                       (double)float_from_bf16(kh[(int64_t)t * D + d]);
+            s[t] = scale * acc;
+            if (s[t] > mx)
+                mx = s[t];
+        }
+        double sum = 0.0;
+        for (int32_t t = 0; t < L; ++t) {
+            s[t] = exp(s[t] - mx);
+            sum += s[t];
+        }
+        for (int32_t d = 0; d < D; ++d) {
+            double acc = 0.0;
+            for (int32_t t = 0; t < L; ++t)
+                acc += s[t] * (double)float_from_bf16(vh[(int64_t)t * D + d]);
+            o[(int64_t)h * D + d] = acc / sum;
+        }
+        free(s);
+    }
+}

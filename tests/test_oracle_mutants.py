@@ -3,7 +3,8 @@ below plants one mistake in a copy of the oracle's C source (nibble order,
 scale, rounding, sign of the bias, router bias or K range, tie-break,
 renormalisation, SwiGLU operand order, stable token order, shared expert,
 down projection index, the RMS norm's mean, eps and weight, the residual add
-after the layer), builds it, and runs the pins against it; at least
+after the layer, the attention's head groups, scale, normalisation and
+position range), builds it, and runs the pins against it; at least
 one pin must fail.  The shipped oracle is never modified."""
 import os
 import subprocess
@@ -50,6 +51,11 @@ MUTANTS = [
      "out[i] = bf16_from_double(y[i]);"),
     ("double_rounding_to_bf16", "return bf16_from_float((float)ldexp(r, e - 8));",
      "return bf16_from_float((float)v);"),
+    ("attention_heads_interleaved", "const int32_t g = h / group;", "const int32_t g = h % Hkv;"),
+    ("attention_scale_dropped", "s[t] = scale * acc;", "s[t] = acc;"),
+    ("attention_not_normalised", "o[(int64_t)h * D + d] = acc / sum;", "o[(int64_t)h * D + d] = acc;"),
+    ("attention_misses_last_position", "        for (int32_t t = 0; t < L; ++t) {\n            double acc = 0.0;",
+     "        for (int32_t t = 0; t < L - 1; ++t) {\n            double acc = 0.0;"),
 ]
 
 

@@ -445,3 +445,80 @@ def test_block_with_zero_experts_is_the_residual_stream():
     blk = oracle.moe_block(a, r, w, 1e-6, L.router_w.numpy(), None, gate, up, down, cfg.E, cfg.k, True)
     plain = oracle.moe_layer(blk["x"], L.router_w.numpy(), None, gate, up, down, cfg.E, cfg.k, True)
     assert np.array_equal(blk["out"], oracle.residual_out(blk["h"], plain["y"]))
+
+
+# ------------------------------------------------ GQA decode attention (second workload)
+
+def _attn_inputs(Hq, Hkv, D, L_cap, seed, scale_kv=1.0):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(Hq, D, generator=g).to(torch.bfloat16)
+    k = (torch.randn(Hkv, L_cap, D, generator=g) * scale_kv).to(torch.bfloat16)
+    v = torch.randn(Hkv, L_cap, D, generator=g).to(torch.bfloat16)
+    bits = lambda t: synthetic.bf16_bits(t).numpy().view(np.uint16)  # noqa: E731
+    return q, k, v, bits(q), bits(k), bits(v)
+
+
+def test_attention_single_position_returns_its_value():
+    """L = 1: the only position gets probability 1, so every query head of a
+    group returns that position's value row exactly."""
+    q, k, v, qb, kb, vb = _attn_inputs(16, 2, 64, 3, seed=101)
+    o = oracle.gqa_attention(qb, kb, vb, 1, 0.125)
+    for h in range(16):
+        np.testing.assert_array_equal(o[h], v[h // 8, 0].float().numpy().astype(np.float64))
+
+
+def test_attention_equal_keys_average_the_values():
+    """Identical keys (or scale 0) give every position the same probability:
+    the output is the plain mean of the value rows."""
+    q, k, v, qb, kb, vb = _attn_inputs(8, 2, 32, 20, seed=102)
+    kb_same = np.broadcast_to(kb[:, :1, :], kb.shape).copy()
+    mean = v[:, :13].float().numpy().astype(np.float64).mean(axis=1)
+    for o in (oracle.gqa_attention(qb, kb_same, vb, 13, 0.177), oracle.gqa_attention(qb, kb, vb, 13, 0.0)):
+        for h in range(8):
+            np.testing.assert_allclose(o[h], mean[h // 4], rtol=1e-12, atol=1e-14)
+
+
+def test_attention_against_scipy_softmax():
+    """Random heads against an independent float64 evaluation with the
+    library softmax: scores K q * scale, probabilities softmax, output p V."""
+    from scipy.special import softmax
+    Hq, Hkv, D, L = 16, 2, 128, 37
+    q, k, v, qb, kb, vb = _attn_inputs(Hq, Hkv, D, 50, seed=103)
+    scale = 1.0 / np.sqrt(D)
+    o = oracle.gqa_attention(qb, kb, vb, L, scale)
+    qf, kf, vf = (t.float().numpy().astype(np.float64) for t in (q, k, v))
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        p = softmax(kf[g, :L] @ qf[h] * scale)
+        np.testing.assert_allclose(o[h], p @ vf[g, :L], rtol=1e-11, atol=1e-13)
+
+
+def test_attention_query_heads_share_consecutive_groups():
+    """Query heads 0-7 read key-value head 0 and heads 8-15 head 1: zeroing
+    head 1's values zeroes exactly heads 8-15, and swapping the two key-value
+    heads swaps the two halves of the output."""
+    q, k, v, qb, kb, vb = _attn_inputs(16, 2, 64, 9, seed=104)
+    vz = vb.copy()
+    vz[1] = 0
+    o = oracle.gqa_attention(qb, kb, vz, 9, 0.125)
+    assert np.all(o[8:] == 0.0) and np.all(np.abs(o[:8]).sum(axis=1) > 0)
+    q_sw = np.concatenate([qb[8:], qb[:8]])
+    o_sw = oracle.gqa_attention(q_sw, kb[::-1].copy(), vb[::-1].copy(), 9, 0.125)
+    base = oracle.gqa_attention(qb, kb, vb, 9, 0.125)
+    np.testing.assert_array_equal(o_sw, np.concatenate([base[8:], base[:8]]))
+
+
+def test_attention_ignores_positions_past_L_and_their_order():
+    """Only the first L cached positions count (huge values past them change
+    nothing), and permuting those positions (keys and values together)
+    leaves the output unchanged up to summation order."""
+    q, k, v, qb, kb, vb = _attn_inputs(8, 1, 32, 40, seed=105)
+    o = oracle.gqa_attention(qb, kb, vb, 29, 0.2)
+    big = synthetic.bf16_bits(torch.full((1, 11, 32), 1e4).to(torch.bfloat16)).numpy().view(np.uint16)
+    kb2, vb2 = kb.copy(), vb.copy()
+    kb2[:, 29:], vb2[:, 29:] = big, big
+    np.testing.assert_array_equal(oracle.gqa_attention(qb, kb2, vb2, 29, 0.2), o)
+    perm = np.random.default_rng(7).permutation(29)
+    kp, vp = kb.copy(), vb.copy()
+    kp[:, :29], vp[:, :29] = kb[:, perm], vb[:, perm]
+    np.testing.assert_allclose(oracle.gqa_attention(qb, kp, vp, 29, 0.2), o, rtol=1e-12, atol=1e-14)
