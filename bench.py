@@ -547,6 +547,78 @@ def run_prefill_other(name, pk, steps=10):
             "experts_touched": touched, "note": cfg.name}
 
 
+def run_attention(pk, steps=20):
+    """GQA decode attention (the second workload): one token over a cache of
+    L positions, 16 query heads sharing 2 key-value heads, head dimension 128;
+    graph-replayed calls, L2 flushed before each; bytes = the key and value
+    rows read (2 * Hkv * L * D * 2), against HBM.  The per-head variant (each
+    query head reading its key-value rows itself) gives the packing's gain."""
+    import math
+    import torch
+    from int4_grouped_gemm_gb300 import _lib, synthetic
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    out = {}
+    for name in ("gqa4k", "gqa32k", "gqa128k"):
+        cfg = synthetic.ATTN_CONFIGS[name]
+        q, k, v = (t.cuda() for t in synthetic.make_attention(cfg, device="cpu"))
+        o = torch.empty_like(q)
+        ws = torch.empty(_lib.gqa_attention_workspace_bytes(cfg.Hq, cfg.Hkv, cfg.D, cfg.L), dtype=torch.uint8,
+                         device="cuda")
+        scale = 1.0 / math.sqrt(cfg.D)
+        res = {}
+        for per_head in (False, True):
+            call = lambda: _lib.gqa_decode_attention(q, k, v, cfg.L, scale, o, ws, per_head=per_head)  # noqa: E731
+            for _ in range(3):
+                call()
+            graph = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                call()
+            torch.cuda.current_stream().wait_stream(side)
+            with torch.cuda.graph(graph):
+                call()
+            torch.cuda.synchronize()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+            for i in range(steps):
+                flush.fill_(i & 0xFF)
+                ev[i][0].record()
+                graph.replay()
+                ev[i][1].record()
+            torch.cuda.synchronize()
+            res[per_head] = statistics.median(a.elapsed_time(b) for a, b in ev)
+            del graph
+        kv_bytes = 2 * cfg.Hkv * cfg.L * cfg.D * 2
+        gbs = kv_bytes / (res[False] * 1e-3) / 1e9
+        out[name] = {"L": cfg.L, "Hq": cfg.Hq, "Hkv": cfg.Hkv, "D": cfg.D, "us_per_call": round(res[False] * 1e3, 2),
+                     "kv_bytes": kv_bytes, "hbm_gbs": round(gbs, 1), "frac_of_hbm": round(gbs / pk["hbm"], 4),
+                     "per_head_us_per_call": round(res[True] * 1e3, 2),
+                     "packing_speedup": round(res[True] / res[False], 3), "gpu_launches_per_call": 2}
+        del q, k, v, o, ws
+    out["note"] = ("gqa_decode_attention: packed = each key-value row read once for the 8 query heads sharing it; "
+                   "per_head = each query head's blocks read the rows themselves (the layout packing replaces)")
+    del flush
+    torch.cuda.empty_cache()
+    return out
+
+
+def cpu_attention_leg():
+    """The oracle on the 32K-position attention (all 16 heads, fp64 loops)."""
+    import math
+    import oracle
+    from int4_grouped_gemm_gb300 import synthetic
+    cfg = synthetic.ATTN_CONFIGS["gqa32k"]
+    q, k, v = synthetic.make_attention(cfg)
+    bits = lambda t: synthetic.bf16_bits(t).numpy().view("uint16")  # noqa: E731
+    qb, kb, vb = bits(q), bits(k), bits(v)
+    t0 = time.perf_counter()
+    oracle.gqa_attention(qb, kb, vb, cfg.L, 1.0 / math.sqrt(cfg.D))
+    t = time.perf_counter() - t0
+    return {"value": round(1.0 / t, 3), "unit": "calls/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "host_cores": len(os.sched_getaffinity(0)), "seconds": round(t, 3),
+            "sample": f"one full call: {cfg.Hq} query heads over {cfg.L} positions, fp64 C loops"}
+
+
 # ------------------------------------------------------------ CPU oracle
 
 
@@ -755,9 +827,11 @@ def main():
     if not args.no_decode and rank == 0:
         D = run_decode(args, pk)
     other = None
+    attn = None
     if rank == 0 and not args.no_other:
         other = {n: run_prefill_other(n, pk) for n in ("prefill512", "skew16384")}
         other["small_batches_through_moe_prefill"], other["small_batch_decode"] = run_small_batches(pk)
+        attn = run_attention(pk)
     cpu = None
     cpu_legs = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -767,6 +841,7 @@ def main():
             "prefill4096_one_thread": cpu_prefill_leg(PREFILL_CFG, 24, threads=1, seed=3),
             "skew16384_sample": cpu_prefill_leg("skew16384", 768, seed=4),
             "decode40_first_step": cpu_decode_leg(),
+            "gqa32k_attention": cpu_attention_leg(),
         }
     if rank == 0:
         line = {
@@ -805,6 +880,10 @@ def main():
                               "cpu_baseline": None if cpu_legs is None else cpu_legs["decode40_first_step"]}
         if other is not None:
             line["other_prefill"] = other
+        if attn is not None:
+            if cpu_legs is not None:
+                attn["cpu_baseline"] = cpu_legs["gqa32k_attention"]
+            line["gqa_decode_attention"] = attn
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

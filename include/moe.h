@@ -404,6 +404,40 @@ int moe_forward_host_stream(const moe_layer_desc *desc, const void *const *x_hos
                             int32_t T, void *const *x_dev, void *const *y_dev, void *ws, size_t ws_bytes,
                             cudaStream_t stream);
 
+/* ------------------------------------------------ GQA decode attention
+ * The second workload: one new token's attention over a key-value cache with
+ * grouped-query heads ("Lily: Perplexity's Custom Inference Engine for Apple
+ * Silicon", section "The architecture that forces the issue: MoE plus Gated
+ * DeltaNet": 16 query heads share 2 key-value heads in the model's
+ * full-attention layers; same page, section "How this compares to what else
+ * is happening on Apple Silicon": GQA packing loads each shared key-value row
+ * once, not once per query head; "Inside Lily ...", "Key Optimizations at a
+ * Glance": +23.8 % decode at 32K context).  For query head h, key-value head
+ * g = h / (Hq / Hkv) (consecutive query heads share one):
+ *   s_t     = scale * sum_d q[h][d] k[g][t][d]        t = 0 .. L-1
+ *   o[h][d] = sum_t softmax(s)_t v[g][t][d]            fp32, bf16 out
+ * q, out: [Hq][D] bf16; k_cache, v_cache: [Hkv][L_cap][D] bf16, the first L
+ * positions attended (the new token's own key and value already in them).
+ * All device pointers, 16-byte aligned, owned by the caller.  Supported:
+ * D in {64, 128}, Hq % Hkv == 0, Hq / Hkv <= 8, Hq <= 256, 1 <= L <= L_cap
+ * <= 2^26 (else MOE_ERR_SHAPE / MOE_ERR_TOKENS).  The workspace holds the
+ * partial outputs of the position ranges (gqa_attention_workspace_bytes, no
+ * initialisation needed).  No synchronisation; work enqueued on `stream`.
+ */
+size_t gqa_attention_workspace_bytes(int32_t Hq, int32_t Hkv, int32_t D, int32_t L);
+
+/* Packed: each block reads a range of one key-value head's rows once and
+ * scores them against all of the head's query heads. */
+int gqa_decode_attention(const void *q, const void *k_cache, const void *v_cache, int32_t Hq, int32_t Hkv, int32_t D,
+                         int32_t L, int32_t L_cap, float scale, void *out, void *ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/* The same result with one query head per block, each reading its
+ * key-value rows itself: the layout that packing replaces, for comparison. */
+int gqa_decode_attention_per_head(const void *q, const void *k_cache, const void *v_cache, int32_t Hq,
+                                  int32_t Hkv, int32_t D, int32_t L, int32_t L_cap, float scale, void *out,
+                                  void *ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Human-readable text for a status code. */
 const char *moe_status_string(int code);
 

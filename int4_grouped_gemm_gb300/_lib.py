@@ -88,6 +88,11 @@ SIGNATURES = {
     "moe_forward_host": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_p, c_p, c_sz, c_p]),
     "moe_forward_host_stream": (ctypes.c_int, [c_p, c_p, c_p, c_i32, c_i32, c_p, c_p, c_p, c_sz, c_p]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "gqa_attention_workspace_bytes": (c_sz, [c_i32, c_i32, c_i32, c_i32]),
+    "gqa_decode_attention": (ctypes.c_int, [c_p, c_p, c_p, c_i32, c_i32, c_i32, c_i32, c_i32, ctypes.c_float, c_p,
+                                            c_p, c_sz, c_p]),
+    "gqa_decode_attention_per_head": (ctypes.c_int, [c_p, c_p, c_p, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                                     ctypes.c_float, c_p, c_p, c_sz, c_p]),
 }
 
 
@@ -292,3 +297,19 @@ def moe_forward_host_stream(desc: moe_layer_desc, x_hosts, T: int, y_hosts, x_de
     _check(load().moe_forward_host_stream(ctypes.byref(desc), xs, ys, n, T, xd, yd, _ptr(ws),
                                           ws.numel() * ws.element_size(), _stream(stream)),
            "moe_forward_host_stream")
+
+
+# ---------------------------------------------------- GQA decode attention
+
+
+def gqa_attention_workspace_bytes(Hq: int, Hkv: int, D: int, L: int) -> int:
+    return int(load().gqa_attention_workspace_bytes(Hq, Hkv, D, L))
+
+
+def gqa_decode_attention(q, k_cache, v_cache, L: int, scale: float, out, ws, per_head: bool = False, stream=None):
+    """q [Hq, D], k_cache / v_cache [Hkv, L_cap, D] bf16 (device); out [Hq, D]."""
+    Hq, D = q.shape
+    Hkv, L_cap, _ = k_cache.shape
+    fn = load().gqa_decode_attention_per_head if per_head else load().gqa_decode_attention
+    _check(fn(_ptr(q), _ptr(k_cache), _ptr(v_cache), Hq, Hkv, D, L, L_cap, float(scale), _ptr(out), _ptr(ws),
+              ws.numel() * ws.element_size(), _stream(stream)), "gqa_decode_attention")

@@ -19,7 +19,8 @@ ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libmoe_gb300.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
-SOURCES = ["api.cu", "pack.cu", "routing.cu", "grouped_gemm.cu", "decode.cu", "small_batch.cu", "block.cu"]
+SOURCES = ["api.cu", "pack.cu", "routing.cu", "grouped_gemm.cu", "decode.cu", "small_batch.cu", "block.cu",
+           "attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I" + os.path.join(ROOT, "include")]

@@ -5,6 +5,7 @@
 
 #include <mutex>
 
+#include "attention.cuh"
 #include "block.cuh"
 #include "kernels.cuh"
 #include "routing_ext.cuh"
@@ -658,6 +659,72 @@ int moe_forward_host_stream(const moe_layer_desc *desc, const void *const *x_hos
     if (h2d) cudaStreamDestroy(h2d);
     if (d2h) cudaStreamDestroy(d2h);
     return rc;
+}
+
+// ------------------------------------------------ GQA decode attention
+
+static constexpr int kGqaMaxSms = 256;  // workspace sized for any GPU up to this many SMs
+
+static int gqa_check(const void *q, const void *k, const void *v, int32_t Hq, int32_t Hkv, int32_t D, int32_t L,
+                     int32_t L_cap, float scale, const void *out, const void *ws) {
+    int rc;
+    if ((rc = check_ptr(q)) || (rc = check_ptr(k)) || (rc = check_ptr(v)) || (rc = check_ptr(out)) ||
+        (rc = check_ptr(ws)))
+        return rc;
+    if (D != 64 && D != 128) return MOE_ERR_SHAPE;
+    if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || Hq / Hkv > 8 || Hq > 256) return MOE_ERR_SHAPE;
+    if (!(scale == scale) || scale > 1e30f || scale < -1e30f) return MOE_ERR_SHAPE;
+    if (L < 1 || L_cap < L || L_cap > (1 << 26)) return MOE_ERR_TOKENS;
+    return MOE_OK;
+}
+
+size_t gqa_attention_workspace_bytes(int32_t Hq, int32_t Hkv, int32_t D, int32_t L) {
+    if (D != 64 && D != 128) return 0;
+    if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || Hq / Hkv > 8 || Hq > 256 || L < 1) return 0;
+    const size_t packed = gqa_part_bytes(Hkv, gqa_splits(L, Hkv, kGqaMaxSms), D);
+    const size_t per_head = gqa_part_bytes(Hq, gqa_splits(L, Hq, kGqaMaxSms), D);
+    return packed > per_head ? packed : per_head;
+}
+
+static int gqa_run(const void *q, const void *k, const void *v, int32_t Hq, int32_t Hkv, int32_t D, int32_t L,
+                   int32_t L_cap, float scale, void *out, void *ws, size_t ws_bytes, bool packed,
+                   cudaStream_t stream) {
+    int rc = gqa_check(q, k, v, Hq, Hkv, D, L, L_cap, scale, out, ws);
+    if (rc) return rc;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    if (dev->num_sms > kGqaMaxSms) return MOE_ERR_DEVICE;
+    GqaArgs a{};
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k = static_cast<const __nv_bfloat16 *>(k);
+    a.v = static_cast<const __nv_bfloat16 *>(v);
+    a.out = static_cast<__nv_bfloat16 *>(out);
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.D = D;
+    a.L = L;
+    a.L_cap = L_cap;
+    a.group = Hq / Hkv;
+    a.qpb = packed ? a.group : 1;
+    a.nsplit = gqa_splits(L, Hq / a.qpb, dev->num_sms);
+    a.scale = scale;
+    const int blocks_y = Hq / a.qpb;
+    if (ws_bytes < gqa_part_bytes(blocks_y, a.nsplit, D)) return MOE_ERR_WORKSPACE;
+    a.part_o = static_cast<float *>(ws);
+    a.part_ml = a.part_o + static_cast<size_t>(blocks_y) * a.nsplit * 8 * D;
+    return cuda_rc(launch_gqa(a, stream));
+}
+
+int gqa_decode_attention(const void *q, const void *k_cache, const void *v_cache, int32_t Hq, int32_t Hkv, int32_t D,
+                         int32_t L, int32_t L_cap, float scale, void *out, void *ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+    return gqa_run(q, k_cache, v_cache, Hq, Hkv, D, L, L_cap, scale, out, ws, ws_bytes, true, stream);
+}
+
+int gqa_decode_attention_per_head(const void *q, const void *k_cache, const void *v_cache, int32_t Hq,
+                                  int32_t Hkv, int32_t D, int32_t L, int32_t L_cap, float scale, void *out,
+                                  void *ws, size_t ws_bytes, cudaStream_t stream) {
+    return gqa_run(q, k_cache, v_cache, Hq, Hkv, D, L, L_cap, scale, out, ws, ws_bytes, false, stream);
 }
 
 const char *moe_status_string(int code) {

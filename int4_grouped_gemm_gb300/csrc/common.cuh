@@ -268,4 +268,19 @@ __device__ __forceinline__ uint4 dequant8_bf16(uint32_t word, __nv_bfloat162 s2,
     return out;
 }
 
+// ------------------------------------------------------- legacy tensor core
+
+// D += A B for one m16n8k16 tile, bf16 operands and fp32 accumulators (the
+// register fragments of mma.sync: thread (g, c) = (lane / 4, lane % 4) holds
+// A rows g and g + 8 at columns 2c, 2c+1 (a[0], a[1]) and 2c+8, 2c+9 (a[2],
+// a[3]), B rows 2c, 2c+1 (b0) and 2c+8, 2c+9 (b1) of column g, and D rows
+// g, g + 8 at columns 2c, 2c+1).
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
 }  // namespace moe

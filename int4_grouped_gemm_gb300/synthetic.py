@@ -155,3 +155,43 @@ def bf16_bits(t: torch.Tensor) -> torch.Tensor:
     """Reinterpret a bf16 tensor as int16 bit patterns (no arithmetic)."""
     return t.contiguous().view(torch.int16)
 
+
+
+@dataclass(frozen=True)
+class AttnConfig:
+    """Decode attention of one token (the second workload): Hq query heads
+    sharing Hkv key-value heads, head dimension D, L cached positions (the
+    cache holds L_cap)."""
+    name: str
+    Hq: int
+    Hkv: int
+    D: int
+    L: int
+    seed: int
+    L_cap: int = 0        # 0: L
+    k_scale: float = 1.0  # standard deviation of the keys
+
+    @property
+    def cap(self) -> int:
+        return self.L_cap or self.L
+
+
+# 16 query heads sharing 2 key-value heads ("Lily: ...", section "The
+# architecture that forces the issue: MoE plus Gated DeltaNet"); head
+# dimension 128 (the pages give none); 32K context, where the pages quote
+# the packing's gain ("Inside Lily ...", "Key Optimizations at a Glance")
+ATTN_CONFIGS = {
+    "gqa32k": AttnConfig("gqa32k", Hq=16, Hkv=2, D=128, L=32768, seed=11),
+    "gqa4k": AttnConfig("gqa4k", Hq=16, Hkv=2, D=128, L=4096, seed=12),
+    "gqa128k": AttnConfig("gqa128k", Hq=16, Hkv=2, D=128, L=131072, seed=13),
+}
+
+
+def make_attention(cfg: AttnConfig, device="cpu"):
+    """Seeded q [Hq, D], k, v [Hkv, L_cap, D] in bf16: q and v N(0, 1), k
+    N(0, k_scale^2); draw order q, k, v."""
+    g = _gen(device, cfg.seed)
+    q = torch.randn(cfg.Hq, cfg.D, generator=g, device=device).to(torch.bfloat16)
+    k = (torch.randn(cfg.Hkv, cfg.cap, cfg.D, generator=g, device=device) * cfg.k_scale).to(torch.bfloat16)
+    v = torch.randn(cfg.Hkv, cfg.cap, cfg.D, generator=g, device=device).to(torch.bfloat16)
+    return q, k, v
