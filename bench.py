@@ -51,6 +51,9 @@ def parse():
                     help="only run warmup + steps prefill calls of the headline layer (for ncu captures)")
     ap.add_argument("--profile-decode", action="store_true",
                     help="only run warmup + steps eager decode passes through 4 layers (for ncu captures)")
+    ap.add_argument("--profile-attention", action="store_true",
+                    help="only run warmup + steps packed GQA decode-attention calls over the 32K cache "
+                         "(for ncu captures)")
     ap.add_argument("--profile-batch", action="store_true",
                     help="only run warmup + steps moe_decode_batch calls with 1 and then 8 tokens on one layer of "
                          "the T=512 shapes (for ncu captures)")
@@ -772,6 +775,18 @@ def profile_only(args):
         y = torch.empty_like(x)
         for _ in range(args.warmup + args.steps):
             _lib.moe_prefill(layer.desc, x, cfg.T, y, ws.buf)
+    elif args.profile_attention:
+        import math
+        cfg = synthetic.ATTN_CONFIGS["gqa32k"]
+        q, k, v = (t.cuda() for t in synthetic.make_attention(cfg))
+        o = torch.empty_like(q)
+        ws = torch.empty(_lib.gqa_attention_workspace_bytes(cfg.Hq, cfg.Hkv, cfg.D, cfg.L), dtype=torch.uint8,
+                         device="cuda")
+        for _ in range(args.warmup + args.steps):
+            _lib.gqa_decode_attention(q, k, v, cfg.L, 1.0 / math.sqrt(cfg.D), o, ws)
+        torch.cuda.synchronize()
+        print(json.dumps({"profile_run": "ok", "status": 0}))
+        return
     elif args.profile_batch:
         cfg = synthetic.CONFIGS["prefill512"]
         layer, x = build_prefill(cfg)
@@ -815,7 +830,7 @@ def main():
     rank, world = dist_setup(args.gpus)
     from int4_grouped_gemm_gb300 import _lib
     _lib.load()
-    if args.profile or args.profile_decode or args.profile_batch:
+    if args.profile or args.profile_decode or args.profile_batch or args.profile_attention:
         profile_only(args)
         return
     pk = peaks()

@@ -432,24 +432,36 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         const int hf = dt / BN;  // 32-element half of the stage
         const int r = dt % BN;   // weight row of the tile
         uint32_t bit = 0, qit = 0, sit = 0;
+        uint4 sv = make_uint4(0u, 0u, 0u, 0u), bv = sv;  // this row's scales and biases of the current block
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
             for (int ks = 0; ks < ksteps; ++ks) {
-                const int ss = sit % NS_S;
                 if (ks % ks_per_sblock == 0) {
+                    // the row's 8 scales and 8 biases in two 16-byte reads (32
+                    // consecutive rows: 512 contiguous bytes per warp, no bank
+                    // conflicts), then the stage goes back to the producer
+                    const int ss = sit % NS_S;
                     ok = wait_or_abort(&s->s_full[ss], (sit / NS_S) & 1, a, s, 8);
                     if (!ok) break;
+                    const uint16_t *sblk = reinterpret_cast<const uint16_t *>(sS + ss * S_STAGE) + r * SG;
+                    sv = *reinterpret_cast<const uint4 *>(sblk);
+                    bv = *reinterpret_cast<const uint4 *>(sblk + BN * SG);  // bias block: 4096 bytes after the scales
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&s->s_empty[ss]);
+                    ++sit;
                 }
                 const int qs = qit % NS_Q, bs = bit % NS_B;
                 ok = wait_or_abort(&s->q_full[qs], (qit / NS_Q) & 1, a, s, 9) &&
                      wait_or_abort(&s->b_empty[bs], ((bit / NS_B) & 1) ^ 1, a, s, 10);
                 if (!ok) break;
                 const uint4 nib = *reinterpret_cast<const uint4 *>(sQ + qs * Q_STAGE + hf * Q_HALF + r * 16);
-                const uint16_t *sblk = reinterpret_cast<const uint16_t *>(sS + ss * S_STAGE) + r * SG;
-                const uint16_t *bblk = sblk + BN * SG;  // bias block: 4096 bytes after the scales
                 const int gl = ((ks * GK + hf * 32) / a.G) % SG;
-                const __nv_bfloat162 s2 = u32_as_bf162(static_cast<uint32_t>(sblk[gl]) * 0x10001u);
-                const __nv_bfloat162 b2 = u32_as_bf162(static_cast<uint32_t>(bblk[gl]) * 0x10001u);
+                const uint32_t sw = (gl >> 1) == 0 ? sv.x : (gl >> 1) == 1 ? sv.y : (gl >> 1) == 2 ? sv.z : sv.w;
+                const uint32_t bw = (gl >> 1) == 0 ? bv.x : (gl >> 1) == 1 ? bv.y : (gl >> 1) == 2 ? bv.z : bv.w;
+                const uint32_t sbits = (gl & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+                const uint32_t bbits = (gl & 1) ? (bw >> 16) : (bw & 0xFFFFu);
+                const __nv_bfloat162 s2 = u32_as_bf162(sbits * 0x10001u);
+                const __nv_bfloat162 b2 = u32_as_bf162(bbits * 0x10001u);
                 uint8_t *brow = sB + bs * B_STAGE + r * 128;
                 const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
 #pragma unroll
@@ -465,10 +477,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 }
                 ++qit;
                 ++bit;
-                if (ks % ks_per_sblock == ks_per_sblock - 1 || ks == ksteps - 1) {
-                    if (lane == 0) mbar_arrive(&s->s_empty[ss]);
-                    ++sit;
-                }
             }
         }
     } else if (warp < kEpiWarps) {
