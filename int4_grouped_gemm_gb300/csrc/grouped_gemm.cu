@@ -24,11 +24,13 @@
 //               token rows straight from x (no permuted copy of x)
 //   warp 10     down/router A producer: TMA loads of both token tiles (2 x 16 KB
 //               boxes per stage) from h (down) or from x (router)
-//   warp 8      W producer: TMA loads of packed nibbles (8 KB per stage, two
-//               16-byte halves per row so that each dequant thread reads 16
-//               contiguous bytes) and of scale/bias blocks (8 groups x 256
-//               rows); router mode: the bf16 router weight tile straight into
-//               the B ring
+//   warp 8      W producer: TMA loads of packed nibbles (16 KB per load: 64
+//               bytes of each of the 256 weight rows, two stages' worth, in
+//               the 64-byte swizzle so that the dequant threads' 16-byte reads
+//               are conflict-free; a TMA load costs per box row, so wide rows
+//               matter) and of scale/bias blocks (8 groups x 256 rows);
+//               router mode: the bf16 router weight tile straight into the B
+//               ring
 //   warps 11-26 dequantisers, two threads per weight row (one per 32-element
 //               half of the stage): nibbles -> bf16 s*q+b in the 128-byte
 //               swizzled K-major layout of the B ring
@@ -54,9 +56,9 @@ constexpr int TPU = 2;                           // token tiles per work unit
 constexpr int BN = 256;                          // weight rows per tile (MMA N)
 constexpr int GK = 64;                           // K elements per stage
 constexpr int SG = 8;                            // quantisation groups per scale block
-constexpr int NS_A = 3, NS_B = 2, NS_S = 2;      // ring depths
-constexpr int kMaxNsQ = 4;
-__host__ __device__ constexpr int ns_q(int mode) { return mode == 1 ? 3 : 4; }
+constexpr int NS_A = 3, NS_B = 2, NS_S = 1;      // ring depths (stages)
+constexpr int QK = 2;                            // stages per nibble load
+constexpr int NS_Q = 2;                          // nibble ring depth (loads)
 constexpr int kEpiWarps = 8, kWProdWarp = 8, kMmaWarp = 9, kAProdWarp = 10, kDeqWarp0 = 11, kDeqWarps = 16;
 constexpr int kLsuWarp0 = kDeqWarp0 + kDeqWarps, kLsuWarps = 4;  // gate/up: token-row copiers
 constexpr int kLsuThreads = kLsuWarps * 32;
@@ -66,8 +68,8 @@ __host__ __device__ constexpr int gemm_threads(int mode) {
 constexpr int TILE_A = BM * 128;                 // 16 KB: 128 token rows x 64 bf16
 constexpr int A_STAGE = TPU * TILE_A;            // 32 KB: both token tiles
 constexpr int B_STAGE = BN * 128;                // 32 KB: 256 weight rows x 64 bf16
-constexpr int Q_HALF = BN * 16;                  // 4 KB: 256 rows x 32 nibbles
-constexpr int Q_STAGE = 2 * Q_HALF;              // 8 KB
+constexpr int Q_ROW = QK * GK / 2;               // 64 bytes of a weight row per nibble load
+constexpr int Q_LOAD = BN * Q_ROW;               // 16 KB: 256 rows x 128 nibbles
 constexpr int S_STAGE = 2 * BN * SG * 2;         // 8 KB: [scale|bias][256 rows][8 groups] bf16
 constexpr int T_PITCH = 20;                      // fp32 pitch of the epilogue transpose rows
 constexpr uint32_t kTmemCols = 512;              // two 256-column fp32 accumulators
@@ -78,7 +80,7 @@ constexpr int kRouterUnits = kRouterParts * kRouterKSplit;  // router units per 
 struct Smem {
     uint64_t a_full[NS_A], a_empty[NS_A];
     uint64_t b_full[NS_B], b_empty[NS_B];
-    uint64_t q_full[kMaxNsQ], q_empty[kMaxNsQ];
+    uint64_t q_full[NS_Q], q_empty[NS_Q];
     uint64_t s_full[NS_S], s_empty[NS_S];
     uint64_t acc_full[TPU], acc_empty[TPU];
     uint64_t drain;
@@ -97,7 +99,7 @@ __host__ __device__ inline SmemMap smem_map(int mode) {
     m.b = m.a + NS_A * A_STAGE;
     m.q = m.b + NS_B * B_STAGE;
     const bool deq = mode != 2;
-    m.s = m.q + (deq ? ns_q(mode) * Q_STAGE : 0);
+    m.s = m.q + (deq ? NS_Q * Q_LOAD : 0);
     m.t = m.s + (deq ? NS_S * S_STAGE : 0);
     m.ctl = m.t + (mode == 1 ? kEpiWarps * 32 * T_PITCH * 4 : 0);
     m.total = m.ctl + static_cast<int>(sizeof(Smem)) + 1024;  // + alignment slack
@@ -179,7 +181,6 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                         const __grid_constant__ CUtensorMap tm_s0, const __grid_constant__ CUtensorMap tm_b0,
                         const __grid_constant__ CUtensorMap tm_s1, const __grid_constant__ CUtensorMap tm_b1,
                         const GemmArgs a) {
-    constexpr int NS_Q = ns_q(MODE);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const SmemMap map = smem_map(MODE);
@@ -351,20 +352,19 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                         }
                         ++sit;
                     }
+                    if (ks % QK != 0) continue;
                     const int st = qit % NS_Q;
                     ok = wait_or_abort(&s->q_empty[st], ((qit / NS_Q) & 1) ^ 1, a, s, 4);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(&s->q_full[st], Q_STAGE);
-                    uint8_t *dst = sQ + st * Q_STAGE;
-#pragma unroll
-                    for (int hf = 0; hf < 2; ++hf) {
-                        const int col = ks * (GK / 8) + hf * 4;  // first nibble word of this half
-                        if (MODE == 0) {
-                            tma_load_2d(dst + hf * Q_HALF, &tm_w0, &s->q_full[st], col, w_row);
-                            tma_load_2d(dst + hf * Q_HALF + (BN / 2) * 16, &tm_w1, &s->q_full[st], col, w_row);
-                        } else {
-                            tma_load_2d(dst + hf * Q_HALF, &tm_w0, &s->q_full[st], col, w_row);
-                        }
+                    mbar_arrive_expect_tx(&s->q_full[st], Q_LOAD);
+                    uint8_t *dst = sQ + st * Q_LOAD;
+                    const int col = ks * (GK / 8);  // first nibble word of the load
+                    if (MODE == 0) {
+                        // gate rows f0.. then up rows f0.. (B rows 0-127, 128-255)
+                        tma_load_2d(dst, &tm_w0, &s->q_full[st], col, w_row);
+                        tma_load_2d(dst + (BN / 2) * Q_ROW, &tm_w1, &s->q_full[st], col, w_row);
+                    } else {
+                        tma_load_2d(dst, &tm_w0, &s->q_full[st], col, w_row);
                     }
                     ++qit;
                 }
@@ -450,11 +450,16 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                     if (lane == 0) mbar_arrive(&s->s_empty[ss]);
                     ++sit;
                 }
+                const int j = ks % QK;  // stage within the nibble load
                 const int qs = qit % NS_Q, bs = bit % NS_B;
-                ok = wait_or_abort(&s->q_full[qs], (qit / NS_Q) & 1, a, s, 9) &&
+                ok = (j != 0 || wait_or_abort(&s->q_full[qs], (qit / NS_Q) & 1, a, s, 9)) &&
                      wait_or_abort(&s->b_empty[bs], ((bit / NS_B) & 1) ^ 1, a, s, 10);
                 if (!ok) break;
-                const uint4 nib = *reinterpret_cast<const uint4 *>(sQ + qs * Q_STAGE + hf * Q_HALF + r * 16);
+                // 16-byte chunk 2j + hf of the row's 64 bytes, at its 64-byte-
+                // swizzle position (chunk ^ bits 7-8 of the row's offset); a
+                // warp's 32 rows then cover every bank once per 8 rows
+                const int chunk = (2 * j + hf) ^ ((r >> 1) & 3);
+                const uint4 nib = *reinterpret_cast<const uint4 *>(sQ + qs * Q_LOAD + r * Q_ROW + (chunk << 4));
                 const int gl = ((ks * GK + hf * 32) / a.G) % SG;
                 const uint32_t sw = (gl >> 1) == 0 ? sv.x : (gl >> 1) == 1 ? sv.y : (gl >> 1) == 2 ? sv.z : sv.w;
                 const uint32_t bw = (gl >> 1) == 0 ? bv.x : (gl >> 1) == 1 ? bv.y : (gl >> 1) == 2 ? bv.z : bv.w;
@@ -473,9 +478,9 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(&s->b_full[bs]);
-                    mbar_arrive(&s->q_empty[qs]);
+                    if (j == QK - 1) mbar_arrive(&s->q_empty[qs]);
                 }
-                ++qit;
+                if (j == QK - 1) ++qit;
                 ++bit;
             }
         }
