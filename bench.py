@@ -33,7 +33,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer prefill tok/s @T=4096; batch-1 decode tok/s; % of roofline"
 PREFILL_CFG = "prefill4096"
 DECODE_CFG = "decode40"
-KERNELS_PER_PREFILL = 8      # prep, router GEMM, top-k, scan, permute, gate/up GEMM, down GEMM, convert
+KERNELS_PER_PREFILL = 7      # router GEMM, top-k, scan, permute, gate/up GEMM, down GEMM, convert (the
+                             # router weights are split once when the layer is packed)
 DECODE_LAYERS_PER_KERNEL = 64  # one persistent decode kernel runs up to 64 layers of a step
 
 
@@ -245,7 +246,7 @@ def run_prefill(args, rank, world, pk):
     st = _lib.moe_read_device_status(ws.buf)
     if st != 0:
         raise RuntimeError(f"device status {st}")
-    # one layer call captured as a CUDA graph (its 9 kernels replayed without
+    # one layer call captured as a CUDA graph (its 7 kernels replayed without
     # host launch gaps); the L2 flush stays outside it
     graph = torch.cuda.CUDAGraph()
     side = torch.cuda.Stream()

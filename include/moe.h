@@ -106,6 +106,10 @@ typedef struct {
     moe_qweight gate, up, down;
     int32_t no_renorm;
     const float *shared_gate; /* [H] fp32 or NULL */
+    /* [2][E16][H] bf16 (E16 = E rounded up to 16), 16-byte aligned: the
+     * router weights split once by moe_split_router; NULL: moe_prefill
+     * splits router_w on every call. */
+    const void *router_split;
 } moe_layer_desc;
 
 /* Byte offsets, inside the workspace, of the routing tables that the last
@@ -139,6 +143,25 @@ typedef struct {
  * zero-filled once before first use (moe_workspace_init does it). */
 size_t moe_workspace_bytes(const moe_layer_desc *desc, int32_t T_max);
 
+/* Bytes of a layer's split router weights (moe_split_router): 2 x E16 x H
+ * bf16, E16 = E rounded up to 16; 0 if E or H is out of range. */
+size_t moe_router_split_bytes(int32_t E, int32_t H);
+
+/*
+ * The router weights as the prefill's tensor-core router GEMM reads them
+ * ("Lily: Perplexity's Custom Inference Engine for Apple Silicon", "The
+ * architecture that forces the issue": the router scores every expert): for
+ * router_w [E][H] fp32, out [2][E16][H] bf16 holds hi = bf16(w) and
+ * lo = bf16(w - hi) (|w - hi - lo| <= 2^-17 |w|, and every product with a
+ * bf16 input is exact); rows E..E16-1 are zero.  The weights are constant, so
+ * a caller splits them once and passes `out` as desc->router_split.
+ * out: device, 16-byte aligned, moe_router_split_bytes(E, H) bytes, owned by
+ * the caller.  Asynchronous on `stream`.  Errors: MOE_ERR_NULL, MOE_ERR_ALIGN,
+ * MOE_ERR_SHAPE (1 <= E <= 256, 256 <= H <= 16384, H % 256 == 0),
+ * MOE_ERR_CUDA.
+ */
+int moe_split_router(const float *router_w, int32_t E, int32_t H, void *out, cudaStream_t stream);
+
 /* Clear the control block (status word, counters) of a workspace. */
 int moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream);
 
@@ -157,8 +180,8 @@ int moe_prefill(const moe_layer_desc *desc, const void *x, int32_t T, void *y, v
 /*
  * moe_prefill that also records CUDA events on `stream` at the stage
  * boundaries, for timing the kernels one by one: events[0] before the router
- * (bf16 split of the router weights, then the router GEMM on the tensor
- * cores), [1] after it, [2] after the routing tables (top-k, scan,
+ * (the bf16 split of the router weights when the layer carries none, then the
+ * router GEMM on the tensor cores), [1] after it, [2] after the routing tables (top-k, scan,
  * permutation), [3] after the gate/up grouped GEMM, [4] after the down
  * grouped GEMM with the combine, [5] after the bf16 conversion of y.
  * events must hold 6 entries (created by the caller); NULL entries are skipped.

@@ -34,7 +34,7 @@ class moe_layer_desc(ctypes.Structure):
     _fields_ = [("E", c_i32), ("k", c_i32), ("H", c_i32), ("I", c_i32), ("group", c_i32),
                 ("has_shared", c_i32), ("router_w", c_p), ("router_bias", c_p),
                 ("gate", moe_qweight), ("up", moe_qweight), ("down", moe_qweight),
-                ("no_renorm", c_i32), ("shared_gate", c_p)]
+                ("no_renorm", c_i32), ("shared_gate", c_p), ("router_split", c_p)]
 
 
 class moe_routing_views(ctypes.Structure):
@@ -65,6 +65,8 @@ _lib = None
 SIGNATURES = {
     "moe_workspace_bytes": (c_sz, [c_p, c_i32]),
     "moe_workspace_init": (ctypes.c_int, [c_p, c_sz, c_p]),
+    "moe_router_split_bytes": (c_sz, [c_i32, c_i32]),
+    "moe_split_router": (ctypes.c_int, [c_p, c_i32, c_i32, c_p, c_p]),
     "moe_routing_views_for": (ctypes.c_int, [c_p, c_i32, c_p]),
     "moe_prefill": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_sz, c_p]),
     "moe_prefill_profiled": (ctypes.c_int, [c_p, c_p, c_i32, c_p, c_p, c_sz, c_p, c_p]),
@@ -143,6 +145,18 @@ def moe_workspace_bytes(desc: moe_layer_desc, T_max: int) -> int:
 def moe_workspace_init(ws, stream=None):
     _check(load().moe_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "moe_workspace_init")
+
+
+def moe_router_split_bytes(E: int, H: int) -> int:
+    return int(load().moe_router_split_bytes(E, H))
+
+
+def moe_split_router(router_w, E: int, H: int, out, stream=None):
+    """out [2][E16][H] bf16 (a uint8 device tensor of moe_router_split_bytes
+    bytes) = the hi/lo bf16 parts of router_w [E][H] fp32."""
+    if out.numel() * out.element_size() < moe_router_split_bytes(E, H):
+        raise MoEError(MOE_ERR_WORKSPACE, "moe_split_router: output too small")
+    _check(load().moe_split_router(_ptr(router_w), E, H, _ptr(out), _stream(stream)), "moe_split_router")
 
 
 def moe_routing_views_for(desc: moe_layer_desc, T: int) -> moe_routing_views:

@@ -8,7 +8,6 @@
 #include "attention.cuh"
 #include "block.cuh"
 #include "kernels.cuh"
-#include "routing_ext.cuh"
 #include "small_batch.cuh"
 
 
@@ -87,6 +86,7 @@ static int check_weights(const moe_layer_desc *d) {
     if ((rc = check_ptr(d->router_w))) return rc;
     if (d->router_bias && !aligned16(d->router_bias)) return MOE_ERR_ALIGN;
     if (d->shared_gate && !aligned16(d->shared_gate)) return MOE_ERR_ALIGN;
+    if (d->router_split && !aligned16(d->router_split)) return MOE_ERR_ALIGN;
     const moe_qweight *ws[3] = {&d->gate, &d->up, &d->down};
     for (const moe_qweight *w : ws) {
         if ((rc = check_ptr(w->q))) return rc;
@@ -184,6 +184,21 @@ int moe_workspace_init(void *ws, size_t ws_bytes, cudaStream_t stream) {
     return cuda_rc(cudaMemsetAsync(ws, 0, kCtrlBytes, stream));
 }
 
+size_t moe_router_split_bytes(int32_t E, int32_t H) {
+    if (E < 1 || E > 256 || H < 256 || H % 256 != 0 || H > 16384) return 0;
+    return sizeof(uint16_t) * 2 * static_cast<size_t>((E + 15) / 16 * 16) * H;
+}
+
+int moe_split_router(const float *router_w, int32_t E, int32_t H, void *out, cudaStream_t stream) {
+    if (!moe_router_split_bytes(E, H)) return MOE_ERR_SHAPE;
+    int rc;
+    if ((rc = check_ptr(router_w)) || (rc = check_ptr(out))) return rc;
+    DeviceInfo *dev = nullptr;
+    if ((rc = current_device(dev))) return rc;
+    return cuda_rc(launch_prep(router_w, E, (E + 15) / 16 * 16, H, static_cast<__nv_bfloat16 *>(out), nullptr, 0,
+                               nullptr, 0, dev->num_sms, stream));
+}
+
 int moe_routing_views_for(const moe_layer_desc *desc, int32_t T, moe_routing_views *v) {
     int rc = check_shape(desc);
     if (rc) return rc;
@@ -258,8 +273,11 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
 
     // router: A = x tiles, B = bf16 parts of the router weights
     GemmMaps mr{}, m1{}, m2{};
+    // router: the layer's split weights when the caller made them, else this
+    // call's own split in the workspace
+    const void *wr_src = desc->router_split ? desc->router_split : static_cast<const void *>(wr3);
     if ((rc = encode_2d(&mr.a0, BF16, 2, x, H, T, 64, 128, SW128)) ||
-        (rc = encode_2d(&mr.w0, BF16, 2, wr3, H, 2 * static_cast<uint64_t>(L.E_pad16), 64, L.E_pad16, SW128)))
+        (rc = encode_2d(&mr.w0, BF16, 2, wr_src, H, 2 * static_cast<uint64_t>(L.E_pad16), 64, L.E_pad16, SW128)))
         return rc;
     mr.a1 = mr.a0;
     mr.w1 = mr.s0 = mr.b0 = mr.s1 = mr.b1 = mr.w0;
@@ -305,19 +323,23 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
 
     cudaError_t e = mark(events, 0, stream);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    // router: bf16 split of the weights (and clearing of the histogram), then
-    // the eight partial router GEMMs on the tensor cores
-    if (launch_prep(desc->router_w, E, L.E_pad16, H, wr3, y_acc, 0, rb.counts_blk, static_cast<int64_t>(rb.nblk) * E,
-                    dev->num_sms, stream) != cudaSuccess)
+    // router: bf16 split of the weights unless the layer carries it, then
+    // the eight partial router GEMMs on the tensor cores, whose idle warps
+    // clear the fp32 combine accumulator and the expert histogram
+    if (!desc->router_split &&
+        launch_prep(desc->router_w, E, L.E_pad16, H, wr3, nullptr, 0, nullptr, 0, dev->num_sms, stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     ga.K = H;
+    ga.clear_f4 = reinterpret_cast<float4 *>(y_acc);
+    ga.clear_f4_n = static_cast<int64_t>(T) * H / 4;
+    ga.clear_i = rb.counts_blk;
+    ga.clear_i_n = static_cast<int64_t>(rb.nblk) * E;
     if (launch_gemm(2, mr, ga, grid_for(router_units(T)), stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(events, 1, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    // routing tables; the top-k kernel clears the fp32 combine accumulator
-    // on the side
+    // routing tables
     const RouteOpts ropts{static_cast<const __nv_bfloat16 *>(x), desc->shared_gate, H, desc->no_renorm};
-    if (launch_routing_tables_clearing(logits_part, L.E_pad16, desc->router_bias, T, E, k, desc->has_shared, ropts, rb,
-                                       y_acc, static_cast<int64_t>(T) * H, stream) != cudaSuccess)
+    if (launch_routing_tables(logits_part, L.E_pad16, nullptr, desc->router_bias, T, E, k, desc->has_shared, ropts,
+                              rb, stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (mark(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
     // gate/up + SwiGLU

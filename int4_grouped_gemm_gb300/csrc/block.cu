@@ -11,6 +11,7 @@
 //                            and the residual stream, rounded once (it takes
 //                            the place of the plain bf16 conversion of y)
 #include "block.cuh"
+#include "common.cuh"
 
 namespace moe {
 
@@ -34,6 +35,8 @@ __global__ void __launch_bounds__(kNormThreads) residual_rmsnorm_kernel(const __
     __shared__ float s_part[kNormThreads / 32];
     __shared__ float s_inv;
     const int t = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
     const int64_t row = static_cast<int64_t>(t) * H;
     const uint4 *a4 = reinterpret_cast<const uint4 *>(a + row);
     const uint4 *r4 = reinterpret_cast<const uint4 *>(r + row);
@@ -81,6 +84,8 @@ __global__ void __launch_bounds__(kNormThreads) residual_rmsnorm_kernel(const __
 __global__ void __launch_bounds__(256) residual_out_kernel(const float4 *__restrict__ y,
                                                            const uint2 *__restrict__ h, uint2 *__restrict__ out,
                                                            int64_t n4) {
+    pdl_wait();
+    pdl_trigger();
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const float4 v = y[i];
@@ -93,8 +98,7 @@ __global__ void __launch_bounds__(256) residual_out_kernel(const float4 *__restr
 cudaError_t launch_residual_rmsnorm(const __nv_bfloat16 *a, const __nv_bfloat16 *r, const float *w, float eps,
                                     int T, int H, __nv_bfloat16 *h, __nv_bfloat16 *x, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    residual_rmsnorm_kernel<<<T, kNormThreads, 0, s>>>(a, r, w, eps, H, h, x);
-    return cudaGetLastError();
+    return launch_dependent(residual_rmsnorm_kernel, dim3(T), dim3(kNormThreads), 0, s, a, r, w, eps, H, h, x);
 }
 
 cudaError_t launch_residual_out(const float *y_acc, const __nv_bfloat16 *h, __nv_bfloat16 *out, int64_t n,
@@ -103,10 +107,9 @@ cudaError_t launch_residual_out(const float *y_acc, const __nv_bfloat16 *h, __nv
     int64_t blocks = (n4 + 255) / 256;
     if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
     if (blocks < 1) blocks = 1;
-    residual_out_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        reinterpret_cast<const float4 *>(y_acc), reinterpret_cast<const uint2 *>(h), reinterpret_cast<uint2 *>(out),
-        n4);
-    return cudaGetLastError();
+    return launch_dependent(residual_out_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                            reinterpret_cast<const float4 *>(y_acc), reinterpret_cast<const uint2 *>(h),
+                            reinterpret_cast<uint2 *>(out), n4);
 }
 
 }  // namespace moe

@@ -34,6 +34,8 @@
 //   warps 11-26 dequantisers, two threads per weight row (one per 32-element
 //               half of the stage): nibbles -> bf16 s*q+b in the 128-byte
 //               swizzled K-major layout of the B ring
+//               (router mode: these warps zero the call's fp32 combine
+//               accumulator and expert histogram instead)
 //   warp 9      one thread issues the MMAs (bf16 x bf16 -> fp32 in tensor
 //               memory): token tile 0 into columns 0-255, tile 1 into 256-511
 //   warps 0-7   epilogue, warp w reads TMEM lanes 32*(w%4).. (token rows) and
@@ -101,7 +103,7 @@ __host__ __device__ inline SmemMap smem_map(int mode) {
     const bool deq = mode != 2;
     m.s = m.q + (deq ? NS_Q * Q_LOAD : 0);
     m.t = m.s + (deq ? NS_S * S_STAGE : 0);
-    m.ctl = m.t + (mode == 1 ? kEpiWarps * 32 * T_PITCH * 4 : 0);
+    m.ctl = m.t + (mode != 0 ? kEpiWarps * 32 * T_PITCH * 4 : 0);
     m.total = m.ctl + static_cast<int>(sizeof(Smem)) + 1024;  // + alignment slack
     return m;
 }
@@ -238,6 +240,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = s->tmem_base;
+    pdl_wait();  // the previous kernel's outputs (routing tables, h, x) are complete
+    pdl_trigger();
 
     const int nunits = num_units<MODE>(a);
     const int ksteps = MODE == 2 ? (a.K / kRouterKSplit) / GK : a.K / GK;
@@ -426,6 +430,15 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             mbar_wait(&s->drain, 0, a.wait_limit);
         }
         __syncwarp();
+    } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps && MODE == 2) {
+        // ------------------------------------------ router: clear on the side
+        // The later kernels of the layer accumulate into these two buffers;
+        // the warps that dequantise in the expert GEMMs are idle here.
+        constexpr int kClearThreads = kDeqWarps * 32;
+        const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kClearThreads + (tid - kDeqWarp0 * 32);
+        const int64_t stride = static_cast<int64_t>(gridDim.x) * kClearThreads;
+        for (int64_t i = i0; i < a.clear_f4_n; i += stride) a.clear_f4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int64_t i = i0; i < a.clear_i_n; i += stride) a.clear_i[i] = 0;
     } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps && MODE != 2) {
         // ---------------------------------------------------------- dequantise
         const int dt = tid - kDeqWarp0 * 32;
@@ -566,17 +579,30 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                         }
                     }
                 } else {
-                    float *lrow = a.logits_part +
-                                  (static_cast<int64_t>(t.part * kRouterKSplit + t.kq) * a.T + t.row0 + rr) * a.E_pad16;
+                    // partial logits, through the same shared-memory transpose as
+                    // the down GEMM's: a store instruction then writes 64
+                    // contiguous bytes of each of 8 rows instead of 16 bytes of
+                    // each of 32
+                    const int64_t plane = static_cast<int64_t>(t.part * kRouterKSplit + t.kq) * a.T;
+                    const int row_base = i * BM + quarter * 32;  // unit row of this warp's lane 0
                     for (int c0 = chalf * 16; c0 < nb; c0 += 32) {
                         float v[16];
                         tmem_ld16(tbase + c0, v);
-                        if (valid) {
-                            float4 *dst = reinterpret_cast<float4 *>(lrow + c0);
 #pragma unroll
-                            for (int j = 0; j < 4; ++j)
-                                dst[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                        for (int j = 0; j < 16; j += 4)
+                            *reinterpret_cast<float4 *>(tbuf + lane * T_PITCH + j) =
+                                make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                        __syncwarp();
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int src = 8 * q + lane / 4;  // row of the warp this lane stores
+                            if (row_base + src < t.n) {
+                                const float4 val = *reinterpret_cast<const float4 *>(tbuf + src * T_PITCH + 4 * (lane % 4));
+                                *reinterpret_cast<float4 *>(a.logits_part + (plane + t.row0 + row_base + src) * a.E_pad16 +
+                                                            c0 + 4 * (lane % 4)) = val;
+                            }
                         }
+                        __syncwarp();
                     }
                 }
                 tc_fence_before();
@@ -599,13 +625,15 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
 
 // Router weights fp32 [E][H] -> two bf16 parts [2][E_pad16][H]: hi = bf16(w)
 // and lo = bf16(w - hi), so that |w - hi - lo| <= 2^-17 |w| and every product
-// with a bf16 input is exact; rows E..E_pad16-1 are zero.  Also clears the
-// fp32 combine accumulator and the per-chunk expert histogram.
+// with a bf16 input is exact; rows E..E_pad16-1 are zero.  Optionally also
+// clears an fp32 buffer and an int buffer (n = 0: none).
 __global__ void __launch_bounds__(256) prep_kernel(const float *__restrict__ Wr, int E, int E_pad, int H,
                                                    __nv_bfloat16 *__restrict__ wr2, float4 *__restrict__ y_acc,
                                                    int64_t y_acc_n4, int *__restrict__ counts_blk, int64_t n_counts) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const int64_t n = static_cast<int64_t>(E_pad) * H;
+    pdl_wait();
+    pdl_trigger();
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n; i += stride) {
         const int64_t e = i / H;
         const float w = e < E ? Wr[i] : 0.0f;
@@ -622,6 +650,8 @@ __global__ void __launch_bounds__(256) prep_kernel(const float *__restrict__ Wr,
 // y (bf16) = y_acc (fp32), four elements per thread
 __global__ void __launch_bounds__(256) convert_out_kernel(const float4 *__restrict__ y_acc,
                                                           uint2 *__restrict__ y, int64_t n4) {
+    pdl_wait();
+    pdl_trigger();
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const float4 v = y_acc[i];
@@ -641,9 +671,8 @@ cudaError_t launch_gemm_t(const GemmMaps &m, const GemmArgs &a, int grid, cudaSt
     const int smem = gemm_smem_bytes(MODE);
     cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    grouped_gemm_kernel<MODE><<<grid, gemm_threads(MODE), smem, s>>>(m.a0, m.a1, m.w0, m.w1, m.s0, m.b0, m.s1,
-                                                                     m.b1, a);
-    return cudaGetLastError();
+    return launch_dependent(grouped_gemm_kernel<MODE>, dim3(grid), dim3(gemm_threads(MODE)), smem, s, m.a0, m.a1, m.w0,
+                            m.w1, m.s0, m.b0, m.s1, m.b1, a);
 }
 
 cudaError_t launch_gemm(int mode, const GemmMaps &m, const GemmArgs &a, int grid, cudaStream_t s) {
@@ -656,9 +685,8 @@ int router_units(int T) { return kRouterUnits * ((T + TPU * BM - 1) / (TPU * BM)
 
 cudaError_t launch_prep(const float *Wr, int E, int E_pad, int H, __nv_bfloat16 *wr2, float *y_acc, int64_t y_elems,
                         int *counts_blk, int64_t n_counts, int num_sms, cudaStream_t s) {
-    prep_kernel<<<4 * num_sms, 256, 0, s>>>(Wr, E, E_pad, H, wr2, reinterpret_cast<float4 *>(y_acc), y_elems / 4,
-                                            counts_blk, n_counts);
-    return cudaGetLastError();
+    return launch_dependent(prep_kernel, dim3(4 * num_sms), dim3(256), 0, s, Wr, E, E_pad, H, wr2,
+                            reinterpret_cast<float4 *>(y_acc), y_elems / 4, counts_blk, n_counts);
 }
 
 cudaError_t launch_convert(const float *y_acc, __nv_bfloat16 *y, int64_t n, int num_sms, cudaStream_t s) {
@@ -666,9 +694,8 @@ cudaError_t launch_convert(const float *y_acc, __nv_bfloat16 *y, int64_t n, int 
     int64_t blocks = (n4 + 255) / 256;
     if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
     if (blocks < 1) blocks = 1;
-    convert_out_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<const float4 *>(y_acc),
-                                                                      reinterpret_cast<uint2 *>(y), n4);
-    return cudaGetLastError();
+    return launch_dependent(convert_out_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, s,
+                            reinterpret_cast<const float4 *>(y_acc), reinterpret_cast<uint2 *>(y), n4);
 }
 
 }  // namespace moe

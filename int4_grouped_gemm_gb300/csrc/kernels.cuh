@@ -21,6 +21,12 @@ struct GemmArgs {
     float *logits_part;        // router: [8][T][E_pad16] (parts x K quarters)
     int *status;
     long long wait_limit;
+    // router mode: buffers of the call that its otherwise idle warps zero
+    // (the fp32 combine accumulator and the per-chunk expert histogram)
+    float4 *clear_f4;
+    int64_t clear_f4_n;
+    int *clear_i;
+    int64_t clear_i_n;
 };
 
 // TMA descriptors of one grouped GEMM launch (unused ones may be copies)

@@ -18,7 +18,6 @@
 // Every table is deterministic: counts and ranks come from per-block counts
 // scanned in token order, never from the order in which atomics land.
 #include "kernels.cuh"
-#include "routing_ext.cuh"
 #include "topk.cuh"
 
 namespace moe {
@@ -32,20 +31,15 @@ namespace moe {
 constexpr int kTopkWarps = 4;
 static_assert(kRouteChunk % kTopkWarps == 0, "a top-k block stays within one chunk");
 
-//
-// clear / clear_n4: a buffer the kernel zeroes on the side (the fp32 combine
-// accumulator of the prefill, 16-byte pieces, grid-strided): the kernel waits
-// on its loads, so the stores ride along.
 __global__ void __launch_bounds__(kTopkWarps * 32)
     topk_hist_kernel(const float *__restrict__ logits_part, int ld, const float *__restrict__ given,
                      const float *__restrict__ bias, int T, int E, int k, int has_shared, RouteOpts opts,
-                     RoutingBufs rb, float4 *__restrict__ clear, int64_t clear_n4) {
+                     RoutingBufs rb) {
     __shared__ int hist[256];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     for (int e = tid; e < 256; e += blockDim.x) hist[e] = 0;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + tid; i < clear_n4;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        clear[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    pdl_wait();
+    pdl_trigger();
     __syncthreads();
 
     const int t = blockIdx.x * kTopkWarps + warp;
@@ -210,6 +204,8 @@ __global__ void __launch_bounds__(512) scan_tiles_kernel(int T, int E, int k, in
     __shared__ int s_wc[16][kUnitRows];   // the same counts per warp
     const int g = threadIdx.x, lane = g % 32, warp = g / 32;
     const int G = E + (has_shared ? 1 : 0);
+    pdl_wait();
+    pdl_trigger();
     for (int i = g; i < kUnitRows; i += 512) s_hist[i] = 0;
     for (int i = g; i < 16 * kUnitRows; i += 512) (&s_wc[0][0])[i] = 0;
 
@@ -298,6 +294,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_kernel(int T, int E, int
     __shared__ int wcnt[kPermWarps][256];  // per warp, per expert: slots picking it
     const int s = threadIdx.x, lane = s % 32, warp = s / 32;
     const int blk = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
     const int t_begin = blk * kRouteChunk;
     const int nslots = (min(T, t_begin + kRouteChunk) - t_begin) * k;
     for (int e = s; e < E; e += kPermThreads)
@@ -342,27 +340,14 @@ cudaError_t launch_zero_i32(int *p, int64_t n, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-static cudaError_t routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
-                                  int E, int k, int has_shared, const RouteOpts &opts, const RoutingBufs &rb,
-                                  float *clear, int64_t clear_elems, cudaStream_t s) {
-    topk_hist_kernel<<<(T + kTopkWarps - 1) / kTopkWarps, kTopkWarps * 32, 0, s>>>(
-        logits_part, ld, given, bias, T, E, k, has_shared, opts, rb, reinterpret_cast<float4 *>(clear),
-        clear_elems / 4);
-    scan_tiles_kernel<<<1, 512, 0, s>>>(T, E, k, has_shared, rb);
-    permute_kernel<<<rb.nblk, kPermThreads, 0, s>>>(T, E, k, rb);
-    return cudaGetLastError();
-}
-
 cudaError_t launch_routing_tables(const float *logits_part, int ld, const float *given, const float *bias, int T,
                                   int E, int k, int has_shared, const RouteOpts &opts, const RoutingBufs &rb,
                                   cudaStream_t s) {
-    return routing_tables(logits_part, ld, given, bias, T, E, k, has_shared, opts, rb, nullptr, 0, s);
-}
-
-cudaError_t launch_routing_tables_clearing(const float *logits_part, int ld, const float *bias, int T, int E, int k,
-                                           int has_shared, const RouteOpts &opts, const RoutingBufs &rb, float *clear,
-                                           int64_t clear_elems, cudaStream_t s) {
-    return routing_tables(logits_part, ld, nullptr, bias, T, E, k, has_shared, opts, rb, clear, clear_elems, s);
+    cudaError_t e = launch_dependent(topk_hist_kernel, dim3((T + kTopkWarps - 1) / kTopkWarps), dim3(kTopkWarps * 32),
+                                     0, s, logits_part, ld, given, bias, T, E, k, has_shared, opts, rb);
+    if (e == cudaSuccess) e = launch_dependent(scan_tiles_kernel, dim3(1), dim3(512), 0, s, T, E, k, has_shared, rb);
+    if (e == cudaSuccess) e = launch_dependent(permute_kernel, dim3(rb.nblk), dim3(kPermThreads), 0, s, T, E, k, rb);
+    return e;
 }
 
 }  // namespace moe

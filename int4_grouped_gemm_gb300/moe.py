@@ -58,10 +58,16 @@ class PackedLayer:
         self.router_bias = None if router_bias is None else router_bias.contiguous()
         self.shared_gate = None if shared_gate is None else shared_gate.contiguous()
         self.gate, self.up, self.down = gate, up, down
+        # the router weights' bf16 hi/lo parts for the prefill's tensor-core
+        # router, split once here instead of on every call
+        self.router_split = torch.empty(_lib.moe_router_split_bytes(E, H), dtype=torch.uint8,
+                                        device=self.router_w.device)
+        _lib.moe_split_router(self.router_w, E, H, self.router_split)
         self.desc = moe_layer_desc(E, k, H, I, group, int(has_shared), self.router_w.data_ptr(),
                                    None if self.router_bias is None else self.router_bias.data_ptr(),
                                    gate.as_c(), up.as_c(), down.as_c(), int(no_renorm),
-                                   None if self.shared_gate is None else self.shared_gate.data_ptr())
+                                   None if self.shared_gate is None else self.shared_gate.data_ptr(),
+                                   self.router_split.data_ptr())
 
     @classmethod
     def from_fp32(cls, cfg, router_w, router_bias, w_gate, w_up, w_down, stream=None, no_renorm: bool = False,

@@ -84,6 +84,23 @@ def test_argument_errors_are_caught_on_the_host(lib):
     assert lib.moe_read_device_status(None, None) == _lib.MOE_ERR_NULL
 
 
+def test_router_split_sizes_and_host_checks(lib):
+    from int4_grouped_gemm_gb300 import _lib
+    assert _lib.moe_router_split_bytes(256, 2048) == 2 * 256 * 2048 * 2
+    assert _lib.moe_router_split_bytes(40, 256) == 2 * 48 * 256 * 2      # rows padded to 16
+    for E, H in ((0, 2048), (257, 2048), (16, 200), (16, 32768)):
+        assert _lib.moe_router_split_bytes(E, H) == 0
+        assert lib.moe_split_router(ctypes.c_void_p(16), E, H, ctypes.c_void_p(32), None) == _lib.MOE_ERR_SHAPE
+    assert lib.moe_split_router(None, 16, 256, ctypes.c_void_p(32), None) == _lib.MOE_ERR_NULL
+    assert lib.moe_split_router(ctypes.c_void_p(16), 16, 256, ctypes.c_void_p(40), None) == _lib.MOE_ERR_ALIGN
+    # a misaligned split in the layer is refused before anything runs
+    q = _lib.moe_qweight(1024, 1024, 1024)
+    d = _lib.moe_layer_desc(256, 8, 2048, 512, 64, 1, 1024, None, q, q, q)
+    d.router_split = 8
+    assert lib.moe_prefill(ctypes.byref(d), ctypes.c_void_p(1024), 16, ctypes.c_void_p(2048),
+                           ctypes.c_void_p(4096), 1 << 40, None) == _lib.MOE_ERR_ALIGN
+
+
 def test_pipelined_host_call_rejects_bad_arguments_on_the_host(lib):
     from int4_grouped_gemm_gb300 import _lib
     d = _desc()

@@ -96,6 +96,45 @@ def test_one_expert_takes_all_tokens_and_empty_experts():
     check_layer(L, L.x)
 
 
+@pytest.mark.parametrize("E,H", [(16, 256), (40, 256), (256, 2048)])
+def test_router_split_is_its_definition_and_both_router_paths_agree(E, H):
+    """moe_split_router writes hi = bf16(w) and lo = bf16(w - hi) with zero
+    padding rows; a layer that carries the split and one that leaves it to
+    each call (router_split NULL) give the same logits, picks and weights bit
+    for bit, and outputs within one bf16 ulp (the combine's fp32 additions
+    land in no fixed order)."""
+    cfg = synthetic.MoEConfig(f"split{E}", T=130, H=H, E=E, k=2, I=128, group=64, seed=300 + E)
+    L = synthetic.make_layer(cfg)
+    layer = PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down)
+    E16 = (E + 15) // 16 * 16
+    assert layer.router_split.numel() == _lib.moe_router_split_bytes(E, H) == 2 * E16 * H * 2
+    parts = layer.router_split.view(torch.bfloat16).view(2, E16, H).cpu()
+    w = L.router_w.float()
+    hi = w.to(torch.bfloat16)
+    lo = (w - hi.float()).to(torch.bfloat16)
+    assert torch.equal(parts[0, :E].view(torch.int16), hi.view(torch.int16))
+    assert torch.equal(parts[1, :E].view(torch.int16), lo.view(torch.int16))
+    assert not parts[:, E:].view(torch.int16).any()
+    x = L.x.cuda()
+    ws = layer.workspace(cfg.T)
+    y_split = layer.prefill(x, ws).clone()
+    rt = {n: v.clone() for n, v in ws.routing(layer.desc, cfg.T).items() if n in ("logits", "topk_idx", "topk_w")}
+    d = _lib.moe_layer_desc.from_buffer_copy(layer.desc)
+    d.router_split = None
+    y_call = torch.empty_like(x)
+    _lib.moe_prefill(d, x, cfg.T, y_call, ws.buf)
+    torch.cuda.synchronize()
+    assert _lib.moe_read_device_status(ws.buf) == 0
+    rt2 = ws.routing(layer.desc, cfg.T)
+    for n, v in rt.items():
+        assert torch.equal(v, rt2[n]), n
+    # one bf16 rounding step, plus the fp32 reassociation error of the k + 1
+    # terms where they cancel
+    a, b = y_split.float(), y_call.float()
+    bound = torch.maximum(a.abs(), b.abs()) * 2.0 ** -7 + 1e-5 * b.abs().max()
+    assert ((a - b).abs() <= bound).all()
+
+
 @pytest.mark.parametrize("T", [1, 2, 8])
 def test_full_shapes_small_batches(T):
     """The speculative-verify shape: a few tokens through the full-size
