@@ -325,13 +325,11 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     // router: bf16 split of the weights unless the layer carries it, then
     // the eight partial router GEMMs on the tensor cores, whose idle warps
-    // clear the fp32 combine accumulator and the expert histogram
+    // clear the expert histogram
     if (!desc->router_split &&
         launch_prep(desc->router_w, E, L.E_pad16, H, wr3, nullptr, 0, nullptr, 0, dev->num_sms, stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     ga.K = H;
-    ga.clear_f4 = reinterpret_cast<float4 *>(y_acc);
-    ga.clear_f4_n = static_cast<int64_t>(T) * H / 4;
     ga.clear_i = rb.counts_blk;
     ga.clear_i_n = static_cast<int64_t>(rb.nblk) * E;
     if (launch_gemm(2, mr, ga, grid_for(router_units(T)), stream) != cudaSuccess) return MOE_ERR_CUDA;
@@ -342,14 +340,19 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
                               rb, stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     if (mark(events, 2, stream) != cudaSuccess) return MOE_ERR_CUDA;
-    // gate/up + SwiGLU
+    // gate/up + SwiGLU; its epilogue warps clear the fp32 combine accumulator
+    // before the first unit's results arrive
     ga.K = H;
     ga.n_ntiles = I / 128;
+    ga.clear_i_n = 0;
+    ga.clear_f4 = reinterpret_cast<float4 *>(y_acc);
+    ga.clear_f4_n = static_cast<int64_t>(T) * H / 4;
     if (launch_gemm(0, m1, ga, grid_for(L.max_tiles * ga.n_ntiles), stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(events, 3, stream) != cudaSuccess) return MOE_ERR_CUDA;
     // down + weighted combine
     ga.K = I;
     ga.n_ntiles = H / 256;
+    ga.clear_f4_n = 0;
     if (launch_gemm(1, m2, ga, grid_for(L.max_tiles * ga.n_ntiles), stream) != cudaSuccess) return MOE_ERR_CUDA;
     if (mark(events, 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
     // y = bf16 of the fp32 combine, or for a decoder block bf16(combine + h)

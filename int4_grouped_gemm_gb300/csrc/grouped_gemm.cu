@@ -34,8 +34,8 @@
 //   warps 11-26 dequantisers, two threads per weight row (one per 32-element
 //               half of the stage): nibbles -> bf16 s*q+b in the 128-byte
 //               swizzled K-major layout of the B ring
-//               (router mode: these warps zero the call's fp32 combine
-//               accumulator and expert histogram instead)
+//               (router mode: these warps zero the call's per-chunk expert
+//               histogram instead)
 //   warp 9      one thread issues the MMAs (bf16 x bf16 -> fp32 in tensor
 //               memory): token tile 0 into columns 0-255, tile 1 into 256-511
 //   warps 0-7   epilogue, warp w reads TMEM lanes 32*(w%4).. (token rows) and
@@ -253,9 +253,13 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         // The unit's 256 token rows are gathered straight from x (it fits in
         // L2) with 16-byte cp.async: 8 threads per 128-byte row segment, a
         // warp covers 4 whole rows per instruction, and each chunk lands at
-        // its 128-byte-swizzle position.  Every copying thread arrives on the
-        // stage's barrier when its copies have landed (no waiting here), so
-        // the copier runs up to NS_A stages ahead of the MMA.
+        // its 128-byte-swizzle position.  Rows past the unit's last are not
+        // fetched: row m of an MMA's result depends on row m of A alone, and
+        // the epilogue drops those rows, so whatever the slot last held there
+        // is harmless (a group of 16 tokens moves 16 rows, not 128).  Every
+        // copying thread arrives on the stage's barrier when its copies have
+        // landed (no waiting here), so the copier runs up to NS_A stages ahead
+        // of the MMA.
         const int pt = tid - kLsuWarp0 * 32;  // 0..127
         const int chunk = pt & 7;             // 16-byte chunk of the row segment
         const int rsub = pt >> 3;             // rows rsub, rsub + 16, ... of the unit
@@ -278,7 +282,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
 #pragma unroll
                 for (int i = 0; i < TPU * BM / 16; ++i) {
                     const int rr = rsub + 16 * i;  // row of the unit: tile rr / 128
-                    if (rr < t.ntiles * BM) {
+                    if (rr < t.n) {
                         const int r = rr & (BM - 1);
                         cp_async<16>(stage + (rr / BM) * TILE_A + r * 128 + ((chunk ^ (r & 7)) << 4),
                                      a.x + static_cast<int64_t>(tok[i]) * a.K + ks * GK + chunk * 8);
@@ -432,12 +436,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         __syncwarp();
     } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps && MODE == 2) {
         // ------------------------------------------ router: clear on the side
-        // The later kernels of the layer accumulate into these two buffers;
-        // the warps that dequantise in the expert GEMMs are idle here.
+        // The top-k kernel adds into the per-chunk expert histogram; the
+        // warps that dequantise in the expert GEMMs are idle here.
         constexpr int kClearThreads = kDeqWarps * 32;
         const int64_t i0 = static_cast<int64_t>(blockIdx.x) * kClearThreads + (tid - kDeqWarp0 * 32);
         const int64_t stride = static_cast<int64_t>(gridDim.x) * kClearThreads;
-        for (int64_t i = i0; i < a.clear_f4_n; i += stride) a.clear_f4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int64_t i = i0; i < a.clear_i_n; i += stride) a.clear_i[i] = 0;
     } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps && MODE != 2) {
         // ---------------------------------------------------------- dequantise
@@ -502,6 +505,15 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         const int quarter = warp & 3;      // TMEM lane quarter = token rows 32*quarter..
         const int chalf = warp >> 2;       // this warp's 16-column chunks: chalf, chalf + 2, ...
         float *tbuf = reinterpret_cast<float *>(base + map.t) + warp * 32 * T_PITCH;
+        if (MODE == 0) {
+            // gate/up: while the first unit's MMAs run, these warps zero the
+            // fp32 combine accumulator that the down GEMM adds into (a few
+            // hundred KB per CTA, off the critical path of a kernel that
+            // uses a small share of the DRAM bandwidth)
+            const int64_t i0 = static_cast<int64_t>(blockIdx.x) * (kEpiWarps * 32) + tid;
+            const int64_t stride = static_cast<int64_t>(gridDim.x) * (kEpiWarps * 32);
+            for (int64_t i = i0; i < a.clear_f4_n; i += stride) a.clear_f4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         uint32_t uses[TPU] = {0, 0};
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {

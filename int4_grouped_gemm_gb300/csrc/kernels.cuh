@@ -21,8 +21,9 @@ struct GemmArgs {
     float *logits_part;        // router: [8][T][E_pad16] (parts x K quarters)
     int *status;
     long long wait_limit;
-    // router mode: buffers of the call that its otherwise idle warps zero
-    // (the fp32 combine accumulator and the per-chunk expert histogram)
+    // buffers of the call that otherwise idle warps zero: the fp32 combine
+    // accumulator (gate/up mode, epilogue warps before the first unit) and
+    // the per-chunk expert histogram (router mode, the dequant warps)
     float4 *clear_f4;
     int64_t clear_f4_n;
     int *clear_i;
