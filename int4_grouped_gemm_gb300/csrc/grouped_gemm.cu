@@ -73,7 +73,7 @@ constexpr int B_STAGE = BN * 128;                // 32 KB: 256 weight rows x 64 
 constexpr int Q_ROW = QK * GK / 2;               // 64 bytes of a weight row per nibble load
 constexpr int Q_LOAD = BN * Q_ROW;               // 16 KB: 256 rows x 128 nibbles
 constexpr int S_STAGE = 2 * BN * SG * 2;         // 8 KB: [scale|bias][256 rows][8 groups] bf16
-constexpr int T_PITCH = 20;                      // fp32 pitch of the epilogue transpose rows
+constexpr int T_PITCH = 16;                      // fp32 pitch of the epilogue transpose rows
 constexpr uint32_t kTmemCols = 512;              // two 256-column fp32 accumulators
 constexpr int kRouterParts = 2;                  // bf16 parts of the fp32 router weights
 constexpr int kRouterKSplit = 4;                 // K quarters of the router GEMM
@@ -505,6 +505,14 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         const int quarter = warp & 3;      // TMEM lane quarter = token rows 32*quarter..
         const int chalf = warp >> 2;       // this warp's 16-column chunks: chalf, chalf + 2, ...
         float *tbuf = reinterpret_cast<float *>(base + map.t) + warp * 32 * T_PITCH;
+        // The warp's transpose buffer (down and router epilogues): 32 rows of
+        // 16 fp32, chunk j (4 values) of row r at position (j + r / 2) mod 4.
+        // Lane l writes row l; in pass q it reads chunk l % 4 of row
+        // 8q + l / 4, whose position does not depend on q.  A quarter warp
+        // then hits 8 distinct 16-byte bank groups in both directions.
+        float *t_wrow = tbuf + lane * T_PITCH;
+        const int t_rot = (lane >> 1) & 3;
+        const float *t_rrow = tbuf + (lane >> 2) * T_PITCH + 4 * (((lane & 3) + (lane >> 3)) & 3);
         if (MODE == 0) {
             // gate/up: while the first unit's MMAs run, these warps zero the
             // fp32 combine accumulator that the down GEMM adds into (a few
@@ -574,7 +582,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                             const int cc = c0 + 32 * h;
 #pragma unroll
                             for (int j = 0; j < 16; j += 4)
-                                *reinterpret_cast<float4 *>(tbuf + lane * T_PITCH + j) =
+                                *reinterpret_cast<float4 *>(t_wrow + 4 * ((j / 4 + t_rot) & 3)) =
                                     make_float4(wgt * __uint_as_float(r2[h][j]), wgt * __uint_as_float(r2[h][j + 1]),
                                                 wgt * __uint_as_float(r2[h][j + 2]), wgt * __uint_as_float(r2[h][j + 3]));
                             __syncwarp();
@@ -582,7 +590,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                             for (int q = 0; q < 4; ++q) {
                                 const int src = 8 * q + lane / 4;  // row of the warp whose values this lane adds
                                 const float4 val =
-                                    *reinterpret_cast<const float4 *>(tbuf + src * T_PITCH + 4 * (lane % 4));
+                                    *reinterpret_cast<const float4 *>(t_rrow + q * 8 * T_PITCH);
                                 if (vvs[q])
                                     red_add_v4(a.y_acc + static_cast<int64_t>(tks[q]) * a.H + f0 + cc + 4 * (lane % 4),
                                                val);
@@ -602,14 +610,14 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                         tmem_ld16(tbase + c0, v);
 #pragma unroll
                         for (int j = 0; j < 16; j += 4)
-                            *reinterpret_cast<float4 *>(tbuf + lane * T_PITCH + j) =
+                            *reinterpret_cast<float4 *>(t_wrow + 4 * ((j / 4 + t_rot) & 3)) =
                                 make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
                         __syncwarp();
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const int src = 8 * q + lane / 4;  // row of the warp this lane stores
                             if (row_base + src < t.n) {
-                                const float4 val = *reinterpret_cast<const float4 *>(tbuf + src * T_PITCH + 4 * (lane % 4));
+                                const float4 val = *reinterpret_cast<const float4 *>(t_rrow + q * 8 * T_PITCH);
                                 *reinterpret_cast<float4 *>(a.logits_part + (plane + t.row0 + row_base + src) * a.E_pad16 +
                                                             c0 + 4 * (lane % 4)) = val;
                             }
