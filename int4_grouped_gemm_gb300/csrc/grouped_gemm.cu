@@ -23,7 +23,8 @@
 //   warps 27-30 gate/up A producers: 16-byte cp.async gathers of the unit's
 //               token rows straight from x (no permuted copy of x)
 //   warp 10     down/router A producer: TMA loads of both token tiles (2 x 16 KB
-//               boxes per stage) from h (down) or from x (router)
+//               boxes per stage) from h (down) or from x (router); gate/up:
+//               the tile-1 MMA issuer
 //   warp 8      W producer: TMA loads of packed nibbles (16 KB per load: 64
 //               bytes of each of the 256 weight rows, two stages' worth, in
 //               the 64-byte swizzle so that the dequant threads' 16-byte reads
@@ -36,8 +37,11 @@
 //               swizzled K-major layout of the B ring
 //               (router mode: these warps zero the call's per-chunk expert
 //               histogram instead)
-//   warp 9      one thread issues the MMAs (bf16 x bf16 -> fp32 in tensor
-//               memory): token tile 0 into columns 0-255, tile 1 into 256-511
+//   warp 9      one thread issues token tile 0's MMAs (bf16 x bf16 -> fp32
+//               in tensor memory, columns 0-255); tile 1's (columns 256-511)
+//               come from one thread of warp 10 (gate/up) or warp 27 (down,
+//               router), so that one issuer's barrier waits overlap the
+//               other's MMAs
 //   warps 0-7   epilogue, warp w reads TMEM lanes 32*(w%4).. (token rows) and
 //               every other 16-column chunk (w/4 picks which):
 //               MODE 0 (gate/up): h = silu(gate) * up -> bf16 h rows
@@ -64,8 +68,9 @@ constexpr int NS_Q = 2;                          // nibble ring depth (loads)
 constexpr int kEpiWarps = 8, kWProdWarp = 8, kMmaWarp = 9, kAProdWarp = 10, kDeqWarp0 = 11, kDeqWarps = 16;
 constexpr int kLsuWarp0 = kDeqWarp0 + kDeqWarps, kLsuWarps = 4;  // gate/up: token-row copiers
 constexpr int kLsuThreads = kLsuWarps * 32;
+constexpr int kMma2Warp = kLsuWarp0;  // down, router: the second MMA issuer's warp (gate/up: kAProdWarp)
 __host__ __device__ constexpr int gemm_threads(int mode) {
-    return (kLsuWarp0 + (mode == 0 ? kLsuWarps : 0)) * 32;  // 992 (gate/up) or 864
+    return (kLsuWarp0 + (mode == 0 ? kLsuWarps : 1)) * 32;  // 992 (gate/up) or 896
 }
 constexpr int TILE_A = BM * 128;                 // 16 KB: 128 token rows x 64 bf16
 constexpr int A_STAGE = TPU * TILE_A;            // 32 KB: both token tiles
@@ -193,15 +198,17 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     Smem *s = reinterpret_cast<Smem *>(base + map.ctl);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // two MMA issuers, one per token tile (see run_mma below)
+    constexpr int kMmaIssuers = 2;
 
     if (tid == 0) {
         for (int i = 0; i < NS_A; ++i) {
             mbar_init(&s->a_full[i], MODE == 0 ? kLsuThreads : 1);
-            mbar_init(&s->a_empty[i], 1);
+            mbar_init(&s->a_empty[i], kMmaIssuers);
         }
         for (int i = 0; i < NS_B; ++i) {
             mbar_init(&s->b_full[i], MODE == 2 ? 1 : kDeqWarps);
-            mbar_init(&s->b_empty[i], 1);
+            mbar_init(&s->b_empty[i], kMmaIssuers);
         }
         for (int i = 0; i < NS_Q; ++i) {
             mbar_init(&s->q_full[i], 1);
@@ -215,7 +222,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             mbar_init(&s->acc_full[i], 1);
             mbar_init(&s->acc_empty[i], kEpiWarps);
         }
-        mbar_init(&s->drain, 1);
+        mbar_init(&s->drain, kMmaIssuers);
         s->abort = 0;
         fence_mbar_init();
     }
@@ -247,6 +254,60 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     const int ksteps = MODE == 2 ? (a.K / kRouterKSplit) / GK : a.K / GK;
     const int ks_per_sblock = SG * a.G / GK;            // stages per scale block
     const int nb = MODE == 2 ? a.E_pad16 : BN;          // MMA N
+
+    // The MMAs of token tiles [i_lo, i_hi) of every unit, issued by one
+    // thread (bf16 x bf16 -> fp32 in tensor memory, tile i into columns
+    // 256 i ..).  An issue blocks for about one MMA's duration, and the
+    // stage's barrier waits come on top: so there are two issuers, tile 0 in
+    // warp kMmaWarp and tile 1 in warp kAProdWarp (gate/up, where that warp
+    // is otherwise idle) or kMma2Warp, so that one's waits overlap the
+    // other's MMAs.  Each issuer waits for the stage, commits its slots (the
+    // empty barriers count one arrival per issuer) and the drain.
+    auto run_mma = [&](int i_lo, int i_hi) {
+        uint32_t ait = 0, bit = 0;
+        uint32_t uses[TPU] = {0, 0};
+        bool ok = true;
+        const uint32_t idesc = idesc_bf16(BM, nb);
+        for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
+            const Unit t = load_unit<MODE>(a, u);
+            const int i_end = min(i_hi, t.ntiles);
+            for (int ks = 0; ks < ksteps; ++ks) {
+                const int as = ait % NS_A, bs = bit % NS_B;
+                ok = wait_or_abort(&s->a_full[as], (ait / NS_A) & 1, a, s, 6) &&
+                     wait_or_abort(&s->b_full[bs], (bit / NS_B) & 1, a, s, 7);
+                if (!ok) break;
+                if (MODE == 0) fence_proxy_async_smem();  // token rows written by cp.async
+                tc_fence_after();
+                const uint32_t a_addr = smem_u32(sA + as * A_STAGE);
+                const uint32_t b_addr = smem_u32(sB + bs * B_STAGE);
+                for (int i = i_lo; i < i_end; ++i) {
+                    if (ks == 0) {
+                        // this accumulator's previous contents have been drained
+                        ok = wait_or_abort(&s->acc_empty[i], (uses[i] & 1) ^ 1, a, s, 5);
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    const uint32_t d_tmem = tmem_base + i * 256;
+                    const uint32_t ai = a_addr + i * TILE_A;
+#pragma unroll
+                    for (int kk = 0; kk < GK / 16; ++kk)
+                        umma_bf16(d_tmem, sdesc_k128(ai + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
+                                  (ks | kk) != 0);
+                    if (ks == ksteps - 1) umma_commit(&s->acc_full[i]);
+                }
+                if (!ok) break;
+                umma_commit(&s->a_empty[as]);
+                umma_commit(&s->b_empty[bs]);
+                ++ait;
+                ++bit;
+            }
+            if (!ok) break;
+            for (int i = i_lo; i < i_end; ++i) ++uses[i];
+        }
+        // every MMA issued by this thread has finished before tensor memory is freed
+        umma_commit(&s->drain);
+        mbar_wait(&s->drain, 0, a.wait_limit);
+    };
 
     if (MODE == 0 && warp >= kLsuWarp0) {
         // -------------------------------------------- token rows (gate/up)
@@ -297,7 +358,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         cp_async_commit();  // nothing of this thread's may still be landing when the block exits
         cp_async_wait<0>();
     } else if (warp == kAProdWarp) {
-        // ------------------------------------------------------- token tiles
+        // ------------------------------- token tiles (gate/up: tile-1 MMAs)
+        if (MODE == 0 && lane == 0) run_mma(1, TPU);
         if (MODE != 0 && lane == 0) {
             uint32_t it = 0;
             bool ok = true;
@@ -389,50 +451,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------------- MMA
-        if (lane == 0) {
-            uint32_t ait = 0, bit = 0;
-            uint32_t uses[TPU] = {0, 0};
-            bool ok = true;
-            const uint32_t idesc = idesc_bf16(BM, nb);
-            for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-                const Unit t = load_unit<MODE>(a, u);
-                for (int ks = 0; ks < ksteps; ++ks) {
-                    const int as = ait % NS_A, bs = bit % NS_B;
-                    ok = wait_or_abort(&s->a_full[as], (ait / NS_A) & 1, a, s, 6) &&
-                         wait_or_abort(&s->b_full[bs], (bit / NS_B) & 1, a, s, 7);
-                    if (!ok) break;
-                    if (MODE == 0) fence_proxy_async_smem();  // token rows written by cp.async
-                    tc_fence_after();
-                    const uint32_t a_addr = smem_u32(sA + as * A_STAGE);
-                    const uint32_t b_addr = smem_u32(sB + bs * B_STAGE);
-                    for (int i = 0; i < t.ntiles; ++i) {
-                        if (ks == 0) {
-                            // this accumulator's previous contents have been drained
-                            ok = wait_or_abort(&s->acc_empty[i], (uses[i] & 1) ^ 1, a, s, 5);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        const uint32_t d_tmem = tmem_base + i * 256;
-                        const uint32_t ai = a_addr + i * TILE_A;
-#pragma unroll
-                        for (int kk = 0; kk < GK / 16; ++kk)
-                            umma_bf16(d_tmem, sdesc_k128(ai + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
-                                      (ks | kk) != 0);
-                        if (ks == ksteps - 1) umma_commit(&s->acc_full[i]);
-                    }
-                    if (!ok) break;
-                    umma_commit(&s->a_empty[as]);
-                    umma_commit(&s->b_empty[bs]);
-                    ++ait;
-                    ++bit;
-                }
-                if (!ok) break;
-                for (int i = 0; i < t.ntiles; ++i) ++uses[i];
-            }
-            // every MMA issued by this thread has finished before tensor memory is freed
-            umma_commit(&s->drain);
-            mbar_wait(&s->drain, 0, a.wait_limit);
-        }
+        if (lane == 0) run_mma(0, 1);
+        __syncwarp();
+    } else if (MODE != 0 && warp == kMma2Warp) {
+        // ------------------------------------- down, router: tile-1 MMAs
+        if (lane == 0) run_mma(1, TPU);
         __syncwarp();
     } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps && MODE == 2) {
         // ------------------------------------------ router: clear on the side

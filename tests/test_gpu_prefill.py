@@ -135,6 +135,41 @@ def test_router_split_is_its_definition_and_both_router_paths_agree(E, H):
     assert ((a - b).abs() <= bound).all()
 
 
+def test_graph_replay_matches_eager():
+    """The layer captured in a CUDA graph (its kernels launched as
+    programmatic dependents) and replayed twice gives the eager call's
+    routing tables bit for bit and its output within one bf16 step (the
+    combine's fp32 additions land in no fixed order)."""
+    cfg = dataclasses.replace(synthetic.CONFIGS["prefill512"], T=700, seed=91)
+    L = synthetic.make_layer(cfg, device="cuda")
+    layer = PackedLayer.from_fp32(cfg, L.router_w, L.router_bias, L.w_gate, L.w_up, L.w_down)
+    ws = layer.workspace(cfg.T)
+    x = L.x.cuda()
+    y_eager = layer.prefill(x, ws).clone()
+    names = ("logits", "topk_idx", "topk_w", "counts", "offsets", "perm", "tile_sched")
+    rt = {n: ws.routing(layer.desc, cfg.T)[n].clone() for n in names}
+    y = torch.empty_like(x)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        _lib.moe_prefill(layer.desc, x, cfg.T, y, ws.buf)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _lib.moe_prefill(layer.desc, x, cfg.T, y, ws.buf)
+    for _ in range(2):
+        y.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert _lib.moe_read_device_status(ws.buf) == 0
+        rt2 = ws.routing(layer.desc, cfg.T)
+        for n in names:
+            assert torch.equal(rt[n], rt2[n]), n
+        a, b = y.float(), y_eager.float()
+        bound = torch.maximum(a.abs(), b.abs()) * 2.0 ** -7 + 1e-5 * b.abs().max()
+        assert ((a - b).abs() <= bound).all()
+
+
 @pytest.mark.parametrize("T", [1, 2, 8])
 def test_full_shapes_small_batches(T):
     """The speculative-verify shape: a few tokens through the full-size
