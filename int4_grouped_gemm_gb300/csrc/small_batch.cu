@@ -164,6 +164,8 @@ __device__ void route_tokens(const BatchArgs &a) {
 __global__ void __launch_bounds__(256) batch_router_kernel(BatchArgs a) {
     __shared__ float part[8][kBatchMax];
     __shared__ int s_last;
+    pdl_wait();  // the tokens (and for a decoder block, their normalised rows) are written
+    pdl_trigger();
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
     const int r = blockIdx.x;
     const float *wrow = r < a.E ? a.Wr + static_cast<int64_t>(r) * a.H : a.shg;
@@ -237,6 +239,8 @@ __device__ __forceinline__ uint32_t codes_pair(uint32_t word, int p) {
 template <int STAGES>
 __global__ void __launch_bounds__(kSbThreads, 1) batch_gate_up_kernel(BatchArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
+    pdl_wait();  // the slot list and weights of the router's last block
+    pdl_trigger();
     const int H = a.H, I = a.I, G = a.G;
     const int xpitch = gu_xpitch(H);
     __nv_bfloat16 *xs = reinterpret_cast<__nv_bfloat16 *>(sm);
@@ -425,6 +429,8 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_gate_up_kernel(BatchArgs 
 // the group's partial output.
 __global__ void __launch_bounds__(kSbThreads, 1) batch_down_kernel(BatchArgs a) {
     extern __shared__ __align__(16) unsigned char sm[];
+    pdl_wait();  // h of every slot
+    pdl_trigger();
     const int H = a.H, I = a.I;
     float *s_w = reinterpret_cast<float *>(sm);
     unsigned char *ring = sm + dn_ring_off(a.S_max);
@@ -563,6 +569,8 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_down_kernel(BatchArgs a) 
 // y[t][f] = bf16(sum over the slot groups, in order, of their partial sums
 // [+ the residual stream's h[t][f]])
 __global__ void __launch_bounds__(256) batch_combine_kernel(BatchArgs a) {
+    pdl_wait();  // every slot group's output rows
+    pdl_trigger();
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= a.B * a.H) return;
     const int n_slots = a.slots[0];
@@ -580,21 +588,24 @@ __global__ void __launch_bounds__(256) batch_combine_kernel(BatchArgs a) {
 // ----------------------------------------------------------------- launch
 
 cudaError_t launch_batch(const BatchArgs &a, int num_sms, cudaStream_t s) {
+    // the four kernels launch as programmatic dependents of their
+    // predecessors (each waits for the previous grid before touching its
+    // outputs), so each one's launch overlaps the previous one's tail
     const int rows = a.E + (a.shg ? 1 : 0);
-    batch_router_kernel<<<rows, 256, 0, s>>>(a);
+    cudaError_t e = launch_dependent(batch_router_kernel, dim3(rows), dim3(256), 0, s, a);
+    if (e != cudaSuccess) return e;
     const bool deep = gu_stages(a.H, a.G, a.S_max) == 8;
     const int gsm = gu_smem(a.H, a.G, a.S_max, deep ? 8 : 6), dsm = dn_smem(a.S_max);
     if (gsm > kSmemMax || dsm > kSmemMax) return cudaErrorInvalidValue;
-    cudaError_t e;
     auto gu = deep ? batch_gate_up_kernel<8> : batch_gate_up_kernel<6>;
     if ((e = cudaFuncSetAttribute(gu, cudaFuncAttributeMaxDynamicSharedMemorySize, gsm)) != cudaSuccess) return e;
-    gu<<<num_sms, kSbThreads, gsm, s>>>(a);
+    if ((e = launch_dependent(gu, dim3(num_sms), dim3(kSbThreads), gsm, s, a)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(batch_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dsm)) !=
         cudaSuccess)
         return e;
-    batch_down_kernel<<<num_sms, kSbThreads, dsm, s>>>(a);
-    batch_combine_kernel<<<(a.B * a.H + 255) / 256, 256, 0, s>>>(a);
-    return cudaGetLastError();
+    if ((e = launch_dependent(batch_down_kernel, dim3(num_sms), dim3(kSbThreads), dsm, s, a)) != cudaSuccess)
+        return e;
+    return launch_dependent(batch_combine_kernel, dim3((a.B * a.H + 255) / 256), dim3(256), 0, s, a);
 }
 
 }  // namespace moe
