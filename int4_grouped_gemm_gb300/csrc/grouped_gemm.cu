@@ -48,8 +48,11 @@
 //               MODE 1 (down):    y_acc[token] += w * o  (fp32 v4 reductions
 //                                 after a transpose through shared memory)
 //               MODE 2 (router):  partial logits of one bf16 part and K quarter
-//               Tile 0's accumulator is handed back first, so that the next
-//               unit's tile-0 MMAs overlap the draining of tile 1.
+//               The two 256-column accumulators rotate over the CTA's token
+//               tiles in order (tile i of a unit takes accumulator
+//               (tiles before it) mod 2, and each MMA issuer owns one), so
+//               that after a one-tile unit the next unit's MMAs overlap the
+//               draining of the previous accumulator.
 //
 // Every mbarrier wait is bounded; a wait that runs out records a status code,
 // raises a block-wide abort flag and the block unwinds.
@@ -263,14 +266,17 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     // is otherwise idle) or kMma2Warp, so that one's waits overlap the
     // other's MMAs.  Each issuer waits for the stage, commits its slots (the
     // empty barriers count one arrival per issuer) and the drain.
-    auto run_mma = [&](int i_lo, int i_hi) {
-        uint32_t ait = 0, bit = 0;
-        uint32_t uses[TPU] = {0, 0};
+    auto run_mma = [&](int slot) {
+        uint32_t ait = 0, bit = 0, uses = 0;
+        uint32_t tiles_done = 0;  // token tiles of this CTA's earlier units (accumulator rotation)
         bool ok = true;
         const uint32_t idesc = idesc_bf16(BM, nb);
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
             const Unit t = load_unit<MODE>(a, u);
-            const int i_end = min(i_hi, t.ntiles);
+            // the unit's tile whose accumulator is `slot` (tile i takes slot
+            // (tiles_done + i) % 2), or none
+            const int mine = static_cast<int>((static_cast<uint32_t>(slot) - tiles_done) & 1u);
+            const bool has = mine < t.ntiles;
             for (int ks = 0; ks < ksteps; ++ks) {
                 const int as = ait % NS_A, bs = bit % NS_B;
                 ok = wait_or_abort(&s->a_full[as], (ait / NS_A) & 1, a, s, 6) &&
@@ -280,29 +286,29 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 tc_fence_after();
                 const uint32_t a_addr = smem_u32(sA + as * A_STAGE);
                 const uint32_t b_addr = smem_u32(sB + bs * B_STAGE);
-                for (int i = i_lo; i < i_end; ++i) {
+                if (has) {
                     if (ks == 0) {
                         // this accumulator's previous contents have been drained
-                        ok = wait_or_abort(&s->acc_empty[i], (uses[i] & 1) ^ 1, a, s, 5);
+                        ok = wait_or_abort(&s->acc_empty[slot], (uses & 1) ^ 1, a, s, 5);
                         if (!ok) break;
                         tc_fence_after();
                     }
-                    const uint32_t d_tmem = tmem_base + i * 256;
-                    const uint32_t ai = a_addr + i * TILE_A;
+                    const uint32_t d_tmem = tmem_base + slot * 256;
+                    const uint32_t ai = a_addr + mine * TILE_A;
 #pragma unroll
                     for (int kk = 0; kk < GK / 16; ++kk)
                         umma_bf16(d_tmem, sdesc_k128(ai + kk * 32), sdesc_k128(b_addr + kk * 32), idesc,
                                   (ks | kk) != 0);
-                    if (ks == ksteps - 1) umma_commit(&s->acc_full[i]);
+                    if (ks == ksteps - 1) umma_commit(&s->acc_full[slot]);
                 }
-                if (!ok) break;
                 umma_commit(&s->a_empty[as]);
                 umma_commit(&s->b_empty[bs]);
                 ++ait;
                 ++bit;
             }
             if (!ok) break;
-            for (int i = i_lo; i < i_end; ++i) ++uses[i];
+            if (has) ++uses;
+            tiles_done += t.ntiles;
         }
         // every MMA issued by this thread has finished before tensor memory is freed
         umma_commit(&s->drain);
@@ -359,7 +365,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         cp_async_wait<0>();
     } else if (warp == kAProdWarp) {
         // ------------------------------- token tiles (gate/up: tile-1 MMAs)
-        if (MODE == 0 && lane == 0) run_mma(1, TPU);
+        if (MODE == 0 && lane == 0) run_mma(1);
         if (MODE != 0 && lane == 0) {
             uint32_t it = 0;
             bool ok = true;
@@ -451,11 +457,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         __syncwarp();
     } else if (warp == kMmaWarp) {
         // ----------------------------------------------------------------- MMA
-        if (lane == 0) run_mma(0, 1);
+        if (lane == 0) run_mma(0);
         __syncwarp();
     } else if (MODE != 0 && warp == kMma2Warp) {
         // ------------------------------------- down, router: tile-1 MMAs
-        if (lane == 0) run_mma(1, TPU);
+        if (lane == 0) run_mma(1);
         __syncwarp();
     } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps && MODE == 2) {
         // ------------------------------------------ router: clear on the side
@@ -546,10 +552,12 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             for (int64_t i = i0; i < a.clear_f4_n; i += stride) a.clear_f4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         uint32_t uses[TPU] = {0, 0};
+        uint32_t tiles_done = 0;  // tile i of a unit sits in accumulator (tiles_done + i) % 2
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
             const Unit t = load_unit<MODE>(a, u);
             for (int i = 0; i < t.ntiles; ++i) {
+                const int slot = static_cast<int>((tiles_done + i) & 1u);
                 const int rr = i * BM + quarter * 32 + lane;  // row of the unit
                 const bool valid = rr < t.n;
                 int tok = 0;
@@ -558,11 +566,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                     tok = a.rb.row_token[t.row0 + rr];
                     wgt = a.rb.row_weight[t.row0 + rr];
                 }
-                ok = wait_or_abort(&s->acc_full[i], uses[i] & 1, a, s, 11);
+                ok = wait_or_abort(&s->acc_full[slot], uses[slot] & 1, a, s, 11);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + i * 256;
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + slot * 256;
                 if (MODE == 0) {
                     __nv_bfloat16 *hrow = a.h + static_cast<int64_t>(t.row0 + rr) * a.I + t.nt * (BN / 2);
                     for (int c0 = chalf * 16; c0 < BN / 2; c0 += 32) {
@@ -650,9 +658,10 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&s->acc_empty[i]);
-                ++uses[i];
+                if (lane == 0) mbar_arrive(&s->acc_empty[slot]);
+                ++uses[slot];
             }
+            tiles_done += t.ntiles;
         }
     }
 
