@@ -255,7 +255,8 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
 
     const int nunits = num_units<MODE>(a);
     const int ksteps = MODE == 2 ? (a.K / kRouterKSplit) / GK : a.K / GK;
-    const int ks_per_sblock = SG * a.G / GK;            // stages per scale block
+    const int ks_per_sblock = SG * a.G / GK;            // stages per scale block (4 or 8)
+    const int gshift = a.G == 64 ? 6 : 5;               // log2 of the group (32 or 64)
     const int nb = MODE == 2 ? a.E_pad16 : BN;          // MMA N
 
     // The MMAs of token tiles [i_lo, i_hi) of every unit, issued by one
@@ -481,7 +482,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
             for (int ks = 0; ks < ksteps; ++ks) {
-                if (ks % ks_per_sblock == 0) {
+                if ((ks & (ks_per_sblock - 1)) == 0) {
                     // the row's 8 scales and 8 biases in two 16-byte reads (32
                     // consecutive rows: 512 contiguous bytes per warp, no bank
                     // conflicts), then the stage goes back to the producer
@@ -505,7 +506,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 // warp's 32 rows then cover every bank once per 8 rows
                 const int chunk = (2 * j + hf) ^ ((r >> 1) & 3);
                 const uint4 nib = *reinterpret_cast<const uint4 *>(sQ + qs * Q_LOAD + r * Q_ROW + (chunk << 4));
-                const int gl = ((ks * GK + hf * 32) / a.G) % SG;
+                const int gl = ((ks * GK + hf * 32) >> gshift) & (SG - 1);
                 const uint32_t sw = (gl >> 1) == 0 ? sv.x : (gl >> 1) == 1 ? sv.y : (gl >> 1) == 2 ? sv.z : sv.w;
                 const uint32_t bw = (gl >> 1) == 0 ? bv.x : (gl >> 1) == 1 ? bv.y : (gl >> 1) == 2 ? bv.z : bv.w;
                 const uint32_t sbits = (gl & 1) ? (sw >> 16) : (sw & 0xFFFFu);
