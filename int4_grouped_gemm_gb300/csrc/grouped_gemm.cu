@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
             mbar_init(&s->a_empty[i], kMmaIssuers);
         }
         for (int i = 0; i < NS_B; ++i) {
-            mbar_init(&s->b_full[i], MODE == 2 ? 1 : kDeqWarps);
+            mbar_init(&s->b_full[i], MODE == 2 ? 1 : kDeqWarps / 2);  // one dequant group per slot
             mbar_init(&s->b_empty[i], kMmaIssuers);
         }
         for (int i = 0; i < NS_Q; ++i) {
@@ -474,18 +474,24 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         for (int64_t i = i0; i < a.clear_i_n; i += stride) a.clear_i[i] = 0;
     } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps && MODE != 2) {
         // ---------------------------------------------------------- dequantise
+        // Two groups of 8 warps take alternate stages: group jg the stages of
+        // parity jg (stage jg of every nibble load), always into weight slot
+        // jg, one thread per weight row over the stage's 64 K.  Each group so
+        // has two stage periods for one pass of its dequant chain.
         const int dt = tid - kDeqWarp0 * 32;
-        const int hf = dt / BN;  // 32-element half of the stage
+        const int jg = dt / BN;  // this group's stage parity
         const int r = dt % BN;   // weight row of the tile
-        uint32_t bit = 0, qit = 0, sit = 0;
+        const int rot = (r >> 1) & 3;  // 64-byte swizzle of the row's nibble chunks
+        uint32_t qit = 0, sit = 0, par = 0;
         uint4 sv = make_uint4(0u, 0u, 0u, 0u), bv = sv;  // this row's scales and biases of the current block
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-            for (int ks = 0; ks < ksteps; ++ks) {
-                if ((ks & (ks_per_sblock - 1)) == 0) {
-                    // the row's 8 scales and 8 biases in two 16-byte reads (32
-                    // consecutive rows: 512 contiguous bytes per warp, no bank
-                    // conflicts), then the stage goes back to the producer
+            for (int ks = jg; ks < ksteps; ks += QK) {
+                if ((ks & (ks_per_sblock - 1)) == jg) {
+                    // the group's first stage of a scale block: the row's 8
+                    // scales and 8 biases in two 16-byte reads (32 consecutive
+                    // rows: 512 contiguous bytes per warp, no bank conflicts),
+                    // then the block goes back to the producer (both groups)
                     const int ss = sit % NS_S;
                     ok = wait_or_abort(&s->s_full[ss], (sit / NS_S) & 1, a, s, 8);
                     if (!ok) break;
@@ -496,38 +502,41 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                     if (lane == 0) mbar_arrive(&s->s_empty[ss]);
                     ++sit;
                 }
-                const int j = ks % QK;  // stage within the nibble load
-                const int qs = qit % NS_Q, bs = bit % NS_B;
-                ok = (j != 0 || wait_or_abort(&s->q_full[qs], (qit / NS_Q) & 1, a, s, 9)) &&
-                     wait_or_abort(&s->b_empty[bs], ((bit / NS_B) & 1) ^ 1, a, s, 10);
+                const int qs = qit % NS_Q;
+                ok = wait_or_abort(&s->q_full[qs], (qit / NS_Q) & 1, a, s, 9) &&
+                     wait_or_abort(&s->b_empty[jg], (par & 1) ^ 1, a, s, 10);
                 if (!ok) break;
-                // 16-byte chunk 2j + hf of the row's 64 bytes, at its 64-byte-
-                // swizzle position (chunk ^ bits 7-8 of the row's offset); a
-                // warp's 32 rows then cover every bank once per 8 rows
-                const int chunk = (2 * j + hf) ^ ((r >> 1) & 3);
-                const uint4 nib = *reinterpret_cast<const uint4 *>(sQ + qs * Q_LOAD + r * Q_ROW + (chunk << 4));
-                const int gl = ((ks * GK + hf * 32) >> gshift) & (SG - 1);
-                const uint32_t sw = (gl >> 1) == 0 ? sv.x : (gl >> 1) == 1 ? sv.y : (gl >> 1) == 2 ? sv.z : sv.w;
-                const uint32_t bw = (gl >> 1) == 0 ? bv.x : (gl >> 1) == 1 ? bv.y : (gl >> 1) == 2 ? bv.z : bv.w;
-                const uint32_t sbits = (gl & 1) ? (sw >> 16) : (sw & 0xFFFFu);
-                const uint32_t bbits = (gl & 1) ? (bw >> 16) : (bw & 0xFFFFu);
-                const __nv_bfloat162 s2 = u32_as_bf162(sbits * 0x10001u);
-                const __nv_bfloat162 b2 = u32_as_bf162(bbits * 0x10001u);
-                uint8_t *brow = sB + bs * B_STAGE + r * 128;
-                const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
+                // the row's two 16-byte chunks of this stage (2 jg, 2 jg + 1),
+                // at their 64-byte-swizzle positions
+                const uint8_t *qrow = sQ + qs * Q_LOAD + r * Q_ROW;
+                const uint4 nib0 = *reinterpret_cast<const uint4 *>(qrow + (((2 * jg) ^ rot) << 4));
+                const uint4 nib1 = *reinterpret_cast<const uint4 *>(qrow + (((2 * jg + 1) ^ rot) << 4));
+                uint8_t *brow = sB + jg * B_STAGE + r * 128;
 #pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    const uint4 out = dequant8_bf16(words[w], s2, b2);
-                    *reinterpret_cast<uint4 *>(brow + (((hf * 4 + w) ^ (r & 7)) << 4)) = out;
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int gl = ((ks * GK + hf * 32) >> gshift) & (SG - 1);
+                    const uint32_t sw = (gl >> 1) == 0 ? sv.x : (gl >> 1) == 1 ? sv.y : (gl >> 1) == 2 ? sv.z : sv.w;
+                    const uint32_t bw = (gl >> 1) == 0 ? bv.x : (gl >> 1) == 1 ? bv.y : (gl >> 1) == 2 ? bv.z : bv.w;
+                    const uint32_t sbits = (gl & 1) ? (sw >> 16) : (sw & 0xFFFFu);
+                    const uint32_t bbits = (gl & 1) ? (bw >> 16) : (bw & 0xFFFFu);
+                    const __nv_bfloat162 s2 = u32_as_bf162(sbits * 0x10001u);
+                    const __nv_bfloat162 b2 = u32_as_bf162(bbits * 0x10001u);
+                    const uint4 nib = hf ? nib1 : nib0;
+                    const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) {
+                        const uint4 out = dequant8_bf16(words[w], s2, b2);
+                        *reinterpret_cast<uint4 *>(brow + (((hf * 4 + w) ^ (r & 7)) << 4)) = out;
+                    }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&s->b_full[bs]);
-                    if (j == QK - 1) mbar_arrive(&s->q_empty[qs]);
+                    mbar_arrive(&s->b_full[jg]);
+                    mbar_arrive(&s->q_empty[qs]);  // this group's only stage of the load
                 }
-                if (j == QK - 1) ++qit;
-                ++bit;
+                ++qit;
+                ++par;
             }
         }
     } else if (warp < kEpiWarps) {
