@@ -68,7 +68,7 @@ enum {
     MOE_ERR_NULL = -1,          /* a required pointer is NULL */
     MOE_ERR_ALIGN = -2,         /* a pointer is not 16-byte aligned */
     MOE_ERR_SHAPE = -3,         /* (E, k, H, I, group) outside the supported set */
-    MOE_ERR_TOKENS = -4,        /* T < 1 or too large */
+    MOE_ERR_TOKENS = -4,        /* T < 1, T x (k + 1) >= 2^30 or T x H > 2^32 */
     MOE_ERR_WORKSPACE = -5,     /* workspace smaller than moe_workspace_bytes() */
     MOE_ERR_CUDA = -6,          /* a CUDA runtime call or launch failed */
     MOE_ERR_TENSOR_MAP = -7,    /* TMA descriptor could not be encoded */

@@ -99,6 +99,8 @@ static int check_weights(const moe_layer_desc *d) {
 static int check_tokens(const moe_layer_desc *d, int32_t T) {
     if (T < 1) return MOE_ERR_TOKENS;
     if (static_cast<int64_t>(T) * (d->k + 1) >= (int64_t(1) << 30)) return MOE_ERR_TOKENS;
+    // the gate/up token copier indexes x[T][H] with 32-bit element offsets
+    if (static_cast<int64_t>(T) * d->H > (int64_t(1) << 32)) return MOE_ERR_TOKENS;
     return MOE_OK;
 }
 

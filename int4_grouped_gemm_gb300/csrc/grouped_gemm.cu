@@ -336,11 +336,14 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
             const Unit t = load_unit<MODE>(a, u);
             const bool shared = t.g == a.E;
-            int tok[TPU * BM / 16];
+            // element offsets in x of this thread's 16-byte chunks of the unit's
+            // rows (rows past the unit repeat its last row), for the whole unit
+            uint32_t off[TPU * BM / 16];
 #pragma unroll
             for (int i = 0; i < TPU * BM / 16; ++i) {
-                const int rr = min(rsub + 16 * i, t.n - 1);  // rows past the unit repeat its last row
-                tok[i] = shared ? t.row0 + rr - a.routed_rows : a.rb.row_token[t.row0 + rr];
+                const int rr = min(rsub + 16 * i, t.n - 1);
+                const int tok = shared ? t.row0 + rr - a.routed_rows : a.rb.row_token[t.row0 + rr];
+                off[i] = static_cast<uint32_t>(tok) * static_cast<uint32_t>(a.K) + chunk * 8;
             }
             for (int ks = 0; ks < ksteps && ok; ++ks, ++it) {
                 const int st = it % NS_A;
@@ -353,7 +356,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                     if (rr < t.n) {
                         const int r = rr & (BM - 1);
                         cp_async<16>(stage + (rr / BM) * TILE_A + r * 128 + ((chunk ^ (r & 7)) << 4),
-                                     a.x + static_cast<int64_t>(tok[i]) * a.K + ks * GK + chunk * 8);
+                                     a.x + (off[i] + ks * GK));
                     }
                 }
                 // this thread's arrival on the stage's barrier happens once its

@@ -64,6 +64,10 @@ def test_workspace_sizes_and_shape_checks(lib):
                 _desc(I=100), _desc(I=192), _desc(G=16), _desc(H=32768), _desc(shared=2)):
         assert _lib.moe_workspace_bytes(bad, 16) == 0
     assert _lib.moe_workspace_bytes(d, 0) == 0
+    # x[T][H] must hold at most 2^32 elements (32-bit offsets in the token copier)
+    wide = _desc(H=16384)
+    assert _lib.moe_workspace_bytes(wide, (1 << 32) // 16384) > 0
+    assert _lib.moe_workspace_bytes(wide, (1 << 32) // 16384 + 1) == 0
 
 
 def test_argument_errors_are_caught_on_the_host(lib):
