@@ -18,11 +18,15 @@
 // (M = 128 each, N = 256) into two 256-column TMEM accumulators, which halves
 // the dequant work and cuts the operand bytes per FLOP compared with one
 // token tile per unit.  Units run on a persistent grid of one CTA per SM in a
-// largest-first order.
+// largest-first order.  The down GEMM is the exception: its epilogue (the
+// combine's fp32 reductions into L2, about 20 bytes per cycle per SM) takes
+// longer than a two-tile unit's MMAs, and with both accumulators in one unit
+// the next unit would wait for it; its units hold one token tile, in tile
+// order, so that each unit's reductions overlap the next unit's MMAs.
 //
 //   warps 27-30 gate/up A producers: 16-byte cp.async gathers of the unit's
 //               token rows straight from x (no permuted copy of x)
-//   warp 10     down/router A producer: TMA loads of both token tiles (2 x 16 KB
+//   warp 10     down/router A producer: TMA loads of the unit's token tiles (16 KB
 //               boxes per stage) from h (down) or from x (router); gate/up:
 //               the tile-1 MMA issuer
 //   warp 8      W producer: TMA loads of packed nibbles (16 KB per load: 64
@@ -65,7 +69,7 @@ constexpr int TPU = 2;                           // token tiles per work unit
 constexpr int BN = 256;                          // weight rows per tile (MMA N)
 constexpr int GK = 64;                           // K elements per stage
 constexpr int SG = 8;                            // quantisation groups per scale block
-constexpr int NS_A = 3, NS_B = 2, NS_S = 1;      // ring depths (stages)
+constexpr int NS_S = 1;                          // scale/bias ring depth (blocks)
 constexpr int QK = 2;                            // stages per nibble load
 constexpr int NS_Q = 2;                          // nibble ring depth (loads)
 constexpr int kEpiWarps = 8, kWProdWarp = 8, kMmaWarp = 9, kAProdWarp = 10, kDeqWarp0 = 11, kDeqWarps = 16;
@@ -76,7 +80,15 @@ __host__ __device__ constexpr int gemm_threads(int mode) {
     return (kLsuWarp0 + (mode == 0 ? kLsuWarps : 1)) * 32;  // 992 (gate/up) or 896
 }
 constexpr int TILE_A = BM * 128;                 // 16 KB: 128 token rows x 64 bf16
-constexpr int A_STAGE = TPU * TILE_A;            // 32 KB: both token tiles
+// Token and weight ring depths (stages) and token-stage bytes.  The down
+// GEMM's units hold one token tile (its epilogue, the combine's fp32
+// reductions, then overlaps the next unit's MMAs in the other accumulator),
+// so its token stages are half as large and both of its rings are deeper.
+__host__ __device__ constexpr int tiles_per_unit(int mode) { return mode == 1 ? 1 : TPU; }
+__host__ __device__ constexpr int ring_a(int mode) { return mode == 1 ? 4 : 3; }
+__host__ __device__ constexpr int ring_b(int mode) { return mode == 1 ? 3 : 2; }
+__host__ __device__ constexpr int a_stage_bytes(int mode) { return tiles_per_unit(mode) * TILE_A; }
+constexpr int kMaxRingA = 4, kMaxRingB = 3;
 constexpr int B_STAGE = BN * 128;                // 32 KB: 256 weight rows x 64 bf16
 constexpr int Q_ROW = QK * GK / 2;               // 64 bytes of a weight row per nibble load
 constexpr int Q_LOAD = BN * Q_ROW;               // 16 KB: 256 rows x 128 nibbles
@@ -88,8 +100,8 @@ constexpr int kRouterKSplit = 4;                 // K quarters of the router GEM
 constexpr int kRouterUnits = kRouterParts * kRouterKSplit;  // router units per token-tile pair (parts x K quarters)
 
 struct Smem {
-    uint64_t a_full[NS_A], a_empty[NS_A];
-    uint64_t b_full[NS_B], b_empty[NS_B];
+    uint64_t a_full[kMaxRingA], a_empty[kMaxRingA];
+    uint64_t b_full[kMaxRingB], b_empty[kMaxRingB];
     uint64_t q_full[NS_Q], q_empty[NS_Q];
     uint64_t s_full[NS_S], s_empty[NS_S];
     uint64_t acc_full[TPU], acc_empty[TPU];
@@ -106,8 +118,8 @@ struct SmemMap {
 __host__ __device__ inline SmemMap smem_map(int mode) {
     SmemMap m{};
     m.a = 0;
-    m.b = m.a + NS_A * A_STAGE;
-    m.q = m.b + NS_B * B_STAGE;
+    m.b = m.a + ring_a(mode) * a_stage_bytes(mode);
+    m.q = m.b + ring_b(mode) * B_STAGE;
     const bool deq = mode != 2;
     m.s = m.q + (deq ? NS_Q * Q_LOAD : 0);
     m.t = m.s + (deq ? NS_S * S_STAGE : 0);
@@ -126,10 +138,11 @@ struct Unit {
     int kq;
 };
 
-// A unit of MODE 0/1 is tiles t0 and t0 + 1 of one group when the scheduled
+// A gate/up unit is tiles t0 and t0 + 1 of one group when the scheduled
 // tile t0 is full and the next tile belongs to the same group (units pair a
 // group's tiles 0-1, 2-3, ..., so a full scheduled tile followed by a tile of
-// its group is always the first of a pair).
+// its group is always the first of a pair).  A down unit is one tile, in
+// tile order.
 template <int MODE>
 __device__ __forceinline__ Unit load_unit(const GemmArgs &a, int u) {
     Unit t{};
@@ -139,6 +152,12 @@ __device__ __forceinline__ Unit load_unit(const GemmArgs &a, int u) {
         t.kq = rem % kRouterKSplit;
         t.row0 = pair * TPU * BM;
         t.n = min(TPU * BM, a.T - t.row0);
+    } else if (MODE == 1) {
+        const int t0 = u / a.n_ntiles;
+        t.nt = u % a.n_ntiles;
+        t.g = a.rb.tile_group[t0];
+        t.row0 = a.rb.tile_row[t0];
+        t.n = a.rb.tile_rows[t0];
     } else {
         const int t0 = a.rb.tile_sched[u / a.n_ntiles];
         t.nt = u % a.n_ntiles;
@@ -154,7 +173,7 @@ __device__ __forceinline__ Unit load_unit(const GemmArgs &a, int u) {
 template <int MODE>
 __device__ __forceinline__ int num_units(const GemmArgs &a) {
     if (MODE == 2) return kRouterUnits * ((a.T + TPU * BM - 1) / (TPU * BM));
-    return a.rb.num_tiles[1] * a.n_ntiles;
+    return a.rb.num_tiles[MODE == 1 ? 0 : 1] * a.n_ntiles;
 }
 
 // Bounded wait that also gives up as soon as another role has aborted.
@@ -201,6 +220,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     Smem *s = reinterpret_cast<Smem *>(base + map.ctl);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int NS_A = ring_a(MODE), NS_B = ring_b(MODE), A_STAGE = a_stage_bytes(MODE);
     // two MMA issuers, one per token tile (see run_mma below)
     constexpr int kMmaIssuers = 2;
 
@@ -478,14 +498,16 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps && MODE != 2) {
         // ---------------------------------------------------------- dequantise
         // Two groups of 8 warps take alternate stages: group jg the stages of
-        // parity jg (stage jg of every nibble load), always into weight slot
-        // jg, one thread per weight row over the stage's 64 K.  Each group so
-        // has two stage periods for one pass of its dequant chain.
+        // parity jg (stage jg of every nibble load; every unit has an even
+        // number of stages), one thread per weight row over the stage's 64 K.
+        // Each group so has two stage periods for one pass of its dequant
+        // chain.  The group's stage c of the CTA goes into weight slot
+        // bs = c % NS_B, with phase bit bph = (c / NS_B) & 1.
         const int dt = tid - kDeqWarp0 * 32;
         const int jg = dt / BN;  // this group's stage parity
         const int r = dt % BN;   // weight row of the tile
         const int rot = (r >> 1) & 3;  // 64-byte swizzle of the row's nibble chunks
-        uint32_t qit = 0, sit = 0, par = 0;
+        uint32_t qit = 0, sit = 0, bs = jg, bph = 0;
         uint4 sv = make_uint4(0u, 0u, 0u, 0u), bv = sv;  // this row's scales and biases of the current block
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
@@ -507,14 +529,14 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 }
                 const int qs = qit % NS_Q;
                 ok = wait_or_abort(&s->q_full[qs], (qit / NS_Q) & 1, a, s, 9) &&
-                     wait_or_abort(&s->b_empty[jg], (par & 1) ^ 1, a, s, 10);
+                     wait_or_abort(&s->b_empty[bs], bph ^ 1, a, s, 10);
                 if (!ok) break;
                 // the row's two 16-byte chunks of this stage (2 jg, 2 jg + 1),
                 // at their 64-byte-swizzle positions
                 const uint8_t *qrow = sQ + qs * Q_LOAD + r * Q_ROW;
                 const uint4 nib0 = *reinterpret_cast<const uint4 *>(qrow + (((2 * jg) ^ rot) << 4));
                 const uint4 nib1 = *reinterpret_cast<const uint4 *>(qrow + (((2 * jg + 1) ^ rot) << 4));
-                uint8_t *brow = sB + jg * B_STAGE + r * 128;
+                uint8_t *brow = sB + bs * B_STAGE + r * 128;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int gl = ((ks * GK + hf * 32) >> gshift) & (SG - 1);
@@ -535,11 +557,15 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    mbar_arrive(&s->b_full[jg]);
+                    mbar_arrive(&s->b_full[bs]);
                     mbar_arrive(&s->q_empty[qs]);  // this group's only stage of the load
                 }
                 ++qit;
-                ++par;
+                bs += 2;  // the other group's stage comes in between
+                if (bs >= static_cast<uint32_t>(NS_B)) {
+                    bs -= NS_B;
+                    bph ^= 1;
+                }
             }
         }
     } else if (warp < kEpiWarps) {
