@@ -36,16 +36,17 @@
 //               matter) and of scale/bias blocks (8 groups x 256 rows);
 //               router mode: the bf16 router weight tile straight into the B
 //               ring
-//   warps 11-26 dequantisers, two threads per weight row (one per 32-element
-//               half of the stage): nibbles -> bf16 s*q+b in the 128-byte
-//               swizzled K-major layout of the B ring
+//   warps 11-26 dequantisers in two groups of 8 warps taking alternate
+//               stages, one thread per weight row over the stage's 64 K:
+//               nibbles -> bf16 s*q+b in the 128-byte swizzled K-major
+//               layout of the B ring
 //               (router mode: these warps zero the call's per-chunk expert
 //               histogram instead)
-//   warp 9      one thread issues token tile 0's MMAs (bf16 x bf16 -> fp32
-//               in tensor memory, columns 0-255); tile 1's (columns 256-511)
-//               come from one thread of warp 10 (gate/up) or warp 27 (down,
-//               router), so that one issuer's barrier waits overlap the
-//               other's MMAs
+//   warp 9      one thread issues the MMAs into accumulator 0 (bf16 x bf16
+//               -> fp32 in tensor memory, columns 0-255); accumulator 1's
+//               (columns 256-511) come from one thread of warp 10 (gate/up)
+//               or warp 27 (down, router), so that one issuer's barrier
+//               waits overlap the other's MMAs
 //   warps 0-7   epilogue, warp w reads TMEM lanes 32*(w%4).. (token rows) and
 //               every other 16-column chunk (w/4 picks which):
 //               MODE 0 (gate/up): h = silu(gate) * up -> bf16 h rows
@@ -279,14 +280,15 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
     const int gshift = a.G == 64 ? 6 : 5;               // log2 of the group (32 or 64)
     const int nb = MODE == 2 ? a.E_pad16 : BN;          // MMA N
 
-    // The MMAs of token tiles [i_lo, i_hi) of every unit, issued by one
-    // thread (bf16 x bf16 -> fp32 in tensor memory, tile i into columns
-    // 256 i ..).  An issue blocks for about one MMA's duration, and the
-    // stage's barrier waits come on top: so there are two issuers, tile 0 in
-    // warp kMmaWarp and tile 1 in warp kAProdWarp (gate/up, where that warp
-    // is otherwise idle) or kMma2Warp, so that one's waits overlap the
-    // other's MMAs.  Each issuer waits for the stage, commits its slots (the
-    // empty barriers count one arrival per issuer) and the drain.
+    // The MMAs into accumulator `slot` (columns 256 slot ..), issued by one
+    // thread (bf16 x bf16 -> fp32 in tensor memory): tile i of a unit
+    // accumulates in accumulator (tiles before it) mod 2.  An issue blocks
+    // for about one MMA's duration, and the stage's barrier waits come on
+    // top: so there are two issuers, accumulator 0 in warp kMmaWarp and 1 in
+    // warp kAProdWarp (gate/up, where that warp is otherwise idle) or
+    // kMma2Warp, so that one's waits overlap the other's MMAs.  Each issuer
+    // waits for every stage, commits its slots (the empty barriers count one
+    // arrival per issuer) and the drain.
     auto run_mma = [&](int slot) {
         uint32_t ait = 0, bit = 0, uses = 0;
         uint32_t tiles_done = 0;  // token tiles of this CTA's earlier units (accumulator rotation)
