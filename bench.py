@@ -213,9 +213,13 @@ def expert_flops(rows, H, I):
     return rows * (2 * H * 2 * I + 2 * I * H)
 
 
+def expert_bytes(cfg):
+    """Bytes of one int4 expert: gate, up and down nibbles plus their bf16 scale and bias per group."""
+    return 3 * cfg.H * cfg.I // 2 + 3 * cfg.H * cfg.I // cfg.group * 4
+
+
 def decode_bytes_per_layer(cfg):
-    per_expert = 3 * cfg.H * cfg.I // 2 + 3 * cfg.H * cfg.I // cfg.group * 4
-    return cfg.E * cfg.H * 4 + (cfg.k + 1) * per_expert
+    return cfg.E * cfg.H * 4 + (cfg.k + 1) * expert_bytes(cfg)
 
 
 def build_prefill(cfg):
@@ -386,6 +390,7 @@ def run_decode(args, pk):
     if st != 0:
         raise RuntimeError(f"decode device status {st}")
     bytes_step = decode_bytes_per_layer(cfg) * cfg.layers
+    expert_step = (cfg.k + 1) * expert_bytes(cfg) * cfg.layers
     gbs = bytes_step / (ms * 1e-3) / 1e9
     # the same 40 layers in the decoder-block form: residual stream and RMS
     # norm around every layer (the stream does not collapse to zero), one
@@ -419,7 +424,10 @@ def run_decode(args, pk):
                                "around each of the 40 layers; the router of every layer runs on its own "
                                "normalised input (one more grid-wide step per layer than the plain chain)"},
                 roofline={"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm"], "unit": "GB/s",
-                          "frac": round(gbs / pk["hbm"], 4), "bytes_per_step": bytes_step},
+                          "frac": round(gbs / pk["hbm"], 4), "bytes_per_step": bytes_step,
+                          # the same on the int4 experts' bytes alone (9 per layer, no router)
+                          "expert_bytes_per_step": expert_step,
+                          "frac_expert_bytes_only": round(expert_step / (ms * 1e-3) / 1e9 / pk["hbm"], 4)},
                 clocks=clk.summary(), launches=-(-cfg.layers // DECODE_LAYERS_PER_KERNEL) * steps)
 
 
