@@ -267,11 +267,11 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_gate_up_kernel(BatchArgs 
     }
     __syncthreads();
 
-    const int rblocks = I / 16, nck = H / 64;
+    const int rblocks = I / 16, nst = H / (64 * kGuChunks);  // stages per task
     const int ntask = n_slots * rblocks;
     const int W = gridDim.x * kSbWarps;
     const int wg = warp * gridDim.x + blockIdx.x;
-    const int nsteps = (wg < ntask ? (ntask - 1 - wg) / W + 1 : 0) * nck;
+    const int nsteps = (wg < ntask ? (ntask - 1 - wg) / W + 1 : 0) * nst;
     const int g = lane >> 2, cc = lane & 3;
     const bool g64 = G == 64;
     unsigned char *wring = ring + warp * STAGES * kGuStage;
@@ -279,36 +279,45 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_gate_up_kernel(BatchArgs 
     // the scale or bias array this lane stages: matrix cc & 1, kind cc >> 1
     const int m_item = cc & 1, sb_item = cc >> 1;
     const uint16_t *sc_arr = m_item ? (sb_item ? a.bu : a.su) : (sb_item ? a.bg : a.sg);
-    const int sc_off0 = kGuQ + (m_item * 16 + g) * 8 + sb_item * 4;
+    const int sc_off0 = kGuQ + (m_item * 16 + g) * 16 + sb_item * 8;
 
-    // loader: next step to issue, its stage, chunk and task, the lane's row
-    // pointers.  Lane L stages 16 bytes (half L & 1) of row L >> 1 of both
-    // matrices, so a stage holds each row's 32 bytes in order; the lanes
-    // then read each other's words (after the warp barrier).
+    // loader: next step to issue, its stage, chunk pair and task, the lane's
+    // row pointers.  Lane L stages 16-byte piece L & 3 of rows L >> 2 and
+    // (L >> 2) + 8 of both matrices, so a stage holds each row's 64 bytes in
+    // order; the lanes then read each other's words (after the warp barrier).
     int i_s = 0, i_st = 0, i_c = 0, i_task = wg;
-    const uint32_t *qg = nullptr, *qu = nullptr;
+    const uint32_t *qg0 = nullptr, *qg1 = nullptr, *qu0 = nullptr, *qu1 = nullptr;
     const uint16_t *sc = nullptr;
-    const int q_off = (lane >> 1) * 32 + (lane & 1) * 16;
+    const int q_off0 = (lane >> 2) * kGuRow + (lane & 3) * 16, q_off1 = q_off0 + 8 * kGuRow;
     auto start_task = [&](int task) {
         const int u = task / rblocks, rb = task - u * rblocks;
         const int64_t row0 = static_cast<int64_t>(s_exp[u]) * I + rb * 16;
-        qg = a.qg + (row0 + (lane >> 1)) * qpitch + 4 * (lane & 1);
-        qu = a.qu + (row0 + (lane >> 1)) * qpitch + 4 * (lane & 1);
+        qg0 = a.qg + (row0 + (lane >> 2)) * qpitch + 4 * (lane & 3);
+        qg1 = qg0 + 8 * qpitch;
+        qu0 = a.qu + (row0 + (lane >> 2)) * qpitch + 4 * (lane & 3);
+        qu1 = qu0 + 8 * qpitch;
         sc = sc_arr + (row0 + g) * a.ldg_h;
     };
     if (nsteps > 0) start_task(wg);
     auto issue = [&]() {
         if (i_s < nsteps) {
             unsigned char *st = wring + i_st * kGuStage;
-            const int qo = i_c * 8;
-            cp_async<16>(st + q_off, qg + qo);
-            cp_async<16>(st + 512 + q_off, qu + qo);
-            const int p0 = g64 ? (i_c & ~1) : 2 * i_c;
-            cp_async<4>(st + sc_off0, sc + p0);
-            cp_async<4>(st + sc_off0 + 8 * 8, sc + 8 * a.ldg_h + p0);
+            const int qo = i_c * 8 * kGuChunks;
+            cp_async<16>(st + q_off0, qg0 + qo);
+            cp_async<16>(st + q_off1, qg1 + qo);
+            cp_async<16>(st + 16 * kGuRow + q_off0, qu0 + qo);
+            cp_async<16>(st + 16 * kGuRow + q_off1, qu1 + qo);
+            // the stage's groups: two (group 64) or four (group 32) values
+            if (g64) {
+                cp_async<4>(st + sc_off0, sc + 2 * i_c);
+                cp_async<4>(st + sc_off0 + 8 * 16, sc + 8 * a.ldg_h + 2 * i_c);
+            } else {
+                cp_async<8>(st + sc_off0, sc + 4 * i_c);
+                cp_async<8>(st + sc_off0 + 8 * 16, sc + 8 * a.ldg_h + 4 * i_c);
+            }
             ++i_s;
             i_st = i_st + 1 == STAGES ? 0 : i_st + 1;
-            if (++i_c == nck) {
+            if (++i_c == nst) {
                 i_c = 0;
                 i_task += W;
                 if (i_s < nsteps) start_task(i_task);
@@ -349,59 +358,72 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_gate_up_kernel(BatchArgs 
         cp_async_wait<STAGES - 1>();
         __syncwarp();
         const unsigned char *st = wring + c_st * kGuStage;
-        uint2 sbp[2][2], qw[2][2];
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
+        for (int c2 = 0; c2 < kGuChunks; ++c2) {
+            const int ch = c * kGuChunks + c2;  // the chunk of the task's K
+            uint2 sbp[2][2], qw[2][2];
 #pragma unroll
-            for (int hr = 0; hr < 2; ++hr) {
-                const int row = g + 8 * hr;
-                sbp[m][hr] = *reinterpret_cast<const uint2 *>(st + kGuQ + (m * 16 + row) * 8);
-                // the lane's words of the row: 2c, 2c+1 (group 64) or c, c+4 (group 32)
-                const unsigned char *qr = st + m * 512 + row * 32;
-                if (g64) {
-                    qw[m][hr] = *reinterpret_cast<const uint2 *>(qr + cc * 8);
-                } else {
-                    qw[m][hr].x = *reinterpret_cast<const uint32_t *>(qr + cc * 4);
-                    qw[m][hr].y = *reinterpret_cast<const uint32_t *>(qr + 16 + cc * 4);
-                }
-            }
-        }
-        if (g64) {
-            const uint4 x0 = *reinterpret_cast<const uint4 *>(xrow + c * 64);
-            const uint4 x1 = *reinterpret_cast<const uint4 *>(xrow + c * 64 + 8);
-            const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int m = 0; m < 2; ++m) {
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const uint32_t af[4] = {codes_pair(qw[m][0].x, ks), codes_pair(qw[m][1].x, ks),
-                                            codes_pair(qw[m][0].y, ks), codes_pair(qw[m][1].y, ks)};
-                    mma_16816(m ? cu : cg, af, xb[ks], xb[4 + ks]);
-                }
-            }
-            fold(cg, cu, sbp, c & 1, c);
-        } else {
-#pragma unroll
-            for (int gi = 0; gi < 2; ++gi) {
-                const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + c * 64 + 32 * gi);
-                const uint32_t xb[4] = {xv.x, xv.y, xv.z, xv.w};
-                float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-#pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const uint32_t wa = gi ? qw[m][0].y : qw[m][0].x, wb = gi ? qw[m][1].y : qw[m][1].x;
-                        const uint32_t af[4] = {codes_pair(wa, 2 * j), codes_pair(wb, 2 * j),
-                                                codes_pair(wa, 2 * j + 1), codes_pair(wb, 2 * j + 1)};
-                        mma_16816(m ? cu : cg, af, xb[2 * j], xb[2 * j + 1]);
+                for (int hr = 0; hr < 2; ++hr) {
+                    const int row = g + 8 * hr;
+                    // the chunk's scale and bias pairs: the stage's entry holds two
+                    // groups (group 64: the pair) or four (group 32: pair c2)
+                    const unsigned char *sb = st + kGuQ + (m * 16 + row) * 16;
+                    if (g64) {
+                        sbp[m][hr] = make_uint2(*reinterpret_cast<const uint32_t *>(sb),
+                                                *reinterpret_cast<const uint32_t *>(sb + 8));
+                    } else {
+                        const uint2 s4 = *reinterpret_cast<const uint2 *>(sb), b4 = *reinterpret_cast<const uint2 *>(sb + 8);
+                        sbp[m][hr] = make_uint2(c2 ? s4.y : s4.x, c2 ? b4.y : b4.x);
+                    }
+                    // the lane's words of the row: 2c, 2c+1 (group 64) or c, c+4 (group 32)
+                    const unsigned char *qr = st + m * 16 * kGuRow + row * kGuRow + c2 * 32;
+                    if (g64) {
+                        qw[m][hr] = *reinterpret_cast<const uint2 *>(qr + cc * 8);
+                    } else {
+                        qw[m][hr].x = *reinterpret_cast<const uint32_t *>(qr + cc * 4);
+                        qw[m][hr].y = *reinterpret_cast<const uint32_t *>(qr + 16 + cc * 4);
                     }
                 }
-                fold(cg, cu, sbp, gi, 2 * c + gi);
+            }
+            if (g64) {
+                const uint4 x0 = *reinterpret_cast<const uint4 *>(xrow + ch * 64);
+                const uint4 x1 = *reinterpret_cast<const uint4 *>(xrow + ch * 64 + 8);
+                const uint32_t xb[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        const uint32_t af[4] = {codes_pair(qw[m][0].x, ks), codes_pair(qw[m][1].x, ks),
+                                                codes_pair(qw[m][0].y, ks), codes_pair(qw[m][1].y, ks)};
+                        mma_16816(m ? cu : cg, af, xb[ks], xb[4 + ks]);
+                    }
+                }
+                fold(cg, cu, sbp, ch & 1, ch);
+            } else {
+#pragma unroll
+                for (int gi = 0; gi < 2; ++gi) {
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(xrow + ch * 64 + 32 * gi);
+                    const uint32_t xb[4] = {xv.x, xv.y, xv.z, xv.w};
+                    float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+#pragma unroll
+                        for (int m = 0; m < 2; ++m) {
+                            const uint32_t wa = gi ? qw[m][0].y : qw[m][0].x, wb = gi ? qw[m][1].y : qw[m][1].x;
+                            const uint32_t af[4] = {codes_pair(wa, 2 * j), codes_pair(wb, 2 * j),
+                                                    codes_pair(wa, 2 * j + 1), codes_pair(wb, 2 * j + 1)};
+                            mma_16816(m ? cu : cg, af, xb[2 * j], xb[2 * j + 1]);
+                        }
+                    }
+                    fold(cg, cu, sbp, gi, 2 * ch + gi);
+                }
             }
         }
         c_st = c_st + 1 == STAGES ? 0 : c_st + 1;
-        if (++c == nck) {
+        if (++c == nst) {
             const int u = c_task / rblocks, rb = c_task - u * rblocks;
             __nv_bfloat16 *hp = a.h + static_cast<int64_t>(u) * kBatchMax * I + rb * 16 + g;
 #pragma unroll
@@ -594,10 +616,10 @@ cudaError_t launch_batch(const BatchArgs &a, int num_sms, cudaStream_t s) {
     const int rows = a.E + (a.shg ? 1 : 0);
     cudaError_t e = launch_dependent(batch_router_kernel, dim3(rows), dim3(256), 0, s, a);
     if (e != cudaSuccess) return e;
-    const bool deep = gu_stages(a.H, a.G, a.S_max) == 8;
-    const int gsm = gu_smem(a.H, a.G, a.S_max, deep ? 8 : 6), dsm = dn_smem(a.S_max);
+    const bool deep = gu_stages(a.H, a.G, a.S_max) == 4;
+    const int gsm = gu_smem(a.H, a.G, a.S_max, deep ? 4 : 3), dsm = dn_smem(a.S_max);
     if (gsm > kSmemMax || dsm > kSmemMax) return cudaErrorInvalidValue;
-    auto gu = deep ? batch_gate_up_kernel<8> : batch_gate_up_kernel<6>;
+    auto gu = deep ? batch_gate_up_kernel<4> : batch_gate_up_kernel<3>;
     if ((e = cudaFuncSetAttribute(gu, cudaFuncAttributeMaxDynamicSharedMemorySize, gsm)) != cudaSuccess) return e;
     if ((e = launch_dependent(gu, dim3(num_sms), dim3(kSbThreads), gsm, s, a)) != cudaSuccess) return e;
     if ((e = cudaFuncSetAttribute(batch_down_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dsm)) !=

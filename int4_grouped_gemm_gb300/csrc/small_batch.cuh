@@ -71,11 +71,14 @@ struct BatchArgs {
 constexpr int kSbWarps = 16;  // warps per block of the streaming kernels (one block per SM)
 constexpr int kSbThreads = kSbWarps * 32;
 constexpr int kSbStages = 8;  // cp.async stages per warp
-// gate/up stage: [2 matrices][16 rows] x 32 B of nibbles (the chunk's 8
-// words of each row), then [2 matrices][16 rows] x (4 B scale pair, 4 B bias
-// pair)
-constexpr int kGuQ = 2 * 16 * 32;
-constexpr int kGuStage = kGuQ + 2 * 16 * 8;
+// gate/up stage: two 64-element chunks, [2 matrices][16 rows] x 64 B of
+// nibbles (each row's 16 words of the two chunks in order: a row is read in
+// 64-byte pieces), then [2 matrices][16 rows] x (8 B of scales, 8 B of
+// biases) of the stage's groups (group 64: two values each; group 32: four)
+constexpr int kGuChunks = 2;
+constexpr int kGuRow = 32 * kGuChunks;
+constexpr int kGuQ = 2 * 16 * kGuRow;
+constexpr int kGuStage = kGuQ + 2 * 16 * 16;
 // down stage: [16 rows] x 32 B of nibbles, [16 rows] x (scale pair, bias
 // pair), then [32 lanes] x 32 B of the slot's h (token g, K = 16c ..)
 constexpr int kDnQ = 16 * 32;
@@ -97,9 +100,9 @@ __host__ __device__ inline int gu_ring_off(int H, int G, int S_max) {
 inline int gu_smem(int H, int G, int S_max, int stages) {
     return gu_ring_off(H, G, S_max) + kSbWarps * stages * kGuStage;
 }
-// Stages per warp of the gate/up kernel: eight where they fit, else six (the
-// widest H with group 32).
-inline int gu_stages(int H, int G, int S_max) { return gu_smem(H, G, S_max, 8) <= kSmemMax ? 8 : 6; }
+// Stages per warp of the gate/up kernel: four where they fit, else three (the
+// widest H).
+inline int gu_stages(int H, int G, int S_max) { return gu_smem(H, G, S_max, 4) <= kSmemMax ? 4 : 3; }
 
 // Shared memory of the down kernel: the slot weights [n_slots][8], then the rings.
 __host__ __device__ inline int dn_ring_off(int S_max) { return align16i(4 * kBatchMax * S_max); }
