@@ -463,7 +463,7 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_down_kernel(BatchArgs a) 
     for (int i = tid; i < n_slots * kBatchMax; i += kSbThreads) s_w[i] = a.slot_w[i];
     __syncthreads();
 
-    const int fblocks = H / 16, nck = I / 64;
+    const int fblocks = H / 16, nst = I / (64 * kDnChunks);  // stages per slot
     const int sg = slot_group(n_slots);
     const int ngrp = (n_slots + sg - 1) / sg;
     const int ntask = ngrp * fblocks;
@@ -471,13 +471,13 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_down_kernel(BatchArgs a) 
     const int wg = warp * gridDim.x + blockIdx.x;
     const int g = lane >> 2, cc = lane & 3;
     const bool g64 = a.G == 64;
-    unsigned char *wring = ring + warp * kSbStages * kDnStage;
+    unsigned char *wring = ring + warp * kDnStages * kDnStage;
     const int64_t qpitch = I / 8;
-    // steps of a task: its slots times nck; only the last group can be short
+    // steps of a task: its slots times nst; only the last group can be short
     auto task_steps = [&](int task) {
         const int j = task / fblocks;
         const int ns = min(sg, n_slots - j * sg);
-        return ns * nck;
+        return ns * nst;
     };
     int nsteps = 0;
     for (int t = wg; t < ntask; t += W) nsteps += task_steps(t);
@@ -486,13 +486,15 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_down_kernel(BatchArgs a) 
 
     // loader: next step, its chunk / slot / task, and the lane's pointers
     int i_s = 0, i_c = 0, i_u = 0, i_uend = 0, i_task = wg;
-    const uint32_t *q = nullptr;
+    const uint32_t *q0 = nullptr, *q1 = nullptr;
     const uint16_t *sc = nullptr;
     const __nv_bfloat16 *hp = nullptr;
     int fb_i = 0;
     auto start_slot = [&](int u) {
         const int64_t row0 = static_cast<int64_t>(s_exp[u]) * H + fb_i * 16;
-        q = a.qd + (row0 + (lane >> 1)) * qpitch + 4 * (lane & 1);  // lane L: 16 bytes of row L >> 1
+        // lane L: 16-byte piece L & 3 of rows L >> 2 and (L >> 2) + 8
+        q0 = a.qd + (row0 + (lane >> 2)) * qpitch + 4 * (lane & 3);
+        q1 = q0 + 8 * qpitch;
         sc = sc_arr + (row0 + row_item) * a.ldg_i;
         hp = a.h + (static_cast<int64_t>(u) * kBatchMax + g) * I + 16 * cc;
     };
@@ -506,15 +508,23 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_down_kernel(BatchArgs a) 
     if (nsteps > 0) start_task(wg);
     auto issue = [&]() {
         if (i_s < nsteps) {
-            unsigned char *st = wring + (i_s & (kSbStages - 1)) * kDnStage;
-            const int qo = i_c * 8;
-            cp_async<16>(st + (lane >> 1) * 32 + (lane & 1) * 16, q + qo);
-            const int p0 = g64 ? (i_c & ~1) : 2 * i_c;
-            cp_async<4>(st + kDnQ + row_item * 8 + sb_item * 4, sc + p0);
-            cp_async<16>(st + kDnH + lane * 32, hp + i_c * 64);
-            cp_async<16>(st + kDnH + lane * 32 + 16, hp + i_c * 64 + 8);
+            unsigned char *st = wring + (i_s & (kDnStages - 1)) * kDnStage;
+            const int qo = i_c * 8 * kDnChunks;
+            cp_async<16>(st + (lane >> 2) * kDnRow + (lane & 3) * 16, q0 + qo);
+            cp_async<16>(st + ((lane >> 2) + 8) * kDnRow + (lane & 3) * 16, q1 + qo);
+            // the stage's groups: two (group 64) or four (group 32) values
+            if (g64)
+                cp_async<4>(st + kDnQ + row_item * 16 + sb_item * 8, sc + 2 * i_c);
+            else
+                cp_async<8>(st + kDnQ + row_item * 16 + sb_item * 8, sc + 4 * i_c);
+#pragma unroll
+            for (int c2 = 0; c2 < kDnChunks; ++c2) {
+                const int ch = i_c * kDnChunks + c2;
+                cp_async<16>(st + kDnH + c2 * 1024 + lane * 32, hp + ch * 64);
+                cp_async<16>(st + kDnH + c2 * 1024 + lane * 32 + 16, hp + ch * 64 + 8);
+            }
             ++i_s;
-            if (++i_c == nck) {
+            if (++i_c == nst) {
                 i_c = 0;
                 if (++i_u == i_uend) {
                     i_task += W;
@@ -528,7 +538,7 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_down_kernel(BatchArgs a) 
     };
 
 #pragma unroll 1
-    for (int s = 0; s < kSbStages - 1; ++s) issue();
+    for (int s = 0; s < kDnStages - 1; ++s) issue();
     float oa[4] = {0.f, 0.f, 0.f, 0.f}, ya[4] = {0.f, 0.f, 0.f, 0.f};
     int c = 0, c_task = wg;
     int c_u = (wg / fblocks) * sg;
@@ -536,30 +546,36 @@ __global__ void __launch_bounds__(kSbThreads, 1) batch_down_kernel(BatchArgs a) 
 #pragma unroll 1
     for (int s = 0; s < nsteps; ++s) {
         issue();
-        cp_async_wait<kSbStages - 1>();
+        cp_async_wait<kDnStages - 1>();
         __syncwarp();
-        const unsigned char *st = wring + (s & (kSbStages - 1)) * kDnStage;
-        const int half = g64 ? (c & 1) : (cc >> 1);
-        uint32_t s2[2], b2[2];
-        uint2 qw[2];
+        const unsigned char *st = wring + (s & (kDnStages - 1)) * kDnStage;
 #pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-            const int row = g + 8 * hr;
-            const uint2 sbp = *reinterpret_cast<const uint2 *>(st + kDnQ + row * 8);
-            s2[hr] = pick_dup(sbp.x, half);
-            b2[hr] = pick_dup(sbp.y, half);
-            qw[hr] = *reinterpret_cast<const uint2 *>(st + row * 32 + cc * 8);
-        }
-        const uint4 h0 = *reinterpret_cast<const uint4 *>(st + kDnH + lane * 32);
-        const uint4 h1 = *reinterpret_cast<const uint4 *>(st + kDnH + lane * 32 + 16);
-        const uint32_t hb[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+        for (int c2 = 0; c2 < kDnChunks; ++c2) {
+            // the chunk's group: the half of its scale pair (group 64: the
+            // stage's pair; group 32: pair c2, split between the lane halves)
+            const int half = g64 ? c2 : (cc >> 1);
+            const int pw = g64 ? 0 : 4 * c2;
+            uint32_t s2[2], b2[2];
+            uint2 qw[2];
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t af[4] = {deq_pair(qw[0].x, ks, s2[0], b2[0]), deq_pair(qw[1].x, ks, s2[1], b2[1]),
-                                    deq_pair(qw[0].y, ks, s2[0], b2[0]), deq_pair(qw[1].y, ks, s2[1], b2[1])};
-            mma_16816(oa, af, hb[ks], hb[4 + ks]);
+            for (int hr = 0; hr < 2; ++hr) {
+                const int row = g + 8 * hr;
+                const unsigned char *sb = st + kDnQ + row * 16 + pw;
+                s2[hr] = pick_dup(*reinterpret_cast<const uint32_t *>(sb), half);
+                b2[hr] = pick_dup(*reinterpret_cast<const uint32_t *>(sb + 8), half);
+                qw[hr] = *reinterpret_cast<const uint2 *>(st + row * kDnRow + c2 * 32 + cc * 8);
+            }
+            const uint4 h0 = *reinterpret_cast<const uint4 *>(st + kDnH + c2 * 1024 + lane * 32);
+            const uint4 h1 = *reinterpret_cast<const uint4 *>(st + kDnH + c2 * 1024 + lane * 32 + 16);
+            const uint32_t hb[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const uint32_t af[4] = {deq_pair(qw[0].x, ks, s2[0], b2[0]), deq_pair(qw[1].x, ks, s2[1], b2[1]),
+                                        deq_pair(qw[0].y, ks, s2[0], b2[0]), deq_pair(qw[1].y, ks, s2[1], b2[1])};
+                mma_16816(oa, af, hb[ks], hb[4 + ks]);
+            }
         }
-        if (++c == nck) {
+        if (++c == nst) {
             // the slot is done: weigh it per token and add it to the task's sum
             c = 0;
             const float w0 = s_w[c_u * kBatchMax + 2 * cc], w1 = s_w[c_u * kBatchMax + 2 * cc + 1];

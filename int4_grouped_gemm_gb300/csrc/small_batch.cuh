@@ -70,7 +70,6 @@ struct BatchArgs {
 // kSbWarps warps per SM, a ring of cp.async stages per warp).
 constexpr int kSbWarps = 16;  // warps per block of the streaming kernels (one block per SM)
 constexpr int kSbThreads = kSbWarps * 32;
-constexpr int kSbStages = 8;  // cp.async stages per warp
 // gate/up stage: two 64-element chunks, [2 matrices][16 rows] x 64 B of
 // nibbles (each row's 16 words of the two chunks in order: a row is read in
 // 64-byte pieces), then [2 matrices][16 rows] x (8 B of scales, 8 B of
@@ -79,11 +78,17 @@ constexpr int kGuChunks = 2;
 constexpr int kGuRow = 32 * kGuChunks;
 constexpr int kGuQ = 2 * 16 * kGuRow;
 constexpr int kGuStage = kGuQ + 2 * 16 * 16;
-// down stage: [16 rows] x 32 B of nibbles, [16 rows] x (scale pair, bias
-// pair), then [32 lanes] x 32 B of the slot's h (token g, K = 16c ..)
-constexpr int kDnQ = 16 * 32;
-constexpr int kDnH = kDnQ + 16 * 8;
-constexpr int kDnStage = kDnH + 32 * 32;
+// down stage: two 64-element chunks, [16 rows] x 64 B of nibbles (each
+// row's 16 words in order: a row is read in 64-byte pieces), [16 rows] x
+// (8 B of scales, 8 B of biases) of the stage's groups (group 64: two
+// values each; group 32: four), then [2 chunks][32 lanes] x 32 B of the
+// slot's h (token g, K = 16c ..)
+constexpr int kDnChunks = 2;
+constexpr int kDnStages = 4;  // cp.async stages per warp of the down kernel
+constexpr int kDnRow = 32 * kDnChunks;
+constexpr int kDnQ = 16 * kDnRow;
+constexpr int kDnH = kDnQ + 16 * 16;
+constexpr int kDnStage = kDnH + kDnChunks * 32 * 32;
 constexpr int kSmemMax = 227 * 1024;
 
 __host__ __device__ inline int align16i(int v) { return (v + 15) & ~15; }
@@ -106,7 +111,7 @@ inline int gu_stages(int H, int G, int S_max) { return gu_smem(H, G, S_max, 4) <
 
 // Shared memory of the down kernel: the slot weights [n_slots][8], then the rings.
 __host__ __device__ inline int dn_ring_off(int S_max) { return align16i(4 * kBatchMax * S_max); }
-inline int dn_smem(int S_max) { return dn_ring_off(S_max) + kSbWarps * kSbStages * kDnStage; }
+inline int dn_smem(int S_max) { return dn_ring_off(S_max) + kSbWarps * kDnStages * kDnStage; }
 
 cudaError_t launch_batch(const BatchArgs &a, int num_sms, cudaStream_t s);
 
