@@ -57,7 +57,7 @@ int main() {
                         for (int G : {32, 64}) {
                             const int st = gu_stages(H, G, B.S_max);
                             expect(gu_smem(H, G, B.S_max, st) <= kSmemMax, "gate/up shared memory", E, k, H, I, G);
-                            expect(st == 8 || H > 2048, "eight gate/up stages up to H = 2048", E, k, H, I, G);
+                            expect(st == 4 || H > 2048, "four two-chunk gate/up stages up to H = 2048", E, k, H, I, G);
                         }
                         expect(dn_smem(B.S_max) + 1024 <= kSmemMax, "down shared memory", E, k, H, I, 0);
                     }
