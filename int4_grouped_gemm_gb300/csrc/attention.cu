@@ -13,42 +13,56 @@
 // sum_t p_t v_gt.  Decode reads every cached key and value row once, so the
 // call is bound by those bytes (2 * Hkv * L * D * 2 bytes) over HBM.
 //
-// gqa_attention_kernel: one block per (key-value head, range of positions);
-// the range streams through shared memory in sub-chunks of 64 rows (three
-// cp.async stages of keys and values, two sub-chunks in flight while one is
-// used; rows padded by 16 bytes so that ldmatrix's eight row addresses fall
-// on different banks).  Per sub-chunk:
-//   scores   S = K Q^T on mma.sync m16n8k16 (bf16 products, fp32 sums): the
-//            key rows as M, the group's query heads as the 8 columns of N
-//            (columns past the group are zero) - every key row is read once
-//            for all the heads that share it;
-//   softmax  online, per head: running maximum m and sum l, the previous
+// gqa_attention_kernel: one block of eight warps per SM and per (key-value
+// head, range of positions).  The range is cut into tiles of 16 positions
+// and warp w takes tiles w, w + 8, ...; each warp streams its tiles through
+// its own ring of three cp.async stages (keys and values of one tile per
+// stage; all three in flight while the warp waits, 192 KB per SM) and keeps
+// its own online softmax, so no block-wide barrier separates the tiles.
+// Rows are 16-byte-chunk swizzled (chunk c of row r at c ^ (r & 7)) so that
+// ldmatrix's eight row addresses fall on different banks.  Per tile, on
+// mma.sync m16n8k16 (bf16 products, fp32 sums):
+//   scores   S = Q K^T with the group's query heads as M (rows past the
+//            group zero) and the tile's 16 positions as N (two MMAs per
+//            16 of D); every key row is read once for all the heads that
+//            share it.  The scores' accumulator layout (head g, positions
+//            2c, 2c+1 and 2c+8, 2c+9 in thread (g, c)) is the layout of
+//            the A operand of the next product, so the probabilities never
+//            leave the registers;
+//   softmax  online, per head: running maximum m (the tile maximum from
+//            two lane shuffles), per-thread partial sums l and the
 //            partial output rescaled by exp(m_old - m_new);
-//   output   O^T += V^T P: the value rows, transposed by ldmatrix, as M
-//            (16 features per warp), P as N; P is split into bf16 hi + lo
-//            parts (|p - hi - lo| <= 2^-17 p) so that the products stay
-//            within fp32 accuracy.
-// Each block writes its unnormalised partial output and (m, l) per head;
-// gqa_combine_kernel merges the ranges of each head in a fixed order:
-// o = sum_r e^(m_r - m) O_r / sum_r e^(m_r - m) l_r, rounded once to bf16.
-// The per-head variant (one query head per block) gives every head its own blocks, which
-// read their key-value rows themselves: the layout that packing replaces,
-// kept for the comparison in the benchmark.
+//   output   O += P V with P as A (split into bf16 hi + lo parts,
+//            |p - hi - lo| <= 2^-17 p, so that the products stay within
+//            fp32 accuracy) and the value rows, transposed by ldmatrix, as
+//            B (8 features per MMA).
+// At the end the eight warps' (m, l, O) are merged through shared memory
+// in warp order, and the block writes its unnormalised partial output and
+// (m, l) per head; gqa_combine_kernel merges the ranges of each head in a
+// fixed order: o = sum_r e^(m_r - m) O_r / sum_r e^(m_r - m) l_r, rounded
+// once to bf16.  The per-head variant (one query head per block) gives
+// every head its own blocks, which read their key-value rows themselves:
+// the layout that packing replaces, kept for the comparison in the
+// benchmark.
 #include "attention.cuh"
 
 namespace moe {
 
-constexpr int kAttnThreads = 256;
-constexpr int kSub = 64;     // rows per sub-chunk
-constexpr int kStages = 3;   // cp.async stages of keys and values (two sub-chunks in flight)
-constexpr int kSP = kSub + 8;  // pitch (floats) of the head-major scores: heads 8 banks apart
-constexpr int kHeads = 8;    // query heads per block (MMA N)
+constexpr int kAttnWarps = 8;
+constexpr int kAttnThreads = kAttnWarps * 32;
+constexpr int kTile = 16;     // positions per tile (MMA N of the scores, K of the output)
+constexpr int kHeads = 8;     // query heads per block (real rows of the MMA M)
 
-__host__ __device__ constexpr int attn_pitch(int D) { return D * 2 + 16; }  // bytes per staged row
-__host__ __device__ constexpr int attn_stage_bytes(int D) { return 2 * kSub * attn_pitch(D); }
+// cp.async stages per warp (24 KB of keys and values per warp either way)
+__host__ __device__ constexpr int attn_stages(int D) { return D == 128 ? 3 : 6; }
+__host__ __device__ constexpr int attn_stage_bytes(int D) { return 2 * kTile * D * 2; }  // keys, then values
 __host__ __device__ constexpr int attn_smem_bytes(int D) {
-    return kStages * attn_stage_bytes(D) + kHeads * kSP * 4;  // rings + scores / probabilities
+    return kAttnWarps * attn_stages(D) * attn_stage_bytes(D);
 }
+// the final merge reuses the rings: per warp, O [8 heads][D] fp32 and (m, l) per head
+static_assert(kAttnWarps * (kHeads * 128 + 2 * kHeads) * 4 <= attn_smem_bytes(128), "merge buffer fits");
+static_assert(kAttnWarps * (kHeads * 64 + 2 * kHeads) * 4 <= attn_smem_bytes(64), "merge buffer fits");
+static_assert(attn_smem_bytes(128) <= 227 * 1024 && attn_smem_bytes(64) <= 227 * 1024, "one block per SM");
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -64,9 +78,9 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
 
 // 16 bytes from global to shared memory, or zeros when `valid` is false (the
 // source is then not read).
-__device__ __forceinline__ void cp_async16_zfill(void *dst, const void *src, bool valid) {
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void *src, bool valid) {
     const int n = valid ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(n) : "memory");
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
@@ -75,17 +89,18 @@ __device__ __forceinline__ uint32_t pack2_bf16(float lo, float hi) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads) gqa_attention_kernel(const __grid_constant__ GqaArgs a) {
+__global__ void __launch_bounds__(kAttnThreads, 1) gqa_attention_kernel(const __grid_constant__ GqaArgs a) {
     static_assert(D == 64 || D == 128, "head dimension 64 or 128");
     // the merge kernel (a programmatic dependent) may be scheduled now; it
     // waits for this grid's results before it reads them
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int KD = D / 16;          // MMA k-steps of the scores
-    constexpr int CH = D * 2 / 16;      // 16-byte pieces of a row
-    constexpr int PITCH = attn_pitch(D);
-    extern __shared__ __align__(16) uint8_t smem[];
-    float *sp = reinterpret_cast<float *>(smem + kStages * attn_stage_bytes(D));  // [kHeads][kSP]
-    __shared__ float s_m[kHeads], s_l[kHeads], s_c[kHeads];
+    constexpr int NT = D / 8;           // 8-feature MMA tiles of the output
+    constexpr int CH = D * 2 / 16;      // 16-byte chunks of a row
+    constexpr int ROW = D * 2;          // bytes per staged row (swizzled, no padding)
+    constexpr int NS = attn_stages(D);
+    constexpr int STAGE = attn_stage_bytes(D);
+    extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g8 = lane >> 2, c = lane & 3;
 
@@ -102,149 +117,160 @@ __global__ void __launch_bounds__(kAttnThreads) gqa_attention_kernel(const __gri
     const __nv_bfloat16 *kbase = a.k + static_cast<int64_t>(kv) * a.L_cap * D;
     const __nv_bfloat16 *vbase = a.v + static_cast<int64_t>(kv) * a.L_cap * D;
 
-    // the group's queries as the B operand of the scores: thread (g8, c)
+    // the group's queries as the A operand of the scores: thread (g8, c)
     // holds q[h0 + g8][16 kd + 2c, +1] and [16 kd + 2c + 8, +9]; heads past
-    // the group are zero
-    uint32_t qb[KD][2];
+    // the group and the MMA's rows 8-15 are zero
+    uint32_t qa[KD][2];
     {
         const bool real = g8 < nq;
         const uint32_t *qrow = reinterpret_cast<const uint32_t *>(a.q + static_cast<int64_t>(h0 + (real ? g8 : 0)) * D);
 #pragma unroll
         for (int kd = 0; kd < KD; ++kd) {
-            qb[kd][0] = real ? __ldg(qrow + kd * 8 + c) : 0u;
-            qb[kd][1] = real ? __ldg(qrow + kd * 8 + c + 4) : 0u;
+            qa[kd][0] = real ? __ldg(qrow + kd * 8 + c) : 0u;
+            qa[kd][1] = real ? __ldg(qrow + kd * 8 + c + 4) : 0u;
         }
-    }
-    if (tid < kHeads) {
-        s_m[tid] = -INFINITY;
-        s_l[tid] = 0.f;
     }
 
-    auto issue = [&](int sub, int stage) {
-        uint8_t *ks = smem + stage * attn_stage_bytes(D);
-        uint8_t *vs = ks + kSub * PITCH;
-        const int r0 = t_begin + sub * kSub;
-        for (int i = tid; i < 2 * kSub * CH; i += kAttnThreads) {
-            const int m = i / (kSub * CH), rem = i - m * kSub * CH;
-            const int r = rem / CH, piece = rem - r * CH;
-            const bool valid = r0 + r < t_end;
-            const __nv_bfloat16 *src = (m ? vbase : kbase) + static_cast<int64_t>(valid ? r0 + r : t_begin) * D + piece * 8;
-            cp_async16_zfill((m ? vs : ks) + r * PITCH + piece * 16, src, valid);
+    // this warp's tiles: w, w + 8, ... of the range's 16-position tiles
+    const int ntile = (t_end - t_begin + kTile - 1) / kTile;
+    const int my_n = ntile > warp ? (ntile - warp + kAttnWarps - 1) / kAttnWarps : 0;
+    const uint32_t ring = smem_u32(smem) + warp * NS * STAGE;
+    // the warp's i-th tile into stage i % NS: keys then values, chunk ch of
+    // row r at (ch ^ (r & 7)); positions past the range are zero-filled
+    auto issue = [&](int i) {
+        const int p0 = t_begin + (warp + kAttnWarps * i) * kTile;
+        const uint32_t st = ring + (i % NS) * STAGE;
+#pragma unroll 4
+        for (int j = lane; j < 2 * kTile * CH; j += 32) {
+            const int m = j / (kTile * CH), rem = j - m * kTile * CH;
+            const int r = rem / CH, ch = rem - r * CH;
+            const bool valid = p0 + r < t_end;
+            const __nv_bfloat16 *src = (m ? vbase : kbase) + static_cast<int64_t>(valid ? p0 + r : t_begin) * D + ch * 8;
+            cp_async16_zfill(st + m * kTile * ROW + r * ROW + ((ch ^ (r & 7)) << 4), src, valid);
         }
-        cp_async_commit();
     };
 
-    // output accumulators: warp w owns features [16 w, 16 w + 16) (D = 128;
-    // D = 64 uses warps 0-3): d0/d1 = (feature g8, heads 2c, 2c+1),
-    // d2/d3 = (feature g8 + 8, heads 2c, 2c+1)
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const int nsub = (t_end - t_begin + kSub - 1) / kSub;
-    for (int i = 0; i < kStages - 1 && i < nsub; ++i) issue(i, i);
-    for (int sub = 0; sub < nsub; ++sub) {
-        const int stage = sub % kStages;
-        // this sub-chunk's copies have landed once at most (stages - 2) later
-        // groups are pending (fewer near the end)
-        const int later = nsub - 1 - sub < kStages - 2 ? nsub - 1 - sub : kStages - 2;
-        if (later >= 1)
-            cp_async_wait<1>();
-        else
-            cp_async_wait<0>();
-        __syncthreads();  // every thread's copies are in; the stage refilled below and the scores were last
-                          // read in the previous sub-chunk, before this barrier
-        if (sub + kStages - 1 < nsub) issue(sub + kStages - 1, (sub + kStages - 1) % kStages);
-        const uint8_t *ks = smem + stage * attn_stage_bytes(D);
-        const uint8_t *vs = ks + kSub * PITCH;
-        const int r0 = t_begin + sub * kSub;
+    // output accumulators: o[n] = (head g8, features 8n + 2c, +1) and the
+    // MMA's rows 8-15 (always zero); running maximum and partial sum of head g8
+    float o[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
 
-        // scores: warps 0-3 one 16-row tile each, stored head-major
-        if (warp < kSub / 16) {
-            float s[4] = {0.f, 0.f, 0.f, 0.f};
-            const int mi = lane >> 3, rr = lane & 7;
-            const uint32_t base = smem_u32(ks) + (warp * 16 + (mi & 1) * 8 + rr) * PITCH + (mi >> 1) * 16;
+    // ldmatrix lane roles: matrix mi = lane / 8, row rr = lane % 8
+    const int mi = lane >> 3, rr = lane & 7;
+    const int kpos = (mi >> 1) * 8 + rr, kch = mi & 1;  // keys: positions 0-7 / 8-15, low / high 8 of the 16 d
+    const int vpos = (mi & 1) * 8 + rr, vch = mi >> 1;  // values: positions 0-7 / 8-15, features low / high 8
+
+    // all NS stages are requested up front and each one is refilled as soon
+    // as its tile has been used; every warp commits one cp.async group per
+    // tile slot (empty ones past its tiles), so that tile i has landed once
+    // at most NS - 1 groups are pending
 #pragma unroll
-            for (int kd = 0; kd < KD; ++kd) {
-                uint32_t af[4];
-                ldsm_x4(af, base + kd * 32);
-                mma_16816(s, af, qb[kd][0], qb[kd][1]);
-            }
-            // rows past the range (zero-filled) never count
-            const int ra = warp * 16 + g8, rb = ra + 8;
-            const bool va = r0 + ra < t_end, vb = r0 + rb < t_end;
-            sp[(2 * c) * kSP + ra] = va ? s[0] * a.scale : -INFINITY;
-            sp[(2 * c + 1) * kSP + ra] = va ? s[1] * a.scale : -INFINITY;
-            sp[(2 * c) * kSP + rb] = vb ? s[2] * a.scale : -INFINITY;
-            sp[(2 * c + 1) * kSP + rb] = vb ? s[3] * a.scale : -INFINITY;
-        }
-        __syncthreads();
-        // online softmax: warp w takes head w (heads past the group: p = 0)
-        {
-            const int h = warp;
-            float *row = sp + h * kSP;
-            if (h < nq) {
-                const float v0 = row[lane], v1 = row[lane + 32];
-                float mx = fmaxf(v0, v1);
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                const float m_old = s_m[h];
-                const float m_new = fmaxf(m_old, mx);  // a sub-chunk has at least one valid row
-                const float p0 = expf(v0 - m_new), p1 = expf(v1 - m_new);
-                float ps = p0 + p1;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-                row[lane] = p0;
-                row[lane + 32] = p1;
-                if (lane == 0) {
-                    const float corr = expf(m_old - m_new);  // 0 on the first sub-chunk (m_old = -inf)
-                    s_c[h] = corr;
-                    s_l[h] = s_l[h] * corr + ps;
-                    s_m[h] = m_new;
-                }
-            } else {
-                row[lane] = 0.f;
-                row[lane + 32] = 0.f;
-                if (lane == 0) s_c[h] = 0.f;
-            }
-        }
-        __syncthreads();
-        // output: rescale, then O^T[16 features][8 heads] += V^T P over the 64 rows
-        if (warp < D / 16) {
-            const float c0 = s_c[2 * c], c1 = s_c[2 * c + 1];
-            acc[0] *= c0;
-            acc[1] *= c1;
-            acc[2] *= c0;
-            acc[3] *= c1;
-            const int mi = lane >> 3, rr = lane & 7;
-            const uint32_t base = smem_u32(vs) + ((mi >> 1) * 8 + rr) * PITCH + (warp * 16 + (mi & 1) * 8) * 2;
-            const float *pr = sp + g8 * kSP;  // head g8's probabilities
-#pragma unroll
-            for (int ks2 = 0; ks2 < kSub / 16; ++ks2) {
-                uint32_t af[4];
-                ldsm_x4_trans(af, base + ks2 * 16 * PITCH);
-                // P rows 16 ks2 + 2c, +1 and + 8, + 9 of head g8, split hi + lo
-                const float p00 = pr[ks2 * 16 + 2 * c], p01 = pr[ks2 * 16 + 2 * c + 1];
-                const float p10 = pr[ks2 * 16 + 2 * c + 8], p11 = pr[ks2 * 16 + 2 * c + 9];
-                const uint32_t hi0 = pack2_bf16(p00, p01), hi1 = pack2_bf16(p10, p11);
-                const uint32_t lo0 = pack2_bf16(p00 - __uint_as_float(hi0 << 16), p01 - __uint_as_float(hi0 & 0xFFFF0000u));
-                const uint32_t lo1 = pack2_bf16(p10 - __uint_as_float(hi1 << 16), p11 - __uint_as_float(hi1 & 0xFFFF0000u));
-                mma_16816(acc, af, hi0, hi1);
-                mma_16816(acc, af, lo0, lo1);
-            }
-        }
+    for (int i = 0; i < NS; ++i) {
+        if (i < my_n) issue(i);
+        cp_async_commit();
     }
+    for (int i = 0; i < my_n; ++i) {
+        cp_async_wait<NS - 1>();
+        __syncwarp();  // the whole tile is in for every lane
+        const uint32_t sk = ring + (i % NS) * STAGE, sv = sk + kTile * ROW;
+        const int p0 = t_begin + (warp + kAttnWarps * i) * kTile;
 
-    // partial output (unnormalised) and (m, l) of this range, per real head
+        // scores of positions p0 + 2c, +1 (s0) and p0 + 8 + 2c, +1 (s1) for
+        // head g8; even and odd k-steps in separate accumulators (two short
+        // dependent chains instead of one long one), added at the end
+        float s0[2][4] = {}, s1[2][4] = {};
+#pragma unroll
+        for (int kd = 0; kd < KD; ++kd) {
+            uint32_t b[4];
+            ldsm_x4(b, sk + kpos * ROW + (((2 * kd + kch) ^ (kpos & 7)) << 4));
+            const uint32_t af[4] = {qa[kd][0], 0u, qa[kd][1], 0u};
+            mma_16816(s0[kd & 1], af, b[0], b[1]);
+            mma_16816(s1[kd & 1], af, b[2], b[3]);
+        }
+        float sc[4] = {s0[0][0] + s0[1][0], s0[0][1] + s0[1][1], s1[0][0] + s1[1][0], s1[0][1] + s1[1][1]};
+        const int pos[4] = {p0 + 2 * c, p0 + 2 * c + 1, p0 + 8 + 2 * c, p0 + 9 + 2 * c};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc[j] = pos[j] < t_end ? sc[j] * a.scale : -INFINITY;
+        float tmax = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 1));
+        tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 2));
+        const float m_new = fmaxf(m_run, tmax);   // finite: a tile holds at least one position of the range
+        const float corr = expf(m_run - m_new);   // 0 on the warp's first tile (m_run = -inf)
+        float p[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) p[j] = expf(sc[j] - m_new);
+        l_run = l_run * corr + ((p[0] + p[1]) + (p[2] + p[3]));
+        m_run = m_new;
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            o[n][0] *= corr;
+            o[n][1] *= corr;
+        }
+        // P as the A operand (rows 8-15 zero), split into bf16 hi + lo
+        const uint32_t hi0 = pack2_bf16(p[0], p[1]), hi1 = pack2_bf16(p[2], p[3]);
+        const uint32_t lo0 = pack2_bf16(p[0] - __uint_as_float(hi0 << 16), p[1] - __uint_as_float(hi0 & 0xFFFF0000u));
+        const uint32_t lo1 = pack2_bf16(p[2] - __uint_as_float(hi1 << 16), p[3] - __uint_as_float(hi1 & 0xFFFF0000u));
+        const uint32_t ph[4] = {hi0, 0u, hi1, 0u}, pl[4] = {lo0, 0u, lo1, 0u};
+#pragma unroll
+        for (int jt = 0; jt < NT / 2; ++jt) {
+            uint32_t b[4];
+            ldsm_x4_trans(b, sv + vpos * ROW + (((2 * jt + vch) ^ (vpos & 7)) << 4));
+            mma_16816(o[2 * jt], ph, b[0], b[1]);
+            mma_16816(o[2 * jt], pl, b[0], b[1]);
+            mma_16816(o[2 * jt + 1], ph, b[2], b[3]);
+            mma_16816(o[2 * jt + 1], pl, b[2], b[3]);
+        }
+        __syncwarp();  // every lane has read the stage before it is refilled
+        if (i + NS < my_n) issue(i + NS);
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+
+    // merge the eight warps in warp order through shared memory (the rings
+    // are free once every warp is past its loop): m = max_w m_w,
+    // O = sum_w e^(m_w - m) O_w, l = sum_w e^(m_w - m) l_w
+    __syncthreads();
+    float *mo = reinterpret_cast<float *>(smem);              // [warp][head][D]
+    float *mm = mo + kAttnWarps * kHeads * D;                  // [warp][head]
+    float *ml = mm + kAttnWarps * kHeads;                      // [warp][head]
+    float l_sum = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
+    l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 2);
+    if (my_n > 0) {
+#pragma unroll
+        for (int n = 0; n < NT; ++n)
+            *reinterpret_cast<float2 *>(mo + (warp * kHeads + g8) * D + 8 * n + 2 * c) = make_float2(o[n][0], o[n][1]);
+    }
+    if (c == 0) {
+        mm[warp * kHeads + g8] = m_run;   // -inf for a warp without tiles
+        ml[warp * kHeads + g8] = l_sum;
+    }
+    __syncthreads();
+    constexpr int FPT = D / 32;  // features per thread: thread t takes head t / 32
+    const int hh = tid >> 5, f0 = lane * FPT;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mm[w * kHeads + hh]);
+    float num[FPT], den = 0.f;
+#pragma unroll
+    for (int f = 0; f < FPT; ++f) num[f] = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAttnWarps; ++w) {
+        const float mw = mm[w * kHeads + hh];
+        if (mw == -INFINITY) continue;  // a warp without tiles
+        const float e = expf(mw - M);
+        den += e * ml[w * kHeads + hh];
+#pragma unroll
+        for (int f = 0; f < FPT; ++f) num[f] += e * mo[(w * kHeads + hh) * D + f0 + f];
+    }
     const int64_t part = static_cast<int64_t>(hb) * a.nsplit + split;
-    if (warp < D / 16) {
-        float *op = a.part_o + part * kHeads * D;
-        const int f = warp * 16 + g8;
-        op[(2 * c) * D + f] = acc[0];
-        op[(2 * c + 1) * D + f] = acc[1];
-        op[(2 * c) * D + f + 8] = acc[2];
-        op[(2 * c + 1) * D + f + 8] = acc[3];
-    }
-    if (tid < kHeads) {
-        a.part_ml[part * 2 * kHeads + tid] = s_m[tid];
-        a.part_ml[part * 2 * kHeads + kHeads + tid] = s_l[tid];
+    float *op = a.part_o + (part * kHeads + hh) * D + f0;
+#pragma unroll
+    for (int f = 0; f < FPT; ++f) op[f] = num[f];
+    if (lane == 0) {
+        a.part_ml[part * 2 * kHeads + hh] = M;
+        a.part_ml[part * 2 * kHeads + kHeads + hh] = den;
     }
 }
 
@@ -308,8 +334,8 @@ __global__ void __launch_bounds__(256) gqa_combine_kernel(const __grid_constant_
 }
 
 int gqa_splits(int L, int blocks_y, int num_sms) {
-    int n = (L + kSub - 1) / kSub;              // at least one sub-chunk per range
-    const int fill = (2 * num_sms) / blocks_y;  // about two blocks per SM
+    int n = (L + 63) / 64;                  // at least 64 positions (four tiles) per range
+    const int fill = num_sms / blocks_y;    // one block per SM
     if (n > fill) n = fill;
     return n < 1 ? 1 : n;
 }

@@ -48,3 +48,30 @@ def test_no_register_spills():
                 limit = next((v for k, v in ALLOWED_SPILL.items() if k in fn), 0)
                 assert stores <= limit, f"{src}: {fn} spills {stores} bytes (allowed {limit})"
     assert seen >= 15  # every kernel of the library was reported
+
+
+def test_attention_kernel_leaves_room_for_the_merge_block():
+    """The GQA attention kernel (one 256-thread block per SM) uses few
+    enough registers that a block of the merge kernel (a programmatic
+    dependent, 256 threads) fits beside it in the SM's 65,536 registers and
+    is resident before the attention blocks finish (at 209 registers it was
+    not, and the 32K call took 3 us longer)."""
+    if not (shutil.which("nvcc") or os.path.exists("/usr/local/cuda/bin/nvcc")):
+        pytest.skip("no nvcc")
+    text = _report("attention.cu")
+    regs, fn = {}, None
+    for line in text.splitlines():
+        m = re.search(r"Compiling entry function '(\S+)'", line)
+        if m:
+            fn = m.group(1)
+            continue
+        m = re.search(r"Used (\d+) registers", line)
+        if m and fn:
+            regs[fn] = int(m.group(1))
+    attn = {f: r for f, r in regs.items() if "gqa_attention_kernel" in f}
+    merge = [r for f, r in regs.items() if "gqa_combine_kernel" in f]
+    assert len(attn) == 2 and len(merge) == 1, regs
+    for f, r in attn.items():
+        # registers are allocated per warp in units of 256 (8 per thread)
+        per_block = lambda n: 256 * ((n + 7) // 8 * 8)  # noqa: E731
+        assert per_block(r) + per_block(merge[0]) <= 65536, (f, r, merge[0])

@@ -1,7 +1,7 @@
 """GQA decode attention (the second workload) against the CPU oracle: one
 token's attention over a key-value cache, query heads sharing key-value
 heads, packed (each key-value row read once for its query heads) and per
-head; ragged cache lengths around the kernel's 64-row sub-chunks, partly
+head; ragged cache lengths around the kernel's 16-position tiles, partly
 filled caches, group sizes 1-8, head dimensions 64 and 128, a peaked softmax,
 the uniform case, and the full 32K-position cache of the benchmark."""
 import math
