@@ -59,9 +59,12 @@ __host__ __device__ constexpr int attn_stage_bytes(int D) { return 2 * kTile * D
 __host__ __device__ constexpr int attn_smem_bytes(int D) {
     return kAttnWarps * attn_stages(D) * attn_stage_bytes(D);
 }
-// the final merge reuses the rings: per warp, O [8 heads][D] fp32 and (m, l) per head
-static_assert(kAttnWarps * (kHeads * 128 + 2 * kHeads) * 4 <= attn_smem_bytes(128), "merge buffer fits");
-static_assert(kAttnWarps * (kHeads * 64 + 2 * kHeads) * 4 <= attn_smem_bytes(64), "merge buffer fits");
+// the final merge reuses the rings: per warp, O [8 heads][D + 8] fp32 (rows
+// padded by 32 bytes: the lanes' float2 writes of four heads fall on
+// different banks) and (m, l) per head
+__host__ __device__ constexpr int attn_merge_pitch(int D) { return D + 8; }
+static_assert(kAttnWarps * (kHeads * attn_merge_pitch(128) + 2 * kHeads) * 4 <= attn_smem_bytes(128), "merge buffer fits");
+static_assert(kAttnWarps * (kHeads * attn_merge_pitch(64) + 2 * kHeads) * 4 <= attn_smem_bytes(64), "merge buffer fits");
 static_assert(attn_smem_bytes(128) <= 227 * 1024 && attn_smem_bytes(64) <= 227 * 1024, "one block per SM");
 
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
@@ -232,15 +235,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_attention_kernel(const __
     // are free once every warp is past its loop): m = max_w m_w,
     // O = sum_w e^(m_w - m) O_w, l = sum_w e^(m_w - m) l_w
     __syncthreads();
-    float *mo = reinterpret_cast<float *>(smem);              // [warp][head][D]
-    float *mm = mo + kAttnWarps * kHeads * D;                  // [warp][head]
+    constexpr int MP = attn_merge_pitch(D);
+    float *mo = reinterpret_cast<float *>(smem);              // [warp][head][MP]
+    float *mm = mo + kAttnWarps * kHeads * MP;                 // [warp][head]
     float *ml = mm + kAttnWarps * kHeads;                      // [warp][head]
     float l_sum = l_run + __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_sum += __shfl_xor_sync(0xffffffffu, l_sum, 2);
     if (my_n > 0) {
 #pragma unroll
         for (int n = 0; n < NT; ++n)
-            *reinterpret_cast<float2 *>(mo + (warp * kHeads + g8) * D + 8 * n + 2 * c) = make_float2(o[n][0], o[n][1]);
+            *reinterpret_cast<float2 *>(mo + (warp * kHeads + g8) * MP + 8 * n + 2 * c) = make_float2(o[n][0], o[n][1]);
     }
     if (c == 0) {
         mm[warp * kHeads + g8] = m_run;   // -inf for a warp without tiles
@@ -261,8 +265,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1) gqa_attention_kernel(const __
         if (mw == -INFINITY) continue;  // a warp without tiles
         const float e = expf(mw - M);
         den += e * ml[w * kHeads + hh];
+        const float *src = mo + (w * kHeads + hh) * MP + f0;  // FPT consecutive floats, one vector load
+        float v[FPT];
+        if constexpr (FPT == 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(src);
+            v[0] = t.x;
+            v[1] = t.y;
+            v[2] = t.z;
+            v[3] = t.w;
+        } else {
+            const float2 t = *reinterpret_cast<const float2 *>(src);
+            v[0] = t.x;
+            v[1] = t.y;
+        }
 #pragma unroll
-        for (int f = 0; f < FPT; ++f) num[f] += e * mo[(w * kHeads + hh) * D + f0 + f];
+        for (int f = 0; f < FPT; ++f) num[f] += e * v[f];
     }
     const int64_t part = static_cast<int64_t>(hb) * a.nsplit + split;
     float *op = a.part_o + (part * kHeads + hh) * D + f0;
