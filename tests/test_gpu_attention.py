@@ -47,6 +47,11 @@ SHAPES = [
     AttnConfig("group3", Hq=12, Hkv=4, D=128, L=300, seed=208),
     AttnConfig("mha_group1", Hq=16, Hkv=16, D=64, L=150, seed=209),
     AttnConfig("peaked", Hq=16, Hkv=2, D=128, L=2000, seed=210, k_scale=6.0),
+    # one position past a 16-position tile; 256 query heads, whose per-head
+    # blocks each take all 257 positions (17 tiles: two or three rounds of
+    # the eight warps, the last tile one position long)
+    AttnConfig("tile_plus_one", Hq=16, Hkv=2, D=128, L=17, seed=211),
+    AttnConfig("heads256_range257", Hq=256, Hkv=32, D=64, L=257, L_cap=300, seed=212),
 ]
 
 
