@@ -270,7 +270,8 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     const int ldg_h = ld_groups(H, G), ldg_i = ld_groups(I, G);
     const auto U16 = CU_TENSOR_MAP_DATA_TYPE_UINT16, U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32,
                BF16 = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    const auto SW0 = CU_TENSOR_MAP_SWIZZLE_NONE, SW64 = CU_TENSOR_MAP_SWIZZLE_64B, SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
+    const auto SW0 = CU_TENSOR_MAP_SWIZZLE_NONE, SW32 = CU_TENSOR_MAP_SWIZZLE_32B, SW64 = CU_TENSOR_MAP_SWIZZLE_64B,
+               SW128 = CU_TENSOR_MAP_SWIZZLE_128B;
     const uint64_t gu_rows = static_cast<uint64_t>(nexp) * I, dn_rows = static_cast<uint64_t>(nexp) * H;
 
     // router: A = x tiles, B = bf16 parts of the router weights
@@ -288,8 +289,8 @@ static int prefill_impl(const moe_layer_desc *desc, const void *x, int32_t T, vo
     // f0..f0+127 of one expert
     if ((rc = encode_2d(&m1.a0, BF16, 2, x, H, T, 64, 128, SW128)) ||
         (rc = encode_2d(&m1.a1, BF16, 2, x, H, T, 64, 128, SW128)) ||
-        (rc = encode_2d(&m1.w0, U32, 4, desc->gate.q, H / 8, gu_rows, 16, 128, SW64)) ||
-        (rc = encode_2d(&m1.w1, U32, 4, desc->up.q, H / 8, gu_rows, 16, 128, SW64)) ||
+        (rc = encode_2d(&m1.w0, U32, 4, desc->gate.q, H / 8, gu_rows, 8, 128, SW32)) ||
+        (rc = encode_2d(&m1.w1, U32, 4, desc->up.q, H / 8, gu_rows, 8, 128, SW32)) ||
         (rc = encode_2d(&m1.s0, U16, 2, desc->gate.scale, ldg_h, gu_rows, 8, 128, SW0)) ||
         (rc = encode_2d(&m1.b0, U16, 2, desc->gate.bias, ldg_h, gu_rows, 8, 128, SW0)) ||
         (rc = encode_2d(&m1.s1, U16, 2, desc->up.scale, ldg_h, gu_rows, 8, 128, SW0)) ||

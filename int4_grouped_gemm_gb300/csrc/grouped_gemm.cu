@@ -29,13 +29,15 @@
 //   warp 10     down/router A producer: TMA loads of the unit's token tiles (16 KB
 //               boxes per stage) from h (down) or from x (router); gate/up:
 //               the tile-1 MMA issuer
-//   warp 8      W producer: TMA loads of packed nibbles (16 KB per load: 64
-//               bytes of each of the 256 weight rows, two stages' worth, in
-//               the 64-byte swizzle so that the dequant threads' 16-byte reads
-//               are conflict-free; a TMA load costs per box row, so wide rows
-//               matter) and of scale/bias blocks (8 groups x 256 rows);
-//               router mode: the bf16 router weight tile straight into the B
-//               ring
+//   warp 8      W producer: TMA loads of packed nibbles and of scale/bias
+//               blocks (8 groups x 256 rows); down: 16 KB per load, 64 bytes
+//               of each of the 256 weight rows (two stages) in the 64-byte
+//               swizzle; gate/up: 8 KB per load, one stage (32 bytes per row,
+//               32-byte swizzle), which leaves room for a third weight stage
+//               (2 % faster than two stages with two-stage loads); either
+//               swizzle keeps the dequant threads' 16-byte reads
+//               conflict-free; router mode: the bf16 router weight tile
+//               straight into the B ring
 //   warps 11-26 dequantisers in two groups of 8 warps taking alternate
 //               stages, one thread per weight row over the stage's 64 K:
 //               nibbles -> bf16 s*q+b in the 128-byte swizzled K-major
@@ -71,8 +73,13 @@ constexpr int BN = 256;                          // weight rows per tile (MMA N)
 constexpr int GK = 64;                           // K elements per stage
 constexpr int SG = 8;                            // quantisation groups per scale block
 constexpr int NS_S = 1;                          // scale/bias ring depth (blocks)
-constexpr int QK = 2;                            // stages per nibble load
-constexpr int NS_Q = 2;                          // nibble ring depth (loads)
+// Nibble loads: gate/up one stage per load (32 bytes of each weight row, in
+// the 32-byte swizzle, three loads deep: the room that a third weight stage
+// needs), down and router two stages per load (64 bytes, 64-byte swizzle,
+// two loads deep).
+__host__ __device__ constexpr int qk(int mode) { return mode == 0 ? 1 : 2; }      // stages per nibble load
+__host__ __device__ constexpr int ns_q(int mode) { return mode == 0 ? 3 : 2; }    // nibble ring depth (loads)
+constexpr int kMaxNsQ = 3;
 constexpr int kEpiWarps = 8, kWProdWarp = 8, kMmaWarp = 9, kAProdWarp = 10, kDeqWarp0 = 11, kDeqWarps = 16;
 constexpr int kLsuWarp0 = kDeqWarp0 + kDeqWarps, kLsuWarps = 4;  // gate/up: token-row copiers
 constexpr int kLsuThreads = kLsuWarps * 32;
@@ -84,15 +91,16 @@ constexpr int TILE_A = BM * 128;                 // 16 KB: 128 token rows x 64 b
 // Token and weight ring depths (stages) and token-stage bytes.  The down
 // GEMM's units hold one token tile (its epilogue, the combine's fp32
 // reductions, then overlaps the next unit's MMAs in the other accumulator),
-// so its token stages are half as large and both of its rings are deeper.
+// so its token stages are half as large and its token ring deeper; both
+// expert GEMMs keep three weight stages (the router two).
 __host__ __device__ constexpr int tiles_per_unit(int mode) { return mode == 1 ? 1 : TPU; }
 __host__ __device__ constexpr int ring_a(int mode) { return mode == 1 ? 4 : 3; }
-__host__ __device__ constexpr int ring_b(int mode) { return mode == 1 ? 3 : 2; }
+__host__ __device__ constexpr int ring_b(int mode) { return mode == 2 ? 2 : 3; }
 __host__ __device__ constexpr int a_stage_bytes(int mode) { return tiles_per_unit(mode) * TILE_A; }
 constexpr int kMaxRingA = 4, kMaxRingB = 3;
 constexpr int B_STAGE = BN * 128;                // 32 KB: 256 weight rows x 64 bf16
-constexpr int Q_ROW = QK * GK / 2;               // 64 bytes of a weight row per nibble load
-constexpr int Q_LOAD = BN * Q_ROW;               // 16 KB: 256 rows x 128 nibbles
+__host__ __device__ constexpr int q_row(int mode) { return qk(mode) * GK / 2; }  // bytes of a weight row per load
+__host__ __device__ constexpr int q_load(int mode) { return BN * q_row(mode); }  // 8 or 16 KB per load
 constexpr int S_STAGE = 2 * BN * SG * 2;         // 8 KB: [scale|bias][256 rows][8 groups] bf16
 constexpr int T_PITCH = 16;                      // fp32 pitch of the epilogue transpose rows
 constexpr uint32_t kTmemCols = 512;              // two 256-column fp32 accumulators
@@ -103,7 +111,7 @@ constexpr int kRouterUnits = kRouterParts * kRouterKSplit;  // router units per 
 struct Smem {
     uint64_t a_full[kMaxRingA], a_empty[kMaxRingA];
     uint64_t b_full[kMaxRingB], b_empty[kMaxRingB];
-    uint64_t q_full[NS_Q], q_empty[NS_Q];
+    uint64_t q_full[kMaxNsQ], q_empty[kMaxNsQ];
     uint64_t s_full[NS_S], s_empty[NS_S];
     uint64_t acc_full[TPU], acc_empty[TPU];
     uint64_t drain;
@@ -122,7 +130,7 @@ __host__ __device__ inline SmemMap smem_map(int mode) {
     m.b = m.a + ring_a(mode) * a_stage_bytes(mode);
     m.q = m.b + ring_b(mode) * B_STAGE;
     const bool deq = mode != 2;
-    m.s = m.q + (deq ? NS_Q * Q_LOAD : 0);
+    m.s = m.q + (deq ? ns_q(mode) * q_load(mode) : 0);
     m.t = m.s + (deq ? NS_S * S_STAGE : 0);
     m.ctl = m.t + (mode != 0 ? kEpiWarps * 32 * T_PITCH * 4 : 0);
     m.total = m.ctl + static_cast<int>(sizeof(Smem)) + 1024;  // + alignment slack
@@ -222,6 +230,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int NS_A = ring_a(MODE), NS_B = ring_b(MODE), A_STAGE = a_stage_bytes(MODE);
+    constexpr int QK = qk(MODE), NS_Q = ns_q(MODE), Q_ROW = q_row(MODE), Q_LOAD = q_load(MODE);
     // two MMA issuers, one per token tile (see run_mma below)
     constexpr int kMmaIssuers = 2;
 
@@ -236,7 +245,7 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         }
         for (int i = 0; i < NS_Q; ++i) {
             mbar_init(&s->q_full[i], 1);
-            mbar_init(&s->q_empty[i], kDeqWarps);
+            mbar_init(&s->q_empty[i], QK == 1 ? kDeqWarps / 2 : kDeqWarps);  // the groups that read the load
         }
         for (int i = 0; i < NS_S; ++i) {
             mbar_init(&s->s_full[i], 1);
@@ -508,12 +517,16 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
         const int dt = tid - kDeqWarp0 * 32;
         const int jg = dt / BN;  // this group's stage parity
         const int r = dt % BN;   // weight row of the tile
-        const int rot = (r >> 1) & 3;  // 64-byte swizzle of the row's nibble chunks
-        uint32_t qit = 0, sit = 0, bs = jg, bph = 0;
+        // swizzle of the row's 16-byte nibble chunks: 64-byte (two stages per
+        // load) or 32-byte (one stage per load)
+        const int rot = QK == 2 ? (r >> 1) & 3 : (r >> 2) & 1;
+        // this group's nibble loads: every load (two stages per load, the
+        // group's stage in it) or every other one (one stage per load)
+        uint32_t qs = QK == 2 ? 0 : jg, qph = 0, sit = 0, bs = jg, bph = 0;
         uint4 sv = make_uint4(0u, 0u, 0u, 0u), bv = sv;  // this row's scales and biases of the current block
         bool ok = true;
         for (int u = blockIdx.x; u < nunits && ok; u += gridDim.x) {
-            for (int ks = jg; ks < ksteps; ks += QK) {
+            for (int ks = jg; ks < ksteps; ks += 2) {
                 if ((ks & (ks_per_sblock - 1)) == jg) {
                     // the group's first stage of a scale block: the row's 8
                     // scales and 8 biases in two 16-byte reads (32 consecutive
@@ -529,15 +542,16 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                     if (lane == 0) mbar_arrive(&s->s_empty[ss]);
                     ++sit;
                 }
-                const int qs = qit % NS_Q;
-                ok = wait_or_abort(&s->q_full[qs], (qit / NS_Q) & 1, a, s, 9) &&
+                ok = wait_or_abort(&s->q_full[qs], qph, a, s, 9) &&
                      wait_or_abort(&s->b_empty[bs], bph ^ 1, a, s, 10);
                 if (!ok) break;
-                // the row's two 16-byte chunks of this stage (2 jg, 2 jg + 1),
-                // at their 64-byte-swizzle positions
+                // the row's two 16-byte chunks of this stage (2 jg, 2 jg + 1
+                // of a two-stage load; 0, 1 of a one-stage load), at their
+                // swizzled positions
                 const uint8_t *qrow = sQ + qs * Q_LOAD + r * Q_ROW;
-                const uint4 nib0 = *reinterpret_cast<const uint4 *>(qrow + (((2 * jg) ^ rot) << 4));
-                const uint4 nib1 = *reinterpret_cast<const uint4 *>(qrow + (((2 * jg + 1) ^ rot) << 4));
+                const int c0 = QK == 2 ? 2 * jg : 0;
+                const uint4 nib0 = *reinterpret_cast<const uint4 *>(qrow + ((c0 ^ rot) << 4));
+                const uint4 nib1 = *reinterpret_cast<const uint4 *>(qrow + (((c0 + 1) ^ rot) << 4));
                 uint8_t *brow = sB + bs * B_STAGE + r * 128;
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
@@ -562,7 +576,11 @@ __global__ void __launch_bounds__(gemm_threads(MODE), 1)
                     mbar_arrive(&s->b_full[bs]);
                     mbar_arrive(&s->q_empty[qs]);  // this group's only stage of the load
                 }
-                ++qit;
+                qs += QK == 2 ? 1 : 2;  // one-stage loads: the other group's load comes in between
+                if (qs >= static_cast<uint32_t>(NS_Q)) {
+                    qs -= NS_Q;
+                    qph ^= 1;
+                }
                 bs += 2;  // the other group's stage comes in between
                 if (bs >= static_cast<uint32_t>(NS_B)) {
                     bs -= NS_B;
